@@ -1,0 +1,386 @@
+"""Decode-attention throughput of the MiKV two-tier cache on GB300.
+
+Workload (default): 32 layers of Llama-3.1-8B KV shape (32 query / 8 key heads,
+head dim 128), batch 64, prompt 8192, 20% important tokens in FP16 (window 32),
+80% retained tokens in INT2 with the channel balancer.  Inputs are seeded
+synthetic activations (outlier channels + RoPE); the per-layer packed cache is
+698 MB, larger than L2, so no flush is needed between steps.
+
+A step is one decode step through every layer: append the new token to the
+important tier, attend over both tiers, update the H2O scores, demote one token
+when the important tier is over budget.  The prompt's prefill (balancer, H2O
+scores, selection, quantisation) runs once per layer before timing.
+
+metric: KV-tokens/s = sum over layers of B * L per step time (L = cached tokens).
+
+`--impl reference` times the CPU oracle's decode attention on a bounded sample of
+the same workload (the slow, obviously-correct restatement the parity tests use).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+ROW_BYTES = {16: 512, 8: 272, 4: 144, 2: 80}    # K+V bytes per token and key head (codes + meta)
+METRIC = "decode-attn KV-tokens/s & achieved HBM GB/s (frac of 8 TB/s), mixed-prec cache"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=16)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="llama31_8b_full")
+    p.add_argument("--layers", type=int, default=None)
+    p.add_argument("--lo-bits", type=int, default=None)
+    p.add_argument("--budget", type=int, default=None)
+    p.add_argument("--batch", type=int, default=None)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    return p.parse_args()
+
+
+def workload(args):
+    from mixed_precision_kv_balancer_gb300 import inputs
+    wl = inputs.WORKLOADS[args.workload]
+    kw = {}
+    if args.layers:
+        kw["layers"] = args.layers
+    if args.lo_bits:
+        kw["lo_bits"] = args.lo_bits
+    if args.budget is not None:
+        kw["budget_pct"] = args.budget
+    if args.batch:
+        kw["B"] = args.batch
+    return wl.scaled(**kw) if kw else wl
+
+
+def cache_bytes(wl, n_hi, n_lo):
+    return wl.B * wl.Hkv * (n_hi * ROW_BYTES[wl.hi_bits] + n_lo * ROW_BYTES[wl.lo_bits])
+
+
+# ------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        self.index = index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------------ CPU oracle leg
+def _oracle_worker(job):
+    """One process of the spawn pool: time the oracle's decode attention on its units."""
+    from oracle import attention
+    hi_bits, lo_bits, units = job
+    t0 = time.perf_counter()
+    for (q, hi, lo, b) in units:
+        attention.decode_attention_unit(q, hi, lo, b, hi_bits, lo_bits, 64)
+    return time.perf_counter() - t0, len(units)
+
+
+def oracle_sample(wl, seconds: float):
+    """Oracle decode attention on a bounded sample of the workload: whole (batch row, key
+    head) units of layer 0 at the full context length, cache built by the oracle's own
+    quantiser.  Returns (KV-tokens/s, cores, description)."""
+    import multiprocessing as mp
+
+    import numpy as np
+    import torch
+
+    from mixed_precision_kv_balancer_gb300 import inputs
+    from oracle import balance, pipeline, select
+
+    small = wl.scaled(B=1)
+    x = inputs.make_prefill(small, 0, "cpu")
+    q, k, v = (x[n].numpy() for n in ("q", "k", "v"))
+    T = wl.T
+    keep = select.n_keep(T, wl.budget_pct, wl.window)
+    # important set: the window plus evenly spread older tokens (selection does not change the
+    # attention cost; the sizes n_hi / n_lo are the workload's)
+    older = np.linspace(0, T - wl.window - 1, keep - wl.window).astype(np.int32)
+    kp = np.sort(np.concatenate([older, np.arange(T - wl.window, T, dtype=np.int32)]))
+    mask = np.ones(T, bool)
+    mask[kp] = False
+    ep = np.nonzero(mask)[0].astype(np.int32)
+    bal = balance.channel_balancer(q, k)
+    oc = pipeline.OracleCache(1, wl.Hkv, wl.Hq, wl.D, 64, wl.hi_bits, wl.lo_bits, keep, T - keep, bal)
+    oc.append("hi", k, v, np.broadcast_to(kp, (1, wl.Hkv, keep)).copy(), 0)
+    oc.append("lo", k, v, np.broadcast_to(ep, (1, wl.Hkv, T - keep)).copy(), 0)
+    rep = wl.rep
+    units = []
+    for g in range(wl.Hkv):
+        hi, lo = oc.unit(0, g)
+        units.append((q[0, g * rep:(g + 1) * rep, -1], hi, lo, bal[0, g]))
+    # calibrate: one unit single-threaded, then size the sample to ~`seconds` on all cores
+    t0 = time.perf_counter()
+    _oracle_worker((wl.hi_bits, wl.lo_bits, units[:1]))
+    per_unit = max(time.perf_counter() - t0, 1e-4)
+    cores = os.cpu_count() or 1
+    n_units = max(cores, int(seconds * cores / per_unit))
+    jobs = [[] for _ in range(cores)]
+    for i in range(n_units):
+        jobs[i % cores].append(units[i % len(units)])
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"          # one BLAS thread per spawned worker
+    ctx = mp.get_context("spawn")
+    t0 = time.perf_counter()
+    with ctx.Pool(cores) as pool:
+        res = pool.map(_oracle_worker, [(wl.hi_bits, wl.lo_bits, j) for j in jobs])
+    wall = time.perf_counter() - t0
+    kv_tokens = n_units * T / wl.Hkv          # B*L counts all key heads of a token once
+    return kv_tokens / wall, cores, (f"{n_units} (batch row, key head) units of one layer at "
+                                     f"L={T} (n_hi={keep}, n_lo={T - keep}) on {cores} spawn workers, "
+                                     f"{wall:.1f} s wall incl. pool start")
+
+
+# ------------------------------------------------------------------------------ GPU leg
+def run_gpu(args, wl, rank, world):
+    import torch
+
+    from mixed_precision_kv_balancer_gb300 import _lib, inputs
+    from mixed_precision_kv_balancer_gb300.cache import MikvCache, n_keep
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    _lib.load()
+    total_steps = args.warmup + args.steps
+    keep0 = n_keep(wl.T, wl.budget_pct, wl.window)
+    e2e_steps = 0 if args.no_e2e else args.steps
+    cap_hi = keep0 + total_steps + e2e_steps + 1
+    cap_lo = (wl.T - keep0) + total_steps + e2e_steps + 1
+    layers = []
+    prefill_ms = []
+    for l in range(wl.layers):
+        c = MikvCache(wl.B, wl.Hq, wl.Hkv, wl.D, wl.hi_bits, wl.lo_bits, cap_hi, cap_lo, dev)
+        x = inputs.make_prefill(wl.scaled(seed=wl.seed + 1000 * rank), l, dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        c.prefill(x["q"], x["k"], x["v"], wl.budget_pct, wl.window)
+        e1.record()
+        torch.cuda.synchronize()
+        prefill_ms.append(e0.elapsed_time(e1))
+        del x
+        layers.append(c)
+    torch.cuda.empty_cache()
+    # decode tokens for every step and layer, resident before timing
+    toks = [[inputs.make_decode_token(wl.scaled(seed=wl.seed + 1000 * rank), l, s, dev)
+             for l in range(wl.layers)] for s in range(total_steps + (0 if args.no_e2e else args.steps))]
+    torch.cuda.synchronize()
+
+    def step(s, ev=None):
+        L_before = wl.T + s
+        launches = 0
+        for l, c in enumerate(layers):
+            t = toks[s][l]
+            will_demote = c.n_hi + 1 > n_keep(L_before + 1, wl.budget_pct, wl.window)
+            if ev is not None:
+                _lib.mikv_quantize_append(_lib.MIKV_TIER_HI, c, t["k"][:, :, None, :], t["v"][:, :, None, :],
+                                          c.zero_pos, 1, L_before)
+                ev[0].record()
+                _lib.mikv_decode_attention(t["q"], c, c.out, c.lse, c.hi_logits, ws=c.ws_decode)
+                ev[1].record()
+                ev_pairs.append((ev[0], ev[1], cache_bytes(wl, c.n_hi, c.n_lo)))
+                ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                _lib.mikv_score_update(_lib.MIKV_DECODE, c, hi_logits=c.hi_logits, lse=c.lse)
+                if c.n_hi > n_keep(L_before + 1, wl.budget_pct, wl.window):
+                    _lib.mikv_select(_lib.MIKV_DEMOTE, c, L_before + 1, wl.budget_pct, wl.window,
+                                     evict_pos=c.victim)
+                    _lib.mikv_quantize_append(_lib.MIKV_TIER_DEMOTE, c, None, None, c.victim, 1)
+            else:
+                c.decode_step(t["q"], t["k"], t["v"], L_before, wl.budget_pct, wl.window)
+            launches += 4 + (2 if will_demote else 0)
+        return launches
+
+    ev_pairs = []
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    kv_tokens = 0
+    launches = 0
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for s in range(args.warmup, total_steps):
+        L = wl.T + s + 1
+        kv_tokens += wl.B * L * wl.layers
+        launches += step(s, (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+    end.record()
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end)
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    attn_ms = [a.elapsed_time(b) for a, b, _ in ev_pairs]
+    attn_bytes = [nb for _, _, nb in ev_pairs]
+    res = dict(ms=ms, kv_tokens=kv_tokens * world, launches=launches, clocks=clk,
+               attn_ms_mean=statistics.mean(attn_ms), attn_bytes_mean=statistics.mean(attn_bytes),
+               attn_ms_sum=sum(attn_ms), prefill_ms_per_layer=statistics.mean(prefill_ms))
+
+    # ---- end to end through the public API with host buffers
+    if not args.no_e2e:
+        host_in = [[{n: t.cpu().pin_memory() for n, t in toks[s][l].items()} for l in range(wl.layers)]
+                   for s in range(total_steps, total_steps + args.steps)]
+        host_out = [torch.empty(wl.B, wl.Hq, wl.D, dtype=torch.float32).pin_memory() for _ in range(wl.layers)]
+        h2d = sum(t.numel() * t.element_size() for t in host_in[0][0].values()) * wl.layers
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+        dev_in = [{n: torch.empty_like(t, device=dev) for n, t in host_in[0][l].items()} for l in range(wl.layers)]
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record()
+        e2e_tokens = 0
+        for i, s in enumerate(range(total_steps, total_steps + args.steps)):
+            L_before = wl.T + s
+            for l, c in enumerate(layers):
+                for n in ("q", "k", "v"):
+                    dev_in[l][n].copy_(host_in[i][l][n], non_blocking=True)
+                out, _ = c.decode_step(dev_in[l]["q"], dev_in[l]["k"], dev_in[l]["v"], L_before,
+                                       wl.budget_pct, wl.window)
+                host_out[l].copy_(out, non_blocking=True)
+            e2e_tokens += wl.B * (L_before + 1) * wl.layers
+        e1.record()
+        torch.cuda.synchronize()
+        e2e_ms = max(e0.elapsed_time(e1), (time.perf_counter() - t0) * 1e3)
+        res.update(e2e_ms=e2e_ms, e2e_tokens=e2e_tokens * world, h2d=h2d, d2h=d2h)
+    return res
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            p = json.load(fh)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    wl = workload(args)
+    keep0 = min(wl.T, max(wl.window, wl.budget_pct * wl.T // 100))
+    config = {"workload": wl.name, "layers": wl.layers, "batch": wl.B, "q_heads": wl.Hq,
+              "kv_heads": wl.Hkv, "head_dim": wl.D, "context": wl.T, "budget_pct": wl.budget_pct,
+              "window": wl.window, "hi_bits": wl.hi_bits, "lo_bits": wl.lo_bits,
+              "balancer": True, "policy": wl.policy,
+              "l2": "inputs larger than L2 (packed cache %.0f MB per layer, no flush)"
+                    % (cache_bytes(wl, keep0, wl.T - keep0) / 1e6)}
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        steps_v = []
+        cores = 1
+        desc = ""
+        for _ in range(args.warmup + args.steps):
+            v, cores, desc = oracle_sample(wl, max(2.0, args.cpu_seconds / max(1, args.steps)))
+            steps_v.append(v)
+        v = statistics.median(steps_v[args.warmup:]) if len(steps_v) > args.warmup else steps_v[-1]
+        ms = (wl.B * (wl.T + 1) * wl.layers) / v * 1e3
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": v, "unit": "KV-tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config,
+            "cpu_baseline": {"value": v, "unit": "KV-tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": v, "unit": "KV-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    res = run_gpu(args, wl, rank, world)
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    value = res["kv_tokens"] / (res["ms"] / 1e3)
+    peak, peak_kind = peaks()
+    achieved = res["attn_bytes_mean"] / (res["attn_ms_mean"] / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "KV-tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["ms"] / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16-mma/f32-acc (u%d codes)" % wl.lo_bits,
+        "data": "synthetic", "config": config,
+        "hbm_gbs_decode_attn": achieved, "frac_of_8tbs": achieved / 8000.0,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "kernel": "mikv_decode_attention (decode_partial_kernel + decode_merge_kernel)",
+                     "bytes_per_launch": res["attn_bytes_mean"], "ms_per_launch": res["attn_ms_mean"],
+                     "traffic": None},
+        "decode_attn_ms_per_step": res["attn_ms_sum"] / args.steps,
+        "prefill_ms_per_layer": res["prefill_ms_per_layer"],
+        "gpu_launches": res["launches"],
+        "clocks": res["clocks"],
+    }
+    if "e2e_ms" in res:
+        line["e2e"] = {"value": res["e2e_tokens"] / (res["e2e_ms"] / 1e3), "unit": "KV-tokens/s",
+                       "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]}
+    if not args.no_cpu and world >= 1:
+        v, cores, desc = oracle_sample(wl, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": "KV-tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,229 @@
+/*
+ * mikv.h - C ABI of libmikv.so, the GB300 (sm_103a) hot path of MiKV, the
+ * importance-aware mixed-precision KV cache ("No Token Left Behind: Reliable KV
+ * Cache Compression via Importance-Aware Mixed Precision Quantization", arXiv
+ * 2402.18096), with the optional CriticalKV two-stage selection (arXiv
+ * 2502.03805).
+ *
+ * Sources cited below:
+ *   [notes]      "No Token Left Behind" reading notes (velog.io), sections
+ *                "Observation", "Key contributions 1)-3)", "3.4 Accelerating the
+ *                Mixed-Precision KV Cache".
+ *   [paperlayer] paperlayer.ai summary of arXiv 2402.18096v1, sections 3.1-3.4,
+ *                4.1, 5, Appendix C.
+ *   [criticalkv] gist.science summary of arXiv 2502.03805 (CriticalKV),
+ *                "Theoretical framework" and "Algorithm: perturbation-constrained
+ *                selection".
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every array pointer is a DEVICE pointer owned by the caller.  The library
+ *   never allocates device memory; scratch comes from a caller workspace whose
+ *   size a *_workspace_bytes query returns.
+ * - fp16 arrays are passed as uint16_t* holding IEEE binary16 bit patterns.
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   Calls are asynchronous on that stream; none synchronises the host.
+ * - All shapes are row-major, innermost dimension last, contiguous.
+ * - Return value: MIKV_OK (0) or a negative status.  On any error nothing is
+ *   launched and nothing is written; mikv_last_error() returns a message
+ *   (thread-local, valid until the next call on the same thread).
+ * - Head dimension D must be 128 (the kernels are specialised for it); the
+ *   quantisation group is gs = D/2 = 64 ([notes] "2) Outlier-aware": group size
+ *   = half the attention head dimension, against RoPE artefacts).
+ * - GQA: Hq query heads, Hkv key/value heads, rep = Hq/Hkv in 1..8; query head
+ *   h reads key head h / rep.
+ */
+#ifndef MIKV_H_
+#define MIKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define MIKV_OK 0
+#define MIKV_EINVAL (-1)       /* null pointer where one is required, bad enum, bad scalar */
+#define MIKV_ESHAPE (-2)       /* dimension, capacity or count out of range */
+#define MIKV_EALIGN (-3)       /* a buffer is not 16-byte aligned */
+#define MIKV_EUNSUPPORTED (-4) /* bit width or head dimension the kernels do not implement */
+#define MIKV_ECUDA (-5)        /* a CUDA launch failed (message in mikv_last_error) */
+
+/* mikv_score_update modes */
+#define MIKV_PREFILL 0
+#define MIKV_DECODE 1
+
+/* mikv_select policies */
+#define MIKV_H2O 0
+#define MIKV_CRITICALKV 1
+#define MIKV_DEMOTE 2
+
+/* mikv_quantize_append tiers */
+#define MIKV_TIER_HI 0
+#define MIKV_TIER_LO 1
+#define MIKV_TIER_DEMOTE 2
+
+/*
+ * One layer's two-tier cache ([notes] "Key contributions 1)" and "3)": tokens
+ * an eviction policy would drop are kept in low precision next to the important
+ * tokens kept in FP16 or INT8; [notes] 3.4: after positional embedding
+ * attention is permutation invariant, so each precision lives in its own
+ * contiguous tier).  Counts are uniform over (batch, key head).
+ *
+ * Slot layouts (all per [B][Hkv][capacity]):
+ *   hi_bits == 16: k_hi, v_hi fp16 [B][Hkv][cap_hi][D]; hi meta unused (NULL).
+ *   hi_bits ==  8: k_hi, v_hi uint8 codes [B][Hkv][cap_hi][D];
+ *                  k_hi_meta, v_hi_meta [B][Hkv][cap_hi][D/64][2] fp16 (scale, zero).
+ *   lo tier:       k_lo, v_lo uint8 [B][Hkv][cap_lo][D*lo_bits/8] packed codes:
+ *                  channel c sits in bits [(c*lo_bits) % 8, +lo_bits) of byte
+ *                  (c*lo_bits)/8, least significant bits first;
+ *                  k_lo_meta, v_lo_meta [B][Hkv][cap_lo][D/64][2] fp16 (scale, zero).
+ *   pos_hi, pos_lo int32: original sequence position of each slot.
+ *   scores         fp32 [B][Hkv][cap_hi]: accumulated H2O importance of each hi slot.
+ *   balancer       fp32 [B][Hkv][D] or NULL (identity).
+ * Quantised keys (INT8 hi tier and the lo tier) hold I(k*b); the FP16 tier holds
+ * the original k.  Values are never balanced.
+ * Code and meta buffers must be 16-byte aligned.
+ */
+typedef struct mikv_cache {
+  int32_t B, Hkv, Hq, D;
+  int32_t hi_bits, lo_bits; /* hi in {16, 8}; lo in {2, 4, 8} */
+  int32_t cap_hi, cap_lo;
+  int32_t n_hi, n_lo; /* current counts; updated on the host by the calls that change them */
+  void* k_hi;
+  void* v_hi;
+  void* k_hi_meta;
+  void* v_hi_meta;
+  void* k_lo;
+  void* v_lo;
+  void* k_lo_meta;
+  void* v_lo_meta;
+  int32_t* pos_hi;
+  int32_t* pos_lo;
+  const float* balancer;
+  float* scores;
+} mikv_cache;
+
+/*
+ * Channel balancer ([notes] "2) Outlier-aware", balancer equation; [paperlayer]
+ * 3.2): b[b][g][c] = sqrt(Mq / Mk), Mq = max over the group's query heads and
+ * the T prompt tokens of |q[b][h][t][c]|, Mk = max over t of |k[b][g][t][c]|;
+ * b = 1 where Mq or Mk is 0.  The ratio and the square root are fp32,
+ * round-to-nearest-even.  q, k are the post-RoPE prompt tensors.
+ *   q    fp16 [B][Hq][T][D]      k fp16 [B][Hkv][T][D]
+ *   b_out fp32 [B][Hkv][D]       (written)
+ *   ws   >= mikv_balance_workspace_bytes(B, Hkv, D) bytes, 16-byte aligned
+ * Errors: EINVAL (null), ESHAPE (T < 1, Hq % Hkv, rep > 8), EUNSUPPORTED (D != 128),
+ * EALIGN, ECUDA.
+ */
+int mikv_balance_prefill(const uint16_t* q, const uint16_t* k, int B, int Hq, int Hkv, int T,
+                         int D, float* b_out, void* ws, size_t ws_bytes, void* stream);
+size_t mikv_balance_workspace_bytes(int B, int Hkv, int D);
+
+/*
+ * H2O importance ([notes] "Observation 1-4" and "Key contributions 1)": H2O,
+ * accumulated attention; read as the plain H2O definition).
+ * MIKV_PREFILL: column sums of the causal softmax over the T prompt rows,
+ *   S^h[b][h][i] = sum_{t >= i} exp(q_t.k_i/sqrt(D) - lse_t), and the group sum
+ *   S[b][g][i] = sum over the group's query heads, h ascending, fp32.
+ *   Uses q fp16 [B][Hq][T][D], k fp16 [B][Hkv][T][D] and the dims of c
+ *   (c->B, Hkv, Hq, D; no cache buffer is touched).
+ *   scores_full fp32 [B][Hkv][T] (written); scores_head fp32 [B][Hq][T] (written if not NULL).
+ *   ws >= mikv_score_workspace_bytes(B, Hq, T) bytes.
+ * MIKV_DECODE: c->scores[b][g][j] += sum_h exp(hi_logits[b][h][j] - lse[b][h]) for
+ *   every hi slot j < c->n_hi; hi_logits fp32 [B][Hq][cap_hi] and lse fp32 [B][Hq]
+ *   as written by mikv_decode_attention.  q, k, T, scores_*, ws unused.
+ * Errors: EINVAL, ESHAPE, EUNSUPPORTED, ECUDA.
+ */
+int mikv_score_update(int mode, const uint16_t* q, const uint16_t* k, int T,
+                      const float* hi_logits, const float* lse, mikv_cache* c,
+                      float* scores_full, float* scores_head, void* ws, size_t ws_bytes,
+                      void* stream);
+size_t mikv_score_workspace_bytes(int B, int Hq, int T);
+
+/*
+ * Selection.  Budget n_keep(L) = min(L, max(window, floor(budget_pct*L/100))):
+ * the `window` most recent positions are always kept and count inside the
+ * budget ([paperlayer] 5: local tokens and heavy hitters).  Ranking key
+ * (score descending, position ascending); ties keep the lower position.
+ * MIKV_H2O ([notes] "Key contributions 1)"): keep the window plus the top
+ *   n_keep - window older tokens by scores [B][Hkv][L].
+ * MIKV_CRITICALKV ([criticalkv] "Algorithm"): bud = n_keep - window,
+ *   b' = floor(alpha*bud), b'' = bud - b'; stage 1 takes the top b' older tokens
+ *   by scores; stage 2 takes the top b'' of the remaining older tokens by
+ *   C_i = sum_h fl(S^h_i * N[b][h][i]) (fp32, h ascending over the group), with
+ *   S^h = scores_head [B][Hq][L] and N the projected-value L1 norms
+ *   ([criticalkv] "Theoretical framework": V W_O):
+ *     N[b][h][i] = || v[b][h/rep][i][:] . w_o[h*D:(h+1)*D][:] ||_1.
+ *   If w_o != NULL, N is computed from v fp16 [B][Hkv][L][D] and w_o fp16
+ *   [Hq*D][hidden] (hidden % 128 == 0) and written to vwo_norm fp32 [B][Hq][L];
+ *   if w_o == NULL, vwo_norm is read as given.
+ * Outputs (H2O, CRITICALKV): keep_pos int32 [B][Hkv][n_keep] ascending,
+ *   evict_pos int32 [B][Hkv][L - n_keep] ascending, keep_scores fp32
+ *   [B][Hkv][n_keep] = scores at keep_pos (written if not NULL).
+ * MIKV_DEMOTE: reads c->scores, c->pos_hi and c->n_hi; among hi slots with
+ *   pos < L - window picks the minimum of (score ascending, position descending)
+ *   and writes its slot index to evict_pos [B][Hkv]; L is the current length.
+ *   Requires c->n_hi > window.
+ * ws >= mikv_select_workspace_bytes(policy, B, Hkv, Hq, L, hidden).
+ * Errors: EINVAL (null, policy, alpha outside [0,1]), ESHAPE (L, budget, window,
+ * hidden), EUNSUPPORTED, ECUDA.
+ */
+int mikv_select(int policy, const mikv_cache* c, int L, int budget_pct, int window, float alpha,
+                const float* scores, const float* scores_head, const uint16_t* v,
+                const uint16_t* w_o, int hidden, float* vwo_norm, int32_t* keep_pos,
+                int32_t* evict_pos, float* keep_scores, void* ws, size_t ws_bytes, void* stream);
+size_t mikv_select_workspace_bytes(int policy, int B, int Hkv, int Hq, int L, int hidden);
+
+/*
+ * Quantise-and-append ([notes] "Key contributions 1)": per-token asymmetric
+ * quantisation (LLM-QAT) of the retained tokens; "2)": keys as I(k*b);
+ * "3)": INT8 important tier).  Per token, key head and 64-channel group:
+ *   x = fl(k*b) for keys of a quantised tier, x = v for values;
+ *   s = fp16(fl(max-min)/qmax), z = fp16(min),
+ *   code = clamp(rint_even(fl(fl(x - z)/s)), 0, qmax), code 0 where s == 0.
+ * MIKV_TIER_HI: slots n_hi..n_hi+n_tokens-1 take source tokens src_pos
+ *   [B][Hkv][n_tokens] (indices into k, v fp16 [B][Hkv][src_len][D]); FP16
+ *   tier: copy; INT8 tier: quantise.  pos_hi = src_pos + pos_base;
+ *   scores = src_scores [B][Hkv][n_tokens] if not NULL, else 0.  n_hi += n_tokens.
+ * MIKV_TIER_LO: same into the lo tier (lo_bits); pos_lo = src_pos + pos_base.
+ *   n_lo += n_tokens.
+ * MIKV_TIER_DEMOTE: n_tokens must be 1; src_pos [B][Hkv] are hi slots.  Each is
+ *   re-quantised into lo slot n_lo from what the hi tier holds (FP16: fl(k*b)
+ *   and v; INT8: fl(fl(s*code)+z), already balanced); then the last hi slot
+ *   (k, v, meta, pos, score) moves into the freed slot.  n_hi -= 1, n_lo += 1.
+ *   k, v, src_len, pos_base, src_scores unused.
+ * Counts in *c are updated on the host after a successful launch.
+ * Errors: EINVAL, ESHAPE (capacity overflow, src_len), EALIGN, EUNSUPPORTED, ECUDA.
+ */
+int mikv_quantize_append(int tier, const uint16_t* k, const uint16_t* v, int src_len,
+                         const int32_t* src_pos, int n_tokens, int pos_base,
+                         const float* src_scores, mikv_cache* c, void* stream);
+
+/*
+ * Decode attention over the two-tier cache ([notes] 3.4 and [paperlayer] 3.4:
+ * tiers grouped by precision, K and V low precision, Q and the attention map
+ * floating point; [notes] "2)": quantised keys are attended with q/b).
+ * For query head h of key head g:
+ *   FP16 hi tier:  logit = q_h . k / sqrt(D)        (original q and k)
+ *   quantised tiers: logit = (q_h / b_g) . k~ / sqrt(D)   (k~ dequantised k*b)
+ *   p = softmax over both tiers; out_h = sum p v~; lse_h = log sum exp(logit).
+ *   q      fp16 [B][Hq][D]
+ *   out    fp32 [B][Hq][D]; lse fp32 [B][Hq] (natural log)
+ *   hi_logits fp32 [B][Hq][cap_hi] (slots < n_hi written) or NULL
+ *   ws >= mikv_decode_workspace_bytes(c) bytes (split-K partial results).
+ * Requires n_hi + n_lo >= 1.  Errors: EINVAL, ESHAPE, EALIGN, EUNSUPPORTED, ECUDA.
+ */
+int mikv_decode_attention(const uint16_t* q, const mikv_cache* c, float* out, float* lse,
+                          float* hi_logits, void* ws, size_t ws_bytes, void* stream);
+size_t mikv_decode_workspace_bytes(const mikv_cache* c);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* mikv_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MIKV_H_ */

@@ -1,0 +1,163 @@
+"""ctypes binding of libmikv.so: the C ABI calls under the same names, taking torch tensors.
+
+Argument marshalling only: every computation runs in the library's CUDA kernels.
+There is no fallback; if the library is missing or a call fails, this raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmikv.so")
+
+MIKV_PREFILL, MIKV_DECODE = 0, 1
+MIKV_H2O, MIKV_CRITICALKV, MIKV_DEMOTE = 0, 1, 2
+MIKV_TIER_HI, MIKV_TIER_LO, MIKV_TIER_DEMOTE = 0, 1, 2
+
+EXPORTS = (
+    "mikv_balance_prefill", "mikv_balance_workspace_bytes",
+    "mikv_score_update", "mikv_score_workspace_bytes",
+    "mikv_select", "mikv_select_workspace_bytes",
+    "mikv_quantize_append",
+    "mikv_decode_attention", "mikv_decode_workspace_bytes",
+    "mikv_last_error",
+)
+
+
+class MikvError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} failed with status {code}: {msg}")
+        self.code = code
+
+
+class mikv_cache(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("Hq", ctypes.c_int32), ("D", ctypes.c_int32),
+        ("hi_bits", ctypes.c_int32), ("lo_bits", ctypes.c_int32),
+        ("cap_hi", ctypes.c_int32), ("cap_lo", ctypes.c_int32),
+        ("n_hi", ctypes.c_int32), ("n_lo", ctypes.c_int32),
+        ("k_hi", ctypes.c_void_p), ("v_hi", ctypes.c_void_p),
+        ("k_hi_meta", ctypes.c_void_p), ("v_hi_meta", ctypes.c_void_p),
+        ("k_lo", ctypes.c_void_p), ("v_lo", ctypes.c_void_p),
+        ("k_lo_meta", ctypes.c_void_p), ("v_lo_meta", ctypes.c_void_p),
+        ("pos_hi", ctypes.c_void_p), ("pos_lo", ctypes.c_void_p),
+        ("balancer", ctypes.c_void_p), ("scores", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libmikv.so (built in-tree by build()); raises if it is absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is not built: run __graft_entry__.build() or "
+                           "python -m mixed_precision_kv_balancer_gb300.build")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, S, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+    CP = ctypes.POINTER(mikv_cache)
+    sig = {
+        "mikv_balance_prefill": (I, [P, P, I, I, I, I, I, P, P, S, P]),
+        "mikv_balance_workspace_bytes": (S, [I, I, I]),
+        "mikv_score_update": (I, [I, P, P, I, P, P, CP, P, P, P, S, P]),
+        "mikv_score_workspace_bytes": (S, [I, I, I]),
+        "mikv_select": (I, [I, CP, I, I, I, F, P, P, P, P, I, P, P, P, P, P, S, P]),
+        "mikv_select_workspace_bytes": (S, [I, I, I, I, I, I]),
+        "mikv_quantize_append": (I, [I, P, P, I, P, I, I, P, CP, P]),
+        "mikv_decode_attention": (I, [P, CP, P, P, P, P, S, P]),
+        "mikv_decode_workspace_bytes": (S, [CP]),
+        "mikv_last_error": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype, fn.argtypes = res, args
+    _lib = lib
+    return lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    assert t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors"
+    return t.data_ptr()
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check(name: str, rc: int):
+    if rc != 0:
+        raise MikvError(name, rc, load().mikv_last_error().decode())
+
+
+def _ws(nbytes: int, device, ws):
+    if ws is not None:
+        return ws, ws.numel() * ws.element_size()
+    if nbytes == 0:
+        return None, 0
+    t = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return t, nbytes
+
+
+# --- the C ABI calls -----------------------------------------------------------------
+
+def mikv_balance_prefill(q, k, b_out, ws=None, stream=None):
+    B, Hq, T, D = q.shape
+    Hkv = k.shape[1]
+    lib = load()
+    w, nb = _ws(lib.mikv_balance_workspace_bytes(B, Hkv, D), q.device, ws)
+    _check("mikv_balance_prefill", lib.mikv_balance_prefill(
+        _ptr(q), _ptr(k), B, Hq, Hkv, T, D, _ptr(b_out), _ptr(w), nb, _stream(stream)))
+
+
+def mikv_score_update(mode, cache, q=None, k=None, T=0, hi_logits=None, lse=None,
+                      scores_full=None, scores_head=None, ws=None, stream=None):
+    lib = load()
+    c = cache.struct if hasattr(cache, "struct") else cache
+    w, nb = None, 0
+    if mode == MIKV_PREFILL:
+        dev = q.device
+        w, nb = _ws(lib.mikv_score_workspace_bytes(c.B, c.Hq, T), dev, ws)
+    _check("mikv_score_update", lib.mikv_score_update(
+        mode, _ptr(q), _ptr(k), T, _ptr(hi_logits), _ptr(lse), ctypes.byref(c),
+        _ptr(scores_full), _ptr(scores_head), _ptr(w), nb, _stream(stream)))
+
+
+def mikv_select(policy, cache, L, budget_pct, window, alpha=0.5, scores=None, scores_head=None,
+                v=None, w_o=None, hidden=0, vwo_norm=None, keep_pos=None, evict_pos=None,
+                keep_scores=None, ws=None, stream=None):
+    lib = load()
+    c = cache.struct if hasattr(cache, "struct") else cache
+    dev = (scores if scores is not None else evict_pos).device
+    w, nb = _ws(lib.mikv_select_workspace_bytes(policy, c.B, c.Hkv, c.Hq, L, hidden), dev, ws)
+    _check("mikv_select", lib.mikv_select(
+        policy, ctypes.byref(c), L, budget_pct, window, float(alpha), _ptr(scores),
+        _ptr(scores_head), _ptr(v), _ptr(w_o), hidden, _ptr(vwo_norm), _ptr(keep_pos),
+        _ptr(evict_pos), _ptr(keep_scores), _ptr(w), nb, _stream(stream)))
+
+
+def mikv_quantize_append(tier, cache, k, v, src_pos, n_tokens, pos_base=0, src_scores=None,
+                         stream=None):
+    lib = load()
+    c = cache.struct if hasattr(cache, "struct") else cache
+    src_len = 0 if k is None else k.shape[2]
+    _check("mikv_quantize_append", lib.mikv_quantize_append(
+        tier, _ptr(k), _ptr(v), src_len, _ptr(src_pos), n_tokens, pos_base, _ptr(src_scores),
+        ctypes.byref(c), _stream(stream)))
+
+
+def mikv_decode_attention(q, cache, out, lse, hi_logits=None, ws=None, stream=None):
+    lib = load()
+    c = cache.struct if hasattr(cache, "struct") else cache
+    w, nb = _ws(lib.mikv_decode_workspace_bytes(ctypes.byref(c)), q.device, ws)
+    _check("mikv_decode_attention", lib.mikv_decode_attention(
+        _ptr(q), ctypes.byref(c), _ptr(out), _ptr(lse), _ptr(hi_logits), _ptr(w), nb,
+        _stream(stream)))

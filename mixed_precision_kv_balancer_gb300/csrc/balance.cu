@@ -1,0 +1,138 @@
+// K1: channel balancer b = sqrt(max|q| / max|k|) over the prompt.
+//
+// Source: "No Token Left Behind" reading notes (velog), "Key contributions, 2)
+// Outlier-aware handling", balancer equation; paperlayer summary of arXiv
+// 2402.18096v1, section 3.2 (balancer computed once at prefill).
+//
+// One HBM pass over the prompt's Q and K.  Grid (B*Hkv, nsplit): each CTA scans a
+// slice of the (rep*T) query rows and T key rows of one (batch, key head) with
+// 16-byte loads (16 threads cover one 256-byte row), keeps per-channel |x| maxima
+// in half precision (max of fp16 values is exact), reduces them in shared memory
+// and folds them into the workspace with an integer atomicMax on the float bits
+// (non-negative floats order like their bit patterns, so the result does not
+// depend on the order).  A second kernel forms b in fp32, RN division then RN
+// square root.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace mikv {
+namespace {
+
+constexpr int kBalThreads = 256;
+constexpr int kRowsPerIter = kBalThreads / 16;  // 16 rows of 256 B per CTA iteration
+
+__device__ __forceinline__ void absmax8(uint4 v, __half2 (&m)[4]) {
+  const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m[i] = __hmax2(m[i], __habs2(h[i]));
+}
+
+__device__ void scan_rows(const uint4* base, long rows, long r0, long r1, float* ws_out,
+                          float (*red)[kD]) {
+  const int tid = threadIdx.x;
+  const int col = tid & 15;          // 16-byte chunk of the row: channels 8*col..8*col+7
+  const int rsub = tid >> 4;         // row within an iteration
+  __half2 m[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m[i] = __float2half2_rn(0.f);
+  long r = r0 + rsub;
+  // 4 independent loads in flight per thread
+  for (; r + 3 * kRowsPerIter < r1; r += 4 * kRowsPerIter) {
+    uint4 v0 = __ldg(base + (r)*16 + col);
+    uint4 v1 = __ldg(base + (r + kRowsPerIter) * 16 + col);
+    uint4 v2 = __ldg(base + (r + 2 * kRowsPerIter) * 16 + col);
+    uint4 v3 = __ldg(base + (r + 3 * kRowsPerIter) * 16 + col);
+    absmax8(v0, m);
+    absmax8(v1, m);
+    absmax8(v2, m);
+    absmax8(v3, m);
+  }
+  for (; r < r1; r += kRowsPerIter) absmax8(__ldg(base + r * 16 + col), m);
+  (void)rows;
+  // CTA reduction over the 16 row lanes of each channel
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 f = __half22float2(m[i]);
+    red[rsub][col * 8 + 2 * i] = f.x;
+    red[rsub][col * 8 + 2 * i + 1] = f.y;
+  }
+  __syncthreads();
+  if (tid < kD) {
+    float mx = 0.f;
+#pragma unroll
+    for (int j = 0; j < kRowsPerIter; ++j) mx = fmaxf(mx, red[j][tid]);
+    atomic_max_nonneg(ws_out + tid, mx);
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kBalThreads) balance_max_kernel(
+    const uint4* __restrict__ q, const uint4* __restrict__ k, int Hq, int Hkv, int T, int nsplit,
+    float* __restrict__ ws_q, float* __restrict__ ws_k) {
+  __shared__ float red[kRowsPerIter][kD];
+  const int unit = blockIdx.x;  // b*Hkv + g
+  const int split = blockIdx.y;
+  const int b = unit / Hkv, g = unit % Hkv;
+  const int rep = Hq / Hkv;
+  // query rows of the group's heads are contiguous: [b][g*rep .. g*rep+rep)[T]
+  const long qrows = static_cast<long>(rep) * T;
+  const uint4* qb = q + (static_cast<long>(b) * Hq + static_cast<long>(g) * rep) * T * 16;
+  const long qs0 = qrows * split / nsplit, qs1 = qrows * (split + 1) / nsplit;
+  scan_rows(qb, qrows, qs0, qs1, ws_q + static_cast<long>(unit) * kD, red);
+  const uint4* kb = k + static_cast<long>(unit) * T * 16;
+  const long ks0 = static_cast<long>(T) * split / nsplit;
+  const long ks1 = static_cast<long>(T) * (split + 1) / nsplit;
+  scan_rows(kb, T, ks0, ks1, ws_k + static_cast<long>(unit) * kD, red);
+}
+
+__global__ void balance_finalize_kernel(const float* __restrict__ ws_q,
+                                        const float* __restrict__ ws_k, float* __restrict__ b,
+                                        int n) {
+  int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float mq = ws_q[i], mk = ws_k[i];
+  b[i] = (mq == 0.f || mk == 0.f) ? 1.f : __fsqrt_rn(__fdiv_rn(mq, mk));
+}
+
+}  // namespace
+}  // namespace mikv
+
+using namespace mikv;
+
+extern "C" size_t mikv_balance_workspace_bytes(int B, int Hkv, int D) {
+  if (B <= 0 || Hkv <= 0 || D <= 0) return 0;
+  return 2 * align_up(static_cast<size_t>(B) * Hkv * D * sizeof(float), 256);
+}
+
+extern "C" int mikv_balance_prefill(const uint16_t* q, const uint16_t* k, int B, int Hq, int Hkv,
+                                    int T, int D, float* b_out, void* ws, size_t ws_bytes,
+                                    void* stream) {
+  clear_error();
+  if (!q || !k || !b_out || !ws) return fail(MIKV_EINVAL, "balance_prefill: null pointer");
+  if (D != kD) return fail(MIKV_EUNSUPPORTED, "balance_prefill: D=%d (only %d)", D, kD);
+  if (B < 1 || Hkv < 1 || Hq < Hkv || Hq % Hkv || Hq / Hkv > 8 || T < 1)
+    return fail(MIKV_ESHAPE, "balance_prefill: bad shape B=%d Hq=%d Hkv=%d T=%d", B, Hq, Hkv, T);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(ws))
+    return fail(MIKV_EALIGN, "balance_prefill: q, k and ws must be 16-byte aligned");
+  const size_t need = mikv_balance_workspace_bytes(B, Hkv, D);
+  if (ws_bytes < need) return fail(MIKV_ESHAPE, "balance_prefill: workspace %zu < %zu", ws_bytes, need);
+  cudaStream_t s = as_stream(stream);
+  const size_t half = need / 2;
+  float* ws_q = static_cast<float*>(ws);
+  float* ws_k = reinterpret_cast<float*>(static_cast<char*>(ws) + half);
+  if (cudaMemsetAsync(ws, 0, need, s) != cudaSuccess) return check_launch("balance_prefill memset");
+  const int units = B * Hkv;
+  // enough CTAs for ~4 per SM, each scanning at least 64 query rows
+  const long qrows = static_cast<long>(Hq / Hkv) * T;
+  int nsplit = (4 * kNumSMs + units - 1) / units;
+  nsplit = static_cast<int>(std::min<long>(nsplit, std::max<long>(1, qrows / 64)));
+  dim3 grid(units, nsplit);
+  balance_max_kernel<<<grid, kBalThreads, 0, s>>>(reinterpret_cast<const uint4*>(q),
+                                                  reinterpret_cast<const uint4*>(k), Hq, Hkv, T,
+                                                  nsplit, ws_q, ws_k);
+  if (int e = check_launch("balance_max_kernel")) return e;
+  const int n = units * D;
+  balance_finalize_kernel<<<(n + 255) / 256, 256, 0, s>>>(ws_q, ws_k, b_out, n);
+  return check_launch("balance_finalize_kernel");
+}

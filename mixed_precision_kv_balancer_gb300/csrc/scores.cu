@@ -1,0 +1,303 @@
+// K3 + K4: H2O accumulated-attention importance.
+//
+// Sources: "No Token Left Behind" reading notes (velog), "Observation 1-4" and
+// "Key contributions 1)" (H2O, heavy hitters by accumulated attention); the
+// pages name H2O without its formula, so the plain definition is used:
+//   prefill  S^h_i = sum_{t >= i} softmax_t(q_t . k / sqrt(D))_i  (causal rows)
+//            S_i   = sum over the key head's query heads, h ascending, fp32
+//   decode   S_j  += sum_h exp(logit_{h,j} - lse_h) for important-tier slots.
+//
+// K3 is a dense causal QK^T: two tensor-core passes (mma.sync m16n8k16, fp16 in,
+// fp32 accumulate) over 64x64 tiles staged by cp.async:
+//   pass 1  per (b, h, 64 query rows): online row max/sum -> lse_t (base 2),
+//   pass 2  per (b, key head, 64 keys): for every query head of the group and
+//           every 64-query tile at or below the diagonal, exp2(s - lse_t) summed
+//           over the queries -> S^h_i, then S_i in head order.
+// Work is triangular, so CTAs are numbered heaviest first.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace mikv {
+int validate_cache_public(const mikv_cache* c, const char* who);
+
+namespace {
+
+constexpr int kTile = 64;
+constexpr int kThr = 128;   // 4 warps x 16 rows
+constexpr int kScoreSmem = 3 * kTile * 256 + 2 * kTile * 4;
+// log2(e)/sqrt(128): logits in base 2, one rounding shared by both passes
+constexpr float kC = 0.12751743082459868f;
+
+// Stage a [64][128] fp16 tile (rows r0.., rows >= nrows zero-filled) into 128B-swizzled smem.
+__device__ __forceinline__ void load_tile(uint32_t s, const __half* g, long r0, int nrows) {
+  for (int i = threadIdx.x; i < kTile * 16; i += kThr) {
+    const int r = i >> 4, cc = i & 15;
+    const bool ok = r < nrows;
+    const __half* src = ok ? g + (r0 + r) * kD + cc * 8 : g;
+    cp_async16(s + r * 256 + ((cc ^ (r & 7)) << 4), src, ok);
+  }
+}
+
+// A fragments (16 rows x 128 ch) of a swizzled [64][128] tile for warp rows w*16..
+__device__ __forceinline__ void load_a_frags(uint32_t s, int w, int lane, uint32_t (&a)[8][4]) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int row = w * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int chunk = 2 * k + (lane >> 4);
+    ldsm_x4(s + row * 256 + ((chunk ^ (row & 7)) << 4), a[k][0], a[k][1], a[k][2], a[k][3]);
+  }
+}
+
+// acc[n][4] = A(16 x 128) . Tile^T for the 64 rows of the tile as 8 n-tiles of 8.
+__device__ __forceinline__ void qk_tile(uint32_t s, const uint32_t (&a)[8][4], int lane,
+                                        float (&acc)[8][4]) {
+#pragma unroll
+  for (int n = 0; n < 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+#pragma unroll
+    for (int np = 0; np < 4; ++np) {  // pairs of n-tiles: rows np*16 .. +16 of the tile
+      const int row = np * 16 + (lane & 7) + ((lane >> 4) << 3);
+      const int chunk = 2 * k + ((lane >> 3) & 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(s + row * 256 + ((chunk ^ (row & 7)) << 4), b0, b1, b2, b3);
+      mma16816(acc[2 * np], a[k][0], a[k][1], a[k][2], a[k][3], b0, b1);
+      mma16816(acc[2 * np + 1], a[k][0], a[k][1], a[k][2], a[k][3], b2, b3);
+    }
+  }
+}
+
+// Pass 1: lse2[b][h][t] = log2 sum_{i <= t} exp2(s2_ti).
+__global__ void __launch_bounds__(kThr) row_lse_kernel(const __half* __restrict__ q,
+                                                       const __half* __restrict__ k, int Hq,
+                                                       int Hkv, int T, float* __restrict__ lse2) {
+  extern __shared__ __align__(128) uint8_t sm[];  // Q tile + 2 K tiles (kScoreSmem)
+  const int nblk = (T + kTile - 1) / kTile;
+  const int rb = nblk - 1 - blockIdx.x;  // heaviest (last) row block first
+  const int bh = blockIdx.y, b = bh / Hq, h = bh % Hq;
+  const int g = h / (Hq / Hkv);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const __half* qb = q + static_cast<long>(bh) * T * kD;
+  const __half* kb = k + (static_cast<long>(b) * Hkv + g) * T * kD;
+  const uint32_t sq = smem_u32(sm), sk0 = sq + kTile * 256;
+  const int t0 = rb * kTile;
+  load_tile(sq, qb, t0, min(kTile, T - t0));
+  load_tile(sk0, kb, 0, min(kTile, T));
+  cp_async_commit();
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f}, lc[2] = {0.f, 0.f};  // lc: compensation
+  uint32_t a[8][4];
+  const int row0 = t0 + warp * 16 + gid;  // rows row0, row0 + 8
+  for (int kt = 0; kt <= rb; ++kt) {
+    if (kt + 1 <= rb) {
+      load_tile(sk0 + ((kt + 1) & 1) * kTile * 256, kb, (kt + 1) * kTile,
+                min(kTile, T - (kt + 1) * kTile));
+    }
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncthreads();
+    if (kt == 0) load_a_frags(sq, warp, lane, a);
+    float acc[8][4];
+    qk_tile(sk0 + (kt & 1) * kTile * 256, a, lane, acc);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int t = row0 + 8 * hh;
+      float mx = -INFINITY;
+      float x[8][2];
+#pragma unroll
+      for (int n = 0; n < 8; ++n)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int i = kt * kTile + n * 8 + 2 * tig + e;
+          const float v = (i <= t && i < T) ? acc[n][2 * hh + e] * kC : -INFINITY;
+          x[n][e] = v;
+          mx = fmaxf(mx, v);
+        }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float mn = fmaxf(m[hh], mx);
+      float sum = 0.f;
+      if (mn != -INFINITY) {
+        // exponent acc*kC - m with a single rounding (fused), so the dominant terms
+        // (exponent near 0) carry no rounding error of the ~40-sized logit itself
+#pragma unroll
+        for (int n = 0; n < 8; ++n)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            if (x[n][e] != -INFINITY) sum += exp2f(fmaf(acc[n][2 * hh + e], kC, -mn));
+        const float alpha = exp2f(m[hh] - mn);
+        // compensated (Kahan) running sum, rescaled with the running max
+        l[hh] = __fmul_rn(l[hh], alpha);
+        lc[hh] = __fmul_rn(lc[hh], alpha);
+        const float y = sum - lc[hh];
+        const float tt = l[hh] + y;
+        lc[hh] = (tt - l[hh]) - y;
+        l[hh] = tt;
+        m[hh] = mn;
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    float s = l[hh] - lc[hh];
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    const int t = row0 + 8 * hh;
+    if (tig == 0 && t < T) lse2[static_cast<long>(bh) * T + t] = m[hh] + log2f(s);
+  }
+}
+
+// Pass 2: S^h_i for 64 keys of one (b, key head), all query heads of the group.
+__global__ void __launch_bounds__(kThr) col_sum_kernel(const __half* __restrict__ q,
+                                                       const __half* __restrict__ k,
+                                                       const float* __restrict__ lse2, int Hq,
+                                                       int Hkv, int T, float* __restrict__ s_full,
+                                                       float* __restrict__ s_head) {
+  extern __shared__ __align__(128) uint8_t sm[];  // K tile + 2 Q tiles + 2 lse rows
+  float (*sl)[kTile] = reinterpret_cast<float (*)[kTile]>(sm + 3 * kTile * 256);
+  const int nblk = (T + kTile - 1) / kTile;
+  const int kb_i = blockIdx.x;  // key block 0 (heaviest) first
+  const int unit = blockIdx.y, b = unit / Hkv, g = unit % Hkv;
+  const int rep = Hq / Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const __half* kbase = k + static_cast<long>(unit) * T * kD;
+  const uint32_t sk = smem_u32(sm), sq0 = sk + kTile * 256;
+  const int i0 = kb_i * kTile;
+  load_tile(sk, kbase, i0, min(kTile, T - i0));
+  cp_async_commit();
+  uint32_t a[8][4];
+  const int key0 = i0 + warp * 16 + gid;  // keys key0, key0 + 8
+  float tot[2] = {0.f, 0.f};
+  for (int hr = 0; hr < rep; ++hr) {
+    const int h = g * rep + hr;
+    const long bh = static_cast<long>(b) * Hq + h;
+    const __half* qb = q + bh * T * kD;
+    const float* lb = lse2 + bh * T;
+    float col[2] = {0.f, 0.f}, colc[2] = {0.f, 0.f};  // colc: Kahan compensation
+    // first query tile is the diagonal one
+    load_tile(sq0, qb, i0, min(kTile, T - i0));
+    for (int j = threadIdx.x; j < kTile; j += kThr) sl[0][j] = (i0 + j < T) ? lb[i0 + j] : 0.f;
+    cp_async_commit();
+    for (int qt = kb_i; qt < nblk; ++qt) {
+      const int buf = (qt - kb_i) & 1;
+      if (qt + 1 < nblk) {
+        const int nt0 = (qt + 1) * kTile;
+        load_tile(sq0 + (buf ^ 1) * kTile * 256, qb, nt0, min(kTile, T - nt0));
+        for (int j = threadIdx.x; j < kTile; j += kThr)
+          sl[buf ^ 1][j] = (nt0 + j < T) ? lb[nt0 + j] : 0.f;
+      }
+      cp_async_commit();
+      cp_async_wait<1>();
+      __syncthreads();
+      if (hr == 0 && qt == kb_i) load_a_frags(sk, warp, lane, a);
+      float acc[8][4];
+      qk_tile(sq0 + buf * kTile * 256, a, lane, acc);
+      float part[2] = {0.f, 0.f};
+#pragma unroll
+      for (int n = 0; n < 8; ++n)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int jq = n * 8 + 2 * tig + e;
+          const int t = qt * kTile + jq;
+          const float lt = sl[buf][jq];
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int i = key0 + 8 * hh;
+            if (t >= i && t < T) part[hh] += exp2f(fmaf(acc[n][2 * hh + e], kC, -lt));
+          }
+        }
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const float y = part[hh] - colc[hh];
+        const float tt = col[hh] + y;
+        colc[hh] = (tt - col[hh]) - y;
+        col[hh] = tt;
+      }
+      __syncthreads();
+    }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      float s = col[hh] - colc[hh];
+      s += __shfl_xor_sync(0xffffffffu, s, 1);
+      s += __shfl_xor_sync(0xffffffffu, s, 2);
+      const int i = key0 + 8 * hh;
+      if (tig == 0 && i < T && s_head) s_head[bh * T + i] = s;
+      tot[hh] = __fadd_rn(tot[hh], s);  // group sum in head order
+    }
+  }
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int i = key0 + 8 * hh;
+    if (tig == 0 && i < T) s_full[static_cast<long>(unit) * T + i] = tot[hh];
+  }
+}
+
+// K4: S[b][g][j] += sum_h exp(logit[b][h][j] - lse[b][h]) for j < n_hi.
+__global__ void score_decode_kernel(const float* __restrict__ logits, const float* __restrict__ lse,
+                                    float* __restrict__ scores, int Hq, int Hkv, int cap, int n) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  const int unit = blockIdx.y, b = unit / Hkv, g = unit % Hkv;
+  if (j >= n) return;
+  const int rep = Hq / Hkv;
+  float add = 0.f;
+  for (int r = 0; r < rep; ++r) {
+    const long bh = static_cast<long>(b) * Hq + g * rep + r;
+    add += expf(logits[bh * cap + j] - lse[bh]);
+  }
+  scores[static_cast<long>(unit) * cap + j] += add;
+}
+
+}  // namespace
+}  // namespace mikv
+
+using namespace mikv;
+
+extern "C" size_t mikv_score_workspace_bytes(int B, int Hq, int T) {
+  if (B < 1 || Hq < 1 || T < 1) return 0;
+  return align_up(static_cast<size_t>(B) * Hq * T * sizeof(float), 256);
+}
+
+extern "C" int mikv_score_update(int mode, const uint16_t* q, const uint16_t* k, int T,
+                                 const float* hi_logits, const float* lse, mikv_cache* c,
+                                 float* scores_full, float* scores_head, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  clear_error();
+  if (!c) return fail(MIKV_EINVAL, "score_update: null cache");
+  if (c->D != kD) return fail(MIKV_EUNSUPPORTED, "score_update: D=%d (only %d)", c->D, kD);
+  if (c->B < 1 || c->Hkv < 1 || c->Hq < c->Hkv || c->Hq % c->Hkv || c->Hq / c->Hkv > 8)
+    return fail(MIKV_ESHAPE, "score_update: bad heads");
+  cudaStream_t s = as_stream(stream);
+  if (mode == MIKV_PREFILL) {
+    if (!q || !k || !scores_full || !ws) return fail(MIKV_EINVAL, "score_update: null pointer");
+    if (T < 1) return fail(MIKV_ESHAPE, "score_update: T=%d", T);
+    if (!aligned16(q) || !aligned16(k)) return fail(MIKV_EALIGN, "score_update: q/k alignment");
+    const size_t need = mikv_score_workspace_bytes(c->B, c->Hq, T);
+    if (ws_bytes < need) return fail(MIKV_ESHAPE, "score_update: workspace %zu < %zu", ws_bytes, need);
+    float* lse2 = static_cast<float*>(ws);
+    const int nblk = (T + kTile - 1) / kTile;
+    if (cudaFuncSetAttribute(row_lse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(col_sum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem) != cudaSuccess)
+      return check_launch("score kernels attribute");
+    row_lse_kernel<<<dim3(nblk, c->B * c->Hq), kThr, kScoreSmem, s>>>(
+        reinterpret_cast<const __half*>(q), reinterpret_cast<const __half*>(k), c->Hq, c->Hkv, T,
+        lse2);
+    if (int e = check_launch("row_lse_kernel")) return e;
+    col_sum_kernel<<<dim3(nblk, c->B * c->Hkv), kThr, kScoreSmem, s>>>(
+        reinterpret_cast<const __half*>(q), reinterpret_cast<const __half*>(k), lse2, c->Hq, c->Hkv,
+        T, scores_full, scores_head);
+    return check_launch("col_sum_kernel");
+  }
+  if (mode == MIKV_DECODE) {
+    if (int e = validate_cache_public(c, "score_update")) return e;
+    if (!hi_logits || !lse || !c->scores) return fail(MIKV_EINVAL, "score_update: null pointer");
+    if (c->n_hi == 0) return MIKV_OK;
+    dim3 grid((c->n_hi + 255) / 256, c->B * c->Hkv);
+    score_decode_kernel<<<grid, 256, 0, s>>>(hi_logits, lse, c->scores, c->Hq, c->Hkv, c->cap_hi,
+                                             c->n_hi);
+    return check_launch("score_decode_kernel");
+  }
+  return fail(MIKV_EINVAL, "score_update: bad mode %d", mode);
+}

@@ -1,0 +1,387 @@
+// K5 + K6: token selection (H2O top-k with a recent window, CriticalKV two-stage
+// selection, the per-step demotion victim) and the projected-value L1 norms.
+//
+// Sources: "No Token Left Behind" reading notes (velog), "Key contributions 1)"
+// (H2O decides the important tokens; the rest are kept in low precision);
+// paperlayer summary, section 5 (local tokens and heavy hitters); CriticalKV
+// summary (gist.science), "Algorithm: perturbation-constrained selection"
+// (b' = alpha*b by attention weight, the remaining b'' by A_i * ||V_i W_O||_1)
+// and "Theoretical framework" (projected value state V W_O).
+//
+// Selection is exact integer work on the float bit patterns: one CTA per
+// (batch, key head) runs an MSB-first radix select (4 x 8-bit digits) over
+// order-preserving 32-bit keys to find the b-th best value, takes every
+// candidate above it and, among candidates equal to it, the lowest positions
+// (block-wide prefix count in position order), then writes the kept and evicted
+// positions in ascending order with a block scan.  The result is unique, so it
+// is bit-exact against any correct implementation given the same scores.
+//
+// K6, N[b][h][i] = || v_i . W_O[h*D:(h+1)*D, :] ||_1, is a dense GEMM
+// (L x 128) x (128 x hidden) per query head on tensor cores (mma.sync
+// m16n8k16, fp32 accumulate) whose output is never stored: the epilogue sums
+// |.| per row (per-step partials added with Kahan compensation).
+#include <algorithm>
+#include <cmath>
+
+#include "common.cuh"
+
+namespace mikv {
+int validate_cache_public(const mikv_cache* c, const char* who);
+
+namespace {
+
+constexpr int kSelThreads = 1024;
+constexpr int kMaxSelectL = 131072;
+
+__device__ __forceinline__ uint32_t order_key(float x) {
+  uint32_t b = __float_as_uint(x);
+  if ((b & 0x7fffffffu) == 0) b = 0;  // -0 == +0
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// Block-wide exclusive scan of one int per thread; returns the exclusive prefix, sets total.
+__device__ int block_exclusive_scan(int v, int* warp_sums, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int s = (lane < (blockDim.x >> 5)) ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    warp_sums[lane] = s;  // inclusive warp prefix
+  }
+  __syncthreads();
+  const int before = (warp > 0) ? warp_sums[warp - 1] : 0;
+  total = warp_sums[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  return before + x - v;
+}
+
+// Mark (flag = 1) the `take` best candidates (flag == 0) by key, ties to lower positions.
+__device__ void topk_mark(const float* __restrict__ key, int L, int take, uint8_t* flag,
+                          unsigned* hist, int* scratch) {
+  if (take <= 0) return;
+  const int tid = threadIdx.x;
+  uint32_t prefix = 0, mask = 0;
+  int remaining = take;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < L; i += blockDim.x) {
+      if (flag[i] != 0) continue;
+      const uint32_t u = order_key(key[i]);
+      if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int above = 0, d = 255;
+      for (; d > 0; --d) {
+        if (above + static_cast<int>(hist[d]) >= remaining) break;
+        above += hist[d];
+      }
+      scratch[0] = d;
+      scratch[1] = remaining - above;
+    }
+    __syncthreads();
+    prefix |= static_cast<uint32_t>(scratch[0]) << shift;
+    mask |= 255u << shift;
+    remaining = scratch[1];
+    __syncthreads();
+  }
+  // every candidate > prefix is taken; `remaining` of those == prefix, lowest positions first
+  const int per = (L + blockDim.x - 1) / blockDim.x;
+  const int lo = min(L, tid * per), hi = min(L, lo + per);
+  int ties = 0;
+  for (int i = lo; i < hi; ++i)
+    if (flag[i] == 0 && order_key(key[i]) == prefix) ++ties;
+  int total;
+  int rank = block_exclusive_scan(ties, scratch + 2, total);
+  for (int i = lo; i < hi; ++i) {
+    if (flag[i] != 0) continue;
+    const uint32_t u = order_key(key[i]);
+    if (u > prefix) flag[i] = 3;  // temporary: taken in this stage
+    else if (u == prefix) {
+      if (rank < remaining) flag[i] = 3;
+      ++rank;
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < L; i += blockDim.x)
+    if (flag[i] == 3) flag[i] = 1;
+  __syncthreads();
+}
+
+// One CTA per (batch, key head).  flag: 0 evicted, 1 taken by a stage, 2 recent window.
+__global__ void __launch_bounds__(kSelThreads) select_kernel(
+    const float* __restrict__ key1, const float* __restrict__ key2, int L, int window, int take1,
+    int take2, int n_keep, int32_t* __restrict__ keep_pos, int32_t* __restrict__ evict_pos,
+    float* __restrict__ keep_scores) {
+  extern __shared__ uint8_t flag[];
+  __shared__ unsigned hist[256];
+  __shared__ int scratch[2 + 32];
+  const long unit = blockIdx.x;
+  const float* k1 = key1 + unit * L;
+  const int w = min(window, L);
+  for (int i = threadIdx.x; i < L; i += blockDim.x) flag[i] = (i >= L - w) ? 2 : 0;
+  __syncthreads();
+  topk_mark(k1, L, take1, flag, hist, scratch);
+  if (key2) topk_mark(key2 + unit * L, L, take2, flag, hist, scratch);
+  // compaction in position order
+  const int per = (L + blockDim.x - 1) / blockDim.x;
+  const int lo = min(L, static_cast<int>(threadIdx.x) * per), hi = min(L, lo + per);
+  int kept = 0;
+  for (int i = lo; i < hi; ++i) kept += flag[i] != 0;
+  int total;
+  int kp = block_exclusive_scan(kept, scratch + 2, total);
+  int ep = lo - kp;
+  int32_t* kout = keep_pos + unit * n_keep;
+  int32_t* eout = evict_pos + unit * (L - n_keep);
+  float* sout = keep_scores ? keep_scores + unit * n_keep : nullptr;
+  for (int i = lo; i < hi; ++i) {
+    if (flag[i] != 0) {
+      if (kp < n_keep) {
+        kout[kp] = i;
+        if (sout) sout[kp] = k1[i];
+      }
+      ++kp;
+    } else {
+      if (ep < L - n_keep) eout[ep] = i;
+      ++ep;
+    }
+  }
+}
+
+// Demotion victim: among slots j < n_hi with pos < L - window, the minimum of
+// (score ascending, position descending).  One CTA per (batch, key head).
+__global__ void __launch_bounds__(256) demote_select_kernel(const float* __restrict__ scores,
+                                                            const int32_t* __restrict__ pos,
+                                                            int cap, int n_hi, int limit,
+                                                            int32_t* __restrict__ victim) {
+  __shared__ float ss[256];
+  __shared__ int sp[256], sj[256];
+  const long unit = blockIdx.x;
+  float bs = INFINITY;
+  int bp = -1, bj = -1;
+  for (int j = threadIdx.x; j < n_hi; j += blockDim.x) {
+    const int p = pos[unit * cap + j];
+    if (p >= limit) continue;
+    const float s = scores[unit * cap + j];
+    if (bj < 0 || s < bs || (s == bs && p > bp)) {
+      bs = s;
+      bp = p;
+      bj = j;
+    }
+  }
+  ss[threadIdx.x] = bs;
+  sp[threadIdx.x] = bp;
+  sj[threadIdx.x] = bj;
+  __syncthreads();
+  for (int o = 128; o > 0; o >>= 1) {
+    if (threadIdx.x < o) {
+      const int t = threadIdx.x + o;
+      const bool better = sj[t] >= 0 &&
+                          (sj[threadIdx.x] < 0 || ss[t] < ss[threadIdx.x] ||
+                           (ss[t] == ss[threadIdx.x] && sp[t] > sp[threadIdx.x]));
+      if (better) {
+        ss[threadIdx.x] = ss[t];
+        sp[threadIdx.x] = sp[t];
+        sj[threadIdx.x] = sj[t];
+      }
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) victim[unit] = sj[0];
+}
+
+// C[b][g][i] = sum_{h in group, ascending} fl(S^h_i * N_{h,i}), fp32 without fusion.
+__global__ void ckey_kernel(const float* __restrict__ s_head, const float* __restrict__ n,
+                            int Hq, int Hkv, int L, float* __restrict__ ckey) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const int unit = blockIdx.y, b = unit / Hkv, g = unit % Hkv;
+  if (i >= L) return;
+  const int rep = Hq / Hkv;
+  float c = 0.f;
+  for (int r = 0; r < rep; ++r) {
+    const long row = (static_cast<long>(b) * Hq + g * rep + r) * L + i;
+    c = __fadd_rn(c, __fmul_rn(s_head[row], n[row]));
+  }
+  ckey[static_cast<long>(unit) * L + i] = c;
+}
+
+// ---------------------------------------------------------------------------------
+// K6: projected-value L1 norms on tensor cores.
+constexpr int kVwoThreads = 256;  // 8 warps x 16 tokens
+constexpr int kVwoM = 128;
+constexpr int kVwoN = 128;
+
+__global__ void __launch_bounds__(kVwoThreads) vwo_norm_kernel(const __half* __restrict__ v,
+                                                               const __half* __restrict__ w,
+                                                               int Hq, int Hkv, int L, int hidden,
+                                                               float* __restrict__ out) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  const uint32_t sv = smem_u32(sm);                 // [128 tokens][128 ch] swizzled
+  const uint32_t sw0 = sv + kVwoM * 256;            // 2 x [128 k][128 n] swizzled
+  const int bh = blockIdx.y, b = bh / Hq, h = bh % Hq;
+  const int g = h / (Hq / Hkv);
+  const int i0 = blockIdx.x * kVwoM;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const __half* vb = v + (static_cast<long>(b) * Hkv + g) * L * kD;
+  const __half* wb = w + static_cast<long>(h) * kD * hidden;
+  const int nrows = min(kVwoM, L - i0);
+  for (int i = threadIdx.x; i < kVwoM * 16; i += kVwoThreads) {
+    const int r = i >> 4, cc = i & 15;
+    const bool ok = r < nrows;
+    cp_async16(sv + r * 256 + ((cc ^ (r & 7)) << 4), ok ? vb + (static_cast<long>(i0) + r) * kD + cc * 8 : vb, ok);
+  }
+  auto load_w = [&](int step, int buf) {
+    const int n0 = step * kVwoN;
+    const uint32_t s = sw0 + buf * (kD * 256);
+    for (int i = threadIdx.x; i < kD * 16; i += kVwoThreads) {
+      const int r = i >> 4, cc = i & 15;
+      cp_async16(s + r * 256 + ((cc ^ (r & 7)) << 4), wb + static_cast<long>(r) * hidden + n0 + cc * 8, true);
+    }
+  };
+  const int nsteps = hidden / kVwoN;
+  load_w(0, 0);
+  cp_async_commit();
+  uint32_t a[8][4];
+  float run[2] = {0.f, 0.f}, comp[2] = {0.f, 0.f};
+  for (int st = 0; st < nsteps; ++st) {
+    if (st + 1 < nsteps) load_w(st + 1, (st + 1) & 1);
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncthreads();
+    if (st == 0) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int row = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int chunk = 2 * k + (lane >> 4);
+        ldsm_x4(sv + row * 256 + ((chunk ^ (row & 7)) << 4), a[k][0], a[k][1], a[k][2], a[k][3]);
+      }
+    }
+    const uint32_t s = sw0 + (st & 1) * (kD * 256);
+    float part[2] = {0.f, 0.f};
+#pragma unroll
+    for (int np = 0; np < 8; ++np) {
+      float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int krow = 16 * k + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int chunk = 2 * np + (lane >> 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(s + krow * 256 + ((chunk ^ (krow & 7)) << 4), b0, b1, b2, b3);
+        mma16816(acc0, a[k][0], a[k][1], a[k][2], a[k][3], b0, b1);
+        mma16816(acc1, a[k][0], a[k][1], a[k][2], a[k][3], b2, b3);
+      }
+      part[0] += fabsf(acc0[0]) + fabsf(acc0[1]) + fabsf(acc1[0]) + fabsf(acc1[1]);
+      part[1] += fabsf(acc0[2]) + fabsf(acc0[3]) + fabsf(acc1[2]) + fabsf(acc1[3]);
+    }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const float y = part[hh] - comp[hh];
+      const float t = run[hh] + y;
+      comp[hh] = (t - run[hh]) - y;
+      run[hh] = t;
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    float x = run[hh] - comp[hh];
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    x += __shfl_xor_sync(0xffffffffu, x, 2);
+    const int i = i0 + warp * 16 + gid + 8 * hh;
+    if (tig == 0 && i < L) out[static_cast<long>(bh) * L + i] = x;
+  }
+}
+
+}  // namespace
+}  // namespace mikv
+
+using namespace mikv;
+
+static int n_keep_of(int L, int pct, int window) {
+  const long p = static_cast<long>(pct) * L / 100;
+  return static_cast<int>(std::min<long>(L, std::max<long>(window, p)));
+}
+
+extern "C" size_t mikv_select_workspace_bytes(int policy, int B, int Hkv, int Hq, int L, int hidden) {
+  (void)Hq;
+  (void)hidden;
+  if (policy != MIKV_CRITICALKV || B < 1 || Hkv < 1 || L < 1) return 0;
+  return align_up(static_cast<size_t>(B) * Hkv * L * sizeof(float), 256);
+}
+
+extern "C" int mikv_select(int policy, const mikv_cache* c, int L, int budget_pct, int window,
+                           float alpha, const float* scores, const float* scores_head,
+                           const uint16_t* v, const uint16_t* w_o, int hidden, float* vwo_norm,
+                           int32_t* keep_pos, int32_t* evict_pos, float* keep_scores, void* ws,
+                           size_t ws_bytes, void* stream) {
+  clear_error();
+  if (!c) return fail(MIKV_EINVAL, "select: null cache");
+  if (c->B < 1 || c->Hkv < 1 || c->Hq < c->Hkv || c->Hq % c->Hkv || c->Hq / c->Hkv > 8)
+    return fail(MIKV_ESHAPE, "select: bad heads");
+  if (L < 1 || window < 0) return fail(MIKV_ESHAPE, "select: L=%d window=%d", L, window);
+  cudaStream_t s = as_stream(stream);
+  const int units = c->B * c->Hkv;
+  if (policy == MIKV_DEMOTE) {
+    if (int e = validate_cache_public(c, "select(DEMOTE)")) return e;
+    if (!evict_pos || !c->scores || !c->pos_hi) return fail(MIKV_EINVAL, "select(DEMOTE): null pointer");
+    if (c->n_hi <= window)
+      return fail(MIKV_ESHAPE, "select(DEMOTE): n_hi=%d must exceed window=%d", c->n_hi, window);
+    demote_select_kernel<<<units, 256, 0, s>>>(c->scores, c->pos_hi, c->cap_hi, c->n_hi,
+                                               L - window, evict_pos);
+    return check_launch("demote_select_kernel");
+  }
+  if (policy != MIKV_H2O && policy != MIKV_CRITICALKV) return fail(MIKV_EINVAL, "select: policy %d", policy);
+  if (budget_pct < 0 || budget_pct > 100) return fail(MIKV_ESHAPE, "select: budget_pct=%d", budget_pct);
+  if (L > kMaxSelectL) return fail(MIKV_ESHAPE, "select: L=%d above %d", L, kMaxSelectL);
+  const int n_keep = n_keep_of(L, budget_pct, window);
+  if (!scores || (!keep_pos && n_keep > 0) || (!evict_pos && L - n_keep > 0))
+    return fail(MIKV_EINVAL, "select: null pointer");
+  const int w = std::min(window, L);
+  const int bud = n_keep - w;
+  int take1 = bud, take2 = 0;
+  const float* key2 = nullptr;
+  if (policy == MIKV_CRITICALKV) {
+    if (!(alpha >= 0.f && alpha <= 1.f)) return fail(MIKV_EINVAL, "select: alpha=%g", alpha);
+    if (!scores_head || !vwo_norm || !ws) return fail(MIKV_EINVAL, "select(CRITICALKV): null pointer");
+    const size_t need = mikv_select_workspace_bytes(policy, c->B, c->Hkv, c->Hq, L, hidden);
+    if (ws_bytes < need) return fail(MIKV_ESHAPE, "select: workspace %zu < %zu", ws_bytes, need);
+    take1 = static_cast<int>(std::floor(static_cast<double>(alpha) * bud));
+    take2 = bud - take1;
+    if (w_o) {
+      if (!v) return fail(MIKV_EINVAL, "select(CRITICALKV): null v");
+      if (c->D != kD) return fail(MIKV_EUNSUPPORTED, "select: D=%d", c->D);
+      if (hidden < kVwoN || hidden % kVwoN) return fail(MIKV_ESHAPE, "select: hidden=%d (multiple of %d)", hidden, kVwoN);
+      if (!aligned16(v) || !aligned16(w_o)) return fail(MIKV_EALIGN, "select: v/w_o alignment");
+      const int smem = kVwoM * 256 + 2 * kD * 256;
+      if (cudaFuncSetAttribute(vwo_norm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return check_launch("vwo_norm_kernel attribute");
+      dim3 grid((L + kVwoM - 1) / kVwoM, c->B * c->Hq);
+      vwo_norm_kernel<<<grid, kVwoThreads, smem, s>>>(reinterpret_cast<const __half*>(v),
+                                                       reinterpret_cast<const __half*>(w_o), c->Hq,
+                                                       c->Hkv, L, hidden, vwo_norm);
+      if (int e = check_launch("vwo_norm_kernel")) return e;
+    }
+    float* ckey = static_cast<float*>(ws);
+    ckey_kernel<<<dim3((L + 255) / 256, units), 256, 0, s>>>(scores_head, vwo_norm, c->Hq, c->Hkv, L, ckey);
+    if (int e = check_launch("ckey_kernel")) return e;
+    key2 = ckey;
+  }
+  if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L) != cudaSuccess)
+    return check_launch("select_kernel attribute");
+  select_kernel<<<units, kSelThreads, L, s>>>(scores, key2, L, window, take1, take2, n_keep,
+                                               keep_pos, evict_pos, keep_scores);
+  return check_launch("select_kernel");
+}
