@@ -123,6 +123,28 @@ int mikv_balance_prefill(const uint16_t* q, const uint16_t* k, int B, int Hq, in
 size_t mikv_balance_workspace_bytes(int B, int Hkv, int D);
 
 /*
+ * Allocation-free variant of mikv_balance_prefill (the paper has no counterpart:
+ * this is a deployment convenience).  Same inputs, output and result, but no
+ * workspace argument: the scratch lives in a static device array inside the
+ * library.  It is meant for callers that cannot allocate device memory, such as
+ * a plugin that its host framework hands only input and output buffers, or a
+ * serving loop that must never enter the allocator (cudaMalloc/cudaFree
+ * synchronise the device and may fail under memory pressure).
+ *   Limit: B * Hkv <= 1024 (the array holds 2 x 1024 x 128 floats, 1 MiB, on
+ *   every device that loads the library, until the process exits); larger
+ *   shapes return MIKV_ESHAPE.
+ *   The first call on a device looks up that array's device address (with the
+ *   device current); make that first call before any stream capture.
+ *   All calls share the one array and each clears it first: calls whose kernels
+ *   can overlap on the GPU (different streams, without ordering) race and
+ *   return wrong results.  Calls allocate nothing.
+ * Errors: as mikv_balance_prefill, plus ESHAPE above the limit and ECUDA if the
+ * array's address cannot be obtained.
+ */
+int mikv_balance_prefill_noalloc(const uint16_t* q, const uint16_t* k, int B, int Hq, int Hkv,
+                                 int T, int D, float* b_out, void* stream);
+
+/*
  * H2O importance ([notes] "Observation 1-4" and "Key contributions 1)": H2O,
  * accumulated attention; read as the plain H2O definition).
  * MIKV_PREFILL: column sums of the causal softmax over the T prompt rows,

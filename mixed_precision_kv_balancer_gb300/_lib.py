@@ -18,7 +18,7 @@ MIKV_H2O, MIKV_CRITICALKV, MIKV_DEMOTE = 0, 1, 2
 MIKV_TIER_HI, MIKV_TIER_LO, MIKV_TIER_DEMOTE = 0, 1, 2
 
 EXPORTS = (
-    "mikv_balance_prefill", "mikv_balance_workspace_bytes",
+    "mikv_balance_prefill", "mikv_balance_workspace_bytes", "mikv_balance_prefill_noalloc",
     "mikv_score_update", "mikv_score_workspace_bytes",
     "mikv_select", "mikv_select_workspace_bytes",
     "mikv_quantize_append",
@@ -65,6 +65,7 @@ def load() -> ctypes.CDLL:
     sig = {
         "mikv_balance_prefill": (I, [P, P, I, I, I, I, I, P, P, S, P]),
         "mikv_balance_workspace_bytes": (S, [I, I, I]),
+        "mikv_balance_prefill_noalloc": (I, [P, P, I, I, I, I, I, P, P]),
         "mikv_score_update": (I, [I, P, P, I, P, P, CP, P, P, P, S, P]),
         "mikv_score_workspace_bytes": (S, [I, I, I]),
         "mikv_select": (I, [I, CP, I, I, I, F, P, P, P, P, I, P, P, P, P, P, S, P]),
@@ -116,6 +117,13 @@ def mikv_balance_prefill(q, k, b_out, ws=None, stream=None):
     w, nb = _ws(lib.mikv_balance_workspace_bytes(B, Hkv, D), q.device, ws)
     _check("mikv_balance_prefill", lib.mikv_balance_prefill(
         _ptr(q), _ptr(k), B, Hq, Hkv, T, D, _ptr(b_out), _ptr(w), nb, _stream(stream)))
+
+
+def mikv_balance_prefill_noalloc(q, k, b_out, stream=None):
+    """Balancer without a workspace: scratch is the library's static device array."""
+    B, Hq, T, D = q.shape
+    _check("mikv_balance_prefill_noalloc", load().mikv_balance_prefill_noalloc(
+        _ptr(q), _ptr(k), B, Hq, k.shape[1], T, D, _ptr(b_out), _stream(stream)))
 
 
 def mikv_score_update(mode, cache, q=None, k=None, T=0, hi_logits=None, lse=None,

@@ -13,6 +13,7 @@
 // depend on the order).  A second kernel forms b in fp32, RN division then RN
 // square root.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -135,4 +136,81 @@ extern "C" int mikv_balance_prefill(const uint16_t* q, const uint16_t* k, int B,
   const int n = units * D;
   balance_finalize_kernel<<<(n + 255) / 256, 256, 0, s>>>(ws_q, ws_k, b_out, n);
   return check_launch("balance_finalize_kernel");
+}
+
+// ---------------------------------------------------------------------------------
+// Allocation-free variant of mikv_balance_prefill.
+//
+// Some callers cannot allocate device memory for the workspace: a plugin that a host
+// framework hands only its input and output buffers, or a serving loop that must never
+// reach the allocator (cudaMalloc and cudaFree synchronise the device and can fail under
+// memory pressure).  This entry point keeps its scratch (the per-channel query and key
+// maxima) in a fixed static device array instead.  The array is sized for
+// kNoAllocMaxUnits (batch x key heads) units of 128 channels, 1 MiB in total, and every
+// device that loads the library holds it until the process exits.
+namespace mikv {
+namespace {
+
+constexpr int kNoAllocMaxUnits = 1024;
+constexpr int kNoAllocFloats = 2 * kNoAllocMaxUnits * kD;  // Mq then Mk
+static __device__ __align__(256) float g_balance_scratch[kNoAllocFloats];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+float* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_balance_scratch on the current device, looked up once per device.
+// (In host code the symbol is only a host-side stand-in, never a device address.)
+int scratch_for_current_device(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(MIKV_ECUDA, "balance_prefill_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(MIKV_ECUDA, "balance_prefill_noalloc: device %d", dev);
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_balance_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(MIKV_ECUDA, "balance_prefill_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    g_scratch_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_scratch_ptr[dev];
+  return MIKV_OK;
+}
+
+}  // namespace
+}  // namespace mikv
+
+extern "C" int mikv_balance_prefill_noalloc(const uint16_t* q, const uint16_t* k, int B, int Hq,
+                                            int Hkv, int T, int D, float* b_out, void* stream) {
+  clear_error();
+  if (!q || !k || !b_out) return fail(MIKV_EINVAL, "balance_prefill_noalloc: null pointer");
+  if (D != kD) return fail(MIKV_EUNSUPPORTED, "balance_prefill_noalloc: D=%d (only %d)", D, kD);
+  if (B < 1 || Hkv < 1 || Hq < Hkv || Hq % Hkv || Hq / Hkv > 8 || T < 1)
+    return fail(MIKV_ESHAPE, "balance_prefill_noalloc: bad shape B=%d Hq=%d Hkv=%d T=%d", B, Hq, Hkv, T);
+  if (static_cast<long>(B) * Hkv > kNoAllocMaxUnits)
+    return fail(MIKV_ESHAPE,
+                "balance_prefill_noalloc: B*Hkv=%ld exceeds the static scratch limit of %d "
+                "(batch x key heads); use mikv_balance_prefill with a workspace",
+                static_cast<long>(B) * Hkv, kNoAllocMaxUnits);
+  if (!aligned16(q) || !aligned16(k))
+    return fail(MIKV_EALIGN, "balance_prefill_noalloc: q and k must be 16-byte aligned");
+  float* scratch = nullptr;
+  if (int e = scratch_for_current_device(&scratch)) return e;
+  cudaStream_t s = as_stream(stream);
+  const int units = B * Hkv;
+  float* ws_q = scratch;
+  float* ws_k = scratch + static_cast<long>(units) * kD;
+  // the maxima are folded in with atomicMax, so the used part must start at zero
+  if (cudaMemsetAsync(scratch, 0, 2 * static_cast<size_t>(units) * kD * sizeof(float), s) != cudaSuccess)
+    return check_launch("balance_prefill_noalloc memset");
+  const long qrows = static_cast<long>(Hq / Hkv) * T;
+  int nsplit = (4 * kNumSMs + units - 1) / units;
+  nsplit = static_cast<int>(std::min<long>(nsplit, std::max<long>(1, qrows / 64)));
+  balance_max_kernel<<<dim3(units, nsplit), kBalThreads, 0, s>>>(
+      reinterpret_cast<const uint4*>(q), reinterpret_cast<const uint4*>(k), Hq, Hkv, T, nsplit, ws_q, ws_k);
+  if (int e = check_launch("balance_max_kernel (noalloc)")) return e;
+  const int n = units * D;
+  balance_finalize_kernel<<<(n + 255) / 256, 256, 0, s>>>(ws_q, ws_k, b_out, n);
+  return check_launch("balance_finalize_kernel (noalloc)");
 }
