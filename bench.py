@@ -203,7 +203,7 @@ def run_gpu(args, wl, rank, world):
     prefill_ms = []
     for l in range(wl.layers):
         c = MikvCache(wl.B, wl.Hq, wl.Hkv, wl.D, wl.hi_bits, wl.lo_bits, cap_hi, cap_lo, dev)
-        x = inputs.make_prefill(wl.scaled(seed=wl.seed + 1000 * rank), l, dev)
+        x = inputs.make_prefill(rank_seed(wl, rank), l, dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         c.prefill(x["q"], x["k"], x["v"], wl.budget_pct, wl.window)
@@ -214,33 +214,23 @@ def run_gpu(args, wl, rank, world):
         layers.append(c)
     torch.cuda.empty_cache()
     # decode tokens for every step and layer, resident before timing
-    toks = [[inputs.make_decode_token(wl.scaled(seed=wl.seed + 1000 * rank), l, s, dev)
+    toks = [[inputs.make_decode_token(rank_seed(wl, rank), l, s, dev)
              for l in range(wl.layers)] for s in range(total_steps + (0 if args.no_e2e else args.steps))]
     torch.cuda.synchronize()
 
-    def step(s, ev=None):
+    def step(s, timed=False):
         L_before = wl.T + s
-        launches = 0
         for l, c in enumerate(layers):
             t = toks[s][l]
-            will_demote = c.n_hi + 1 > n_keep(L_before + 1, wl.budget_pct, wl.window)
-            if ev is not None:
-                _lib.mikv_quantize_append(_lib.MIKV_TIER_HI, c, t["k"][:, :, None, :], t["v"][:, :, None, :],
-                                          c.zero_pos, 1, L_before)
-                ev[0].record()
-                _lib.mikv_decode_attention(t["q"], c, c.out, c.lse, c.hi_logits, ws=c.ws_decode)
-                ev[1].record()
-                ev_pairs.append((ev[0], ev[1], cache_bytes(wl, c.n_hi, c.n_lo)))
-                ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                _lib.mikv_score_update(_lib.MIKV_DECODE, c, hi_logits=c.hi_logits, lse=c.lse)
-                if c.n_hi > n_keep(L_before + 1, wl.budget_pct, wl.window):
-                    _lib.mikv_select(_lib.MIKV_DEMOTE, c, L_before + 1, wl.budget_pct, wl.window,
-                                     evict_pos=c.victim)
-                    _lib.mikv_quantize_append(_lib.MIKV_TIER_DEMOTE, c, None, None, c.victim, 1)
-            else:
-                c.decode_step(t["q"], t["k"], t["v"], L_before, wl.budget_pct, wl.window)
-            launches += 4 + (2 if will_demote else 0)
-        return launches
+            if timed:
+                read = cache_bytes(wl, c.n_hi + 1, c.n_lo)   # tiers as attended (after the append)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+            c.decode_step(t["q"], t["k"], t["v"], L_before, wl.budget_pct, wl.window)
+            if timed:
+                e1.record()
+                ev_pairs.append((e0, e1, read))
+        return 3 * len(layers)   # append, split-K attention, fused merge/score/demotion
 
     ev_pairs = []
     for s in range(args.warmup):
@@ -259,15 +249,12 @@ def run_gpu(args, wl, rank, world):
     for s in range(args.warmup, total_steps):
         L = wl.T + s + 1
         kv_tokens += wl.B * L * wl.layers
-        launches += step(s, (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+        launches += step(s, timed=True)
     end.record()
     torch.cuda.synchronize()
     ms = start.elapsed_time(end)
     clk = clocks.stop()
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_over_ranks(ms, world, dev)
     attn_ms = [a.elapsed_time(b) for a, b, _ in ev_pairs]
     attn_bytes = [nb for _, _, nb in ev_pairs]
     res = dict(ms=ms, kv_tokens=kv_tokens * world, launches=launches, clocks=clk,
@@ -301,6 +288,21 @@ def run_gpu(args, wl, rank, world):
         e2e_ms = max(e0.elapsed_time(e1), (time.perf_counter() - t0) * 1e3)
         res.update(e2e_ms=e2e_ms, e2e_tokens=e2e_tokens * world, h2d=h2d, d2h=d2h)
     return res
+
+
+def rank_seed(wl, rank: int):
+    """Each rank is an independent replica (its own batch of sequences): distinct seeds."""
+    return wl.scaled(seed=wl.seed + 1000 * rank)
+
+
+def reduce_over_ranks(ms: float, world: int, device=None) -> float:
+    """Job time = the slowest rank's time (max over ranks); identity for one rank."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
 
 
 def peaks():
@@ -362,7 +364,8 @@ def main():
         "hbm_gbs_decode_attn": achieved, "frac_of_8tbs": achieved / 8000.0,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "kernel": "mikv_decode_attention (decode_partial_kernel + decode_merge_kernel)",
+                     "kernel": "mikv_decode_step per layer (append_kernel + decode_partial_kernel + "
+                               "decode_epilogue_kernel); bytes = packed cache read",
                      "bytes_per_launch": res["attn_bytes_mean"], "ms_per_launch": res["attn_ms_mean"],
                      "traffic": None},
         "decode_attn_ms_per_step": res["attn_ms_sum"] / args.steps,

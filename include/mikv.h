@@ -242,6 +242,28 @@ int mikv_decode_attention(const uint16_t* q, const mikv_cache* c, float* out, fl
                           float* hi_logits, void* ws, size_t ws_bytes, void* stream);
 size_t mikv_decode_workspace_bytes(const mikv_cache* c);
 
+/*
+ * One whole decode step in three launches (the same arithmetic as the sequence
+ * quantize_append(HI) -> decode_attention -> score_update(DECODE) ->
+ * select(DEMOTE) -> quantize_append(DEMOTE), with identical results):
+ *   1. the new token (k_new, v_new fp16 [B][Hkv][D], position `pos`) is appended
+ *      to the important tier with score 0;
+ *   2. q fp16 [B][Hq][D] attends over both tiers (split-K partials);
+ *   3. one kernel per (batch, key head) merges the partials into out fp32
+ *      [B][Hq][D] and lse fp32 [B][Hq], adds the step's attention to the H2O score
+ *      of every important slot, and, if policy == MIKV_H2O and the important tier
+ *      now holds more than n_keep(pos + 1) tokens, demotes the victim (see
+ *      mikv_select(MIKV_DEMOTE)).  MIKV_CRITICALKV never demotes.
+ * The order follows H2O: evict after the step's attention ([notes] "Key
+ * contributions 1)"; [paperlayer] 5).  ws >= mikv_decode_step_workspace_bytes(c)
+ * (partials plus the important-tier logits).  Counts in *c are updated.
+ * Errors: EINVAL, ESHAPE (capacity, budget, workspace), EALIGN, EUNSUPPORTED, ECUDA.
+ */
+int mikv_decode_step(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new, int pos,
+                     int budget_pct, int window, int policy, mikv_cache* c, float* out, float* lse,
+                     void* ws, size_t ws_bytes, void* stream);
+size_t mikv_decode_step_workspace_bytes(const mikv_cache* c);
+
 /* Message of the last failed call on this thread ("" if none). */
 const char* mikv_last_error(void);
 

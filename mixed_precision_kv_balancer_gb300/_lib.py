@@ -23,6 +23,7 @@ EXPORTS = (
     "mikv_select", "mikv_select_workspace_bytes",
     "mikv_quantize_append",
     "mikv_decode_attention", "mikv_decode_workspace_bytes",
+    "mikv_decode_step", "mikv_decode_step_workspace_bytes",
     "mikv_last_error",
 )
 
@@ -73,6 +74,8 @@ def load() -> ctypes.CDLL:
         "mikv_quantize_append": (I, [I, P, P, I, P, I, I, P, CP, P]),
         "mikv_decode_attention": (I, [P, CP, P, P, P, P, S, P]),
         "mikv_decode_workspace_bytes": (S, [CP]),
+        "mikv_decode_step": (I, [P, P, P, I, I, I, I, CP, P, P, P, S, P]),
+        "mikv_decode_step_workspace_bytes": (S, [CP]),
         "mikv_last_error": (ctypes.c_char_p, []),
     }
     for name, (res, args) in sig.items():
@@ -169,3 +172,13 @@ def mikv_decode_attention(q, cache, out, lse, hi_logits=None, ws=None, stream=No
     _check("mikv_decode_attention", lib.mikv_decode_attention(
         _ptr(q), ctypes.byref(c), _ptr(out), _ptr(lse), _ptr(hi_logits), _ptr(w), nb,
         _stream(stream)))
+
+
+def mikv_decode_step(q, k_new, v_new, pos, budget_pct, window, policy, cache, out, lse, ws=None,
+                     stream=None):
+    lib = load()
+    c = cache.struct if hasattr(cache, "struct") else cache
+    w, nb = _ws(lib.mikv_decode_step_workspace_bytes(ctypes.byref(c)), q.device, ws)
+    _check("mikv_decode_step", lib.mikv_decode_step(
+        _ptr(q), _ptr(k_new), _ptr(v_new), pos, budget_pct, window, policy, ctypes.byref(c),
+        _ptr(out), _ptr(lse), _ptr(w), nb, _stream(stream)))

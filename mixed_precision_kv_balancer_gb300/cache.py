@@ -8,7 +8,8 @@ which call comes next, with which counts:
            CRITICALKV) -> mikv_quantize_append(HI, kept) -> mikv_quantize_append(LO, evicted)
   decode   mikv_quantize_append(HI, new token) -> mikv_decode_attention ->
            mikv_score_update(DECODE) -> [H2O, over budget] mikv_select(DEMOTE) ->
-           mikv_quantize_append(DEMOTE)
+           mikv_quantize_append(DEMOTE); mikv_decode_step runs the same step in three
+           launches (append, split-K attention, fused merge/score/demotion)
 
 (MiKV reading notes, "Key contributions 1)-3)" and section 3.4; CriticalKV
 summary, "Algorithm".)  The budget is n_keep(L) = min(L, max(W, floor(p*L/100)))
@@ -65,7 +66,7 @@ class MikvCache:
         self.struct = s
         lib = _lib.load()
         import ctypes
-        self.ws_decode = torch.empty(max(256, lib.mikv_decode_workspace_bytes(ctypes.byref(s))),
+        self.ws_decode = torch.empty(max(256, lib.mikv_decode_step_workspace_bytes(ctypes.byref(s))),
                                      dtype=torch.uint8, device=dev)
         self.out = torch.empty(B, Hq, D, dtype=torch.float32, device=dev)
         self.lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
@@ -124,7 +125,15 @@ class MikvCache:
 
     # --- decode --------------------------------------------------------------------
     def decode_step(self, q, k, v, L_before, budget_pct, window, policy="h2o"):
-        """One decode step; q [B,Hq,D], k/v [B,Hkv,D] fp16.  Returns (out, lse) views."""
+        """One decode step through mikv_decode_step (append, attention, fused merge + score
+        update + demotion); q [B,Hq,D], k/v [B,Hkv,D] fp16.  Returns (out, lse) views."""
+        pol = _lib.MIKV_H2O if policy == "h2o" else _lib.MIKV_CRITICALKV
+        _lib.mikv_decode_step(q, k, v, L_before, budget_pct, window, pol, self, self.out, self.lse,
+                              ws=self.ws_decode)
+        return self.out, self.lse
+
+    def decode_step_calls(self, q, k, v, L_before, budget_pct, window, policy="h2o"):
+        """The same step as the sequence of the five separate calls."""
         L = L_before + 1
         _lib.mikv_quantize_append(_lib.MIKV_TIER_HI, self, k[:, :, None, :], v[:, :, None, :],
                                   self.zero_pos, 1, L - 1)

@@ -34,7 +34,7 @@
 // (512 / 272 / 144 / 80 B per token and key head for FP16 / INT8 / INT4 / INT2).
 #include <algorithm>
 
-#include "common.cuh"
+#include "quant_device.cuh"
 
 namespace mikv {
 int validate_cache_public(const mikv_cache* c, const char* who);
@@ -43,19 +43,23 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 3;        // ring depth per warp
-constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kStages = 2;        // ring depth per warp (3 CTAs of 4 warps fit per SM)
+constexpr float kLogitScale = 0.12751743082459868f;  // log2(e) / sqrt(128)
 
 template <int BITS>
 struct Fmt {
   static constexpr bool kQuant = BITS != 16;
-  static constexpr int kRB = kD * BITS / 8;                        // bytes per token row
+  static constexpr int kRB = kD * BITS / 8;                            // bytes per token row
+  static constexpr int kRS = kQuant ? kRB : kRB + 16;                  // smem row stride (FP16 padded)
   static constexpr int kST = BITS == 16 ? 16 : (BITS == 8 ? 32 : 64);  // tokens per stage
-  static constexpr int kMetaB = kQuant ? 8 : 0;                    // (scale, zero) x 2 groups
-  static constexpr int kStageBytes = kST * (2 * kRB + 2 * kMetaB);
-  static constexpr int kOffV = kST * kRB;
-  static constexpr int kOffKM = 2 * kST * kRB;
-  static constexpr int kOffVM = 2 * kST * kRB + kST * kMetaB;
+  static constexpr int kMetaB = kQuant ? 8 : 0;                        // (scale, zero) x 2 groups
+  static constexpr int kOffV = kST * kRS;
+  static constexpr int kOffKM = 2 * kST * kRS;
+  static constexpr int kOffVM = kOffKM + kST * kMetaB;
+  static constexpr int kStageBytes = 2 * kST * kRS + 2 * kST * kMetaB;
+  static constexpr int kCPR = kRB / 16;          // 16-byte chunks per row
+  static constexpr int kRowsPerIt = 32 / kCPR;   // rows one warp-wide copy covers
+  static constexpr int kGB = 64 * BITS / 8;      // bytes of one 64-channel group
 };
 
 struct TierPtrs {
@@ -80,60 +84,121 @@ struct Params {
 };
 
 // ---------------------------------------------------------------------------------
-// stage loads
+// Shared-memory tiles.  FP16 rows are padded to 272 B, which puts the 8 rows of an
+// ldmatrix phase in 8 different 16-byte bank groups.  Code rows (32/64/128 B) keep their
+// size and XOR-swizzle their 16-byte chunks with the row bits that repeat the bank
+// pattern (every 4 / 2 / 1 rows), so the rows of one fragment load hit different banks.
+// The swizzle only depends on row bits below 8, so a thread's fragment offsets are the
+// same for every 16-row sub-tile and are computed once.
 template <int BITS>
-__device__ __forceinline__ void load_stage(uint32_t sb, const TierPtrs& t, long row0, int nvalid,
+__device__ __forceinline__ int qswz(int r) {
+  if constexpr (BITS == 2) return (r >> 2) & 1;
+  else if constexpr (BITS == 4) return (r >> 1) & 3;
+  else return r & 7;
+}
+template <int BITS>
+__device__ __forceinline__ uint32_t qaddr(int r, int off) {
+  return r * Fmt<BITS>::kRS + ((((off >> 4) ^ qswz<BITS>(r))) << 4) + (off & 15);
+}
+
+// One warp copies a stage: the K and V rows of the stage are contiguous in global
+// memory (gk, gv point at its first row), so lane l copies chunks l, l+32, ...; rows at
+// or past `nvalid` are zero-filled without being read.
+template <int BITS>
+__device__ __forceinline__ void load_stage(uint32_t sb, const uint8_t* gk, const uint8_t* gv,
+                                           const uint8_t* gkm, const uint8_t* gvm, int nvalid,
                                            int lane) {
   using F = Fmt<BITS>;
-  constexpr int kChunksPerRow = F::kRB / 16;
-  constexpr int kChunks = F::kST * kChunksPerRow;
+  const int cc = lane % F::kCPR, rl = lane / F::kCPR;
 #pragma unroll
-  for (int i = lane; i < kChunks; i += 32) {
-    const int r = i / kChunksPerRow, cc = i % kChunksPerRow;
+  for (int it = 0; it < F::kST / F::kRowsPerIt; ++it) {
+    const int r = rl + it * F::kRowsPerIt;
     const bool ok = r < nvalid;
-    uint32_t off;
-    if constexpr (BITS == 16) off = r * F::kRB + ((cc ^ (r & 7)) << 4);  // 128B-swizzled rows
-    else off = i * 16;
-    const long g = ok ? (row0 + r) * F::kRB + cc * 16 : 0;
-    cp_async16(sb + off, t.k + g, ok);
-    cp_async16(sb + F::kOffV + off, t.v + g, ok);
+    uint32_t dst;
+    if constexpr (BITS == 16) dst = r * F::kRS + cc * 16;
+    else dst = r * F::kRS + ((cc ^ qswz<BITS>(r)) << 4);
+    const int g = ok ? lane * 16 + it * 512 : 0;
+    cp_async16(sb + dst, gk + g, ok);
+    cp_async16(sb + F::kOffV + dst, gv + g, ok);
   }
   if constexpr (F::kQuant) {
 #pragma unroll
-    for (int r = lane; r < F::kST; r += 32) {
-      const bool ok = r < nvalid;
-      const long g = ok ? (row0 + r) * 8 : 0;
-      cp_async8(sb + F::kOffKM + r * 8, t.km + g, ok);
-      cp_async8(sb + F::kOffVM + r * 8, t.vm + g, ok);
+    for (int it = 0; it < (F::kST + 31) / 32; ++it) {
+      const int r = lane + 32 * it;
+      if (r < F::kST) {
+        const bool ok = r < nvalid;
+        cp_async8(sb + F::kOffKM + r * 8, gkm + (ok ? r * 8 : 0), ok);
+        cp_async8(sb + F::kOffVM + r * 8, gvm + (ok ? r * 8 : 0), ok);
+      }
     }
   }
 }
 
 // ---------------------------------------------------------------------------------
-// unpacking: codes -> fp16 pairs holding exact integers
+// unpacking: codes -> fp16 pairs holding exact integers.
+// A code c masked in place at mantissa bit 2p (INT2) or 4p (INT4) of a half whose
+// exponent field is 0x64 reads as 1024 + c*2^k; one fma.rn.f16x2 by 2^-k with addend
+// -1024*2^-k returns c exactly (the true result is a small integer).  Positions past
+// the 10 mantissa bits are reached with one shift of the whole word.
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+// (2^-k, -1024*2^-k) as f16x2 pairs for k = 0, 2, 4, 6, 8
+__device__ __forceinline__ uint32_t mul4p(int p) {
+  return p == 0 ? 0x3C003C00u : p == 1 ? 0x34003400u : p == 2 ? 0x2C002C00u
+       : p == 3 ? 0x24002400u : 0x1C001C00u;
+}
+__device__ __forceinline__ uint32_t add4p(int p) {
+  return p == 0 ? 0xE400E400u : p == 1 ? 0xDC00DC00u : p == 2 ? 0xD400D400u
+       : p == 3 ? 0xCC00CC00u : 0xC400C400u;
+}
+// 16 two-bit codes of a word (code j at bits 2j of the low half, 2j+16 of the high) ->
+// 8 pairs, pair p = (code p, code p + 8).
+// (w & MASK) | 0x64006400 as one LOP3 (lut 0xEA = (a & b) | c).
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t mask_magic(uint32_t w) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;\n" : "=r"(d) : "r"(w), "n"(MASK), "r"(0x64006400u));
+  return d;
+}
+__device__ __forceinline__ void unpack_int2_word(uint32_t w, uint32_t (&pr)[8]) {
+  pr[0] = hfma2_u32(mask_magic<0x00030003u>(w), mul4p(0), add4p(0));
+  pr[1] = hfma2_u32(mask_magic<0x000C000Cu>(w), mul4p(1), add4p(1));
+  pr[2] = hfma2_u32(mask_magic<0x00300030u>(w), mul4p(2), add4p(2));
+  pr[3] = hfma2_u32(mask_magic<0x00C000C0u>(w), mul4p(3), add4p(3));
+  pr[4] = hfma2_u32(mask_magic<0x03000300u>(w), mul4p(4), add4p(4));
+  const uint32_t w2 = w >> 10;
+  pr[5] = hfma2_u32(mask_magic<0x00030003u>(w2), mul4p(0), add4p(0));
+  pr[6] = hfma2_u32(mask_magic<0x000C000Cu>(w2), mul4p(1), add4p(1));
+  pr[7] = hfma2_u32(mask_magic<0x00300030u>(w2), mul4p(2), add4p(2));
+}
+// 8 four-bit codes (code j at bits 4j of the low half, 4j+16 of the high) -> 4 pairs,
+// pair p = (code p, code p + 4).
+__device__ __forceinline__ void unpack_int4_word(uint32_t w, uint32_t* pr) {
+  pr[0] = hfma2_u32(mask_magic<0x000F000Fu>(w), 0x3C003C00u, 0xE400E400u);
+  pr[1] = hfma2_u32(mask_magic<0x00F000F0u>(w), 0x2C002C00u, 0xD400D400u);
+  const uint32_t w2 = w >> 8;
+  pr[2] = hfma2_u32(mask_magic<0x000F000Fu>(w2), 0x3C003C00u, 0xE400E400u);
+  pr[3] = hfma2_u32(mask_magic<0x00F000F0u>(w2), 0x2C002C00u, 0xD400D400u);
+}
 __device__ __forceinline__ uint32_t fix1024(uint32_t bits_with_magic) {
-  __half2 h = *reinterpret_cast<__half2*>(&bits_with_magic);
-  h = __hsub2(h, __half2half2(__ushort_as_half(0x6400)));
-  return *reinterpret_cast<uint32_t*>(&h);
+  return hfma2_u32(bits_with_magic, 0x3C003C00u, 0xE400E400u);
 }
 
-// K side: the 16 channels [gr*64 + tig*16, +16) of one token row -> 8 pairs.
-// Pair p holds local channels (ca(p), cb(p)) in its (low, high) halves.
+// K side: the 16 channels [gr*64 + tig*16, +16) of one token row (at smem address
+// `addr`) -> 8 pairs; pair p holds local channels (ca(p), cb(p)) in its (low, high) halves.
 template <int BITS>
-__device__ __forceinline__ void unpack_k16(uint32_t srow, int gr, int tig, uint32_t (&pr)[8]) {
+__device__ __forceinline__ void unpack_k16(uint32_t addr, uint32_t (&pr)[8]) {
   if constexpr (BITS == 2) {
-    const uint32_t w = lds32(srow + gr * 16 + tig * 4);
-#pragma unroll
-    for (int p = 0; p < 8; ++p) pr[p] = fix1024(((w >> (2 * p)) & 0x00030003u) | 0x64006400u);
+    unpack_int2_word(lds32(addr), pr);
   } else if constexpr (BITS == 4) {
-    const uint2 w = lds64(srow + gr * 32 + tig * 8);
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      pr[p] = fix1024(((w.x >> (4 * p)) & 0x000F000Fu) | 0x64006400u);
-      pr[p + 4] = fix1024(((w.y >> (4 * p)) & 0x000F000Fu) | 0x64006400u);
-    }
+    const uint2 w = lds64(addr);
+    unpack_int4_word(w.x, pr);
+    unpack_int4_word(w.y, pr + 4);
   } else {
-    const uint4 w = lds128(srow + gr * 64 + tig * 16);
+    const uint4 w = lds128(addr);
     const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -142,35 +207,29 @@ __device__ __forceinline__ void unpack_k16(uint32_t srow, int gr, int tig, uint3
     }
   }
 }
+// INT4 word pairs: (w & 0xF..) -> codes (0, 4), (w & 0xF0..) -> (1, 5), then after >> 8:
+// (2, 6), (3, 7); the second word adds 8.
 template <int BITS>
 __host__ __device__ constexpr int k_ca(int p) {
-  return BITS == 2 ? p : (BITS == 4 ? (p < 4 ? p : p + 4) : 2 * p);
+  return BITS == 2 ? p : (BITS == 4 ? (p & 3) + (p >> 2) * 8 : 2 * p);
 }
 template <int BITS>
 __host__ __device__ constexpr int k_cb(int p) {
-  return BITS == 2 ? p + 8 : (BITS == 4 ? (p < 4 ? p + 4 : p + 8) : 2 * p + 1);
+  return BITS == 2 ? p + 8 : (BITS == 4 ? (p & 3) + 4 + (p >> 2) * 8 : 2 * p + 1);
 }
 
-// V side: the 8 channels [gr*64 + gid*8, +8) of two tokens (ta, tb) -> 8 pairs,
-// pair c = (code[ta][c], code[tb][c]).
+// V side: the 8 channels [gr*64 + gid*8, +8) of two consecutive token rows (at smem
+// addresses aa, ab) -> 8 pairs, pair c = (code[row a][c], code[row b][c]).
 template <int BITS>
-__device__ __forceinline__ void unpack_v8(uint32_t sa, uint32_t sb_, int gr, int gid,
-                                          uint32_t (&pr)[8]) {
+__device__ __forceinline__ void unpack_v8(uint32_t aa, uint32_t ab, uint32_t (&pr)[8]) {
   if constexpr (BITS == 2) {
-    const uint32_t ua = lds16(sa + gr * 16 + gid * 2), ub = lds16(sb_ + gr * 16 + gid * 2);
-    const uint32_t w = ua | (ub << 16);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) pr[c] = fix1024(((w >> (2 * c)) & 0x00030003u) | 0x64006400u);
+    unpack_int2_word(__byte_perm(lds16(aa), lds16(ab), 0x5410), pr);
   } else if constexpr (BITS == 4) {
-    const uint32_t ua = lds32(sa + gr * 32 + gid * 4), ub = lds32(sb_ + gr * 32 + gid * 4);
-    const uint32_t wl = __byte_perm(ua, ub, 0x5410), wh = __byte_perm(ua, ub, 0x7632);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      pr[c] = fix1024(((wl >> (4 * c)) & 0x000F000Fu) | 0x64006400u);
-      pr[c + 4] = fix1024(((wh >> (4 * c)) & 0x000F000Fu) | 0x64006400u);
-    }
+    const uint32_t ua = lds32(aa), ub = lds32(ab);
+    unpack_int4_word(__byte_perm(ua, ub, 0x5410), pr);      // channels 0..3
+    unpack_int4_word(__byte_perm(ua, ub, 0x7632), pr + 4);  // channels 4..7
   } else {
-    const uint2 ua = lds64(sa + gr * 64 + gid * 8), ub = lds64(sb_ + gr * 64 + gid * 8);
+    const uint2 ua = lds64(aa), ub = lds64(ab);
     const uint32_t t0 = __byte_perm(ua.x, ub.x, 0x5140), t1 = __byte_perm(ua.x, ub.x, 0x7362);
     const uint32_t t2 = __byte_perm(ua.y, ub.y, 0x5140), t3 = __byte_perm(ua.y, ub.y, 0x7362);
     pr[0] = fix1024(__byte_perm(t0, 0x64u, 0x4140));
@@ -184,6 +243,21 @@ __device__ __forceinline__ void unpack_v8(uint32_t sa, uint32_t sb_, int gr, int
   }
 }
 
+// 2^x with one MUFU instruction (ex2.approx.ftz: relative error ~2^-22, exp2(-inf) = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+// (hi, lo) fp16 pair with hi + lo carrying ~21 bits of x: hi = x with its low 13
+// mantissa bits cleared (exact in fp16 over the normal range), lo = fp16(x - hi); both
+// packed by a single cvt.
+__device__ __forceinline__ uint32_t split_pack(float x) {
+  const float hi = __uint_as_float(__float_as_uint(x) & 0xffffe000u);
+  const __half2 h = __floats2half2_rn(hi, x - hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 // ---------------------------------------------------------------------------------
 template <int NT>
 struct State {
@@ -193,39 +267,64 @@ struct State {
   float o[NT][8][4];    // PV accumulators: 8 channel tiles x (2 rows x (hi, lo))
 };
 
-// One stage of BITS-format tokens for one warp.
-template <int BITS, int NT>
+// Per-thread byte offsets of the warp's fragments inside a stage tile (sub-tile 0).
+struct FragOffs {
+  uint32_t k0, k1;            // codes: K row gid, groups 0/1; FP16: ldmatrix row offset of K
+  uint32_t va0, va1, vb0, vb1;  // codes: V rows 2tig / 2tig+1, groups 0/1; FP16: va0 for V^T
+};
+
+template <int BITS>
+__device__ __forceinline__ FragOffs frag_offsets(int lane) {
+  using F = Fmt<BITS>;
+  const int gid = lane >> 2, tig = lane & 3;
+  FragOffs f{};
+  if constexpr (BITS == 16) {
+    f.k0 = ((lane & 7) + ((lane >> 3) & 1) * 8) * F::kRS + (lane >> 4) * 16;
+    f.va0 = ((lane & 7) + ((lane >> 4) << 3)) * F::kRS + ((lane >> 3) & 1) * 16;
+  } else {
+    constexpr int TB = 16 * BITS / 8, VB = 8 * BITS / 8;
+    f.k0 = qaddr<BITS>(gid, tig * TB);
+    f.k1 = qaddr<BITS>(gid, F::kGB + tig * TB);
+    f.va0 = qaddr<BITS>(2 * tig, gid * VB);
+    f.va1 = qaddr<BITS>(2 * tig, F::kGB + gid * VB);
+    f.vb0 = qaddr<BITS>(2 * tig + 1, gid * VB);
+    f.vb1 = qaddr<BITS>(2 * tig + 1, F::kGB + gid * VB);
+  }
+  return f;
+}
+
+// One stage of BITS-format tokens for one warp.  The query fragments are pre-scaled by
+// log2(e)/sqrt(D), so the accumulators hold base-2 logits.  FULL: all kST rows valid.
+template <int BITS, int NT, bool FULL>
 __device__ __forceinline__ void compute_stage(uint32_t sb, int nvalid, const uint32_t (&bq)[NT][8][2],
                                               const float (&qsum)[NT][2], State<NT>& st,
                                               float* logit_out, int logit_stride, int rep,
-                                              int lane) {
+                                              int lane, const FragOffs& fo) {
   using F = Fmt<BITS>;
   constexpr int kSub = F::kST / 16;
+  constexpr float kLn2 = 0.6931471805599453f;
   const int gid = lane >> 2, tig = lane & 3;
-  const float kScale = rsqrtf(static_cast<float>(kD));  // 1/sqrt(128), exact power-of-two root
   float x[kSub][NT][2];  // base-2 logits of rows gid, gid+8
 
   // ---- QK^T for every 16-token sub-tile of the stage
 #pragma unroll
   for (int sub = 0; sub < kSub; ++sub) {
-    const int r0 = sub * 16;
+    const uint32_t st_k = sb + sub * 16 * F::kRS;
     if constexpr (!F::kQuant) {
       float acc[NT][4];
 #pragma unroll
       for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        const int row = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int chunk = 2 * s + (lane >> 4);
         uint32_t a0, a1, a2, a3;
-        ldsm_x4(sb + row * F::kRB + ((chunk ^ (row & 7)) << 4), a0, a1, a2, a3);
+        ldsm_x4(st_k + fo.k0 + 32 * s, a0, a1, a2, a3);
 #pragma unroll
         for (int t = 0; t < NT; ++t) mma16816(acc[t], a0, a1, a2, a3, bq[t][s][0], bq[t][s][1]);
       }
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
-        x[sub][t][0] = (acc[t][0] + acc[t][1]) * kScale;
-        x[sub][t][1] = (acc[t][2] + acc[t][3]) * kScale;
+        x[sub][t][0] = acc[t][0] + acc[t][1];
+        x[sub][t][1] = acc[t][2] + acc[t][3];
       }
     } else {
       float acc[NT][2][4];
@@ -236,8 +335,9 @@ __device__ __forceinline__ void compute_stage(uint32_t sb, int nvalid, const uin
 #pragma unroll
       for (int gr = 0; gr < 2; ++gr) {
         uint32_t pa[8], pb[8];
-        unpack_k16<BITS>(sb + (r0 + gid) * F::kRB, gr, tig, pa);
-        unpack_k16<BITS>(sb + (r0 + gid + 8) * F::kRB, gr, tig, pb);
+        const uint32_t ka = st_k + (gr ? fo.k1 : fo.k0);
+        unpack_k16<BITS>(ka, pa);
+        unpack_k16<BITS>(ka + 8 * F::kRS, pb);
 #pragma unroll
         for (int s = 0; s < 4; ++s)
 #pragma unroll
@@ -245,8 +345,8 @@ __device__ __forceinline__ void compute_stage(uint32_t sb, int nvalid, const uin
             mma16816(acc[t][gr], pa[2 * s], pb[2 * s], pa[2 * s + 1], pb[2 * s + 1],
                      bq[t][gr * 4 + s][0], bq[t][gr * 4 + s][1]);
       }
-      const uint2 ma = lds64(sb + F::kOffKM + (r0 + gid) * 8);
-      const uint2 mb = lds64(sb + F::kOffKM + (r0 + gid + 8) * 8);
+      const uint2 ma = lds64(sb + F::kOffKM + (sub * 16 + gid) * 8);
+      const uint2 mb = lds64(sb + F::kOffKM + (sub * 16 + gid + 8) * 8);
       const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(&ma.x));
       const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&ma.y));
       const float2 b0 = __half22float2(*reinterpret_cast<const __half2*>(&mb.x));
@@ -255,8 +355,8 @@ __device__ __forceinline__ void compute_stage(uint32_t sb, int nvalid, const uin
       for (int t = 0; t < NT; ++t) {
         const float da0 = acc[t][0][0] + acc[t][0][1], da1 = acc[t][1][0] + acc[t][1][1];
         const float db0 = acc[t][0][2] + acc[t][0][3], db1 = acc[t][1][2] + acc[t][1][3];
-        x[sub][t][0] = (a0.x * da0 + a1.x * da1 + a0.y * qsum[t][0] + a1.y * qsum[t][1]) * kScale;
-        x[sub][t][1] = (b0.x * db0 + b1.x * db1 + b0.y * qsum[t][0] + b1.y * qsum[t][1]) * kScale;
+        x[sub][t][0] = a0.x * da0 + a1.x * da1 + a0.y * qsum[t][0] + a1.y * qsum[t][1];
+        x[sub][t][1] = b0.x * db0 + b1.x * db1 + b0.y * qsum[t][0] + b1.y * qsum[t][1];
       }
     }
     // natural logits out (important tier) and masking of rows past the end
@@ -265,48 +365,54 @@ __device__ __forceinline__ void compute_stage(uint32_t sb, int nvalid, const uin
       const int head = t * 4 + tig;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int r = r0 + gid + 8 * h;
-        if (r < nvalid) {
-          if (logit_out != nullptr && head < rep) logit_out[head * logit_stride + r] = x[sub][t][h];
-          x[sub][t][h] *= kLog2e;
-        } else {
-          x[sub][t][h] = -INFINITY;
-        }
+        const int r = sub * 16 + gid + 8 * h;
+        const bool valid = FULL || r < nvalid;
+        if (logit_out != nullptr && head < rep && valid)
+          logit_out[head * logit_stride + r] = x[sub][t][h] * kLn2;
+        if (!valid) x[sub][t][h] = -INFINITY;
       }
     }
   }
 
-  // ---- online softmax update (one max per stage)
+  // ---- online softmax update: one max per stage; the accumulators are rescaled only
+  // when some head's running max moved (warp vote)
   float mnew[NT];
+  bool moved = false;
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
-    float mx = -INFINITY;
+    float mx = x[0][t][0];
 #pragma unroll
     for (int sub = 0; sub < kSub; ++sub) mx = fmaxf(mx, fmaxf(x[sub][t][0], x[sub][t][1]));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
     mnew[t] = fmaxf(st.m[t], mx);
-    const float alpha = exp2f(st.m[t] - mnew[t]);  // 0 on the first stage (m = -inf)
-    st.m[t] = mnew[t];
-    st.l[t] *= alpha;
-    st.zs[t][0] *= alpha;
-    st.zs[t][1] *= alpha;
+    moved |= mnew[t] > st.m[t];
+  }
+  if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+    for (int t = 0; t < NT; ++t) {
+      const float alpha = fast_exp2(st.m[t] - mnew[t]);  // 0 on the first stage (m = -inf)
+      st.m[t] = mnew[t];
+      st.l[t] *= alpha;
+      st.zs[t][0] *= alpha;
+      st.zs[t][1] *= alpha;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) st.o[t][j][e] *= alpha;
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) st.o[t][j][e] *= alpha;
+    }
   }
 
   // ---- P V for every sub-tile
 #pragma unroll
   for (int sub = 0; sub < kSub; ++sub) {
-    const int r0 = sub * 16;
+    const uint32_t st_v = sb + F::kOffV + sub * 16 * F::kRS;
     float p[NT][2];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-      p[t][0] = exp2f(x[sub][t][0] - mnew[t]);
-      p[t][1] = exp2f(x[sub][t][1] - mnew[t]);
+      p[t][0] = fast_exp2(x[sub][t][0] - mnew[t]);
+      p[t][1] = fast_exp2(x[sub][t][1] - mnew[t]);
       st.l[t] += p[t][0] + p[t][1];
     }
     if constexpr (!F::kQuant) {
@@ -314,25 +420,19 @@ __device__ __forceinline__ void compute_stage(uint32_t sb, int nvalid, const uin
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          __half hi, lo;
-          split_f16(p[t][h], hi, lo);
-          bp[t][h] = movmatrix_t(pack_half2(hi, lo));
-        }
+        for (int h = 0; h < 2; ++h) bp[t][h] = movmatrix_t(split_pack(p[t][h]));
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const int row = r0 + (lane & 7) + ((lane >> 4) << 3);
-        const int chunk = 2 * j + ((lane >> 3) & 1);
         uint32_t a0, a1, a2, a3;
-        ldsm_x4_t(sb + F::kOffV + row * F::kRB + ((chunk ^ (row & 7)) << 4), a0, a1, a2, a3);
+        ldsm_x4_t(st_v + fo.va0 + 32 * j, a0, a1, a2, a3);
 #pragma unroll
         for (int t = 0; t < NT; ++t) mma16816(st.o[t][j], a0, a1, a2, a3, bp[t][0], bp[t][1]);
       }
     } else {
       // value scale/zero of rows gid, gid+8 for both groups
-      const uint2 ma = lds64(sb + F::kOffVM + (r0 + gid) * 8);
-      const uint2 mb = lds64(sb + F::kOffVM + (r0 + gid + 8) * 8);
+      const uint2 ma = lds64(sb + F::kOffVM + (sub * 16 + gid) * 8);
+      const uint2 mb = lds64(sb + F::kOffVM + (sub * 16 + gid + 8) * 8);
       const float2 va[2] = {__half22float2(*reinterpret_cast<const __half2*>(&ma.x)),
                             __half22float2(*reinterpret_cast<const __half2*>(&ma.y))};
       const float2 vb[2] = {__half22float2(*reinterpret_cast<const __half2*>(&mb.x)),
@@ -343,22 +443,16 @@ __device__ __forceinline__ void compute_stage(uint32_t sb, int nvalid, const uin
 #pragma unroll
         for (int gr = 0; gr < 2; ++gr) {
           st.zs[t][gr] += p[t][0] * va[gr].y + p[t][1] * vb[gr].y;
-          __half hi, lo;
-          split_f16(p[t][0] * va[gr].x, hi, lo);
-          bp[t][gr][0] = movmatrix_t(pack_half2(hi, lo));
-          split_f16(p[t][1] * vb[gr].x, hi, lo);
-          bp[t][gr][1] = movmatrix_t(pack_half2(hi, lo));
+          bp[t][gr][0] = movmatrix_t(split_pack(p[t][0] * va[gr].x));
+          bp[t][gr][1] = movmatrix_t(split_pack(p[t][1] * vb[gr].x));
         }
       }
-      const uint32_t s01a = sb + F::kOffV + (r0 + 2 * tig) * F::kRB;
-      const uint32_t s01b = s01a + F::kRB;
-      const uint32_t s89a = sb + F::kOffV + (r0 + 2 * tig + 8) * F::kRB;
-      const uint32_t s89b = s89a + F::kRB;
 #pragma unroll
       for (int gr = 0; gr < 2; ++gr) {
         uint32_t v01[8], v89[8];
-        unpack_v8<BITS>(s01a, s01b, gr, gid, v01);
-        unpack_v8<BITS>(s89a, s89b, gr, gid, v89);
+        const uint32_t aa = st_v + (gr ? fo.va1 : fo.va0), ab = st_v + (gr ? fo.vb1 : fo.vb0);
+        unpack_v8<BITS>(aa, ab, v01);
+        unpack_v8<BITS>(aa + 8 * F::kRS, ab + 8 * F::kRS, v89);
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
@@ -377,21 +471,18 @@ __device__ __forceinline__ int out_channel(int j, int gid, int h) {
   else return (j >> 2) * 64 + gid * 8 + 4 * h + (j & 3);
 }
 
-// Build the query fragments of this CTA's tier: columns (head, hi|lo) of n-tile t.
+// Build the query fragments of this CTA's tier: columns (head, hi|lo) of n-tile t, read
+// from the staged (hi, lo) fp16 pairs; qsum from the staged per-(head, group) sums.
 template <int BITS, int NT>
-__device__ __forceinline__ void build_q(const float* qs /*smem [8][kD]*/, int rep, int lane,
+__device__ __forceinline__ void build_q(const uint32_t* qhl /*smem [8][kD] (hi,lo) pairs*/,
+                                        const float* qgs /*smem [8][2]*/, int lane,
                                         uint32_t (&bq)[NT][8][2], float (&qsum)[NT][2]) {
   const int gid = lane >> 2, tig = lane & 3;
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
     const int head = t * 4 + (gid >> 1);
-    const bool part_lo = gid & 1;
-    auto val = [&](int c) -> __half {
-      const float x = head < rep ? qs[head * kD + c] : 0.f;
-      __half hi, lo;
-      split_f16(x, hi, lo);
-      return part_lo ? lo : hi;
-    };
+    const int shift = (gid & 1) * 16;  // hi part in the low half, lo part in the high half
+    const uint32_t* row = qhl + head * kD;
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
       int c0, c1, c2, c3;
@@ -407,18 +498,11 @@ __device__ __forceinline__ void build_q(const float* qs /*smem [8][kD]*/, int re
         c2 = base + k_ca<BITS>(2 * sp + 1);
         c3 = base + k_cb<BITS>(2 * sp + 1);
       }
-      bq[t][s][0] = pack_half2(val(c0), val(c1));
-      bq[t][s][1] = pack_half2(val(c2), val(c3));
+      bq[t][s][0] = ((row[c0] >> shift) & 0xffffu) | (((row[c1] >> shift) & 0xffffu) << 16);
+      bq[t][s][1] = ((row[c2] >> shift) & 0xffffu) | (((row[c3] >> shift) & 0xffffu) << 16);
     }
-    // per-group query sums for the zero-point term (thread's own head t*4+tig)
-    const int myhead = t * 4 + tig;
-#pragma unroll
-    for (int gr = 0; gr < 2; ++gr) {
-      float sum = 0.f;
-      if (myhead < rep)
-        for (int c = 0; c < kGS; ++c) sum += qs[myhead * kD + gr * kGS + c];
-      qsum[t][gr] = sum;
-    }
+    qsum[t][0] = qgs[(t * 4 + tig) * 2];
+    qsum[t][1] = qgs[(t * 4 + tig) * 2 + 1];
   }
 }
 
@@ -430,20 +514,40 @@ __device__ void run_tier(const Params& P, const TierPtrs& tier, int unit, int sp
   const int b = unit / P.Hkv, g = unit % P.Hkv;
   const int rep = P.rep;
 
-  // query (balanced for quantised tiers) staged in shared memory as fp32
-  for (int i = threadIdx.x; i < 8 * kD; i += kThreads) {
-    const int h = i / kD, c = i % kD;
-    float x = 0.f;
-    if (h < rep) {
-      x = __half2float(P.q[(static_cast<long>(b) * P.Hq + g * rep + h) * kD + c]);
-      if (F::kQuant && P.bal) x = __fdiv_rn(x, P.bal[static_cast<long>(unit) * kD + c]);
+  // query (balanced for quantised tiers, pre-scaled so logits come out of the mma in base-2
+  // units) staged as (hi, lo) fp16 pairs, plus its per-(head, group) sums for the zero-point
+  // term: thread i handles channels 8*(i%16) .. +8 of head i/16.
+  uint32_t* qhl = reinterpret_cast<uint32_t*>(qs);   // [8][kD]
+  float* qgs = qs + 8 * kD;                          // [8][2]
+  {
+    const int h = threadIdx.x >> 4, c0 = (threadIdx.x & 15) * 8;
+    float part = 0.f;
+#pragma unroll
+    for (int h2 = 0; h2 < 8; h2 += kThreads / 16) {
+      const int hh = h + h2;
+      part = 0.f;
+#pragma unroll
+      for (int c = c0; c < c0 + 8; ++c) {
+        float x = 0.f;
+        if (hh < rep) {
+          x = __half2float(P.q[(static_cast<long>(b) * P.Hq + g * rep + hh) * kD + c]);
+          if (F::kQuant && P.bal) x = __fdiv_rn(x, P.bal[static_cast<long>(unit) * kD + c]);
+          x *= kLogitScale;
+        }
+        qhl[hh * kD + c] = split_pack(x);
+        part += x;
+      }
+      // 8 lanes per 64-channel group: reduce, lane 0 of each octet stores
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+      part += __shfl_xor_sync(0xffffffffu, part, 4);
+      if ((threadIdx.x & 7) == 0) qgs[hh * 2 + ((threadIdx.x >> 3) & 1)] = part;
     }
-    qs[i] = x;
   }
   __syncthreads();
   uint32_t bq[NT][8][2];
   float qsum[NT][2];
-  build_q<BITS, NT>(qs, rep, lane, bq, qsum);
+  build_q<BITS, NT>(qhl, qgs, lane, bq, qsum);
 
   State<NT> st;
 #pragma unroll
@@ -468,13 +572,16 @@ __device__ void run_tier(const Params& P, const TierPtrs& tier, int unit, int sp
   if (is_hi && P.hi_logits)
     lrow = P.hi_logits + (static_cast<long>(b) * P.Hq + g * rep) * tier.cap;
 
+  const FragOffs fo = frag_offsets<BITS>(lane);
   // warp w handles stages w, w+4, ...
   int issued = 0;
   auto issue = [&](int k) {  // k-th stage of this warp
     const int sidx = warp + k * kWarps;
     if (sidx < nst) {
       const int tok0 = t_begin + sidx * F::kST;
-      load_stage<BITS>(ring_s + (k % kStages) * F::kStageBytes, tier, row_base + tok0,
+      const long row = row_base + tok0;
+      load_stage<BITS>(ring_s + (k % kStages) * F::kStageBytes, tier.k + row * F::kRB,
+                       tier.v + row * F::kRB, tier.km + row * 8, tier.vm + row * 8,
                        min(F::kST, t_end - tok0), lane);
     }
     cp_async_commit();
@@ -485,8 +592,11 @@ __device__ void run_tier(const Params& P, const TierPtrs& tier, int unit, int sp
     cp_async_wait<kStages - 1>();
     __syncwarp();
     const int tok0 = t_begin + (warp + k * kWarps) * F::kST;
-    compute_stage<BITS, NT>(ring_s + (k % kStages) * F::kStageBytes, min(F::kST, t_end - tok0), bq,
-                            qsum, st, lrow ? lrow + tok0 : nullptr, tier.cap, rep, lane);
+    const int nv = min(F::kST, t_end - tok0);
+    const uint32_t sb = ring_s + (k % kStages) * F::kStageBytes;
+    float* lo = lrow ? lrow + tok0 : nullptr;
+    if (nv == F::kST) compute_stage<BITS, NT, true>(sb, nv, bq, qsum, st, lo, tier.cap, rep, lane, fo);
+    else compute_stage<BITS, NT, false>(sb, nv, bq, qsum, st, lo, tier.cap, rep, lane, fo);
     __syncwarp();
   }
   cp_async_wait<0>();
@@ -556,22 +666,19 @@ __device__ void run_tier(const Params& P, const TierPtrs& tier, int unit, int sp
 template <int HI, int LO, int NT>
 __global__ void __launch_bounds__(kThreads) decode_partial_kernel(Params P) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ float qs[8 * kD];
+  __shared__ __align__(16) float qs[8 * kD + 16];
   const int unit = blockIdx.y;
   const int sx = blockIdx.x;
   if (sx < P.nsplit_hi) run_tier<HI, NT>(P, P.hi, unit, sx, P.chunk_hi, true, smem, qs);
   else run_tier<LO, NT>(P, P.lo, unit, sx - P.nsplit_hi, P.chunk_lo, false, smem, qs);
 }
 
-// K8: merge the split partials (base-2 max m, sum l, unnormalised o) of one query head.
-__global__ void __launch_bounds__(kD) decode_merge_kernel(const float* __restrict__ ws_o,
-                                                          const float* __restrict__ ws_ml,
-                                                          int smax, int nsplit,
-                                                          float* __restrict__ out,
-                                                          float* __restrict__ lse) {
-  const int row = blockIdx.x;  // b*Hq + h
-  const int c = threadIdx.x;
-  const float* ml = ws_ml + static_cast<long>(row) * smax * 2;
+// K8: merge the split partials (base-2 max m, sum l, unnormalised o) of one query head
+// (row = b*Hq + h), thread c = channel; returns the row's natural log-sum-exp.
+__device__ __forceinline__ float merge_head(const float* __restrict__ ws_o,
+                                           const float* __restrict__ ws_ml, int smax, int nsplit,
+                                           long row, int c, float* __restrict__ out) {
+  const float* ml = ws_ml + row * smax * 2;
   float M = -INFINITY;
   for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ml[2 * s]);
   float L = 0.f, O = 0.f;
@@ -579,10 +686,92 @@ __global__ void __launch_bounds__(kD) decode_merge_kernel(const float* __restric
     const float ms = ml[2 * s];
     const float sc = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
     L += sc * ml[2 * s + 1];
-    O += sc * ws_o[(static_cast<long>(row) * smax + s) * kD + c];
+    O += sc * ws_o[(row * smax + s) * kD + c];
   }
-  out[static_cast<long>(row) * kD + c] = O / L;
-  if (c == 0) lse[row] = (M + log2f(L)) * 0.69314718055994531f;
+  out[row * kD + c] = O / L;
+  return (M + log2f(L)) * 0.69314718055994531f;
+}
+
+__global__ void __launch_bounds__(kD) decode_merge_kernel(const float* __restrict__ ws_o,
+                                                          const float* __restrict__ ws_ml,
+                                                          int smax, int nsplit,
+                                                          float* __restrict__ out,
+                                                          float* __restrict__ lse) {
+  const long row = blockIdx.x;
+  const float l = merge_head(ws_o, ws_ml, smax, nsplit, row, threadIdx.x, out);
+  if (threadIdx.x == 0) lse[row] = l;
+}
+
+// Fused end of a decode step, one CTA per (batch, key head): merge the split partials of
+// the group's query heads (as decode_merge_kernel), add this step's attention to the H2O
+// score of every important slot (as the decode score update), and, when the important
+// tier is over budget, pick the victim (score ascending, position descending, among
+// positions < limit) and demote it (as the separate demotion calls).  The arithmetic of
+// every part is the same code as its separate kernel, so results are identical.
+struct EpiArgs {
+  const float* ws_o;
+  const float* ws_ml;
+  int smax, nsplit;
+  float* out;
+  float* lse;
+  const float* logits;  // [B][Hq][cap_hi]
+  int Hq, Hkv, rep;
+  int demote, limit;
+  DemoteArgs da;        // counts after this step's append
+};
+
+__global__ void __launch_bounds__(kD) decode_epilogue_kernel(EpiArgs a) {
+  __shared__ float s_lse[8];
+  __shared__ float rs[kD];
+  __shared__ int rp[kD], rj[kD];
+  const long unit = blockIdx.x;
+  const int b = static_cast<int>(unit / a.Hkv), g = static_cast<int>(unit % a.Hkv);
+  const int c = threadIdx.x;
+  const long row0 = static_cast<long>(b) * a.Hq + static_cast<long>(g) * a.rep;
+  for (int h = 0; h < a.rep; ++h) {
+    const float l = merge_head(a.ws_o, a.ws_ml, a.smax, a.nsplit, row0 + h, c, a.out);
+    if (c == 0) {
+      a.lse[row0 + h] = l;
+      s_lse[h] = l;
+    }
+  }
+  __syncthreads();
+  const int cap = a.da.cap_hi, n = a.da.n_hi;
+  float bs = INFINITY;
+  int bp = -1, bj = -1;
+  for (int j = c; j < n; j += kD) {
+    float add = 0.f;
+    for (int r = 0; r < a.rep; ++r) add += expf(a.logits[(row0 + r) * cap + j] - s_lse[r]);
+    const long idx = unit * cap + j;
+    const float sv = a.da.scores[idx] + add;
+    a.da.scores[idx] = sv;
+    if (a.demote) {
+      const int p = a.da.pos_hi[idx];
+      if (p < a.limit && (bj < 0 || sv < bs || (sv == bs && p > bp))) {
+        bs = sv;
+        bp = p;
+        bj = j;
+      }
+    }
+  }
+  if (!a.demote) return;
+  rs[c] = bs;
+  rp[c] = bp;
+  rj[c] = bj;
+  __syncthreads();
+  for (int o = kD / 2; o > 0; o >>= 1) {
+    if (c < o) {
+      const int t = c + o;
+      const bool better = rj[t] >= 0 && (rj[c] < 0 || rs[t] < rs[c] || (rs[t] == rs[c] && rp[t] > rp[c]));
+      if (better) {
+        rs[c] = rs[t];
+        rp[c] = rp[t];
+        rj[c] = rj[t];
+      }
+    }
+    __syncthreads();
+  }
+  if (c < 32) demote_one(a.da, unit, rj[0], c);
 }
 
 // ---------------------------------------------------------------------------------
@@ -596,20 +785,22 @@ struct Plan {
 };
 
 Plan make_plan(const mikv_cache* c) {
-  // chunk sizes from the capacities, so the workspace fits every count <= capacity
+  // From the capacities (so the workspace fits every count up to them): a target of
+  // ~5 waves of 3 CTAs per SM, each tier cut into equal chunks of whole warp-stages.
   const double units = static_cast<double>(c->B) * c->Hkv;
-  const double total = units * (static_cast<double>(c->cap_hi) * row_cost(c->hi_bits) +
-                                 static_cast<double>(c->cap_lo) * row_cost(c->lo_bits));
-  double target = total / (kNumSMs * 2.0 * 6.0);       // ~6 waves of 2 CTAs per SM
-  target = std::min(std::max(target, 16.0 * 1024), 192.0 * 1024);
-  auto chunk_for = [&](int bits) {
-    int per_warp = static_cast<int>(target / (kWarps * stage_bytes(bits)) + 0.5);
-    per_warp = std::max(per_warp, 1);
-    return per_warp * kWarps * stage_tokens(bits);
+  const double hi_b = static_cast<double>(c->cap_hi) * row_cost(c->hi_bits);
+  const double lo_b = static_cast<double>(c->cap_lo) * row_cost(c->lo_bits);
+  double target = units * (hi_b + lo_b) / (kNumSMs * 3.0 * 5.0);
+  target = std::min(std::max(target, 32.0 * 1024), 384.0 * 1024);
+  auto chunk_for = [&](int cap, double bytes, int bits) {
+    const int quantum = kWarps * stage_tokens(bits);
+    const int ns = std::max(1, static_cast<int>(bytes / target + 0.5));
+    int chunk = (std::max(cap, 1) + ns - 1) / ns;
+    return std::max(quantum, (chunk + quantum - 1) / quantum * quantum);
   };
   Plan p;
-  p.chunk_hi = chunk_for(c->hi_bits);
-  p.chunk_lo = chunk_for(c->lo_bits);
+  p.chunk_hi = chunk_for(c->cap_hi, hi_b, c->hi_bits);
+  p.chunk_lo = chunk_for(c->cap_lo, lo_b, c->lo_bits);
   p.smax_hi = (c->cap_hi + p.chunk_hi - 1) / p.chunk_hi;
   p.smax_lo = (c->cap_lo + p.chunk_lo - 1) / p.chunk_lo;
   return p;
@@ -642,26 +833,29 @@ extern "C" size_t mikv_decode_workspace_bytes(const mikv_cache* c) {
   return align_up(rows * kD * sizeof(float), 256) + align_up(rows * 2 * sizeof(float), 256);
 }
 
-extern "C" int mikv_decode_attention(const uint16_t* q, const mikv_cache* c, float* out,
-                                     float* lse, float* hi_logits, void* ws, size_t ws_bytes,
-                                     void* stream) {
-  clear_error();
-  if (int e = validate_cache_public(c, "decode_attention")) return e;
-  if (!q || !out || !lse || !ws) return fail(MIKV_EINVAL, "decode_attention: null pointer");
-  if (c->n_hi + c->n_lo < 1) return fail(MIKV_ESHAPE, "decode_attention: empty cache");
+namespace mikv {
+int append_tokens(bool hi, const uint16_t* k, const uint16_t* v, int src_len, const int32_t* src_pos,
+                  int n_tokens, int pos_base, const float* src_scores, const mikv_cache* c,
+                  cudaStream_t s);
+int demote_args(const mikv_cache* c, const int32_t* victim, DemoteArgs& a);
+
+namespace {
+// Validate the cache for attention and fill the partial-kernel parameters.
+int prepare_decode(const uint16_t* q, const mikv_cache* c, float* hi_logits, void* ws,
+                   size_t ws_bytes, Params& P, int& nsplit, const char* who) {
+  if (c->n_hi + c->n_lo < 1) return fail(MIKV_ESHAPE, "%s: empty cache", who);
   if (c->n_hi > 0 && (!c->k_hi || !c->v_hi || (c->hi_bits == 8 && (!c->k_hi_meta || !c->v_hi_meta))))
-    return fail(MIKV_EINVAL, "decode_attention: null hi-tier buffer");
+    return fail(MIKV_EINVAL, "%s: null hi-tier buffer", who);
   if (c->n_lo > 0 && (!c->k_lo || !c->v_lo || !c->k_lo_meta || !c->v_lo_meta))
-    return fail(MIKV_EINVAL, "decode_attention: null lo-tier buffer");
+    return fail(MIKV_EINVAL, "%s: null lo-tier buffer", who);
   const void* al[] = {c->k_hi, c->v_hi, c->k_hi_meta, c->v_hi_meta, c->k_lo,
                       c->v_lo, c->k_lo_meta, c->v_lo_meta, ws};
   for (const void* p : al)
-    if (p && !aligned16(p)) return fail(MIKV_EALIGN, "decode_attention: cache/ws not 16-byte aligned");
+    if (p && !aligned16(p)) return fail(MIKV_EALIGN, "%s: cache/ws not 16-byte aligned", who);
   const size_t need = mikv_decode_workspace_bytes(c);
-  if (ws_bytes < need) return fail(MIKV_ESHAPE, "decode_attention: workspace %zu < %zu", ws_bytes, need);
-
+  if (ws_bytes < need) return fail(MIKV_ESHAPE, "%s: workspace %zu < %zu", who, ws_bytes, need);
   const Plan pl = make_plan(c);
-  Params P{};
+  P = Params{};
   P.q = reinterpret_cast<const __half*>(q);
   P.bal = c->balancer;
   P.hi = TierPtrs{static_cast<const uint8_t*>(c->k_hi), static_cast<const uint8_t*>(c->v_hi),
@@ -682,20 +876,110 @@ extern "C" int mikv_decode_attention(const uint16_t* q, const mikv_cache* c, flo
   const size_t rows = static_cast<size_t>(c->B) * c->Hq * P.smax;
   P.ws_o = static_cast<float*>(ws);
   P.ws_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + align_up(rows * kD * sizeof(float), 256));
-  const int nsplit = P.nsplit_hi + nsplit_lo;
-  dim3 grid(nsplit, c->B * c->Hkv);
-  cudaStream_t s = as_stream(stream);
-  int e;
+  nsplit = P.nsplit_hi + nsplit_lo;
+  if (c->hi_bits * 100 + c->lo_bits != 1602 && c->hi_bits * 100 + c->lo_bits != 1604 &&
+      c->hi_bits * 100 + c->lo_bits != 1608 && c->hi_bits * 100 + c->lo_bits != 802 &&
+      c->hi_bits * 100 + c->lo_bits != 804 && c->hi_bits * 100 + c->lo_bits != 808)
+    return fail(MIKV_EUNSUPPORTED, "%s: bits %d/%d", who, c->hi_bits, c->lo_bits);
+  return MIKV_OK;
+}
+
+int launch_partials(const Params& P, const mikv_cache* c, int nsplit, cudaStream_t s) {
+  const dim3 grid(nsplit, c->B * c->Hkv);
   switch (c->hi_bits * 100 + c->lo_bits) {
-    case 1602: e = launch_nt<16, 2>(P, grid, s); break;
-    case 1604: e = launch_nt<16, 4>(P, grid, s); break;
-    case 1608: e = launch_nt<16, 8>(P, grid, s); break;
-    case 802: e = launch_nt<8, 2>(P, grid, s); break;
-    case 804: e = launch_nt<8, 4>(P, grid, s); break;
-    case 808: e = launch_nt<8, 8>(P, grid, s); break;
-    default: return fail(MIKV_EUNSUPPORTED, "decode_attention: bits %d/%d", c->hi_bits, c->lo_bits);
+    case 1602: return launch_nt<16, 2>(P, grid, s);
+    case 1604: return launch_nt<16, 4>(P, grid, s);
+    case 1608: return launch_nt<16, 8>(P, grid, s);
+    case 802: return launch_nt<8, 2>(P, grid, s);
+    case 804: return launch_nt<8, 4>(P, grid, s);
+    default: return launch_nt<8, 8>(P, grid, s);
   }
-  if (e) return e;
+}
+
+int n_keep_of(int L, int pct, int window) {
+  const long p = static_cast<long>(pct) * L / 100;
+  return static_cast<int>(std::min<long>(L, std::max<long>(window, p)));
+}
+}  // namespace
+}  // namespace mikv
+
+extern "C" int mikv_decode_attention(const uint16_t* q, const mikv_cache* c, float* out,
+                                     float* lse, float* hi_logits, void* ws, size_t ws_bytes,
+                                     void* stream) {
+  clear_error();
+  if (int e = validate_cache_public(c, "decode_attention")) return e;
+  if (!q || !out || !lse || !ws) return fail(MIKV_EINVAL, "decode_attention: null pointer");
+  Params P;
+  int nsplit = 0;
+  if (int e = prepare_decode(q, c, hi_logits, ws, ws_bytes, P, nsplit, "decode_attention")) return e;
+  cudaStream_t s = as_stream(stream);
+  if (int e = launch_partials(P, c, nsplit, s)) return e;
   decode_merge_kernel<<<c->B * c->Hq, kD, 0, s>>>(P.ws_o, P.ws_ml, P.smax, nsplit, out, lse);
   return check_launch("decode_merge_kernel");
+}
+
+extern "C" size_t mikv_decode_step_workspace_bytes(const mikv_cache* c) {
+  const size_t a = mikv_decode_workspace_bytes(c);
+  if (a == 0) return 0;
+  return a + align_up(static_cast<size_t>(c->B) * c->Hq * c->cap_hi * sizeof(float), 256);
+}
+
+extern "C" int mikv_decode_step(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                                int pos, int budget_pct, int window, int policy, mikv_cache* c,
+                                float* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  clear_error();
+  if (int e = validate_cache_public(c, "decode_step")) return e;
+  if (!q || !k_new || !v_new || !out || !lse || !ws) return fail(MIKV_EINVAL, "decode_step: null pointer");
+  if (policy != MIKV_H2O && policy != MIKV_CRITICALKV) return fail(MIKV_EINVAL, "decode_step: policy %d", policy);
+  if (pos < 0 || budget_pct < 0 || budget_pct > 100 || window < 0)
+    return fail(MIKV_ESHAPE, "decode_step: pos=%d budget_pct=%d window=%d", pos, budget_pct, window);
+  if (c->n_hi + 1 > c->cap_hi) return fail(MIKV_ESHAPE, "decode_step: important tier full (%d)", c->cap_hi);
+  const size_t need = mikv_decode_step_workspace_bytes(c);
+  if (ws_bytes < need) return fail(MIKV_ESHAPE, "decode_step: workspace %zu < %zu", ws_bytes, need);
+  const int L = pos + 1;
+  const bool demote = policy == MIKV_H2O && c->n_hi + 1 > n_keep_of(L, budget_pct, window);
+  mikv_cache after = *c;  // counts once the new token is appended
+  after.n_hi += 1;
+  DemoteArgs da;
+  if (int e = demote_args(&after, nullptr, da)) {
+    if (demote) return e;
+    da = DemoteArgs{};
+    da.cap_hi = after.cap_hi;
+    da.n_hi = after.n_hi;
+    da.scores = after.scores;
+    da.pos_hi = after.pos_hi;
+  }
+  const size_t dec_ws = mikv_decode_workspace_bytes(c);
+  float* logits = reinterpret_cast<float*>(static_cast<char*>(ws) + dec_ws);
+  Params P;
+  int nsplit = 0;
+  if (int e = prepare_decode(q, &after, logits, ws, dec_ws, P, nsplit, "decode_step")) return e;
+  cudaStream_t s = as_stream(stream);
+  // 1. the new token joins the important tier at slot n_hi (position pos, score 0)
+  if (int e = append_tokens(true, k_new, v_new, 1, nullptr, 1, pos, nullptr, c, s)) return e;
+  c->n_hi += 1;
+  // 2. split-K attention over both tiers
+  if (int e = launch_partials(P, &after, nsplit, s)) return e;
+  // 3. merge + score update + demotion
+  EpiArgs ea{};
+  ea.ws_o = P.ws_o;
+  ea.ws_ml = P.ws_ml;
+  ea.smax = P.smax;
+  ea.nsplit = nsplit;
+  ea.out = out;
+  ea.lse = lse;
+  ea.logits = logits;
+  ea.Hq = c->Hq;
+  ea.Hkv = c->Hkv;
+  ea.rep = c->Hq / c->Hkv;
+  ea.demote = demote ? 1 : 0;
+  ea.limit = L - window;
+  ea.da = da;
+  decode_epilogue_kernel<<<c->B * c->Hkv, kD, 0, s>>>(ea);
+  if (int e = check_launch("decode_epilogue_kernel")) return e;
+  if (demote) {
+    c->n_hi -= 1;
+    c->n_lo += 1;
+  }
+  return MIKV_OK;
 }

@@ -15,63 +15,10 @@
 // Codes are packed LSB-first (channel c at bit c*bits of the row), meta is the
 // fp16 pair (scale, zero) per group.  HBM-bound: 512 B read per token-head,
 // 80/144/272/512 B written.
-#include "common.cuh"
+#include "quant_device.cuh"
 
 namespace mikv {
 namespace {
-
-struct Row4 {
-  float x[4];
-};
-
-__device__ __forceinline__ Row4 load_fp16x4(const __half* p) {
-  uint2 u = *reinterpret_cast<const uint2*>(p);
-  __half2 a = *reinterpret_cast<__half2*>(&u.x), b = *reinterpret_cast<__half2*>(&u.y);
-  Row4 r;
-  r.x[0] = __low2float(a);
-  r.x[1] = __high2float(a);
-  r.x[2] = __low2float(b);
-  r.x[3] = __high2float(b);
-  return r;
-}
-
-// Quantise the 4 channels this lane owns (its half-warp is one group); returns the
-// codes packed LSB-first in a 32-bit word (bits*4 significant bits) and the meta pair.
-__device__ __forceinline__ uint32_t quantize4(const Row4& r, int bits, uint32_t& meta) {
-  float mn = fminf(fminf(r.x[0], r.x[1]), fminf(r.x[2], r.x[3]));
-  float mx = fmaxf(fmaxf(r.x[0], r.x[1]), fmaxf(r.x[2], r.x[3]));
-#pragma unroll
-  for (int o = 8; o >= 1; o >>= 1) {
-    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  }
-  const int qmax = (1 << bits) - 1;
-  const float s32 = __fdiv_rn(__fsub_rn(mx, mn), static_cast<float>(qmax));
-  const __half sh = __float2half_rn(s32), zh = __float2half_rn(mn);
-  const float sf = __half2float(sh), zf = __half2float(zh);
-  meta = pack_half2(sh, zh);
-  uint32_t packed = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    int c = 0;
-    if (sf != 0.f) {
-      c = __float2int_rn(__fdiv_rn(__fsub_rn(r.x[i], zf), sf));
-      c = min(max(c, 0), qmax);
-    }
-    packed |= static_cast<uint32_t>(c) << (i * bits);
-  }
-  return packed;
-}
-
-__device__ __forceinline__ void store_codes(uint8_t* row, int lane, int bits, uint32_t packed) {
-  if (bits == 2) row[lane] = static_cast<uint8_t>(packed);
-  else if (bits == 4) reinterpret_cast<uint16_t*>(row)[lane] = static_cast<uint16_t>(packed);
-  else reinterpret_cast<uint32_t*>(row)[lane] = packed;
-}
-
-__device__ __forceinline__ void store_meta(__half2* meta_row, int lane, uint32_t meta) {
-  if ((lane & 15) == 0) reinterpret_cast<uint32_t*>(meta_row)[lane >> 4] = meta;
-}
 
 struct AppendArgs {
   const __half* k;        // [B][Hkv][src_len][D]
@@ -96,7 +43,7 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
   if (item >= a.units_tokens) return;
   const long unit = item / a.n_tokens;
   const int j = static_cast<int>(item % a.n_tokens);
-  const int src = a.src_pos[item];
+  const int src = a.src_pos ? a.src_pos[item] : j;  // no list: token j of the source
   if (src < 0 || src >= a.src_len) return;  // out-of-range source: slot left unchanged
   const long slot = unit * a.cap + a.base_slot + j;
   const __half* ks = a.k + (unit * a.src_len + src) * kD + lane * 4;
@@ -128,82 +75,11 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
   }
 }
 
-struct DemoteArgs {
-  const int32_t* victim;  // [B*Hkv]
-  const float* bal;
-  int units, hi_bits, lo_bits, cap_hi, cap_lo, n_hi, n_lo;
-  uint8_t *k_hi, *v_hi;
-  __half2 *k_hi_meta, *v_hi_meta;
-  uint8_t *k_lo, *v_lo;
-  __half2 *k_lo_meta, *v_lo_meta;
-  int32_t *pos_hi, *pos_lo;
-  float* scores;
-};
-
-__device__ __forceinline__ Row4 dequant_int8x4(const uint8_t* row, const __half2* meta, int lane) {
-  const uint32_t w = reinterpret_cast<const uint32_t*>(row)[lane];
-  const __half2 m = meta[lane >> 4];
-  const float sf = __low2float(m), zf = __high2float(m);
-  Row4 r;
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    r.x[i] = __fadd_rn(__fmul_rn(sf, static_cast<float>((w >> (8 * i)) & 0xffu)), zf);
-  return r;
-}
-
 __global__ void __launch_bounds__(256) demote_kernel(DemoteArgs a) {
   const int lane = threadIdx.x & 31;
   const long unit = static_cast<long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   if (unit >= a.units) return;
-  const int vslot = a.victim[unit];
-  if (vslot < 0 || vslot >= a.n_hi) return;  // invalid victim: nothing moves
-  const long hs = unit * a.cap_hi + vslot;
-  const long last = unit * a.cap_hi + (a.n_hi - 1);
-  const long ls = unit * a.cap_lo + a.n_lo;
-  Row4 xk, xv;
-  if (a.hi_bits == 16) {
-    xk = load_fp16x4(reinterpret_cast<const __half*>(a.k_hi) + hs * kD + lane * 4);
-    xv = load_fp16x4(reinterpret_cast<const __half*>(a.v_hi) + hs * kD + lane * 4);
-    if (a.bal) {
-      const float4 bb = *reinterpret_cast<const float4*>(a.bal + unit * kD + lane * 4);
-      xk.x[0] = __fmul_rn(xk.x[0], bb.x);
-      xk.x[1] = __fmul_rn(xk.x[1], bb.y);
-      xk.x[2] = __fmul_rn(xk.x[2], bb.z);
-      xk.x[3] = __fmul_rn(xk.x[3], bb.w);
-    }
-  } else {  // INT8 tier holds balanced keys already
-    xk = dequant_int8x4(a.k_hi + hs * kD, a.k_hi_meta + hs * 2, lane);
-    xv = dequant_int8x4(a.v_hi + hs * kD, a.v_hi_meta + hs * 2, lane);
-  }
-  const int rb = kD * a.lo_bits / 8;
-  uint32_t mk, mv;
-  const uint32_t pk = quantize4(xk, a.lo_bits, mk);
-  const uint32_t pv = quantize4(xv, a.lo_bits, mv);
-  store_codes(a.k_lo + ls * rb, lane, a.lo_bits, pk);
-  store_codes(a.v_lo + ls * rb, lane, a.lo_bits, pv);
-  store_meta(a.k_lo_meta + ls * 2, lane, mk);
-  store_meta(a.v_lo_meta + ls * 2, lane, mv);
-  if (lane == 0) a.pos_lo[ls] = a.pos_hi[hs];
-  __syncwarp();
-  // swap-remove: the last important slot moves into the freed one
-  if (hs != last) {
-    const int hrb = a.hi_bits == 16 ? kD * 2 : kD;
-    const int words = hrb / 4;
-    for (int i = lane; i < words; i += 32) {
-      reinterpret_cast<uint32_t*>(a.k_hi + hs * hrb)[i] =
-          reinterpret_cast<const uint32_t*>(a.k_hi + last * hrb)[i];
-      reinterpret_cast<uint32_t*>(a.v_hi + hs * hrb)[i] =
-          reinterpret_cast<const uint32_t*>(a.v_hi + last * hrb)[i];
-    }
-    if (a.hi_bits == 8 && lane < 2) {
-      a.k_hi_meta[hs * 2 + lane] = a.k_hi_meta[last * 2 + lane];
-      a.v_hi_meta[hs * 2 + lane] = a.v_hi_meta[last * 2 + lane];
-    }
-    if (lane == 0) {
-      a.pos_hi[hs] = a.pos_hi[last];
-      a.scores[hs] = a.scores[last];
-    }
-  }
+  demote_one(a, unit, a.victim[unit], lane);
 }
 
 int validate_cache(const mikv_cache* c, const char* who) {
@@ -230,6 +106,92 @@ int validate_cache_public(const mikv_cache* c, const char* who) { return validat
 
 using namespace mikv;
 
+namespace mikv {
+
+// Validate and launch an append of n_tokens source tokens into the HI or LO tier (counts
+// in *c are not changed here).  src_pos == nullptr means source token j goes to slot j.
+int append_tokens(bool hi, const uint16_t* k, const uint16_t* v, int src_len, const int32_t* src_pos,
+                  int n_tokens, int pos_base, const float* src_scores, const mikv_cache* c,
+                  cudaStream_t s) {
+  const long units = static_cast<long>(c->B) * c->Hkv;
+  const int bits = hi ? c->hi_bits : c->lo_bits;
+  if ((!k || !v) && n_tokens > 0) return fail(MIKV_EINVAL, "quantize_append: null k/v");
+  if (n_tokens < 0 || src_len < 1) return fail(MIKV_ESHAPE, "quantize_append: n_tokens/src_len");
+  const int base = hi ? c->n_hi : c->n_lo;
+  const int cap = hi ? c->cap_hi : c->cap_lo;
+  if (base + n_tokens > cap)
+    return fail(MIKV_ESHAPE, "quantize_append: tier capacity %d exceeded (%d + %d)", cap, base,
+                n_tokens);
+  AppendArgs a{};
+  a.k = reinterpret_cast<const __half*>(k);
+  a.v = reinterpret_cast<const __half*>(v);
+  a.src_pos = src_pos;
+  a.src_scores = src_scores;
+  a.bal = (bits != 16) ? c->balancer : nullptr;
+  a.Hkv = c->Hkv;
+  a.src_len = src_len;
+  a.n_tokens = n_tokens;
+  a.pos_base = pos_base;
+  a.cap = cap;
+  a.base_slot = base;
+  a.bits = bits;
+  a.dk = static_cast<uint8_t*>(hi ? c->k_hi : c->k_lo);
+  a.dv = static_cast<uint8_t*>(hi ? c->v_hi : c->v_lo);
+  a.dkm = static_cast<__half2*>(hi ? c->k_hi_meta : c->k_lo_meta);
+  a.dvm = static_cast<__half2*>(hi ? c->v_hi_meta : c->v_lo_meta);
+  a.dpos = hi ? c->pos_hi : c->pos_lo;
+  a.dscores = hi ? c->scores : nullptr;
+  if (!a.dk || !a.dv || !a.dpos || (hi && !a.dscores))
+    return fail(MIKV_EINVAL, "quantize_append: null tier buffer");
+  if (bits != 16 && (!a.dkm || !a.dvm)) return fail(MIKV_EINVAL, "quantize_append: null meta");
+  if (!aligned16(a.dk) || !aligned16(a.dv) || (k && !aligned16(k)) || (v && !aligned16(v)) ||
+      (bits != 16 && (!aligned16(a.dkm) || !aligned16(a.dvm))) || (a.bal && !aligned16(a.bal)))
+    return fail(MIKV_EALIGN, "quantize_append: buffers must be 16-byte aligned");
+  a.units_tokens = units * n_tokens;
+  if (n_tokens > 0) {
+    const long blocks = (a.units_tokens + 7) / 8;
+    append_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+    if (int e = check_launch("append_kernel")) return e;
+  }
+  return MIKV_OK;
+}
+
+// Demotion arguments for the current counts of *c (victim list: [B*Hkv] hi slots).
+int demote_args(const mikv_cache* c, const int32_t* victim, DemoteArgs& a) {
+  if (c->n_hi < 1 || c->n_lo + 1 > c->cap_lo)
+    return fail(MIKV_ESHAPE, "demotion: n_hi=%d n_lo=%d cap_lo=%d", c->n_hi, c->n_lo, c->cap_lo);
+  a = DemoteArgs{};
+  a.victim = victim;
+  a.bal = c->balancer;
+  a.units = c->B * c->Hkv;
+  a.hi_bits = c->hi_bits;
+  a.lo_bits = c->lo_bits;
+  a.cap_hi = c->cap_hi;
+  a.cap_lo = c->cap_lo;
+  a.n_hi = c->n_hi;
+  a.n_lo = c->n_lo;
+  a.k_hi = static_cast<uint8_t*>(c->k_hi);
+  a.v_hi = static_cast<uint8_t*>(c->v_hi);
+  a.k_hi_meta = static_cast<__half2*>(c->k_hi_meta);
+  a.v_hi_meta = static_cast<__half2*>(c->v_hi_meta);
+  a.k_lo = static_cast<uint8_t*>(c->k_lo);
+  a.v_lo = static_cast<uint8_t*>(c->v_lo);
+  a.k_lo_meta = static_cast<__half2*>(c->k_lo_meta);
+  a.v_lo_meta = static_cast<__half2*>(c->v_lo_meta);
+  a.pos_hi = c->pos_hi;
+  a.pos_lo = c->pos_lo;
+  a.scores = c->scores;
+  if (!a.k_hi || !a.v_hi || !a.k_lo || !a.v_lo || !a.k_lo_meta || !a.v_lo_meta || !a.pos_hi ||
+      !a.pos_lo || !a.scores || (c->hi_bits == 8 && (!a.k_hi_meta || !a.v_hi_meta)))
+    return fail(MIKV_EINVAL, "demotion: null cache buffer");
+  if (!aligned16(a.k_hi) || !aligned16(a.v_hi) || !aligned16(a.k_lo) || !aligned16(a.v_lo) ||
+      !aligned16(a.k_lo_meta) || !aligned16(a.v_lo_meta))
+    return fail(MIKV_EALIGN, "demotion: buffers must be 16-byte aligned");
+  return MIKV_OK;
+}
+
+}  // namespace mikv
+
 extern "C" int mikv_quantize_append(int tier, const uint16_t* k, const uint16_t* v, int src_len,
                                     const int32_t* src_pos, int n_tokens, int pos_base,
                                     const float* src_scores, mikv_cache* c, void* stream) {
@@ -237,85 +199,18 @@ extern "C" int mikv_quantize_append(int tier, const uint16_t* k, const uint16_t*
   if (int e = validate_cache(c, "quantize_append")) return e;
   if (!src_pos && n_tokens > 0) return fail(MIKV_EINVAL, "quantize_append: null src_pos");
   cudaStream_t s = as_stream(stream);
-  const long units = static_cast<long>(c->B) * c->Hkv;
   if (tier == MIKV_TIER_HI || tier == MIKV_TIER_LO) {
     const bool hi = tier == MIKV_TIER_HI;
-    const int bits = hi ? c->hi_bits : c->lo_bits;
-    if ((!k || !v) && n_tokens > 0) return fail(MIKV_EINVAL, "quantize_append: null k/v");
-    if (n_tokens < 0 || src_len < 1) return fail(MIKV_ESHAPE, "quantize_append: n_tokens/src_len");
-    const int base = hi ? c->n_hi : c->n_lo;
-    const int cap = hi ? c->cap_hi : c->cap_lo;
-    if (base + n_tokens > cap)
-      return fail(MIKV_ESHAPE, "quantize_append: tier capacity %d exceeded (%d + %d)", cap, base,
-                  n_tokens);
-    AppendArgs a{};
-    a.k = reinterpret_cast<const __half*>(k);
-    a.v = reinterpret_cast<const __half*>(v);
-    a.src_pos = src_pos;
-    a.src_scores = src_scores;
-    a.bal = (bits != 16) ? c->balancer : nullptr;
-    a.Hkv = c->Hkv;
-    a.src_len = src_len;
-    a.n_tokens = n_tokens;
-    a.pos_base = pos_base;
-    a.cap = cap;
-    a.base_slot = base;
-    a.bits = bits;
-    a.dk = static_cast<uint8_t*>(hi ? c->k_hi : c->k_lo);
-    a.dv = static_cast<uint8_t*>(hi ? c->v_hi : c->v_lo);
-    a.dkm = static_cast<__half2*>(hi ? c->k_hi_meta : c->k_lo_meta);
-    a.dvm = static_cast<__half2*>(hi ? c->v_hi_meta : c->v_lo_meta);
-    a.dpos = hi ? c->pos_hi : c->pos_lo;
-    a.dscores = hi ? c->scores : nullptr;
-    if (!a.dk || !a.dv || !a.dpos || (hi && !a.dscores))
-      return fail(MIKV_EINVAL, "quantize_append: null tier buffer");
-    if (bits != 16 && (!a.dkm || !a.dvm)) return fail(MIKV_EINVAL, "quantize_append: null meta");
-    if (!aligned16(a.dk) || !aligned16(a.dv) || (k && !aligned16(k)) || (v && !aligned16(v)) ||
-        (bits != 16 && (!aligned16(a.dkm) || !aligned16(a.dvm))) ||
-        (a.bal && !aligned16(a.bal)))
-      return fail(MIKV_EALIGN, "quantize_append: buffers must be 16-byte aligned");
-    a.units_tokens = units * n_tokens;
-    if (n_tokens > 0) {
-      const long blocks = (a.units_tokens + 7) / 8;
-      append_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
-      if (int e = check_launch("append_kernel")) return e;
-    }
+    if (int e = append_tokens(hi, k, v, src_len, src_pos, n_tokens, pos_base, src_scores, c, s)) return e;
     if (hi) c->n_hi += n_tokens;
     else c->n_lo += n_tokens;
     return MIKV_OK;
   }
   if (tier == MIKV_TIER_DEMOTE) {
     if (n_tokens != 1) return fail(MIKV_ESHAPE, "quantize_append(DEMOTE): n_tokens must be 1");
-    if (c->n_hi < 1 || c->n_lo + 1 > c->cap_lo)
-      return fail(MIKV_ESHAPE, "quantize_append(DEMOTE): n_hi=%d n_lo=%d cap_lo=%d", c->n_hi,
-                  c->n_lo, c->cap_lo);
-    DemoteArgs a{};
-    a.victim = src_pos;
-    a.bal = c->balancer;
-    a.units = static_cast<int>(units);
-    a.hi_bits = c->hi_bits;
-    a.lo_bits = c->lo_bits;
-    a.cap_hi = c->cap_hi;
-    a.cap_lo = c->cap_lo;
-    a.n_hi = c->n_hi;
-    a.n_lo = c->n_lo;
-    a.k_hi = static_cast<uint8_t*>(c->k_hi);
-    a.v_hi = static_cast<uint8_t*>(c->v_hi);
-    a.k_hi_meta = static_cast<__half2*>(c->k_hi_meta);
-    a.v_hi_meta = static_cast<__half2*>(c->v_hi_meta);
-    a.k_lo = static_cast<uint8_t*>(c->k_lo);
-    a.v_lo = static_cast<uint8_t*>(c->v_lo);
-    a.k_lo_meta = static_cast<__half2*>(c->k_lo_meta);
-    a.v_lo_meta = static_cast<__half2*>(c->v_lo_meta);
-    a.pos_hi = c->pos_hi;
-    a.pos_lo = c->pos_lo;
-    a.scores = c->scores;
-    if (!a.k_hi || !a.v_hi || !a.k_lo || !a.v_lo || !a.k_lo_meta || !a.v_lo_meta || !a.pos_hi ||
-        !a.pos_lo || !a.scores || (c->hi_bits == 8 && (!a.k_hi_meta || !a.v_hi_meta)))
-      return fail(MIKV_EINVAL, "quantize_append(DEMOTE): null cache buffer");
-    if (!aligned16(a.k_hi) || !aligned16(a.v_hi) || !aligned16(a.k_lo) || !aligned16(a.v_lo) ||
-        !aligned16(a.k_lo_meta) || !aligned16(a.v_lo_meta))
-      return fail(MIKV_EALIGN, "quantize_append(DEMOTE): buffers must be 16-byte aligned");
+    DemoteArgs a;
+    if (int e = demote_args(c, src_pos, a)) return e;
+    const long units = static_cast<long>(c->B) * c->Hkv;
     demote_kernel<<<static_cast<unsigned>((units + 7) / 8), 256, 0, s>>>(a);
     if (int e = check_launch("demote_kernel")) return e;
     c->n_hi -= 1;

@@ -29,6 +29,13 @@ constexpr int kScoreSmem = 3 * kTile * 256 + 2 * kTile * 4;
 // log2(e)/sqrt(128): logits in base 2, one rounding shared by both passes
 constexpr float kC = 0.12751743082459868f;
 
+// 2^x in one MUFU instruction (ex2.approx.ftz: relative error ~2^-22, exp2(-inf) = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Stage a [64][128] fp16 tile (rows r0.., rows >= nrows zero-filled) into 128B-swizzled smem.
 __device__ __forceinline__ void load_tile(uint32_t s, const __half* g, long r0, int nrows) {
   for (int i = threadIdx.x; i < kTile * 16; i += kThr) {
@@ -125,8 +132,8 @@ __global__ void __launch_bounds__(kThr) row_lse_kernel(const __half* __restrict_
         for (int n = 0; n < 8; ++n)
 #pragma unroll
           for (int e = 0; e < 2; ++e)
-            if (x[n][e] != -INFINITY) sum += exp2f(fmaf(acc[n][2 * hh + e], kC, -mn));
-        const float alpha = exp2f(m[hh] - mn);
+            if (x[n][e] != -INFINITY) sum += fast_exp2(fmaf(acc[n][2 * hh + e], kC, -mn));
+        const float alpha = fast_exp2(m[hh] - mn);
         // compensated (Kahan) running sum, rescaled with the running max
         l[hh] = __fmul_rn(l[hh], alpha);
         lc[hh] = __fmul_rn(lc[hh], alpha);
@@ -206,7 +213,7 @@ __global__ void __launch_bounds__(kThr) col_sum_kernel(const __half* __restrict_
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             const int i = key0 + 8 * hh;
-            if (t >= i && t < T) part[hh] += exp2f(fmaf(acc[n][2 * hh + e], kC, -lt));
+            if (t >= i && t < T) part[hh] += fast_exp2(fmaf(acc[n][2 * hh + e], kC, -lt));
           }
         }
 #pragma unroll

@@ -355,3 +355,35 @@ def test_pipeline_matches_oracle(name, scale):
         compare_tiers(gc, oc)
         assert_scores_close(to_np(gc.scores[:, :, :gc.n_hi]), oc.scores[:, :, :oc.n_hi])
     assert worst <= 1e-4
+
+
+@pytest.mark.parametrize("name,scale", [("tiny", dict(steps=12)), ("llama31_8b", dict(B=2, T=600, steps=5)),
+                                        ("llama2_7b", dict(B=2, Hq=8, Hkv=8, T=300, steps=6)),
+                                        ("qwen25_32b", dict(T=400, steps=3, Hq=10, Hkv=2))])
+def test_fused_step_equals_separate_calls(name, scale):
+    """mikv_decode_step (3 launches) leaves every buffer and output bit-identical to the
+    five-call sequence."""
+    wl = inputs.WORKLOADS[name].scaled(**scale)
+    x = inputs.make_prefill(wl, 1, "cpu")
+    d = {k: v.to(dev()) for k, v in x.items()}
+    keep = osel.n_keep(wl.T, wl.budget_pct, wl.window)
+    caches = []
+    for _ in range(2):
+        gc = MikvCache(wl.B, wl.Hq, wl.Hkv, 128, wl.hi_bits, wl.lo_bits, keep + wl.steps + 1,
+                       wl.T - keep + wl.steps + 1, dev())
+        gc.prefill(d["q"], d["k"], d["v"], wl.budget_pct, wl.window)
+        caches.append(gc)
+    fused, calls = caches
+    for s in range(wl.steps):
+        t = {k: v.to(dev()) for k, v in inputs.make_decode_token(wl, 1, s, "cpu").items()}
+        o1, l1 = fused.decode_step(t["q"], t["k"], t["v"], wl.T + s, wl.budget_pct, wl.window, wl.policy)
+        o1, l1 = o1.clone(), l1.clone()
+        o2, l2 = calls.decode_step_calls(t["q"], t["k"], t["v"], wl.T + s, wl.budget_pct, wl.window, wl.policy)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+        assert (fused.n_hi, fused.n_lo) == (calls.n_hi, calls.n_lo)
+        for name_ in ("k_hi", "v_hi", "k_lo", "v_lo", "k_lo_meta", "v_lo_meta", "pos_hi", "pos_lo"):
+            a, b = getattr(fused, name_), getattr(calls, name_)
+            n = fused.n_hi if "hi" in name_ else fused.n_lo
+            assert torch.equal(a[:, :, :n], b[:, :, :n]), name_
+        assert torch.equal(fused.scores[:, :, :fused.n_hi], calls.scores[:, :, :calls.n_hi])
