@@ -44,6 +44,7 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 2;        // ring depth per warp (3 CTAs of 4 warps fit per SM)
+constexpr int kPrefetch = 2;      // L2 prefetch distance, in stages of the same warp
 constexpr float kLogitScale = 0.12751743082459868f;  // log2(e) / sqrt(128)
 
 template <int BITS>
@@ -136,74 +137,63 @@ __device__ __forceinline__ void load_stage(uint32_t sb, const uint8_t* gk, const
 
 // ---------------------------------------------------------------------------------
 // unpacking: codes -> fp16 pairs holding exact integers.
-// A code c masked in place at mantissa bit 2p (INT2) or 4p (INT4) of a half whose
-// exponent field is 0x64 reads as 1024 + c*2^k; one fma.rn.f16x2 by 2^-k with addend
-// -1024*2^-k returns c exactly (the true result is a small integer).  Positions past
-// the 10 mantissa bits are reached with one shift of the whole word.
+// A code c masked in place at bit 2p (INT2) / 4p (INT4) of a half whose exponent field is
+// 0x64 reads as 1024 + c*2^k; one fma.rn.f16x2 by 2^-k with addend -1024*2^-k returns c
+// exactly (the true result is a small integer).  Codes above bit 9 are reached with one
+// shift of the whole word.  (Feeding the raw bits as fp16 subnormals c*2^k*2^-24 would
+// save the fma, but mma.sync on sm_103a did not multiply such operands exactly in our
+// measurements: attention errors rose from <1e-4 to ~3e-4.)
 __device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
   asm("fma.rn.f16x2 %0, %1, %2, %3;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
-// (2^-k, -1024*2^-k) as f16x2 pairs for k = 0, 2, 4, 6, 8
-__device__ __forceinline__ uint32_t mul4p(int p) {
-  return p == 0 ? 0x3C003C00u : p == 1 ? 0x34003400u : p == 2 ? 0x2C002C00u
-       : p == 3 ? 0x24002400u : 0x1C001C00u;
-}
-__device__ __forceinline__ uint32_t add4p(int p) {
-  return p == 0 ? 0xE400E400u : p == 1 ? 0xDC00DC00u : p == 2 ? 0xD400D400u
-       : p == 3 ? 0xCC00CC00u : 0xC400C400u;
-}
-// 16 two-bit codes of a word (code j at bits 2j of the low half, 2j+16 of the high) ->
-// 8 pairs, pair p = (code p, code p + 8).
-// (w & MASK) | 0x64006400 as one LOP3 (lut 0xEA = (a & b) | c).
 template <uint32_t MASK>
-__device__ __forceinline__ uint32_t mask_magic(uint32_t w) {
+__device__ __forceinline__ uint32_t mask_magic(uint32_t w) {  // (w & MASK) | 0x64006400, one LOP3
   uint32_t d;
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;\n" : "=r"(d) : "r"(w), "n"(MASK), "r"(0x64006400u));
   return d;
 }
-__device__ __forceinline__ void unpack_int2_word(uint32_t w, uint32_t (&pr)[8]) {
-  pr[0] = hfma2_u32(mask_magic<0x00030003u>(w), mul4p(0), add4p(0));
-  pr[1] = hfma2_u32(mask_magic<0x000C000Cu>(w), mul4p(1), add4p(1));
-  pr[2] = hfma2_u32(mask_magic<0x00300030u>(w), mul4p(2), add4p(2));
-  pr[3] = hfma2_u32(mask_magic<0x00C000C0u>(w), mul4p(3), add4p(3));
-  pr[4] = hfma2_u32(mask_magic<0x03000300u>(w), mul4p(4), add4p(4));
+// (2^-k, -1024*2^-k) f16x2 constants for k = 0, 2, 4, 6, 8
+#define MIKV_M4(p) ((p) == 0 ? 0x3C003C00u : (p) == 1 ? 0x34003400u : (p) == 2 ? 0x2C002C00u : (p) == 3 ? 0x24002400u : 0x1C001C00u)
+#define MIKV_A4(p) ((p) == 0 ? 0xE400E400u : (p) == 1 ? 0xDC00DC00u : (p) == 2 ? 0xD400D400u : (p) == 3 ? 0xCC00CC00u : 0xC400C400u)
+__device__ __forceinline__ void unpack_int2_word_int(uint32_t w, uint32_t (&pr)[8]) {
+  pr[0] = hfma2_u32(mask_magic<0x00030003u>(w), MIKV_M4(0), MIKV_A4(0));
+  pr[1] = hfma2_u32(mask_magic<0x000C000Cu>(w), MIKV_M4(1), MIKV_A4(1));
+  pr[2] = hfma2_u32(mask_magic<0x00300030u>(w), MIKV_M4(2), MIKV_A4(2));
+  pr[3] = hfma2_u32(mask_magic<0x00C000C0u>(w), MIKV_M4(3), MIKV_A4(3));
+  pr[4] = hfma2_u32(mask_magic<0x03000300u>(w), MIKV_M4(4), MIKV_A4(4));
   const uint32_t w2 = w >> 10;
-  pr[5] = hfma2_u32(mask_magic<0x00030003u>(w2), mul4p(0), add4p(0));
-  pr[6] = hfma2_u32(mask_magic<0x000C000Cu>(w2), mul4p(1), add4p(1));
-  pr[7] = hfma2_u32(mask_magic<0x00300030u>(w2), mul4p(2), add4p(2));
+  pr[5] = hfma2_u32(mask_magic<0x00030003u>(w2), MIKV_M4(0), MIKV_A4(0));
+  pr[6] = hfma2_u32(mask_magic<0x000C000Cu>(w2), MIKV_M4(1), MIKV_A4(1));
+  pr[7] = hfma2_u32(mask_magic<0x00300030u>(w2), MIKV_M4(2), MIKV_A4(2));
 }
-// 8 four-bit codes (code j at bits 4j of the low half, 4j+16 of the high) -> 4 pairs,
-// pair p = (code p, code p + 4).
-__device__ __forceinline__ void unpack_int4_word(uint32_t w, uint32_t* pr) {
+__device__ __forceinline__ void unpack_int4_word_int(uint32_t w, uint32_t* pr) {
   pr[0] = hfma2_u32(mask_magic<0x000F000Fu>(w), 0x3C003C00u, 0xE400E400u);
   pr[1] = hfma2_u32(mask_magic<0x00F000F0u>(w), 0x2C002C00u, 0xD400D400u);
   const uint32_t w2 = w >> 8;
   pr[2] = hfma2_u32(mask_magic<0x000F000Fu>(w2), 0x3C003C00u, 0xE400E400u);
   pr[3] = hfma2_u32(mask_magic<0x00F000F0u>(w2), 0x2C002C00u, 0xD400D400u);
 }
-__device__ __forceinline__ uint32_t fix1024(uint32_t bits_with_magic) {
-  return hfma2_u32(bits_with_magic, 0x3C003C00u, 0xE400E400u);
-}
+
 
 // K side: the 16 channels [gr*64 + tig*16, +16) of one token row (at smem address
 // `addr`) -> 8 pairs; pair p holds local channels (ca(p), cb(p)) in its (low, high) halves.
 template <int BITS>
 __device__ __forceinline__ void unpack_k16(uint32_t addr, uint32_t (&pr)[8]) {
   if constexpr (BITS == 2) {
-    unpack_int2_word(lds32(addr), pr);
+    unpack_int2_word_int(lds32(addr), pr);
   } else if constexpr (BITS == 4) {
     const uint2 w = lds64(addr);
-    unpack_int4_word(w.x, pr);
-    unpack_int4_word(w.y, pr + 4);
+    unpack_int4_word_int(w.x, pr);
+    unpack_int4_word_int(w.y, pr + 4);
   } else {
     const uint4 w = lds128(addr);
     const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      pr[2 * i] = fix1024(__byte_perm(ww[i], 0x64u, 0x4140));
-      pr[2 * i + 1] = fix1024(__byte_perm(ww[i], 0x64u, 0x4342));
+      pr[2 * i] = hfma2_u32(__byte_perm(ww[i], 0x64u, 0x4140), 0x3C003C00u, 0xE400E400u);
+      pr[2 * i + 1] = hfma2_u32(__byte_perm(ww[i], 0x64u, 0x4342), 0x3C003C00u, 0xE400E400u);
     }
   }
 }
@@ -223,23 +213,24 @@ __host__ __device__ constexpr int k_cb(int p) {
 template <int BITS>
 __device__ __forceinline__ void unpack_v8(uint32_t aa, uint32_t ab, uint32_t (&pr)[8]) {
   if constexpr (BITS == 2) {
-    unpack_int2_word(__byte_perm(lds16(aa), lds16(ab), 0x5410), pr);
+    unpack_int2_word_int(__byte_perm(lds16(aa), lds16(ab), 0x5410), pr);
   } else if constexpr (BITS == 4) {
     const uint32_t ua = lds32(aa), ub = lds32(ab);
-    unpack_int4_word(__byte_perm(ua, ub, 0x5410), pr);      // channels 0..3
-    unpack_int4_word(__byte_perm(ua, ub, 0x7632), pr + 4);  // channels 4..7
+    unpack_int4_word_int(__byte_perm(ua, ub, 0x5410), pr);      // channels 0..3
+    unpack_int4_word_int(__byte_perm(ua, ub, 0x7632), pr + 4);  // channels 4..7
   } else {
     const uint2 ua = lds64(aa), ub = lds64(ab);
     const uint32_t t0 = __byte_perm(ua.x, ub.x, 0x5140), t1 = __byte_perm(ua.x, ub.x, 0x7362);
     const uint32_t t2 = __byte_perm(ua.y, ub.y, 0x5140), t3 = __byte_perm(ua.y, ub.y, 0x7362);
-    pr[0] = fix1024(__byte_perm(t0, 0x64u, 0x4140));
-    pr[1] = fix1024(__byte_perm(t0, 0x64u, 0x4342));
-    pr[2] = fix1024(__byte_perm(t1, 0x64u, 0x4140));
-    pr[3] = fix1024(__byte_perm(t1, 0x64u, 0x4342));
-    pr[4] = fix1024(__byte_perm(t2, 0x64u, 0x4140));
-    pr[5] = fix1024(__byte_perm(t2, 0x64u, 0x4342));
-    pr[6] = fix1024(__byte_perm(t3, 0x64u, 0x4140));
-    pr[7] = fix1024(__byte_perm(t3, 0x64u, 0x4342));
+    const uint32_t m = 0x3C003C00u, a = 0xE400E400u;  // exact integers: (1024 + c) * 1 - 1024
+    pr[0] = hfma2_u32(__byte_perm(t0, 0x64u, 0x4140), m, a);
+    pr[1] = hfma2_u32(__byte_perm(t0, 0x64u, 0x4342), m, a);
+    pr[2] = hfma2_u32(__byte_perm(t1, 0x64u, 0x4140), m, a);
+    pr[3] = hfma2_u32(__byte_perm(t1, 0x64u, 0x4342), m, a);
+    pr[4] = hfma2_u32(__byte_perm(t2, 0x64u, 0x4140), m, a);
+    pr[5] = hfma2_u32(__byte_perm(t2, 0x64u, 0x4342), m, a);
+    pr[6] = hfma2_u32(__byte_perm(t3, 0x64u, 0x4140), m, a);
+    pr[7] = hfma2_u32(__byte_perm(t3, 0x64u, 0x4342), m, a);
   }
 }
 
@@ -514,6 +505,46 @@ __device__ void run_tier(const Params& P, const TierPtrs& tier, int unit, int sp
   const int b = unit / P.Hkv, g = unit % P.Hkv;
   const int rep = P.rep;
 
+  const int t_begin = split * chunk;
+  const int t_end = min(tier.n, t_begin + chunk);
+  const int nst = (t_end - t_begin + F::kST - 1) / F::kST;   // stages in this CTA
+  const long row_base = static_cast<long>(unit) * tier.cap;
+  uint8_t* ring = smem + warp * (kStages * F::kStageBytes);  // this warp's ring
+  const uint32_t ring_s = smem_u32(ring);
+  // warp w handles stages w, w+4, ...; when it issues its k-th stage it also asks L2 for
+  // its (k + kPrefetch)-th, so HBM keeps streaming beyond what the rings can hold
+  int issued = 0;
+  auto issue = [&](int k) {
+    const int sidx = warp + k * kWarps;
+    if (sidx < nst) {
+      const int tok0 = t_begin + sidx * F::kST;
+      const long row = row_base + tok0;
+      load_stage<BITS>(ring_s + (k % kStages) * F::kStageBytes, tier.k + row * F::kRB,
+                       tier.v + row * F::kRB, tier.km + row * 8, tier.vm + row * 8,
+                       min(F::kST, t_end - tok0), lane);
+    }
+    const int pidx = warp + (k + kPrefetch) * kWarps;
+    if (lane == 0 && pidx < nst) {
+      const int tok0 = t_begin + pidx * F::kST;
+      const int nv = min(F::kST, t_end - tok0);
+      const long row = row_base + tok0;
+      prefetch_l2(tier.k + row * F::kRB, nv * F::kRB);
+      prefetch_l2(tier.v + row * F::kRB, nv * F::kRB);
+      if constexpr (F::kQuant) {
+        // meta rows are 8 bytes: both ends rounded down to 16 bytes (bulk-copy alignment),
+        // which stays inside rows [row - 1, row + nv) of the buffer
+        const long m0 = (row * 8) & ~15L, m1 = ((row + nv) * 8) & ~15L;
+        if (m1 > m0) {
+          prefetch_l2(tier.km + m0, static_cast<uint32_t>(m1 - m0));
+          prefetch_l2(tier.vm + m0, static_cast<uint32_t>(m1 - m0));
+        }
+      }
+    }
+    cp_async_commit();
+  };
+  issue(0);  // first stage in flight while the query is staged
+  ++issued;
+
   // query (balanced for quantised tiers, pre-scaled so logits come out of the mma in base-2
   // units) staged as (hi, lo) fp16 pairs, plus its per-(head, group) sums for the zero-point
   // term: thread i handles channels 8*(i%16) .. +8 of head i/16.
@@ -561,31 +592,11 @@ __device__ void run_tier(const Params& P, const TierPtrs& tier, int unit, int sp
       for (int e = 0; e < 4; ++e) st.o[t][j][e] = 0.f;
   }
 
-  const int t_begin = split * chunk;
-  const int t_end = min(tier.n, t_begin + chunk);
-  const int nst = (t_end - t_begin + F::kST - 1) / F::kST;   // stages in this CTA
-  const long row_base = static_cast<long>(unit) * tier.cap;
-  // this warp's ring
-  uint8_t* ring = smem + warp * (kStages * F::kStageBytes);
-  const uint32_t ring_s = smem_u32(ring);
   float* lrow = nullptr;
   if (is_hi && P.hi_logits)
     lrow = P.hi_logits + (static_cast<long>(b) * P.Hq + g * rep) * tier.cap;
 
   const FragOffs fo = frag_offsets<BITS>(lane);
-  // warp w handles stages w, w+4, ...
-  int issued = 0;
-  auto issue = [&](int k) {  // k-th stage of this warp
-    const int sidx = warp + k * kWarps;
-    if (sidx < nst) {
-      const int tok0 = t_begin + sidx * F::kST;
-      const long row = row_base + tok0;
-      load_stage<BITS>(ring_s + (k % kStages) * F::kStageBytes, tier.k + row * F::kRB,
-                       tier.v + row * F::kRB, tier.km + row * 8, tier.vm + row * 8,
-                       min(F::kST, t_end - tok0), lane);
-    }
-    cp_async_commit();
-  };
   for (; issued < kStages - 1; ++issued) issue(issued);
   for (int k = 0; warp + k * kWarps < nst; ++k) {
     issue(issued++);

@@ -148,7 +148,9 @@ def test_decode_attention(hi, lo, B, Hq, Hkv, T, p, W):
     err = np.abs(to_np(gc.out) - out_o).max()
     assert err <= ATTN_TOL, err
     assert err <= 1e-4, f"attention error {err} far above the expected fp32 level"
-    np.testing.assert_allclose(to_np(gc.lse), lse_o, atol=1e-4, rtol=0)
+    # lse reaches ~1e2 on these outlier-heavy inputs; fp32 carries ~1e-7 relative per
+    # rounding, so the bar is relative (about a hundred ulps)
+    np.testing.assert_allclose(to_np(gc.lse), lse_o, rtol=1e-5, atol=1e-5)
     if keep:
         lg = to_np(gc.hi_logits[:, :, :keep])
         np.testing.assert_allclose(lg, logit_o, atol=1e-4 * max(1, np.abs(logit_o).max()), rtol=0)
