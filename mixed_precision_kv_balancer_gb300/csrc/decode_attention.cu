@@ -44,7 +44,6 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 2;        // ring depth per warp (3 CTAs of 4 warps fit per SM)
-constexpr int kPrefetch = 2;      // L2 prefetch distance, in stages of the same warp
 constexpr float kLogitScale = 0.12751743082459868f;  // log2(e) / sqrt(128)
 
 template <int BITS>
@@ -102,34 +101,50 @@ __device__ __forceinline__ uint32_t qaddr(int r, int off) {
   return r * Fmt<BITS>::kRS + ((((off >> 4) ^ qswz<BITS>(r))) << 4) + (off & 15);
 }
 
-// One warp copies a stage: the K and V rows of the stage are contiguous in global
-// memory (gk, gv point at its first row), so lane l copies chunks l, l+32, ...; rows at
-// or past `nvalid` are zero-filled without being read.
+// Per-lane constants of the stage copy: lane l copies the 16-byte chunks l, l+32, ... of
+// the stage's contiguous K and V rows; its first chunk lands at smem offset d0 (d1 for odd
+// copy iterations of INT8 rows, whose swizzle changes every 4 rows).
 template <int BITS>
+struct CopyLane {
+  uint32_t d0, d1;  // smem offsets of iteration 0 (and odd iterations for INT8)
+  int rl;           // row of iteration 0
+  __device__ __forceinline__ explicit CopyLane(int lane) {
+    using F = Fmt<BITS>;
+    const int cc = lane % F::kCPR;
+    rl = lane / F::kCPR;
+    if constexpr (BITS == 16) {
+      d0 = d1 = rl * F::kRS + cc * 16;
+    } else {
+      d0 = rl * F::kRS + ((cc ^ qswz<BITS>(rl)) << 4);
+      d1 = rl * F::kRS + ((cc ^ qswz<BITS>(rl + F::kRowsPerIt)) << 4);
+    }
+  }
+};
+
+// One warp copies a stage: gk/gv point at this lane's first chunk of the stage (stage rows
+// are contiguous), gkm/gvm at the stage's first meta row.  FULL: all kST rows valid; else
+// rows at or past `nvalid` are zero-filled without being read.
+template <int BITS, bool FULL>
 __device__ __forceinline__ void load_stage(uint32_t sb, const uint8_t* gk, const uint8_t* gv,
                                            const uint8_t* gkm, const uint8_t* gvm, int nvalid,
-                                           int lane) {
+                                           int lane, const CopyLane<BITS>& cl) {
   using F = Fmt<BITS>;
-  const int cc = lane % F::kCPR, rl = lane / F::kCPR;
 #pragma unroll
   for (int it = 0; it < F::kST / F::kRowsPerIt; ++it) {
-    const int r = rl + it * F::kRowsPerIt;
-    const bool ok = r < nvalid;
-    uint32_t dst;
-    if constexpr (BITS == 16) dst = r * F::kRS + cc * 16;
-    else dst = r * F::kRS + ((cc ^ qswz<BITS>(r)) << 4);
-    const int g = ok ? lane * 16 + it * 512 : 0;
-    cp_async16(sb + dst, gk + g, ok);
-    cp_async16(sb + F::kOffV + dst, gv + g, ok);
+    const bool ok = FULL || cl.rl + it * F::kRowsPerIt < nvalid;
+    const uint32_t dst = ((it & 1) ? cl.d1 : cl.d0) + it * F::kRowsPerIt * F::kRS;
+    // a zero-filled chunk reads nothing; it still gets the stage's first chunk (valid)
+    cp_async16(sb + dst, ok ? gk + it * 512 : gk - lane * 16, ok);
+    cp_async16(sb + F::kOffV + dst, ok ? gv + it * 512 : gv - lane * 16, ok);
   }
   if constexpr (F::kQuant) {
 #pragma unroll
     for (int it = 0; it < (F::kST + 31) / 32; ++it) {
       const int r = lane + 32 * it;
-      if (r < F::kST) {
-        const bool ok = r < nvalid;
-        cp_async8(sb + F::kOffKM + r * 8, gkm + (ok ? r * 8 : 0), ok);
-        cp_async8(sb + F::kOffVM + r * 8, gvm + (ok ? r * 8 : 0), ok);
+      if (F::kST % 32 == 0 || r < F::kST) {
+        const bool ok = FULL || r < nvalid;
+        cp_async8(sb + F::kOffKM + r * 8, ok ? gkm + r * 8 : gkm, ok);
+        cp_async8(sb + F::kOffVM + r * 8, ok ? gvm + r * 8 : gvm, ok);
       }
     }
   }
@@ -508,42 +523,37 @@ __device__ void run_tier(const Params& P, const TierPtrs& tier, int unit, int sp
   const int t_begin = split * chunk;
   const int t_end = min(tier.n, t_begin + chunk);
   const int nst = (t_end - t_begin + F::kST - 1) / F::kST;   // stages in this CTA
-  const long row_base = static_cast<long>(unit) * tier.cap;
+  const int my_st = nst > warp ? (nst - warp + kWarps - 1) / kWarps : 0;  // this warp's share
   uint8_t* ring = smem + warp * (kStages * F::kStageBytes);  // this warp's ring
   const uint32_t ring_s = smem_u32(ring);
-  // warp w handles stages w, w+4, ...; when it issues its k-th stage it also asks L2 for
-  // its (k + kPrefetch)-th, so HBM keeps streaming beyond what the rings can hold
+  // warp w handles stages w, w+4, ...; stage pointers advance by a constant stride
+  const long row0 = static_cast<long>(unit) * tier.cap + t_begin + warp * F::kST;
+  constexpr long kRowStride = static_cast<long>(kWarps) * F::kST;
+  const CopyLane<BITS> cl(lane);
+  const uint8_t* gk = tier.k + row0 * F::kRB + lane * 16;
+  const uint8_t* gv = tier.v + row0 * F::kRB + lane * 16;
+  const uint8_t* gkm = F::kQuant ? tier.km + row0 * 8 : nullptr;
+  const uint8_t* gvm = F::kQuant ? tier.vm + row0 * 8 : nullptr;
+  int tok_issue = t_begin + warp * F::kST;  // first token of the next stage to issue
   int issued = 0;
-  auto issue = [&](int k) {
-    const int sidx = warp + k * kWarps;
-    if (sidx < nst) {
-      const int tok0 = t_begin + sidx * F::kST;
-      const long row = row_base + tok0;
-      load_stage<BITS>(ring_s + (k % kStages) * F::kStageBytes, tier.k + row * F::kRB,
-                       tier.v + row * F::kRB, tier.km + row * 8, tier.vm + row * 8,
-                       min(F::kST, t_end - tok0), lane);
-    }
-    const int pidx = warp + (k + kPrefetch) * kWarps;
-    if (lane == 0 && pidx < nst) {
-      const int tok0 = t_begin + pidx * F::kST;
-      const int nv = min(F::kST, t_end - tok0);
-      const long row = row_base + tok0;
-      prefetch_l2(tier.k + row * F::kRB, nv * F::kRB);
-      prefetch_l2(tier.v + row * F::kRB, nv * F::kRB);
+  auto issue = [&]() {
+    if (issued < my_st) {
+      const uint32_t sb = ring_s + (issued % kStages) * F::kStageBytes;
+      const int nv = t_end - tok_issue;
+      if (nv >= F::kST) load_stage<BITS, true>(sb, gk, gv, gkm, gvm, nv, lane, cl);
+      else load_stage<BITS, false>(sb, gk, gv, gkm, gvm, nv, lane, cl);
+      gk += kRowStride * F::kRB;
+      gv += kRowStride * F::kRB;
       if constexpr (F::kQuant) {
-        // meta rows are 8 bytes: both ends rounded down to 16 bytes (bulk-copy alignment),
-        // which stays inside rows [row - 1, row + nv) of the buffer
-        const long m0 = (row * 8) & ~15L, m1 = ((row + nv) * 8) & ~15L;
-        if (m1 > m0) {
-          prefetch_l2(tier.km + m0, static_cast<uint32_t>(m1 - m0));
-          prefetch_l2(tier.vm + m0, static_cast<uint32_t>(m1 - m0));
-        }
+        gkm += kRowStride * 8;
+        gvm += kRowStride * 8;
       }
+      tok_issue += kRowStride;
     }
+    ++issued;
     cp_async_commit();
   };
-  issue(0);  // first stage in flight while the query is staged
-  ++issued;
+  issue();  // first stage in flight while the query is staged
 
   // query (balanced for quantised tiers, pre-scaled so logits come out of the mma in base-2
   // units) staged as (hi, lo) fp16 pairs, plus its per-(head, group) sums for the zero-point
@@ -597,18 +607,19 @@ __device__ void run_tier(const Params& P, const TierPtrs& tier, int unit, int sp
     lrow = P.hi_logits + (static_cast<long>(b) * P.Hq + g * rep) * tier.cap;
 
   const FragOffs fo = frag_offsets<BITS>(lane);
-  for (; issued < kStages - 1; ++issued) issue(issued);
-  for (int k = 0; warp + k * kWarps < nst; ++k) {
-    issue(issued++);
+  for (int i = 1; i < kStages - 1; ++i) issue();  // ring prologue (stage 0 is already issued)
+  int tok0 = t_begin + warp * F::kST;
+  for (int k = 0; k < my_st; ++k) {
+    issue();  // stage k + kStages - 1 (or an empty group)
     cp_async_wait<kStages - 1>();
     __syncwarp();
-    const int tok0 = t_begin + (warp + k * kWarps) * F::kST;
     const int nv = min(F::kST, t_end - tok0);
     const uint32_t sb = ring_s + (k % kStages) * F::kStageBytes;
     float* lo = lrow ? lrow + tok0 : nullptr;
     if (nv == F::kST) compute_stage<BITS, NT, true>(sb, nv, bq, qsum, st, lo, tier.cap, rep, lane, fo);
     else compute_stage<BITS, NT, false>(sb, nv, bq, qsum, st, lo, tier.cap, rep, lane, fo);
     __syncwarp();
+    tok0 += kRowStride;
   }
   cp_async_wait<0>();
 
@@ -675,7 +686,7 @@ __device__ void run_tier(const Params& P, const TierPtrs& tier, int unit, int sp
 }
 
 template <int HI, int LO, int NT>
-__global__ void __launch_bounds__(kThreads) decode_partial_kernel(Params P) {
+__global__ void __launch_bounds__(kThreads, 3) decode_partial_kernel(Params P) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(16) float qs[8 * kD + 16];
   const int unit = blockIdx.y;
