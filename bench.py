@@ -66,6 +66,21 @@ def workload(args):
     return wl.scaled(**kw) if kw else wl
 
 
+# DRAM bytes (read + write) of one decode_partial_kernel launch per (batch, key head) unit,
+# from ncu (dram__bytes_read.sum + dram__bytes_write.sum) on the full-depth workload at
+# batch 32, one layer; the launch's traffic grows with the units it processes.
+TRAFFIC_PER_UNIT = {"llama31_8b_full": (349.7664e6 + 11.2704e6) / (32 * 8)}
+
+
+def same_cache_shape(wl):
+    """Per-unit cache as in the named workload (batch and layer count may differ)."""
+    import dataclasses
+
+    from mixed_precision_kv_balancer_gb300 import inputs
+    base = inputs.WORKLOADS[wl.name]
+    return dataclasses.replace(wl, B=base.B, layers=base.layers) == base
+
+
 def cache_bytes(wl, n_hi, n_lo):
     return wl.B * wl.Hkv * (n_hi * ROW_BYTES[wl.hi_bits] + n_lo * ROW_BYTES[wl.lo_bits])
 
@@ -218,19 +233,34 @@ def run_gpu(args, wl, rank, world):
              for l in range(wl.layers)] for s in range(total_steps + (0 if args.no_e2e else args.steps))]
     torch.cuda.synchronize()
 
+    def new_event():
+        e = torch.cuda.Event(enable_timing=True)
+        e.record()              # creates the CUDA event; the library records it again later
+        return e
+
+    # events for every timed (step, layer): the whole step, and the split-K attention kernel
+    # alone (recorded by the library on the launching stream, around that one launch)
+    n_timed = args.steps * wl.layers
+    step_ev = [(new_event(), new_event()) for _ in range(n_timed)]
+    attn_ev = [(new_event(), new_event()) for _ in range(n_timed)]
+    torch.cuda.synchronize()
+
     def step(s, timed=False):
         L_before = wl.T + s
         for l, c in enumerate(layers):
             t = toks[s][l]
             if timed:
+                i = len(ev_pairs)
                 read = cache_bytes(wl, c.n_hi + 1, c.n_lo)   # tiers as attended (after the append)
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0, e1 = step_ev[i]
+                a0, a1 = attn_ev[i]
+                _lib.mikv_set_attention_events(a0, a1)
                 e0.record()
             c.decode_step(t["q"], t["k"], t["v"], L_before, wl.budget_pct, wl.window)
             if timed:
                 e1.record()
-                ev_pairs.append((e0, e1, read))
-        return 3 * len(layers)   # append, split-K attention, fused merge/score/demotion
+                ev_pairs.append((e0, e1, a0, a1, read))
+        return 4 * len(layers)   # append, split-K attention, merge, score update/demotion
 
     ev_pairs = []
     for s in range(args.warmup):
@@ -252,14 +282,17 @@ def run_gpu(args, wl, rank, world):
         launches += step(s, timed=True)
     end.record()
     torch.cuda.synchronize()
+    _lib.mikv_set_attention_events(None, None)
     ms = start.elapsed_time(end)
     clk = clocks.stop()
     ms = reduce_over_ranks(ms, world, dev)
-    attn_ms = [a.elapsed_time(b) for a, b, _ in ev_pairs]
-    attn_bytes = [nb for _, _, nb in ev_pairs]
+    step_ms = [e0.elapsed_time(e1) for e0, e1, _, _, _ in ev_pairs]
+    attn_ms = [a0.elapsed_time(a1) for _, _, a0, a1, _ in ev_pairs]
+    attn_bytes = [nb for *_, nb in ev_pairs]
     res = dict(ms=ms, kv_tokens=kv_tokens * world, launches=launches, clocks=clk,
                attn_ms_mean=statistics.mean(attn_ms), attn_bytes_mean=statistics.mean(attn_bytes),
-               attn_ms_sum=sum(attn_ms), prefill_ms_per_layer=statistics.mean(prefill_ms))
+               step_ms_mean=statistics.mean(step_ms), attn_ms_sum=sum(attn_ms),
+               prefill_ms_per_layer=statistics.mean(prefill_ms))
 
     # ---- end to end through the public API with host buffers
     if not args.no_e2e:
@@ -356,6 +389,10 @@ def main():
     value = res["kv_tokens"] / (res["ms"] / 1e3)
     peak, peak_kind = peaks()
     achieved = res["attn_bytes_mean"] / (res["attn_ms_mean"] / 1e3) / 1e9
+    step_gbs = res["attn_bytes_mean"] / (res["step_ms_mean"] / 1e3) / 1e9
+    traffic = None
+    if wl.name in TRAFFIC_PER_UNIT and same_cache_shape(wl):
+        traffic = TRAFFIC_PER_UNIT[wl.name] * wl.B * wl.Hkv
     line = {
         "metric": METRIC, "value": value, "unit": "KV-tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": res["ms"] / args.steps, "higher_is_better": True,
@@ -364,10 +401,11 @@ def main():
         "hbm_gbs_decode_attn": achieved, "frac_of_8tbs": achieved / 8000.0,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "kernel": "mikv_decode_step per layer (append_kernel + decode_partial_kernel + "
-                               "decode_epilogue_kernel); bytes = packed cache read",
+                     "kernel": "decode_partial_kernel (split-K attention over both tiers), one "
+                               "launch per layer per step; bytes = packed cache as attended",
                      "bytes_per_launch": res["attn_bytes_mean"], "ms_per_launch": res["attn_ms_mean"],
-                     "traffic": None},
+                     "traffic": traffic},
+        "decode_step_gbs": step_gbs, "decode_step_ms_per_layer": res["step_ms_mean"],
         "decode_attn_ms_per_step": res["attn_ms_sum"] / args.steps,
         "prefill_ms_per_layer": res["prefill_ms_per_layer"],
         "gpu_launches": res["launches"],

@@ -243,26 +243,39 @@ int mikv_decode_attention(const uint16_t* q, const mikv_cache* c, float* out, fl
 size_t mikv_decode_workspace_bytes(const mikv_cache* c);
 
 /*
- * One whole decode step in three launches (the same arithmetic as the sequence
+ * One whole decode step in four launches (the same arithmetic as the sequence
  * quantize_append(HI) -> decode_attention -> score_update(DECODE) ->
  * select(DEMOTE) -> quantize_append(DEMOTE), with identical results):
  *   1. the new token (k_new, v_new fp16 [B][Hkv][D], position `pos`) is appended
  *      to the important tier with score 0;
  *   2. q fp16 [B][Hq][D] attends over both tiers (split-K partials);
- *   3. one kernel per (batch, key head) merges the partials into out fp32
- *      [B][Hq][D] and lse fp32 [B][Hq], adds the step's attention to the H2O score
- *      of every important slot, and, if policy == MIKV_H2O and the important tier
- *      now holds more than n_keep(pos + 1) tokens, demotes the victim (see
- *      mikv_select(MIKV_DEMOTE)).  MIKV_CRITICALKV never demotes.
+ *   3. the partials are merged into out fp32 [B][Hq][D] and lse fp32 [B][Hq];
+ *   4. the step's attention is added to the H2O score of every important slot,
+ *      and, if policy == MIKV_H2O and the important tier now holds more than
+ *      n_keep(pos + 1) tokens, the victim (see mikv_select(MIKV_DEMOTE)) is
+ *      demoted.  MIKV_CRITICALKV never demotes.
  * The order follows H2O: evict after the step's attention ([notes] "Key
  * contributions 1)"; [paperlayer] 5).  ws >= mikv_decode_step_workspace_bytes(c)
- * (partials plus the important-tier logits).  Counts in *c are updated.
- * Errors: EINVAL, ESHAPE (capacity, budget, workspace), EALIGN, EUNSUPPORTED, ECUDA.
+ * (partials, the important-tier logits, per-chunk victim candidates).  Counts in
+ * *c are updated.  Two calls must not share a workspace concurrently.
+ * Errors: EINVAL, ESHAPE (capacity, budget, workspace), EALIGN, EUNSUPPORTED
+ * (cap_hi above 65535*1024), ECUDA.
  */
 int mikv_decode_step(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new, int pos,
                      int budget_pct, int window, int policy, mikv_cache* c, float* out, float* lse,
                      void* ws, size_t ws_bytes, void* stream);
 size_t mikv_decode_step_workspace_bytes(const mikv_cache* c);
+
+/*
+ * Measurement hook (no counterpart in the papers): while set, every
+ * mikv_decode_attention and mikv_decode_step call made by this thread records
+ * `begin` (a cudaEvent_t) on its stream just before the split-K attention
+ * launch and `end` just after it, so that a caller can time that kernel alone
+ * with cudaEventElapsedTime.  The events are owned by the caller and must stay
+ * valid while set; (NULL, NULL) clears the hook.  Setting only one of the two
+ * is EINVAL.  A failed record is reported as ECUDA by the call that made it.
+ */
+int mikv_set_attention_events(void* begin, void* end);
 
 /* Message of the last failed call on this thread ("" if none). */
 const char* mikv_last_error(void);

@@ -24,7 +24,7 @@ EXPORTS = (
     "mikv_quantize_append",
     "mikv_decode_attention", "mikv_decode_workspace_bytes",
     "mikv_decode_step", "mikv_decode_step_workspace_bytes",
-    "mikv_last_error",
+    "mikv_set_attention_events", "mikv_last_error",
 )
 
 
@@ -76,6 +76,7 @@ def load() -> ctypes.CDLL:
         "mikv_decode_workspace_bytes": (S, [CP]),
         "mikv_decode_step": (I, [P, P, P, I, I, I, I, CP, P, P, P, S, P]),
         "mikv_decode_step_workspace_bytes": (S, [CP]),
+        "mikv_set_attention_events": (I, [P, P]),
         "mikv_last_error": (ctypes.c_char_p, []),
     }
     for name, (res, args) in sig.items():
@@ -182,3 +183,12 @@ def mikv_decode_step(q, k_new, v_new, pos, budget_pct, window, policy, cache, ou
     _check("mikv_decode_step", lib.mikv_decode_step(
         _ptr(q), _ptr(k_new), _ptr(v_new), pos, budget_pct, window, policy, ctypes.byref(c),
         _ptr(out), _ptr(lse), _ptr(w), nb, _stream(stream)))
+
+
+def mikv_set_attention_events(begin=None, end=None):
+    """Record two torch.cuda.Event objects around the split-K attention launch of every
+    following decode call of this thread (None, None clears).  Each event must have been
+    recorded once through torch, so that its CUDA event exists."""
+    lib = load()
+    h = lambda e: None if e is None else e.cuda_event
+    _check("mikv_set_attention_events", lib.mikv_set_attention_events(h(begin), h(end)))

@@ -8,8 +8,8 @@ which call comes next, with which counts:
            CRITICALKV) -> mikv_quantize_append(HI, kept) -> mikv_quantize_append(LO, evicted)
   decode   mikv_quantize_append(HI, new token) -> mikv_decode_attention ->
            mikv_score_update(DECODE) -> [H2O, over budget] mikv_select(DEMOTE) ->
-           mikv_quantize_append(DEMOTE); mikv_decode_step runs the same step in three
-           launches (append, split-K attention, fused merge/score/demotion)
+           mikv_quantize_append(DEMOTE); mikv_decode_step runs the same step in four
+           launches (append, split-K attention, merge, score update + demotion)
 
 (MiKV reading notes, "Key contributions 1)-3)" and section 3.4; CriticalKV
 summary, "Algorithm".)  The budget is n_keep(L) = min(L, max(W, floor(p*L/100)))
@@ -125,8 +125,8 @@ class MikvCache:
 
     # --- decode --------------------------------------------------------------------
     def decode_step(self, q, k, v, L_before, budget_pct, window, policy="h2o"):
-        """One decode step through mikv_decode_step (append, attention, fused merge + score
-        update + demotion); q [B,Hq,D], k/v [B,Hkv,D] fp16.  Returns (out, lse) views."""
+        """One decode step through mikv_decode_step (append, attention, merge, score update +
+        demotion); q [B,Hq,D], k/v [B,Hkv,D] fp16.  Returns (out, lse) views."""
         pol = _lib.MIKV_H2O if policy == "h2o" else _lib.MIKV_CRITICALKV
         _lib.mikv_decode_step(q, k, v, L_before, budget_pct, window, pol, self, self.out, self.lse,
                               ws=self.ws_decode)

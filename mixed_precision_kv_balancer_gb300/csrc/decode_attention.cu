@@ -696,80 +696,144 @@ __global__ void __launch_bounds__(kThreads, 3) decode_partial_kernel(Params P) {
 }
 
 // K8: merge the split partials (base-2 max m, sum l, unnormalised o) of one query head
-// (row = b*Hq + h), thread c = channel; returns the row's natural log-sum-exp.
-__device__ __forceinline__ float merge_head(const float* __restrict__ ws_o,
-                                           const float* __restrict__ ws_ml, int smax, int nsplit,
-                                           long row, int c, float* __restrict__ out) {
+// (row = b*Hq + h) into its output row and natural log-sum-exp.  The CTA holds G groups of
+// kD threads (thread = channel); group g folds splits g, g+G, g+2G, ... in ascending order
+// and the group sums are then added in group order.  G depends on nsplit only, so every
+// caller of this kernel gets the same bits.  With `ticket` set, the first head of each
+// (batch, key head) also clears that unit's ticket for the score/demotion kernel after it.
+int merge_groups(int nsplit) { return nsplit >= 96 ? 8 : (nsplit >= 48 ? 4 : (nsplit >= 12 ? 2 : 1)); }
+
+__global__ void __launch_bounds__(8 * kD) decode_merge_kernel(const float* __restrict__ ws_o,
+                                                              const float* __restrict__ ws_ml,
+                                                              int smax, int nsplit,
+                                                              float* __restrict__ out,
+                                                              float* __restrict__ lse,
+                                                              unsigned* __restrict__ ticket, int rep) {
+  __shared__ float so[7][kD];
+  __shared__ float sl[7];
+  __shared__ float smx[32];
+  const int G = blockDim.x / kD;
+  const int c = threadIdx.x % kD, gi = threadIdx.x / kD;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long row = blockIdx.x;
   const float* ml = ws_ml + row * smax * 2;
+  // the running maxima: max is exact in any order
   float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ml[2 * s]);
+  for (int s = threadIdx.x; s < nsplit; s += blockDim.x) M = fmaxf(M, ml[2 * s]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) smx[warp] = M;
+  __syncthreads();
+  M = smx[0];
+  for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) M = fmaxf(M, smx[w]);
   float L = 0.f, O = 0.f;
-  for (int s = 0; s < nsplit; ++s) {
+#pragma unroll 8
+  for (int s = gi; s < nsplit; s += G) {
     const float ms = ml[2 * s];
     const float sc = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
     L += sc * ml[2 * s + 1];
     O += sc * ws_o[(row * smax + s) * kD + c];
   }
-  out[row * kD + c] = O / L;
-  return (M + log2f(L)) * 0.69314718055994531f;
-}
-
-__global__ void __launch_bounds__(kD) decode_merge_kernel(const float* __restrict__ ws_o,
-                                                          const float* __restrict__ ws_ml,
-                                                          int smax, int nsplit,
-                                                          float* __restrict__ out,
-                                                          float* __restrict__ lse) {
-  const long row = blockIdx.x;
-  const float l = merge_head(ws_o, ws_ml, smax, nsplit, row, threadIdx.x, out);
-  if (threadIdx.x == 0) lse[row] = l;
-}
-
-// Fused end of a decode step, one CTA per (batch, key head): merge the split partials of
-// the group's query heads (as decode_merge_kernel), add this step's attention to the H2O
-// score of every important slot (as the decode score update), and, when the important
-// tier is over budget, pick the victim (score ascending, position descending, among
-// positions < limit) and demote it (as the separate demotion calls).  The arithmetic of
-// every part is the same code as its separate kernel, so results are identical.
-struct EpiArgs {
-  const float* ws_o;
-  const float* ws_ml;
-  int smax, nsplit;
-  float* out;
-  float* lse;
-  const float* logits;  // [B][Hq][cap_hi]
-  int Hq, Hkv, rep;
-  int demote, limit;
-  DemoteArgs da;        // counts after this step's append
-};
-
-__global__ void __launch_bounds__(kD) decode_epilogue_kernel(EpiArgs a) {
-  __shared__ float s_lse[8];
-  __shared__ float rs[kD];
-  __shared__ int rp[kD], rj[kD];
-  const long unit = blockIdx.x;
-  const int b = static_cast<int>(unit / a.Hkv), g = static_cast<int>(unit % a.Hkv);
-  const int c = threadIdx.x;
-  const long row0 = static_cast<long>(b) * a.Hq + static_cast<long>(g) * a.rep;
-  for (int h = 0; h < a.rep; ++h) {
-    const float l = merge_head(a.ws_o, a.ws_ml, a.smax, a.nsplit, row0 + h, c, a.out);
-    if (c == 0) {
-      a.lse[row0 + h] = l;
-      s_lse[h] = l;
-    }
+  if (gi > 0) {
+    so[gi - 1][c] = O;
+    if (c == 0) sl[gi - 1] = L;
   }
   __syncthreads();
+  if (gi > 0) return;
+  for (int g = 1; g < G; ++g) {
+    O += so[g - 1][c];
+    L += sl[g - 1];
+  }
+  out[row * kD + c] = O / L;
+  if (c == 0) {
+    lse[row] = (M + log2f(L)) * 0.69314718055994531f;
+    if (ticket != nullptr && row % rep == 0) ticket[row / rep] = 0u;
+  }
+}
+
+// End of a decode step after the merge: add this step's attention to the H2O score of every
+// important slot (the same arithmetic as the separate decode score update) and, when the
+// important tier is over budget, demote the victim: the slot with the lowest score, latest
+// position first among equal scores, among positions < limit (as the separate demotion
+// select + append).  Grid (B*Hkv units, chunks of kEpiChunk slots).  Each CTA reduces its
+// chunk's candidate, publishes it, and takes a ticket; the CTA that takes the unit's last
+// ticket reduces the published candidates and moves the victim.  No CTA waits on another.
+constexpr int kEpiThreads = 256;
+constexpr int kEpiPer = 4;
+constexpr int kEpiChunk = kEpiThreads * kEpiPer;
+
+struct EpiArgs {
+  const float* logits;  // [B][Hq][cap_hi]
+  const float* lse;     // [B][Hq], from the merge
+  int Hq, Hkv, rep, nchunk;
+  int demote, limit;
+  DemoteArgs da;        // counts after this step's append
+  float* cand_s;        // [B*Hkv][nchunk] per-chunk candidates
+  int* cand_p;
+  int* cand_j;
+  unsigned* ticket;     // [B*Hkv], cleared by the merge
+};
+
+// (s1, p1, j1) is a better victim than (s0, p0, j0); j < 0 marks "no candidate"
+__device__ __forceinline__ bool victim_better(float s1, int p1, int j1, float s0, int p0, int j0) {
+  return j1 >= 0 && (j0 < 0 || s1 < s0 || (s1 == s0 && p1 > p0));
+}
+
+__device__ __forceinline__ void victim_warp_min(float& s, int& p, int& j) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    const int p2 = __shfl_xor_sync(0xffffffffu, p, o);
+    const int j2 = __shfl_xor_sync(0xffffffffu, j, o);
+    if (victim_better(s2, p2, j2, s, p, j)) {
+      s = s2;
+      p = p2;
+      j = j2;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kEpiThreads) decode_score_demote_kernel(EpiArgs a) {
+  __shared__ float s_lse[8];
+  __shared__ float ws_s[kEpiThreads / 32];
+  __shared__ int ws_p[kEpiThreads / 32], ws_j[kEpiThreads / 32];
+  __shared__ int s_last;
+  const long unit = blockIdx.x;
+  const int chunk = blockIdx.y;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int b = static_cast<int>(unit / a.Hkv), g = static_cast<int>(unit % a.Hkv);
+  const long row0 = static_cast<long>(b) * a.Hq + static_cast<long>(g) * a.rep;
+  if (t < a.rep) s_lse[t] = a.lse[row0 + t];
+  __syncthreads();
   const int cap = a.da.cap_hi, n = a.da.n_hi;
+  const long ubase = unit * cap;
+  // every load of the thread's slots is issued before the first use
+  float lg[kEpiPer][8], sc[kEpiPer];
+  int ps[kEpiPer];
+#pragma unroll
+  for (int i = 0; i < kEpiPer; ++i) {
+    const int j = chunk * kEpiChunk + i * kEpiThreads + t;
+    const bool in = j < n;
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      lg[i][r] = (in && r < a.rep) ? a.logits[(row0 + r) * cap + j] : 0.f;
+    sc[i] = in ? a.da.scores[ubase + j] : 0.f;
+    ps[i] = (in && a.demote) ? a.da.pos_hi[ubase + j] : 0;
+  }
   float bs = INFINITY;
   int bp = -1, bj = -1;
-  for (int j = c; j < n; j += kD) {
-    float add = 0.f;
-    for (int r = 0; r < a.rep; ++r) add += expf(a.logits[(row0 + r) * cap + j] - s_lse[r]);
-    const long idx = unit * cap + j;
-    const float sv = a.da.scores[idx] + add;
-    a.da.scores[idx] = sv;
-    if (a.demote) {
-      const int p = a.da.pos_hi[idx];
-      if (p < a.limit && (bj < 0 || sv < bs || (sv == bs && p > bp))) {
+#pragma unroll
+  for (int i = 0; i < kEpiPer; ++i) {
+    const int j = chunk * kEpiChunk + i * kEpiThreads + t;
+    if (j < n) {
+      float add = 0.f;
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        if (r < a.rep) add += expf(lg[i][r] - s_lse[r]);
+      const float sv = sc[i] + add;
+      a.da.scores[ubase + j] = sv;
+      const int p = ps[i];
+      if (a.demote && p < a.limit && victim_better(sv, p, j, bs, bp, bj)) {
         bs = sv;
         bp = p;
         bj = j;
@@ -777,23 +841,44 @@ __global__ void __launch_bounds__(kD) decode_epilogue_kernel(EpiArgs a) {
     }
   }
   if (!a.demote) return;
-  rs[c] = bs;
-  rp[c] = bp;
-  rj[c] = bj;
-  __syncthreads();
-  for (int o = kD / 2; o > 0; o >>= 1) {
-    if (c < o) {
-      const int t = c + o;
-      const bool better = rj[t] >= 0 && (rj[c] < 0 || rs[t] < rs[c] || (rs[t] == rs[c] && rp[t] > rp[c]));
-      if (better) {
-        rs[c] = rs[t];
-        rp[c] = rp[t];
-        rj[c] = rj[t];
-      }
-    }
-    __syncthreads();
+  victim_warp_min(bs, bp, bj);
+  if (lane == 0) {
+    ws_s[warp] = bs;
+    ws_p[warp] = bp;
+    ws_j[warp] = bj;
   }
-  if (c < 32) demote_one(a.da, unit, rj[0], c);
+  __syncthreads();
+  if (t == 0) {
+    for (int w = 1; w < kEpiThreads / 32; ++w)
+      if (victim_better(ws_s[w], ws_p[w], ws_j[w], bs, bp, bj)) {
+        bs = ws_s[w];
+        bp = ws_p[w];
+        bj = ws_j[w];
+      }
+    const long ci = unit * a.nchunk + chunk;
+    a.cand_s[ci] = bs;
+    a.cand_p[ci] = bp;
+    a.cand_j[ci] = bj;
+    __threadfence();  // scores and candidate visible before the ticket is taken
+    s_last = atomicAdd(&a.ticket[unit], 1u) == static_cast<unsigned>(a.nchunk - 1);
+  }
+  __syncthreads();
+  if (!s_last || warp != 0) return;
+  __threadfence();  // every other chunk's scores and candidate are visible from here on
+  bs = INFINITY;
+  bp = bj = -1;
+  for (int k = lane; k < a.nchunk; k += 32) {
+    const long ci = unit * a.nchunk + k;
+    const float s2 = __ldcg(a.cand_s + ci);
+    const int p2 = __ldcg(a.cand_p + ci), j2 = __ldcg(a.cand_j + ci);
+    if (victim_better(s2, p2, j2, bs, bp, bj)) {
+      bs = s2;
+      bp = p2;
+      bj = j2;
+    }
+  }
+  victim_warp_min(bs, bp, bj);
+  demote_one(a.da, unit, bj, lane);
 }
 
 // ---------------------------------------------------------------------------------
@@ -906,16 +991,30 @@ int prepare_decode(const uint16_t* q, const mikv_cache* c, float* hi_logits, voi
   return MIKV_OK;
 }
 
+thread_local cudaEvent_t t_ev_begin = nullptr, t_ev_end = nullptr;
+
+int record_hook(cudaEvent_t ev, cudaStream_t s) {
+  if (ev == nullptr) return MIKV_OK;
+  const cudaError_t err = cudaEventRecord(ev, s);
+  if (err == cudaSuccess) return MIKV_OK;
+  (void)cudaGetLastError();
+  return fail(MIKV_ECUDA, "attention event record: %s", cudaGetErrorString(err));
+}
+
 int launch_partials(const Params& P, const mikv_cache* c, int nsplit, cudaStream_t s) {
   const dim3 grid(nsplit, c->B * c->Hkv);
+  if (int e = record_hook(t_ev_begin, s)) return e;
+  int e;
   switch (c->hi_bits * 100 + c->lo_bits) {
-    case 1602: return launch_nt<16, 2>(P, grid, s);
-    case 1604: return launch_nt<16, 4>(P, grid, s);
-    case 1608: return launch_nt<16, 8>(P, grid, s);
-    case 802: return launch_nt<8, 2>(P, grid, s);
-    case 804: return launch_nt<8, 4>(P, grid, s);
-    default: return launch_nt<8, 8>(P, grid, s);
+    case 1602: e = launch_nt<16, 2>(P, grid, s); break;
+    case 1604: e = launch_nt<16, 4>(P, grid, s); break;
+    case 1608: e = launch_nt<16, 8>(P, grid, s); break;
+    case 802: e = launch_nt<8, 2>(P, grid, s); break;
+    case 804: e = launch_nt<8, 4>(P, grid, s); break;
+    default: e = launch_nt<8, 8>(P, grid, s); break;
   }
+  if (e) return e;
+  return record_hook(t_ev_end, s);
 }
 
 int n_keep_of(int L, int pct, int window) {
@@ -924,6 +1023,15 @@ int n_keep_of(int L, int pct, int window) {
 }
 }  // namespace
 }  // namespace mikv
+
+extern "C" int mikv_set_attention_events(void* begin, void* end) {
+  clear_error();
+  if ((begin == nullptr) != (end == nullptr))
+    return fail(MIKV_EINVAL, "set_attention_events: give both events or neither");
+  t_ev_begin = static_cast<cudaEvent_t>(begin);
+  t_ev_end = static_cast<cudaEvent_t>(end);
+  return MIKV_OK;
+}
 
 extern "C" int mikv_decode_attention(const uint16_t* q, const mikv_cache* c, float* out,
                                      float* lse, float* hi_logits, void* ws, size_t ws_bytes,
@@ -936,14 +1044,37 @@ extern "C" int mikv_decode_attention(const uint16_t* q, const mikv_cache* c, flo
   if (int e = prepare_decode(q, c, hi_logits, ws, ws_bytes, P, nsplit, "decode_attention")) return e;
   cudaStream_t s = as_stream(stream);
   if (int e = launch_partials(P, c, nsplit, s)) return e;
-  decode_merge_kernel<<<c->B * c->Hq, kD, 0, s>>>(P.ws_o, P.ws_ml, P.smax, nsplit, out, lse);
+  decode_merge_kernel<<<c->B * c->Hq, kD * merge_groups(nsplit), 0, s>>>(
+      P.ws_o, P.ws_ml, P.smax, nsplit, out, lse, nullptr, c->Hq / c->Hkv);
   return check_launch("decode_merge_kernel");
 }
+
+namespace mikv {
+namespace {
+// Step workspace after the attention workspace: per-head logits of the important tier, then
+// per-chunk victim candidates (score, position, slot) and one ticket per (batch, key head).
+struct StepWs {
+  size_t logits, cand_s, cand_p, cand_j, ticket, total;
+};
+StepWs step_ws_layout(const mikv_cache* c, size_t dec_ws) {
+  const size_t units = static_cast<size_t>(c->B) * c->Hkv;
+  const size_t nchunk = std::max<size_t>(1, (static_cast<size_t>(c->cap_hi) + kEpiChunk - 1) / kEpiChunk);
+  StepWs w;
+  w.logits = dec_ws;
+  w.cand_s = w.logits + align_up(static_cast<size_t>(c->B) * c->Hq * c->cap_hi * sizeof(float), 256);
+  w.cand_p = w.cand_s + align_up(units * nchunk * sizeof(float), 256);
+  w.cand_j = w.cand_p + align_up(units * nchunk * sizeof(int), 256);
+  w.ticket = w.cand_j + align_up(units * nchunk * sizeof(int), 256);
+  w.total = w.ticket + align_up(units * sizeof(unsigned), 256);
+  return w;
+}
+}  // namespace
+}  // namespace mikv
 
 extern "C" size_t mikv_decode_step_workspace_bytes(const mikv_cache* c) {
   const size_t a = mikv_decode_workspace_bytes(c);
   if (a == 0) return 0;
-  return a + align_up(static_cast<size_t>(c->B) * c->Hq * c->cap_hi * sizeof(float), 256);
+  return step_ws_layout(c, a).total;
 }
 
 extern "C" int mikv_decode_step(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
@@ -956,6 +1087,8 @@ extern "C" int mikv_decode_step(const uint16_t* q, const uint16_t* k_new, const 
   if (pos < 0 || budget_pct < 0 || budget_pct > 100 || window < 0)
     return fail(MIKV_ESHAPE, "decode_step: pos=%d budget_pct=%d window=%d", pos, budget_pct, window);
   if (c->n_hi + 1 > c->cap_hi) return fail(MIKV_ESHAPE, "decode_step: important tier full (%d)", c->cap_hi);
+  if ((c->cap_hi + kEpiChunk - 1) / kEpiChunk > 65535)
+    return fail(MIKV_EUNSUPPORTED, "decode_step: cap_hi %d above %d", c->cap_hi, 65535 * kEpiChunk);
   const size_t need = mikv_decode_step_workspace_bytes(c);
   if (ws_bytes < need) return fail(MIKV_ESHAPE, "decode_step: workspace %zu < %zu", ws_bytes, need);
   const int L = pos + 1;
@@ -972,7 +1105,9 @@ extern "C" int mikv_decode_step(const uint16_t* q, const uint16_t* k_new, const 
     da.pos_hi = after.pos_hi;
   }
   const size_t dec_ws = mikv_decode_workspace_bytes(c);
-  float* logits = reinterpret_cast<float*>(static_cast<char*>(ws) + dec_ws);
+  const StepWs wl = step_ws_layout(c, dec_ws);
+  char* wsb = static_cast<char*>(ws);
+  float* logits = reinterpret_cast<float*>(wsb + wl.logits);
   Params P;
   int nsplit = 0;
   if (int e = prepare_decode(q, &after, logits, ws, dec_ws, P, nsplit, "decode_step")) return e;
@@ -982,23 +1117,29 @@ extern "C" int mikv_decode_step(const uint16_t* q, const uint16_t* k_new, const 
   c->n_hi += 1;
   // 2. split-K attention over both tiers
   if (int e = launch_partials(P, &after, nsplit, s)) return e;
-  // 3. merge + score update + demotion
+  // 3. merge (clears the demotion tickets)
+  unsigned* ticket = reinterpret_cast<unsigned*>(wsb + wl.ticket);
+  const int rep = c->Hq / c->Hkv;
+  decode_merge_kernel<<<c->B * c->Hq, kD * merge_groups(nsplit), 0, s>>>(
+      P.ws_o, P.ws_ml, P.smax, nsplit, out, lse, ticket, rep);
+  if (int e = check_launch("decode_merge_kernel")) return e;
+  // 4. score update + demotion
   EpiArgs ea{};
-  ea.ws_o = P.ws_o;
-  ea.ws_ml = P.ws_ml;
-  ea.smax = P.smax;
-  ea.nsplit = nsplit;
-  ea.out = out;
-  ea.lse = lse;
   ea.logits = logits;
+  ea.lse = lse;
   ea.Hq = c->Hq;
   ea.Hkv = c->Hkv;
-  ea.rep = c->Hq / c->Hkv;
+  ea.rep = rep;
+  ea.nchunk = std::max(1, (after.n_hi + kEpiChunk - 1) / kEpiChunk);
   ea.demote = demote ? 1 : 0;
   ea.limit = L - window;
   ea.da = da;
-  decode_epilogue_kernel<<<c->B * c->Hkv, kD, 0, s>>>(ea);
-  if (int e = check_launch("decode_epilogue_kernel")) return e;
+  ea.cand_s = reinterpret_cast<float*>(wsb + wl.cand_s);
+  ea.cand_p = reinterpret_cast<int*>(wsb + wl.cand_p);
+  ea.cand_j = reinterpret_cast<int*>(wsb + wl.cand_j);
+  ea.ticket = ticket;
+  decode_score_demote_kernel<<<dim3(c->B * c->Hkv, ea.nchunk), kEpiThreads, 0, s>>>(ea);
+  if (int e = check_launch("decode_score_demote_kernel")) return e;
   if (demote) {
     c->n_hi -= 1;
     c->n_lo += 1;

@@ -132,7 +132,7 @@ __device__ __forceinline__ void demote_one(const DemoteArgs& a, long unit, int v
     }
     if (lane == 0) {
       a.pos_hi[hs] = a.pos_hi[last];
-      a.scores[hs] = a.scores[last];
+      a.scores[hs] = __ldcg(a.scores + last);  // may have been updated by another CTA
     }
   }
 }

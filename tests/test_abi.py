@@ -94,3 +94,7 @@ def test_host_side_rejections(lib):
                            None, fake, None, None, 0, None) == ESHAPE     # n_hi <= window
     assert lib.mikv_score_update(9, None, None, 0, None, None, ctypes.byref(_cache()), None, None,
                                  None, 0, None) == EINVAL
+    # the attention timing hook takes both events or neither
+    assert lib.mikv_set_attention_events(fake, None) == EINVAL
+    assert lib.mikv_set_attention_events(None, fake) == EINVAL
+    assert lib.mikv_set_attention_events(None, None) == 0
