@@ -47,6 +47,8 @@ def parse():
     p.add_argument("--batch", type=int, default=None)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-attn-events", action="store_true",
+                   help="do not time the attention kernel alone (roofline from the whole step)")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     return p.parse_args()
 
@@ -210,10 +212,13 @@ def run_gpu(args, wl, rank, world):
     torch.cuda.set_device(dev)
     _lib.load()
     total_steps = args.warmup + args.steps
-    keep0 = n_keep(wl.T, wl.budget_pct, wl.window)
+    # after the timed steps: K steps with the attention kernel timed alone, then K e2e steps
+    attn_steps = 0 if args.no_attn_events else args.steps
     e2e_steps = 0 if args.no_e2e else args.steps
-    cap_hi = keep0 + total_steps + e2e_steps + 1
-    cap_lo = (wl.T - keep0) + total_steps + e2e_steps + 1
+    keep0 = n_keep(wl.T, wl.budget_pct, wl.window)
+    extra = attn_steps + e2e_steps
+    cap_hi = keep0 + total_steps + extra + 1
+    cap_lo = (wl.T - keep0) + total_steps + extra + 1
     layers = []
     prefill_ms = []
     for l in range(wl.layers):
@@ -230,7 +235,7 @@ def run_gpu(args, wl, rank, world):
     torch.cuda.empty_cache()
     # decode tokens for every step and layer, resident before timing
     toks = [[inputs.make_decode_token(rank_seed(wl, rank), l, s, dev)
-             for l in range(wl.layers)] for s in range(total_steps + (0 if args.no_e2e else args.steps))]
+             for l in range(wl.layers)] for s in range(total_steps + extra)]
     torch.cuda.synchronize()
 
     def new_event():
@@ -238,31 +243,34 @@ def run_gpu(args, wl, rank, world):
         e.record()              # creates the CUDA event; the library records it again later
         return e
 
-    # events for every timed (step, layer): the whole step, and the split-K attention kernel
-    # alone (recorded by the library on the launching stream, around that one launch)
-    n_timed = args.steps * wl.layers
-    step_ev = [(new_event(), new_event()) for _ in range(n_timed)]
-    attn_ev = [(new_event(), new_event()) for _ in range(n_timed)]
+    # events per (step, layer): the whole layer step in the timed steps; the split-K attention
+    # kernel alone in the attention pass (recorded by the library on the launching stream
+    # around that one launch).  Events between the step's kernels stop them from overlapping
+    # one another's launch, so the timed steps run without them.
+    n_ev = args.steps * wl.layers
+    step_ev = [(new_event(), new_event()) for _ in range(n_ev)]
+    attn_ev = [(new_event(), new_event()) for _ in range(n_ev if attn_steps else 0)]
     torch.cuda.synchronize()
 
-    def step(s, timed=False):
+    def step(s, mode=None):
         L_before = wl.T + s
         for l, c in enumerate(layers):
             t = toks[s][l]
-            if timed:
-                i = len(ev_pairs)
-                read = cache_bytes(wl, c.n_hi + 1, c.n_lo)   # tiers as attended (after the append)
-                e0, e1 = step_ev[i]
-                a0, a1 = attn_ev[i]
-                _lib.mikv_set_attention_events(a0, a1)
+            if mode == "step":
+                e0, e1 = step_ev[len(step_pairs)]
+                step_pairs.append((e0, e1))
                 e0.record()
+            elif mode == "attn":
+                a0, a1 = attn_ev[len(attn_pairs)]
+                # tiers as attended (after the append)
+                attn_pairs.append((a0, a1, cache_bytes(wl, c.n_hi + 1, c.n_lo)))
+                _lib.mikv_set_attention_events(a0, a1)
             c.decode_step(t["q"], t["k"], t["v"], L_before, wl.budget_pct, wl.window)
-            if timed:
+            if mode == "step":
                 e1.record()
-                ev_pairs.append((e0, e1, a0, a1, read))
         return 4 * len(layers)   # append, split-K attention, merge, score update/demotion
 
-    ev_pairs = []
+    step_pairs, attn_pairs = [], []
     for s in range(args.warmup):
         step(s)
     torch.cuda.synchronize()
@@ -273,31 +281,41 @@ def run_gpu(args, wl, rank, world):
     time.sleep(0.3)
     kv_tokens = 0
     launches = 0
+    read_bytes = []
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record()
     for s in range(args.warmup, total_steps):
         L = wl.T + s + 1
         kv_tokens += wl.B * L * wl.layers
-        launches += step(s, timed=True)
+        read_bytes += [cache_bytes(wl, c.n_hi + 1, c.n_lo) for c in layers]
+        launches += step(s, mode="step")
     end.record()
     torch.cuda.synchronize()
-    _lib.mikv_set_attention_events(None, None)
     ms = start.elapsed_time(end)
+    # attention pass: the same steps continued, the attention kernel of every layer timed alone
+    for s in range(total_steps, total_steps + attn_steps):
+        step(s, mode="attn")
+    torch.cuda.synchronize()
+    _lib.mikv_set_attention_events(None, None)
     clk = clocks.stop()
     ms = reduce_over_ranks(ms, world, dev)
-    step_ms = [e0.elapsed_time(e1) for e0, e1, _, _, _ in ev_pairs]
-    attn_ms = [a0.elapsed_time(a1) for _, _, a0, a1, _ in ev_pairs]
-    attn_bytes = [nb for *_, nb in ev_pairs]
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in step_pairs]
+    if attn_pairs:
+        attn_ms = [a0.elapsed_time(a1) for a0, a1, _ in attn_pairs]
+        attn_bytes = [nb for *_, nb in attn_pairs]
+    else:
+        attn_ms, attn_bytes = step_ms, read_bytes
     res = dict(ms=ms, kv_tokens=kv_tokens * world, launches=launches, clocks=clk,
                attn_ms_mean=statistics.mean(attn_ms), attn_bytes_mean=statistics.mean(attn_bytes),
-               step_ms_mean=statistics.mean(step_ms), attn_ms_sum=sum(attn_ms),
+               step_ms_mean=statistics.mean(step_ms), step_bytes_mean=statistics.mean(read_bytes),
                prefill_ms_per_layer=statistics.mean(prefill_ms))
+    e2e_first = total_steps + attn_steps
 
     # ---- end to end through the public API with host buffers
     if not args.no_e2e:
         host_in = [[{n: t.cpu().pin_memory() for n, t in toks[s][l].items()} for l in range(wl.layers)]
-                   for s in range(total_steps, total_steps + args.steps)]
+                   for s in range(e2e_first, e2e_first + args.steps)]
         host_out = [torch.empty(wl.B, wl.Hq, wl.D, dtype=torch.float32).pin_memory() for _ in range(wl.layers)]
         h2d = sum(t.numel() * t.element_size() for t in host_in[0][0].values()) * wl.layers
         d2h = sum(t.numel() * t.element_size() for t in host_out)
@@ -307,7 +325,7 @@ def run_gpu(args, wl, rank, world):
         t0 = time.perf_counter()
         e0.record()
         e2e_tokens = 0
-        for i, s in enumerate(range(total_steps, total_steps + args.steps)):
+        for i, s in enumerate(range(e2e_first, e2e_first + args.steps)):
             L_before = wl.T + s
             for l, c in enumerate(layers):
                 for n in ("q", "k", "v"):
@@ -389,7 +407,7 @@ def main():
     value = res["kv_tokens"] / (res["ms"] / 1e3)
     peak, peak_kind = peaks()
     achieved = res["attn_bytes_mean"] / (res["attn_ms_mean"] / 1e3) / 1e9
-    step_gbs = res["attn_bytes_mean"] / (res["step_ms_mean"] / 1e3) / 1e9
+    step_gbs = res["step_bytes_mean"] / (res["step_ms_mean"] / 1e3) / 1e9
     traffic = None
     if wl.name in TRAFFIC_PER_UNIT and same_cache_shape(wl):
         traffic = TRAFFIC_PER_UNIT[wl.name] * wl.B * wl.Hkv
@@ -401,12 +419,19 @@ def main():
         "hbm_gbs_decode_attn": achieved, "frac_of_8tbs": achieved / 8000.0,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "kernel": "decode_partial_kernel (split-K attention over both tiers), one "
-                               "launch per layer per step; bytes = packed cache as attended",
+                     "kernel": ("whole mikv_decode_step per layer (4 launches)" if args.no_attn_events
+                                else "decode_partial_kernel (split-K attention over both tiers), "
+                                     "one launch per layer per step")
+                               + "; bytes = packed cache as attended",
                      "bytes_per_launch": res["attn_bytes_mean"], "ms_per_launch": res["attn_ms_mean"],
+                     "timing": ("CUDA events around each layer step in the timed steps"
+                                if args.no_attn_events else
+                                "CUDA events recorded by the library on the launching stream around "
+                                "each layer's attention launch, over %d further steps after the "
+                                "timed ones" % args.steps),
                      "traffic": traffic},
         "decode_step_gbs": step_gbs, "decode_step_ms_per_layer": res["step_ms_mean"],
-        "decode_attn_ms_per_step": res["attn_ms_sum"] / args.steps,
+        "decode_attn_ms_per_step": res["attn_ms_mean"] * wl.layers,
         "prefill_ms_per_layer": res["prefill_ms_per_layer"],
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],

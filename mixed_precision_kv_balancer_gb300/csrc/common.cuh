@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "mikv.h"
 
 namespace mikv {
@@ -107,6 +109,41 @@ __device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
 __device__ __forceinline__ void split_f16(float x, __half& hi, __half& lo) {
   hi = __float2half_rn(x);
   lo = __float2half_rn(__fsub_rn(x, __half2float(hi)));
+}
+
+// Programmatic dependent launch.  A kernel started by launch_after() may begin while the
+// kernel before it in the stream is still running; pdl_wait() returns once that kernel has
+// completed and its writes are visible (at once for a normal launch).  Every CTA of such a
+// kernel calls pdl_wait() before its first global access, so each kernel of a chain also
+// completes after its predecessor.  pdl_trigger() lets the next kernel start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::); }
+
+// Launch `kern` on `s` so that it may overlap the tail of the kernel launched just before it
+// on the same stream (that kernel must be one of ours, and `kern` must call pdl_wait()).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                         cudaStream_t s, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// Status of a launch_after(): its own error, else any pending launch error.
+inline int check_launch_after(cudaError_t err, const char* what) {
+  if (err != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(MIKV_ECUDA, "%s: %s", what, cudaGetErrorString(err));
+  }
+  return check_launch(what);
 }
 
 // Non-negative floats order like their bit patterns.

@@ -46,12 +46,16 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 2;        // ring depth per warp (3 CTAs of 4 warps fit per SM)
 constexpr float kLogitScale = 0.12751743082459868f;  // log2(e) / sqrt(128)
 
+// Tokens per warp-stage: 16 FP16 rows (8.5 KB with padding), 32 INT8 or INT4 rows, 64 INT2
+// rows, so that 4 warps x 2 stages of any format pairing fit 3 CTAs per SM.
+__host__ __device__ constexpr int stage_tokens(int bits) { return bits == 16 ? 16 : (bits == 2 ? 64 : 32); }
+
 template <int BITS>
 struct Fmt {
   static constexpr bool kQuant = BITS != 16;
   static constexpr int kRB = kD * BITS / 8;                            // bytes per token row
   static constexpr int kRS = kQuant ? kRB : kRB + 16;                  // smem row stride (FP16 padded)
-  static constexpr int kST = BITS == 16 ? 16 : (BITS == 8 ? 32 : 64);  // tokens per stage
+  static constexpr int kST = stage_tokens(BITS);                      // tokens per stage
   static constexpr int kMetaB = kQuant ? 8 : 0;                        // (scale, zero) x 2 groups
   static constexpr int kOffV = kST * kRS;
   static constexpr int kOffKM = 2 * kST * kRS;
@@ -689,6 +693,8 @@ template <int HI, int LO, int NT>
 __global__ void __launch_bounds__(kThreads, 3) decode_partial_kernel(Params P) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(16) float qs[8 * kD + 16];
+  pdl_wait();
+  pdl_trigger();
   const int unit = blockIdx.y;
   const int sx = blockIdx.x;
   if (sx < P.nsplit_hi) run_tier<HI, NT>(P, P.hi, unit, sx, P.chunk_hi, true, smem, qs);
@@ -712,6 +718,8 @@ __global__ void __launch_bounds__(8 * kD) decode_merge_kernel(const float* __res
   __shared__ float so[7][kD];
   __shared__ float sl[7];
   __shared__ float smx[32];
+  pdl_wait();
+  pdl_trigger();
   const int G = blockDim.x / kD;
   const int c = threadIdx.x % kD, gi = threadIdx.x / kD;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -798,6 +806,8 @@ __global__ void __launch_bounds__(kEpiThreads) decode_score_demote_kernel(EpiArg
   __shared__ float ws_s[kEpiThreads / 32];
   __shared__ int ws_p[kEpiThreads / 32], ws_j[kEpiThreads / 32];
   __shared__ int s_last;
+  pdl_wait();
+  pdl_trigger();
   const long unit = blockIdx.x;
   const int chunk = blockIdx.y;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -883,49 +893,77 @@ __global__ void __launch_bounds__(kEpiThreads) decode_score_demote_kernel(EpiArg
 
 // ---------------------------------------------------------------------------------
 // host-side split plan
-int stage_tokens(int bits) { return bits == 16 ? 16 : (bits == 8 ? 32 : 64); }
 int row_cost(int bits) { return bits == 16 ? 512 : 2 * (kD * bits / 8) + 16; }
-int stage_bytes(int bits) { return stage_tokens(bits) * row_cost(bits); }
+// Relative time per byte of a tier: low-bit codes cost more unpacking per byte.
+double byte_weight(int bits) { return bits == 16 ? 1.0 : bits == 8 ? 1.25 : bits == 4 ? 1.5 : 2.0; }
+// Makespan model of the split-K grid, fitted to measured attention times over several
+// plans and cache shapes: a CTA costs its weighted bytes plus a fixed kCtaOverhead, the
+// resident slots share the total, and the tail adds kTailFactor times the largest CTA.
+constexpr double kCtaOverhead = 183.0 * 1024;
+constexpr double kTailFactor = 2.13;
+constexpr double kMinWaves = 2.5;  // keep at least this many waves when the cache allows
+constexpr int kCtasPerSm = 3;
 
 struct Plan {
   int chunk_hi, chunk_lo, smax_hi, smax_lo;
 };
 
+// Split plan from the capacities (so the workspace fits every count up to them).  Each tier
+// is cut into equal chunks of whole warp-stages; over a geometric range of per-CTA targets
+// the plan with the lowest modelled makespan (among those with >= kMinWaves waves) wins.
 Plan make_plan(const mikv_cache* c) {
-  // From the capacities (so the workspace fits every count up to them): a target of
-  // ~5 waves of 3 CTAs per SM, each tier cut into equal chunks of whole warp-stages.
   const double units = static_cast<double>(c->B) * c->Hkv;
-  const double hi_b = static_cast<double>(c->cap_hi) * row_cost(c->hi_bits);
-  const double lo_b = static_cast<double>(c->cap_lo) * row_cost(c->lo_bits);
-  double target = units * (hi_b + lo_b) / (kNumSMs * 3.0 * 5.0);
-  target = std::min(std::max(target, 32.0 * 1024), 384.0 * 1024);
-  auto chunk_for = [&](int cap, double bytes, int bits) {
+  const double slots = static_cast<double>(kNumSMs) * kCtasPerSm;
+  const double wb_hi = row_cost(c->hi_bits) * byte_weight(c->hi_bits);  // per token
+  const double wb_lo = row_cost(c->lo_bits) * byte_weight(c->lo_bits);
+  const double total = units * (c->cap_hi * wb_hi + c->cap_lo * wb_lo);
+  auto chunk_for = [](int cap, double wb, int bits, double target) {
     const int quantum = kWarps * stage_tokens(bits);
-    const int ns = std::max(1, static_cast<int>(bytes / target + 0.5));
-    int chunk = (std::max(cap, 1) + ns - 1) / ns;
+    const int ns = std::max(1, static_cast<int>(cap * wb / target + 0.5));
+    const int chunk = (std::max(cap, 1) + ns - 1) / ns;
     return std::max(quantum, (chunk + quantum - 1) / quantum * quantum);
   };
-  Plan p;
-  p.chunk_hi = chunk_for(c->cap_hi, hi_b, c->hi_bits);
-  p.chunk_lo = chunk_for(c->cap_lo, lo_b, c->lo_bits);
-  p.smax_hi = (c->cap_hi + p.chunk_hi - 1) / p.chunk_hi;
-  p.smax_lo = (c->cap_lo + p.chunk_lo - 1) / p.chunk_lo;
-  return p;
+  Plan best{}, first{};
+  double best_t = INFINITY;
+  bool have_first = false;
+  for (double target = 32.0 * 1024; target <= 2048.0 * 1024; target *= 1.125) {
+    Plan p;
+    p.chunk_hi = chunk_for(c->cap_hi, wb_hi, c->hi_bits, target);
+    p.chunk_lo = chunk_for(c->cap_lo, wb_lo, c->lo_bits, target);
+    p.smax_hi = (c->cap_hi + p.chunk_hi - 1) / p.chunk_hi;
+    p.smax_lo = (c->cap_lo + p.chunk_lo - 1) / p.chunk_lo;
+    if (!have_first) {
+      first = p;
+      have_first = true;
+    }
+    const double ctas = units * (p.smax_hi + p.smax_lo);
+    if (ctas < kMinWaves * slots) continue;
+    const double largest = std::max(std::min(p.chunk_hi, c->cap_hi) * wb_hi,
+                                    std::min(p.chunk_lo, c->cap_lo) * wb_lo);
+    const double t = (total + ctas * kCtaOverhead) / slots + kTailFactor * largest;
+    if (t < best_t) {
+      best_t = t;
+      best = p;
+    }
+  }
+  return best_t < INFINITY ? best : first;
 }
 
 template <int HI, int LO, int NT>
-int launch(const Params& P, dim3 grid, cudaStream_t s) {
+int launch(const Params& P, dim3 grid, cudaStream_t s, bool after) {
   const int smem = kWarps * kStages * std::max(Fmt<HI>::kStageBytes, Fmt<LO>::kStageBytes);
   auto kern = decode_partial_kernel<HI, LO, NT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return check_launch("decode_partial_kernel attribute");
+  if (after) return check_launch_after(launch_after(kern, grid, dim3(kThreads), smem, s, P),
+                                       "decode_partial_kernel");
   kern<<<grid, kThreads, smem, s>>>(P);
   return check_launch("decode_partial_kernel");
 }
 
 template <int HI, int LO>
-int launch_nt(const Params& P, dim3 grid, cudaStream_t s) {
-  return P.rep <= 4 ? launch<HI, LO, 1>(P, grid, s) : launch<HI, LO, 2>(P, grid, s);
+int launch_nt(const Params& P, dim3 grid, cudaStream_t s, bool after) {
+  return P.rep <= 4 ? launch<HI, LO, 1>(P, grid, s, after) : launch<HI, LO, 2>(P, grid, s, after);
 }
 
 }  // namespace
@@ -1001,17 +1039,18 @@ int record_hook(cudaEvent_t ev, cudaStream_t s) {
   return fail(MIKV_ECUDA, "attention event record: %s", cudaGetErrorString(err));
 }
 
-int launch_partials(const Params& P, const mikv_cache* c, int nsplit, cudaStream_t s) {
+// after: the kernel launched just before on `s` is one of ours (the step's append)
+int launch_partials(const Params& P, const mikv_cache* c, int nsplit, cudaStream_t s, bool after) {
   const dim3 grid(nsplit, c->B * c->Hkv);
   if (int e = record_hook(t_ev_begin, s)) return e;
   int e;
   switch (c->hi_bits * 100 + c->lo_bits) {
-    case 1602: e = launch_nt<16, 2>(P, grid, s); break;
-    case 1604: e = launch_nt<16, 4>(P, grid, s); break;
-    case 1608: e = launch_nt<16, 8>(P, grid, s); break;
-    case 802: e = launch_nt<8, 2>(P, grid, s); break;
-    case 804: e = launch_nt<8, 4>(P, grid, s); break;
-    default: e = launch_nt<8, 8>(P, grid, s); break;
+    case 1602: e = launch_nt<16, 2>(P, grid, s, after); break;
+    case 1604: e = launch_nt<16, 4>(P, grid, s, after); break;
+    case 1608: e = launch_nt<16, 8>(P, grid, s, after); break;
+    case 802: e = launch_nt<8, 2>(P, grid, s, after); break;
+    case 804: e = launch_nt<8, 4>(P, grid, s, after); break;
+    default: e = launch_nt<8, 8>(P, grid, s, after); break;
   }
   if (e) return e;
   return record_hook(t_ev_end, s);
@@ -1043,10 +1082,12 @@ extern "C" int mikv_decode_attention(const uint16_t* q, const mikv_cache* c, flo
   int nsplit = 0;
   if (int e = prepare_decode(q, c, hi_logits, ws, ws_bytes, P, nsplit, "decode_attention")) return e;
   cudaStream_t s = as_stream(stream);
-  if (int e = launch_partials(P, c, nsplit, s)) return e;
-  decode_merge_kernel<<<c->B * c->Hq, kD * merge_groups(nsplit), 0, s>>>(
-      P.ws_o, P.ws_ml, P.smax, nsplit, out, lse, nullptr, c->Hq / c->Hkv);
-  return check_launch("decode_merge_kernel");
+  if (int e = launch_partials(P, c, nsplit, s, false)) return e;
+  return check_launch_after(
+      launch_after(decode_merge_kernel, dim3(c->B * c->Hq), dim3(kD * merge_groups(nsplit)), 0, s,
+                   P.ws_o, P.ws_ml, P.smax, nsplit, out, lse, static_cast<unsigned*>(nullptr),
+                   c->Hq / c->Hkv),
+      "decode_merge_kernel");
 }
 
 namespace mikv {
@@ -1116,13 +1157,15 @@ extern "C" int mikv_decode_step(const uint16_t* q, const uint16_t* k_new, const 
   if (int e = append_tokens(true, k_new, v_new, 1, nullptr, 1, pos, nullptr, c, s)) return e;
   c->n_hi += 1;
   // 2. split-K attention over both tiers
-  if (int e = launch_partials(P, &after, nsplit, s)) return e;
+  if (int e = launch_partials(P, &after, nsplit, s, true)) return e;
   // 3. merge (clears the demotion tickets)
   unsigned* ticket = reinterpret_cast<unsigned*>(wsb + wl.ticket);
   const int rep = c->Hq / c->Hkv;
-  decode_merge_kernel<<<c->B * c->Hq, kD * merge_groups(nsplit), 0, s>>>(
-      P.ws_o, P.ws_ml, P.smax, nsplit, out, lse, ticket, rep);
-  if (int e = check_launch("decode_merge_kernel")) return e;
+  if (int e = check_launch_after(
+          launch_after(decode_merge_kernel, dim3(c->B * c->Hq), dim3(kD * merge_groups(nsplit)), 0,
+                       s, P.ws_o, P.ws_ml, P.smax, nsplit, out, lse, ticket, rep),
+          "decode_merge_kernel"))
+    return e;
   // 4. score update + demotion
   EpiArgs ea{};
   ea.logits = logits;
@@ -1138,8 +1181,10 @@ extern "C" int mikv_decode_step(const uint16_t* q, const uint16_t* k_new, const 
   ea.cand_p = reinterpret_cast<int*>(wsb + wl.cand_p);
   ea.cand_j = reinterpret_cast<int*>(wsb + wl.cand_j);
   ea.ticket = ticket;
-  decode_score_demote_kernel<<<dim3(c->B * c->Hkv, ea.nchunk), kEpiThreads, 0, s>>>(ea);
-  if (int e = check_launch("decode_score_demote_kernel")) return e;
+  if (int e = check_launch_after(launch_after(decode_score_demote_kernel, dim3(c->B * c->Hkv, ea.nchunk),
+                                              dim3(kEpiThreads), 0, s, ea),
+                                 "decode_score_demote_kernel"))
+    return e;
   if (demote) {
     c->n_hi -= 1;
     c->n_lo += 1;

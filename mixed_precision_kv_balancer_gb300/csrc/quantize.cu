@@ -38,6 +38,8 @@ struct AppendArgs {
 };
 
 __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const long item = static_cast<long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   if (item >= a.units_tokens) return;
