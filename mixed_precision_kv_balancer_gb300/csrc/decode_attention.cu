@@ -705,16 +705,14 @@ __global__ void __launch_bounds__(kThreads, 3) decode_partial_kernel(Params P) {
 // (row = b*Hq + h) into its output row and natural log-sum-exp.  The CTA holds G groups of
 // kD threads (thread = channel); group g folds splits g, g+G, g+2G, ... in ascending order
 // and the group sums are then added in group order.  G depends on nsplit only, so every
-// caller of this kernel gets the same bits.  With `ticket` set, the first head of each
-// (batch, key head) also clears that unit's ticket for the score/demotion kernel after it.
+// caller of this kernel gets the same bits.
 int merge_groups(int nsplit) { return nsplit >= 96 ? 8 : (nsplit >= 48 ? 4 : (nsplit >= 12 ? 2 : 1)); }
 
 __global__ void __launch_bounds__(8 * kD) decode_merge_kernel(const float* __restrict__ ws_o,
                                                               const float* __restrict__ ws_ml,
                                                               int smax, int nsplit,
                                                               float* __restrict__ out,
-                                                              float* __restrict__ lse,
-                                                              unsigned* __restrict__ ticket, int rep) {
+                                                              float* __restrict__ lse) {
   __shared__ float so[7][kD];
   __shared__ float sl[7];
   __shared__ float smx[32];
@@ -753,19 +751,17 @@ __global__ void __launch_bounds__(8 * kD) decode_merge_kernel(const float* __res
     L += sl[g - 1];
   }
   out[row * kD + c] = O / L;
-  if (c == 0) {
-    lse[row] = (M + log2f(L)) * 0.69314718055994531f;
-    if (ticket != nullptr && row % rep == 0) ticket[row / rep] = 0u;
-  }
+  if (c == 0) lse[row] = (M + log2f(L)) * 0.69314718055994531f;
 }
 
-// End of a decode step after the merge: add this step's attention to the H2O score of every
-// important slot (the same arithmetic as the separate decode score update) and, when the
-// important tier is over budget, demote the victim: the slot with the lowest score, latest
-// position first among equal scores, among positions < limit (as the separate demotion
-// select + append).  Grid (B*Hkv units, chunks of kEpiChunk slots).  Each CTA reduces its
+// End of a decode step after the merge, grid (B*Hkv units, chunks of kEpiChunk slots): add
+// this step's attention to the H2O score of every important slot (the arithmetic of the
+// separate decode score update) and, when the important tier is over budget, demote the
+// victim: the slot with the lowest score, latest position first among equal scores, among
+// positions < limit (as the separate demotion select + append).  Each CTA reduces its
 // chunk's candidate, publishes it, and takes a ticket; the CTA that takes the unit's last
 // ticket reduces the published candidates and moves the victim.  No CTA waits on another.
+// The tickets are cleared by the step's append.
 constexpr int kEpiThreads = 256;
 constexpr int kEpiPer = 4;
 constexpr int kEpiChunk = kEpiThreads * kEpiPer;
@@ -773,13 +769,13 @@ constexpr int kEpiChunk = kEpiThreads * kEpiPer;
 struct EpiArgs {
   const float* logits;  // [B][Hq][cap_hi]
   const float* lse;     // [B][Hq], from the merge
-  int Hq, Hkv, rep, nchunk;
+  int Hq, Hkv, nchunk;
   int demote, limit;
   DemoteArgs da;        // counts after this step's append
   float* cand_s;        // [B*Hkv][nchunk] per-chunk candidates
   int* cand_p;
   int* cand_j;
-  unsigned* ticket;     // [B*Hkv], cleared by the merge
+  unsigned* ticket;     // [B*Hkv]
 };
 
 // (s1, p1, j1) is a better victim than (s0, p0, j0); j < 0 marks "no candidate"
@@ -801,8 +797,9 @@ __device__ __forceinline__ void victim_warp_min(float& s, int& p, int& j) {
   }
 }
 
+template <int REP>
 __global__ void __launch_bounds__(kEpiThreads) decode_score_demote_kernel(EpiArgs a) {
-  __shared__ float s_lse[8];
+  __shared__ float s_lse[REP];
   __shared__ float ws_s[kEpiThreads / 32];
   __shared__ int ws_p[kEpiThreads / 32], ws_j[kEpiThreads / 32];
   __shared__ int s_last;
@@ -812,24 +809,23 @@ __global__ void __launch_bounds__(kEpiThreads) decode_score_demote_kernel(EpiArg
   const int chunk = blockIdx.y;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int b = static_cast<int>(unit / a.Hkv), g = static_cast<int>(unit % a.Hkv);
-  const long row0 = static_cast<long>(b) * a.Hq + static_cast<long>(g) * a.rep;
-  if (t < a.rep) s_lse[t] = a.lse[row0 + t];
-  __syncthreads();
+  const long row0 = static_cast<long>(b) * a.Hq + static_cast<long>(g) * REP;
   const int cap = a.da.cap_hi, n = a.da.n_hi;
   const long ubase = unit * cap;
   // every load of the thread's slots is issued before the first use
-  float lg[kEpiPer][8], sc[kEpiPer];
+  float lg[kEpiPer][REP], sc[kEpiPer];
   int ps[kEpiPer];
 #pragma unroll
   for (int i = 0; i < kEpiPer; ++i) {
     const int j = chunk * kEpiChunk + i * kEpiThreads + t;
     const bool in = j < n;
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
-      lg[i][r] = (in && r < a.rep) ? a.logits[(row0 + r) * cap + j] : 0.f;
+    for (int r = 0; r < REP; ++r) lg[i][r] = in ? a.logits[(row0 + r) * cap + j] : 0.f;
     sc[i] = in ? a.da.scores[ubase + j] : 0.f;
     ps[i] = (in && a.demote) ? a.da.pos_hi[ubase + j] : 0;
   }
+  if (t < REP) s_lse[t] = a.lse[row0 + t];
+  __syncthreads();
   float bs = INFINITY;
   int bp = -1, bj = -1;
 #pragma unroll
@@ -838,8 +834,7 @@ __global__ void __launch_bounds__(kEpiThreads) decode_score_demote_kernel(EpiArg
     if (j < n) {
       float add = 0.f;
 #pragma unroll
-      for (int r = 0; r < 8; ++r)
-        if (r < a.rep) add += expf(lg[i][r] - s_lse[r]);
+      for (int r = 0; r < REP; ++r) add += expf(lg[i][r] - s_lse[r]);
       const float sv = sc[i] + add;
       a.da.scores[ubase + j] = sv;
       const int p = ps[i];
@@ -981,7 +976,7 @@ extern "C" size_t mikv_decode_workspace_bytes(const mikv_cache* c) {
 namespace mikv {
 int append_tokens(bool hi, const uint16_t* k, const uint16_t* v, int src_len, const int32_t* src_pos,
                   int n_tokens, int pos_base, const float* src_scores, const mikv_cache* c,
-                  cudaStream_t s);
+                  cudaStream_t s, unsigned* ticket, bool after);
 int demote_args(const mikv_cache* c, const int32_t* victim, DemoteArgs& a);
 
 namespace {
@@ -1085,8 +1080,7 @@ extern "C" int mikv_decode_attention(const uint16_t* q, const mikv_cache* c, flo
   if (int e = launch_partials(P, c, nsplit, s, false)) return e;
   return check_launch_after(
       launch_after(decode_merge_kernel, dim3(c->B * c->Hq), dim3(kD * merge_groups(nsplit)), 0, s,
-                   P.ws_o, P.ws_ml, P.smax, nsplit, out, lse, static_cast<unsigned*>(nullptr),
-                   c->Hq / c->Hkv),
+                   P.ws_o, P.ws_ml, P.smax, nsplit, out, lse),
       "decode_merge_kernel");
 }
 
@@ -1153,26 +1147,27 @@ extern "C" int mikv_decode_step(const uint16_t* q, const uint16_t* k_new, const 
   int nsplit = 0;
   if (int e = prepare_decode(q, &after, logits, ws, dec_ws, P, nsplit, "decode_step")) return e;
   cudaStream_t s = as_stream(stream);
-  // 1. the new token joins the important tier at slot n_hi (position pos, score 0)
-  if (int e = append_tokens(true, k_new, v_new, 1, nullptr, 1, pos, nullptr, c, s)) return e;
+  unsigned* ticket = reinterpret_cast<unsigned*>(wsb + wl.ticket);
+  // 1. the new token joins the important tier at slot n_hi (position pos, score 0); the
+  //    demotion tickets are cleared on the way
+  if (int e = append_tokens(true, k_new, v_new, 1, nullptr, 1, pos, nullptr, c, s, ticket, true))
+    return e;
   c->n_hi += 1;
   // 2. split-K attention over both tiers
   if (int e = launch_partials(P, &after, nsplit, s, true)) return e;
-  // 3. merge (clears the demotion tickets)
-  unsigned* ticket = reinterpret_cast<unsigned*>(wsb + wl.ticket);
-  const int rep = c->Hq / c->Hkv;
+  // 3. merge
   if (int e = check_launch_after(
           launch_after(decode_merge_kernel, dim3(c->B * c->Hq), dim3(kD * merge_groups(nsplit)), 0,
-                       s, P.ws_o, P.ws_ml, P.smax, nsplit, out, lse, ticket, rep),
+                       s, P.ws_o, P.ws_ml, P.smax, nsplit, out, lse),
           "decode_merge_kernel"))
     return e;
   // 4. score update + demotion
+  const int rep = c->Hq / c->Hkv;
   EpiArgs ea{};
   ea.logits = logits;
   ea.lse = lse;
   ea.Hq = c->Hq;
   ea.Hkv = c->Hkv;
-  ea.rep = rep;
   ea.nchunk = std::max(1, (after.n_hi + kEpiChunk - 1) / kEpiChunk);
   ea.demote = demote ? 1 : 0;
   ea.limit = L - window;
@@ -1181,10 +1176,19 @@ extern "C" int mikv_decode_step(const uint16_t* q, const uint16_t* k_new, const 
   ea.cand_p = reinterpret_cast<int*>(wsb + wl.cand_p);
   ea.cand_j = reinterpret_cast<int*>(wsb + wl.cand_j);
   ea.ticket = ticket;
-  if (int e = check_launch_after(launch_after(decode_score_demote_kernel, dim3(c->B * c->Hkv, ea.nchunk),
-                                              dim3(kEpiThreads), 0, s, ea),
-                                 "decode_score_demote_kernel"))
-    return e;
+  const dim3 egrid(c->B * c->Hkv, ea.nchunk);
+  cudaError_t err;
+  switch (rep) {
+    case 1: err = launch_after(decode_score_demote_kernel<1>, egrid, dim3(kEpiThreads), 0, s, ea); break;
+    case 2: err = launch_after(decode_score_demote_kernel<2>, egrid, dim3(kEpiThreads), 0, s, ea); break;
+    case 3: err = launch_after(decode_score_demote_kernel<3>, egrid, dim3(kEpiThreads), 0, s, ea); break;
+    case 4: err = launch_after(decode_score_demote_kernel<4>, egrid, dim3(kEpiThreads), 0, s, ea); break;
+    case 5: err = launch_after(decode_score_demote_kernel<5>, egrid, dim3(kEpiThreads), 0, s, ea); break;
+    case 6: err = launch_after(decode_score_demote_kernel<6>, egrid, dim3(kEpiThreads), 0, s, ea); break;
+    case 7: err = launch_after(decode_score_demote_kernel<7>, egrid, dim3(kEpiThreads), 0, s, ea); break;
+    default: err = launch_after(decode_score_demote_kernel<8>, egrid, dim3(kEpiThreads), 0, s, ea); break;
+  }
+  if (int e = check_launch_after(err, "decode_score_demote_kernel")) return e;
   if (demote) {
     c->n_hi -= 1;
     c->n_lo += 1;

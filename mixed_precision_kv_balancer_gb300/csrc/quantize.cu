@@ -35,6 +35,7 @@ struct AppendArgs {
   int32_t* dpos;
   float* dscores;         // hi tier only, else null
   long units_tokens;      // B*Hkv*n_tokens
+  unsigned* ticket;       // [B*Hkv] cleared by token 0 of each unit, or null
 };
 
 __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
@@ -45,6 +46,7 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
   if (item >= a.units_tokens) return;
   const long unit = item / a.n_tokens;
   const int j = static_cast<int>(item % a.n_tokens);
+  if (a.ticket != nullptr && j == 0 && lane == 0) a.ticket[unit] = 0u;
   const int src = a.src_pos ? a.src_pos[item] : j;  // no list: token j of the source
   if (src < 0 || src >= a.src_len) return;  // out-of-range source: slot left unchanged
   const long slot = unit * a.cap + a.base_slot + j;
@@ -112,9 +114,11 @@ namespace mikv {
 
 // Validate and launch an append of n_tokens source tokens into the HI or LO tier (counts
 // in *c are not changed here).  src_pos == nullptr means source token j goes to slot j.
+// ticket (optional): per-unit counters the kernel clears; after: the kernel launched just
+// before on `s` is one of ours and this launch may overlap its tail.
 int append_tokens(bool hi, const uint16_t* k, const uint16_t* v, int src_len, const int32_t* src_pos,
                   int n_tokens, int pos_base, const float* src_scores, const mikv_cache* c,
-                  cudaStream_t s) {
+                  cudaStream_t s, unsigned* ticket, bool after) {
   const long units = static_cast<long>(c->B) * c->Hkv;
   const int bits = hi ? c->hi_bits : c->lo_bits;
   if ((!k || !v) && n_tokens > 0) return fail(MIKV_EINVAL, "quantize_append: null k/v");
@@ -150,10 +154,18 @@ int append_tokens(bool hi, const uint16_t* k, const uint16_t* v, int src_len, co
       (bits != 16 && (!aligned16(a.dkm) || !aligned16(a.dvm))) || (a.bal && !aligned16(a.bal)))
     return fail(MIKV_EALIGN, "quantize_append: buffers must be 16-byte aligned");
   a.units_tokens = units * n_tokens;
+  a.ticket = ticket;
   if (n_tokens > 0) {
     const long blocks = (a.units_tokens + 7) / 8;
-    append_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
-    if (int e = check_launch("append_kernel")) return e;
+    if (after) {
+      if (int e = check_launch_after(
+              launch_after(append_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, a),
+              "append_kernel"))
+        return e;
+    } else {
+      append_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+      if (int e = check_launch("append_kernel")) return e;
+    }
   }
   return MIKV_OK;
 }
@@ -203,7 +215,9 @@ extern "C" int mikv_quantize_append(int tier, const uint16_t* k, const uint16_t*
   cudaStream_t s = as_stream(stream);
   if (tier == MIKV_TIER_HI || tier == MIKV_TIER_LO) {
     const bool hi = tier == MIKV_TIER_HI;
-    if (int e = append_tokens(hi, k, v, src_len, src_pos, n_tokens, pos_base, src_scores, c, s)) return e;
+    if (int e = append_tokens(hi, k, v, src_len, src_pos, n_tokens, pos_base, src_scores, c, s,
+                              nullptr, false))
+      return e;
     if (hi) c->n_hi += n_tokens;
     else c->n_lo += n_tokens;
     return MIKV_OK;

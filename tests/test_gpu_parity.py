@@ -363,7 +363,7 @@ def test_pipeline_matches_oracle(name, scale):
                                         ("llama2_7b", dict(B=2, Hq=8, Hkv=8, T=300, steps=6)),
                                         ("qwen25_32b", dict(T=400, steps=3, Hq=10, Hkv=2))])
 def test_fused_step_equals_separate_calls(name, scale):
-    """mikv_decode_step (3 launches) leaves every buffer and output bit-identical to the
+    """mikv_decode_step (4 launches) leaves every buffer and output bit-identical to the
     five-call sequence."""
     wl = inputs.WORKLOADS[name].scaled(**scale)
     x = inputs.make_prefill(wl, 1, "cpu")
