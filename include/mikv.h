@@ -235,7 +235,8 @@ int mikv_quantize_append(int tier, const uint16_t* k, const uint16_t* v, int src
  *   q      fp16 [B][Hq][D]
  *   out    fp32 [B][Hq][D]; lse fp32 [B][Hq] (natural log)
  *   hi_logits fp32 [B][Hq][cap_hi] (slots < n_hi written) or NULL
- *   ws >= mikv_decode_workspace_bytes(c) bytes (split-K partial results).
+ *   ws >= mikv_decode_workspace_bytes(c) bytes (split-K partial results and the
+ *   per-(batch, key head) query fragments).
  * Requires n_hi + n_lo >= 1.  Errors: EINVAL, ESHAPE, EALIGN, EUNSUPPORTED, ECUDA.
  */
 int mikv_decode_attention(const uint16_t* q, const mikv_cache* c, float* out, float* lse,
@@ -247,7 +248,7 @@ size_t mikv_decode_workspace_bytes(const mikv_cache* c);
  * quantize_append(HI) -> decode_attention -> score_update(DECODE) ->
  * select(DEMOTE) -> quantize_append(DEMOTE), with identical results):
  *   1. the new token (k_new, v_new fp16 [B][Hkv][D], position `pos`) is appended
- *      to the important tier with score 0;
+ *      to the important tier with score 0 (the same launch prepares the query);
  *   2. q fp16 [B][Hq][D] attends over both tiers (split-K partials);
  *   3. the partials are merged into out fp32 [B][Hq][D] and lse fp32 [B][Hq];
  *   4. the step's attention is added to the H2O score of every important slot,

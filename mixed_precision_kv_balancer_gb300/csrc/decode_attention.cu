@@ -85,6 +85,8 @@ struct Params {
   float* hi_logits;        // [B][Hq][cap_hi] or null
   float* ws_o;             // [B*Hq][smax][D]
   float* ws_ml;            // [B*Hq][smax][2]
+  const uint32_t* qf;      // query fragments, [B*Hkv][2][32][kQW]
+  uint32_t* qf_out;        // the same buffer, written by the prep kernel
 };
 
 // ---------------------------------------------------------------------------------
@@ -481,44 +483,133 @@ __device__ __forceinline__ int out_channel(int j, int gid, int h) {
   else return (j >> 2) * 64 + gid * 8 + 4 * h + (j & 3);
 }
 
-// Build the query fragments of this CTA's tier: columns (head, hi|lo) of n-tile t, read
-// from the staged (hi, lo) fp16 pairs; qsum from the staged per-(head, group) sums.
-template <int BITS, int NT>
-__device__ __forceinline__ void build_q(const uint32_t* qhl /*smem [8][kD] (hi,lo) pairs*/,
-                                        const float* qgs /*smem [8][2]*/, int lane,
-                                        uint32_t (&bq)[NT][8][2], float (&qsum)[NT][2]) {
-  const int gid = lane >> 2, tig = lane & 3;
+// Query fragments in the lane order of the partial kernel: word 16t + 2s + i of a lane is
+// bq[t][s][i], words 32..35 qsum[NT][2]; [units][2 formats][32 lanes][kQW].
+constexpr int kQW = 36;
+
+template <int NT>
+__device__ __forceinline__ void load_qfrag(const uint32_t* qf, int unit, int tier, int lane,
+                                           uint32_t (&bq)[NT][8][2], float (&qsum)[NT][2]) {
+  const uint4* src =
+      reinterpret_cast<const uint4*>(qf + ((static_cast<long>(unit) * 2 + tier) * 32 + lane) * kQW);
 #pragma unroll
-  for (int t = 0; t < NT; ++t) {
-    const int head = t * 4 + (gid >> 1);
-    const int shift = (gid & 1) * 16;  // hi part in the low half, lo part in the high half
-    const uint32_t* row = qhl + head * kD;
+  for (int t = 0; t < NT; ++t)
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      int c0, c1, c2, c3;
-      if constexpr (BITS == 16) {
-        c0 = s * 16 + 2 * tig;
-        c1 = c0 + 1;
-        c2 = c0 + 8;
-        c3 = c0 + 9;
-      } else {
-        const int gr = s >> 2, sp = s & 3, base = gr * 64 + tig * 16;
-        c0 = base + k_ca<BITS>(2 * sp);
-        c1 = base + k_cb<BITS>(2 * sp);
-        c2 = base + k_ca<BITS>(2 * sp + 1);
-        c3 = base + k_cb<BITS>(2 * sp + 1);
-      }
-      bq[t][s][0] = ((row[c0] >> shift) & 0xffffu) | (((row[c1] >> shift) & 0xffffu) << 16);
-      bq[t][s][1] = ((row[c2] >> shift) & 0xffffu) | (((row[c3] >> shift) & 0xffffu) << 16);
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const uint4 w = src[t * 4 + q4];
+      bq[t][2 * q4][0] = w.x;
+      bq[t][2 * q4][1] = w.y;
+      bq[t][2 * q4 + 1][0] = w.z;
+      bq[t][2 * q4 + 1][1] = w.w;
     }
-    qsum[t][0] = qgs[(t * 4 + tig) * 2];
-    qsum[t][1] = qgs[(t * 4 + tig) * 2 + 1];
+  const uint4 s = src[8];
+  qsum[0][0] = __uint_as_float(s.x);
+  qsum[0][1] = __uint_as_float(s.y);
+  if constexpr (NT == 2) {
+    qsum[1][0] = __uint_as_float(s.z);
+    qsum[1][1] = __uint_as_float(s.w);
   }
+}
+
+// Query fragments of one (batch, key head) for both tier formats, by one CTA of >= 256
+// threads.  Thread (f, c) of the first 256 stages channel c of every query head of the group
+// for format f (0 = important tier, 1 = low tier): pre-scaled by log2(e)/sqrt(D) and, for a
+// quantised format, divided by the balancer, as an fp16 (hi, lo) pair; with the 64-channel
+// group sums of the same scaled values.  Warp 0 (format 0) and warp 4 (format 1) then gather
+// their lane-order fragments (word 16t + 2s + i = bq[t][s][i], words 32..35 = qsum[NT][2]).
+// Every thread of the CTA must call this (it holds a barrier).
+template <int HI, int LO, int NT>
+__device__ __forceinline__ void prep_unit(const Params& P, int unit) {
+  __shared__ uint32_t sq[2][8][kD];   // (hi, lo) pairs
+  __shared__ float sgs[2][8][4];      // per-warp partial sums: [format][head][warp of the format]
+  const int t = threadIdx.x, lane = t & 31;
+  const int b = unit / P.Hkv, g = unit % P.Hkv;
+  if (t < 256) {
+    const int f = t >> 7, c = t & (kD - 1);
+    const bool quant = f == 0 ? Fmt<HI>::kQuant : Fmt<LO>::kQuant;
+    const float bb = (quant && P.bal) ? P.bal[static_cast<long>(unit) * kD + c] : 1.f;
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      float x = 0.f;
+      if (h < P.rep) {
+        x = __half2float(P.q[(static_cast<long>(b) * P.Hq + g * P.rep + h) * kD + c]);
+        if (quant && P.bal) x = __fdiv_rn(x, bb);
+        x *= kLogitScale;
+      }
+      sq[f][h][c] = split_pack(x);
+      float sum = x;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      if (lane == 0) sgs[f][h][c >> 5] = sum;
+    }
+  }
+  __syncthreads();
+  if (t < 256 && (t & 127) < 32) {
+    const int f = t >> 7;
+    const int gid = lane >> 2, tig = lane & 3;
+    uint32_t w[kQW];
+#pragma unroll
+    for (int tt = 0; tt < NT; ++tt) {
+      const int head = tt * 4 + (gid >> 1);
+      const int shift = (gid & 1) * 16;  // hi part in column 2h, lo part in column 2h + 1
+#pragma unroll
+      for (int s2 = 0; s2 < 8; ++s2) {
+        int c0, c1, c2, c3;
+        if ((f == 0 ? HI : LO) == 16) {
+          c0 = s2 * 16 + 2 * tig;
+          c1 = c0 + 1;
+          c2 = c0 + 8;
+          c3 = c0 + 9;
+        } else {
+          const int bits = f == 0 ? HI : LO;
+          const int gr = s2 >> 2, sp = s2 & 3, base = gr * 64 + tig * 16;
+          c0 = base + (bits == 2 ? k_ca<2>(2 * sp) : bits == 4 ? k_ca<4>(2 * sp) : k_ca<8>(2 * sp));
+          c1 = base + (bits == 2 ? k_cb<2>(2 * sp) : bits == 4 ? k_cb<4>(2 * sp) : k_cb<8>(2 * sp));
+          c2 = base + (bits == 2 ? k_ca<2>(2 * sp + 1) : bits == 4 ? k_ca<4>(2 * sp + 1) : k_ca<8>(2 * sp + 1));
+          c3 = base + (bits == 2 ? k_cb<2>(2 * sp + 1) : bits == 4 ? k_cb<4>(2 * sp + 1) : k_cb<8>(2 * sp + 1));
+        }
+        const uint32_t* row = sq[f][head];
+        w[tt * 16 + 2 * s2] = ((row[c0] >> shift) & 0xffffu) | (((row[c1] >> shift) & 0xffffu) << 16);
+        w[tt * 16 + 2 * s2 + 1] = ((row[c2] >> shift) & 0xffffu) | (((row[c3] >> shift) & 0xffffu) << 16);
+      }
+    }
+#pragma unroll
+    for (int i = 16 * NT; i < 32; ++i) w[i] = 0u;
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt) {
+      const int head = tt * 4 + tig;
+      const bool on = tt < NT;
+      w[32 + 2 * tt] = __float_as_uint(on ? sgs[f][head][0] + sgs[f][head][1] : 0.f);
+      w[33 + 2 * tt] = __float_as_uint(on ? sgs[f][head][2] + sgs[f][head][3] : 0.f);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(P.qf_out + ((static_cast<long>(unit) * 2 + f) * 32 + lane) * kQW);
+#pragma unroll
+    for (int i = 0; i < kQW / 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  }
+}
+
+// The query fragments of every (batch, key head): one CTA of 256 threads per unit.
+template <int HI, int LO, int NT>
+__global__ void __launch_bounds__(256) decode_qprep_kernel(Params P) {
+  pdl_wait();
+  pdl_trigger();
+  prep_unit<HI, LO, NT>(P, blockIdx.x);
+}
+
+// First kernel of a decode step, one CTA of 288 threads per (batch, key head): the last warp
+// appends the new token to the important tier (and clears the unit's demotion ticket), the
+// rest prepare the query fragments.
+template <int HI, int LO, int NT>
+__global__ void __launch_bounds__(288) decode_step_prep_kernel(AppendArgs a, Params P) {
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x >= 256) append_item(a, blockIdx.x, threadIdx.x & 31);
+  prep_unit<HI, LO, NT>(P, blockIdx.x);
 }
 
 template <int BITS, int NT>
 __device__ void run_tier(const Params& P, const TierPtrs& tier, int unit, int split, int chunk,
-                         bool is_hi, uint8_t* smem, float* qs) {
+                         bool is_hi, uint8_t* smem) {
   using F = Fmt<BITS>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = unit / P.Hkv, g = unit % P.Hkv;
@@ -557,42 +648,12 @@ __device__ void run_tier(const Params& P, const TierPtrs& tier, int unit, int sp
     ++issued;
     cp_async_commit();
   };
-  issue();  // first stage in flight while the query is staged
+  issue();  // first stage in flight while the query fragments load
 
-  // query (balanced for quantised tiers, pre-scaled so logits come out of the mma in base-2
-  // units) staged as (hi, lo) fp16 pairs, plus its per-(head, group) sums for the zero-point
-  // term: thread i handles channels 8*(i%16) .. +8 of head i/16.
-  uint32_t* qhl = reinterpret_cast<uint32_t*>(qs);   // [8][kD]
-  float* qgs = qs + 8 * kD;                          // [8][2]
-  {
-    const int h = threadIdx.x >> 4, c0 = (threadIdx.x & 15) * 8;
-    float part = 0.f;
-#pragma unroll
-    for (int h2 = 0; h2 < 8; h2 += kThreads / 16) {
-      const int hh = h + h2;
-      part = 0.f;
-#pragma unroll
-      for (int c = c0; c < c0 + 8; ++c) {
-        float x = 0.f;
-        if (hh < rep) {
-          x = __half2float(P.q[(static_cast<long>(b) * P.Hq + g * rep + hh) * kD + c]);
-          if (F::kQuant && P.bal) x = __fdiv_rn(x, P.bal[static_cast<long>(unit) * kD + c]);
-          x *= kLogitScale;
-        }
-        qhl[hh * kD + c] = split_pack(x);
-        part += x;
-      }
-      // 8 lanes per 64-channel group: reduce, lane 0 of each octet stores
-      part += __shfl_xor_sync(0xffffffffu, part, 1);
-      part += __shfl_xor_sync(0xffffffffu, part, 2);
-      part += __shfl_xor_sync(0xffffffffu, part, 4);
-      if ((threadIdx.x & 7) == 0) qgs[hh * 2 + ((threadIdx.x >> 3) & 1)] = part;
-    }
-  }
-  __syncthreads();
+  // this tier's query fragments, prepared once per (batch, key head) by the prep kernel
   uint32_t bq[NT][8][2];
   float qsum[NT][2];
-  build_q<BITS, NT>(qhl, qgs, lane, bq, qsum);
+  load_qfrag<NT>(P.qf, unit, is_hi ? 0 : 1, lane, bq, qsum);
 
   State<NT> st;
 #pragma unroll
@@ -692,13 +753,12 @@ __device__ void run_tier(const Params& P, const TierPtrs& tier, int unit, int sp
 template <int HI, int LO, int NT>
 __global__ void __launch_bounds__(kThreads, 3) decode_partial_kernel(Params P) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(16) float qs[8 * kD + 16];
   pdl_wait();
   pdl_trigger();
   const int unit = blockIdx.y;
   const int sx = blockIdx.x;
-  if (sx < P.nsplit_hi) run_tier<HI, NT>(P, P.hi, unit, sx, P.chunk_hi, true, smem, qs);
-  else run_tier<LO, NT>(P, P.lo, unit, sx - P.nsplit_hi, P.chunk_lo, false, smem, qs);
+  if (sx < P.nsplit_hi) run_tier<HI, NT>(P, P.hi, unit, sx, P.chunk_hi, true, smem);
+  else run_tier<LO, NT>(P, P.lo, unit, sx - P.nsplit_hi, P.chunk_lo, false, smem);
 }
 
 // K8: merge the split partials (base-2 max m, sum l, unnormalised o) of one query head
@@ -944,21 +1004,50 @@ Plan make_plan(const mikv_cache* c) {
   return best_t < INFINITY ? best : first;
 }
 
+thread_local cudaEvent_t t_ev_begin = nullptr, t_ev_end = nullptr;
+
+int record_hook(cudaEvent_t ev, cudaStream_t s) {
+  if (ev == nullptr) return MIKV_OK;
+  const cudaError_t err = cudaEventRecord(ev, s);
+  if (err == cudaSuccess) return MIKV_OK;
+  (void)cudaGetLastError();
+  return fail(MIKV_ECUDA, "attention event record: %s", cudaGetErrorString(err));
+}
+
+// The query-fragment prep, then the split-K partial kernel (PDL after the prep); `after`:
+// the kernel launched just before on `s` is one of ours, so the prep may overlap its tail.
 template <int HI, int LO, int NT>
-int launch(const Params& P, dim3 grid, cudaStream_t s, bool after) {
+int launch(const Params& P, dim3 grid, cudaStream_t s, bool after, const AppendArgs* step) {
+  const dim3 pgrid(grid.y);
+  if (step != nullptr) {  // the step's token append and the query prep in one launch
+    if (int e = check_launch_after(launch_after(decode_step_prep_kernel<HI, LO, NT>, pgrid, dim3(288),
+                                                0, s, *step, P),
+                                   "decode_step_prep_kernel"))
+      return e;
+  } else if (after) {
+    auto prep = decode_qprep_kernel<HI, LO, NT>;
+    const dim3 pblock(256);
+    if (int e = check_launch_after(launch_after(prep, pgrid, pblock, 0, s, P), "decode_qprep_kernel"))
+      return e;
+  } else {
+    decode_qprep_kernel<HI, LO, NT><<<pgrid, 256, 0, s>>>(P);
+    if (int e = check_launch("decode_qprep_kernel")) return e;
+  }
   const int smem = kWarps * kStages * std::max(Fmt<HI>::kStageBytes, Fmt<LO>::kStageBytes);
   auto kern = decode_partial_kernel<HI, LO, NT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return check_launch("decode_partial_kernel attribute");
-  if (after) return check_launch_after(launch_after(kern, grid, dim3(kThreads), smem, s, P),
-                                       "decode_partial_kernel");
-  kern<<<grid, kThreads, smem, s>>>(P);
-  return check_launch("decode_partial_kernel");
+  if (int e = record_hook(t_ev_begin, s)) return e;
+  if (int e = check_launch_after(launch_after(kern, grid, dim3(kThreads), smem, s, P),
+                                 "decode_partial_kernel"))
+    return e;
+  return record_hook(t_ev_end, s);
 }
 
 template <int HI, int LO>
-int launch_nt(const Params& P, dim3 grid, cudaStream_t s, bool after) {
-  return P.rep <= 4 ? launch<HI, LO, 1>(P, grid, s, after) : launch<HI, LO, 2>(P, grid, s, after);
+int launch_nt(const Params& P, dim3 grid, cudaStream_t s, bool after, const AppendArgs* step) {
+  return P.rep <= 4 ? launch<HI, LO, 1>(P, grid, s, after, step)
+                    : launch<HI, LO, 2>(P, grid, s, after, step);
 }
 
 }  // namespace
@@ -970,13 +1059,15 @@ extern "C" size_t mikv_decode_workspace_bytes(const mikv_cache* c) {
   if (validate_cache_public(c, "decode_workspace_bytes") != MIKV_OK) return 0;
   const Plan p = make_plan(c);
   const size_t rows = static_cast<size_t>(c->B) * c->Hq * (p.smax_hi + p.smax_lo);
-  return align_up(rows * kD * sizeof(float), 256) + align_up(rows * 2 * sizeof(float), 256);
+  const size_t units = static_cast<size_t>(c->B) * c->Hkv;
+  return align_up(rows * kD * sizeof(float), 256) + align_up(rows * 2 * sizeof(float), 256) +
+         align_up(units * 2 * 32 * kQW * sizeof(uint32_t), 256);
 }
 
 namespace mikv {
-int append_tokens(bool hi, const uint16_t* k, const uint16_t* v, int src_len, const int32_t* src_pos,
-                  int n_tokens, int pos_base, const float* src_scores, const mikv_cache* c,
-                  cudaStream_t s, unsigned* ticket, bool after);
+int append_args(bool hi, const uint16_t* k, const uint16_t* v, int src_len, const int32_t* src_pos,
+                int n_tokens, int pos_base, const float* src_scores, const mikv_cache* c,
+                unsigned* ticket, AppendArgs& a);
 int demote_args(const mikv_cache* c, const int32_t* victim, DemoteArgs& a);
 
 namespace {
@@ -1016,6 +1107,9 @@ int prepare_decode(const uint16_t* q, const mikv_cache* c, float* hi_logits, voi
   const size_t rows = static_cast<size_t>(c->B) * c->Hq * P.smax;
   P.ws_o = static_cast<float*>(ws);
   P.ws_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + align_up(rows * kD * sizeof(float), 256));
+  P.qf_out = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + align_up(rows * kD * sizeof(float), 256) +
+                                         align_up(rows * 2 * sizeof(float), 256));
+  P.qf = P.qf_out;
   nsplit = P.nsplit_hi + nsplit_lo;
   if (c->hi_bits * 100 + c->lo_bits != 1602 && c->hi_bits * 100 + c->lo_bits != 1604 &&
       c->hi_bits * 100 + c->lo_bits != 1608 && c->hi_bits * 100 + c->lo_bits != 802 &&
@@ -1024,31 +1118,21 @@ int prepare_decode(const uint16_t* q, const mikv_cache* c, float* hi_logits, voi
   return MIKV_OK;
 }
 
-thread_local cudaEvent_t t_ev_begin = nullptr, t_ev_end = nullptr;
-
-int record_hook(cudaEvent_t ev, cudaStream_t s) {
-  if (ev == nullptr) return MIKV_OK;
-  const cudaError_t err = cudaEventRecord(ev, s);
-  if (err == cudaSuccess) return MIKV_OK;
-  (void)cudaGetLastError();
-  return fail(MIKV_ECUDA, "attention event record: %s", cudaGetErrorString(err));
-}
-
-// after: the kernel launched just before on `s` is one of ours (the step's append)
-int launch_partials(const Params& P, const mikv_cache* c, int nsplit, cudaStream_t s, bool after) {
+// after: the kernel launched just before on `s` is one of ours; step: the decode step's
+// token append, launched together with the query prep
+int launch_partials(const Params& P, const mikv_cache* c, int nsplit, cudaStream_t s, bool after,
+                    const AppendArgs* step) {
   const dim3 grid(nsplit, c->B * c->Hkv);
-  if (int e = record_hook(t_ev_begin, s)) return e;
   int e;
   switch (c->hi_bits * 100 + c->lo_bits) {
-    case 1602: e = launch_nt<16, 2>(P, grid, s, after); break;
-    case 1604: e = launch_nt<16, 4>(P, grid, s, after); break;
-    case 1608: e = launch_nt<16, 8>(P, grid, s, after); break;
-    case 802: e = launch_nt<8, 2>(P, grid, s, after); break;
-    case 804: e = launch_nt<8, 4>(P, grid, s, after); break;
-    default: e = launch_nt<8, 8>(P, grid, s, after); break;
+    case 1602: e = launch_nt<16, 2>(P, grid, s, after, step); break;
+    case 1604: e = launch_nt<16, 4>(P, grid, s, after, step); break;
+    case 1608: e = launch_nt<16, 8>(P, grid, s, after, step); break;
+    case 802: e = launch_nt<8, 2>(P, grid, s, after, step); break;
+    case 804: e = launch_nt<8, 4>(P, grid, s, after, step); break;
+    default: e = launch_nt<8, 8>(P, grid, s, after, step); break;
   }
-  if (e) return e;
-  return record_hook(t_ev_end, s);
+  return e;
 }
 
 int n_keep_of(int L, int pct, int window) {
@@ -1077,7 +1161,7 @@ extern "C" int mikv_decode_attention(const uint16_t* q, const mikv_cache* c, flo
   int nsplit = 0;
   if (int e = prepare_decode(q, c, hi_logits, ws, ws_bytes, P, nsplit, "decode_attention")) return e;
   cudaStream_t s = as_stream(stream);
-  if (int e = launch_partials(P, c, nsplit, s, false)) return e;
+  if (int e = launch_partials(P, c, nsplit, s, false, nullptr)) return e;
   return check_launch_after(
       launch_after(decode_merge_kernel, dim3(c->B * c->Hq), dim3(kD * merge_groups(nsplit)), 0, s,
                    P.ws_o, P.ws_ml, P.smax, nsplit, out, lse),
@@ -1148,13 +1232,13 @@ extern "C" int mikv_decode_step(const uint16_t* q, const uint16_t* k_new, const 
   if (int e = prepare_decode(q, &after, logits, ws, dec_ws, P, nsplit, "decode_step")) return e;
   cudaStream_t s = as_stream(stream);
   unsigned* ticket = reinterpret_cast<unsigned*>(wsb + wl.ticket);
-  // 1. the new token joins the important tier at slot n_hi (position pos, score 0); the
-  //    demotion tickets are cleared on the way
-  if (int e = append_tokens(true, k_new, v_new, 1, nullptr, 1, pos, nullptr, c, s, ticket, true))
-    return e;
+  // 1.+2. one launch appends the new token to the important tier at slot n_hi (position pos,
+  //    score 0), clears the demotion tickets and prepares the query fragments; then the
+  //    split-K attention over both tiers
+  AppendArgs aa;
+  if (int e = append_args(true, k_new, v_new, 1, nullptr, 1, pos, nullptr, c, ticket, aa)) return e;
+  if (int e = launch_partials(P, &after, nsplit, s, true, &aa)) return e;
   c->n_hi += 1;
-  // 2. split-K attention over both tiers
-  if (int e = launch_partials(P, &after, nsplit, s, true)) return e;
   // 3. merge
   if (int e = check_launch_after(
           launch_after(decode_merge_kernel, dim3(c->B * c->Hq), dim3(kD * merge_groups(nsplit)), 0,

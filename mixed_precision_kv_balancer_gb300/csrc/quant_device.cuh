@@ -137,4 +137,62 @@ __device__ __forceinline__ void demote_one(const DemoteArgs& a, long unit, int v
   }
 }
 
+// Arguments of an append of source tokens into one tier (one warp per (token, key head)).
+struct AppendArgs {
+  const __half* k;        // [B][Hkv][src_len][D]
+  const __half* v;
+  const int32_t* src_pos; // [B][Hkv][n_tokens]
+  const float* src_scores;
+  const float* bal;       // [B][Hkv][D] or null
+  int Hkv, src_len, n_tokens, pos_base;
+  int cap, base_slot, bits;  // destination tier
+  uint8_t* dk;            // codes [unit][cap][RB] or fp16 rows
+  uint8_t* dv;
+  __half2* dkm;           // [unit][cap][2]
+  __half2* dvm;
+  int32_t* dpos;
+  float* dscores;         // hi tier only, else null
+  long units_tokens;      // B*Hkv*n_tokens
+  unsigned* ticket;       // [B*Hkv] cleared by token 0 of each unit, or null
+};
+
+// Append item `item` = (unit, token j) of `a`: one warp, lanes own 4 channels each.  Keys of a
+// quantised tier are balanced first; the slot gets position src + pos_base and the source
+// score (or 0) in the important tier.  Token 0 of each unit also clears the unit's ticket.
+__device__ __forceinline__ void append_item(const AppendArgs& a, long item, int lane) {
+  const long unit = item / a.n_tokens;
+  const int j = static_cast<int>(item % a.n_tokens);
+  if (a.ticket != nullptr && j == 0 && lane == 0) a.ticket[unit] = 0u;
+  const int src = a.src_pos ? a.src_pos[item] : j;  // no list: token j of the source
+  if (src < 0 || src >= a.src_len) return;  // out-of-range source: slot left unchanged
+  const long slot = unit * a.cap + a.base_slot + j;
+  const __half* ks = a.k + (unit * a.src_len + src) * kD + lane * 4;
+  const __half* vs = a.v + (unit * a.src_len + src) * kD + lane * 4;
+  if (a.bits == 16) {
+    reinterpret_cast<uint2*>(a.dk + slot * kD * 2)[lane] = *reinterpret_cast<const uint2*>(ks);
+    reinterpret_cast<uint2*>(a.dv + slot * kD * 2)[lane] = *reinterpret_cast<const uint2*>(vs);
+  } else {
+    Row4 xk = load_fp16x4(ks), xv = load_fp16x4(vs);
+    if (a.bal) {
+      const float4 bb = *reinterpret_cast<const float4*>(a.bal + unit * kD + lane * 4);
+      xk.x[0] = __fmul_rn(xk.x[0], bb.x);
+      xk.x[1] = __fmul_rn(xk.x[1], bb.y);
+      xk.x[2] = __fmul_rn(xk.x[2], bb.z);
+      xk.x[3] = __fmul_rn(xk.x[3], bb.w);
+    }
+    const int rb = kD * a.bits / 8;
+    uint32_t mk, mv;
+    const uint32_t pk = quantize4(xk, a.bits, mk);
+    const uint32_t pv = quantize4(xv, a.bits, mv);
+    store_codes(a.dk + slot * rb, lane, a.bits, pk);
+    store_codes(a.dv + slot * rb, lane, a.bits, pv);
+    store_meta(a.dkm + slot * 2, lane, mk);
+    store_meta(a.dvm + slot * 2, lane, mv);
+  }
+  if (lane == 0) {
+    a.dpos[slot] = src + a.pos_base;
+    if (a.dscores) a.dscores[slot] = a.src_scores ? a.src_scores[item] : 0.f;
+  }
+}
+
 }  // namespace mikv

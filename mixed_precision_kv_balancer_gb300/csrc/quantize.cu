@@ -20,63 +20,13 @@
 namespace mikv {
 namespace {
 
-struct AppendArgs {
-  const __half* k;        // [B][Hkv][src_len][D]
-  const __half* v;
-  const int32_t* src_pos; // [B][Hkv][n_tokens]
-  const float* src_scores;
-  const float* bal;       // [B][Hkv][D] or null
-  int Hkv, src_len, n_tokens, pos_base;
-  int cap, base_slot, bits;  // destination tier
-  uint8_t* dk;            // codes [unit][cap][RB] or fp16 rows
-  uint8_t* dv;
-  __half2* dkm;           // [unit][cap][2]
-  __half2* dvm;
-  int32_t* dpos;
-  float* dscores;         // hi tier only, else null
-  long units_tokens;      // B*Hkv*n_tokens
-  unsigned* ticket;       // [B*Hkv] cleared by token 0 of each unit, or null
-};
-
 __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31;
   const long item = static_cast<long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   if (item >= a.units_tokens) return;
-  const long unit = item / a.n_tokens;
-  const int j = static_cast<int>(item % a.n_tokens);
-  if (a.ticket != nullptr && j == 0 && lane == 0) a.ticket[unit] = 0u;
-  const int src = a.src_pos ? a.src_pos[item] : j;  // no list: token j of the source
-  if (src < 0 || src >= a.src_len) return;  // out-of-range source: slot left unchanged
-  const long slot = unit * a.cap + a.base_slot + j;
-  const __half* ks = a.k + (unit * a.src_len + src) * kD + lane * 4;
-  const __half* vs = a.v + (unit * a.src_len + src) * kD + lane * 4;
-  if (a.bits == 16) {
-    reinterpret_cast<uint2*>(a.dk + slot * kD * 2)[lane] = *reinterpret_cast<const uint2*>(ks);
-    reinterpret_cast<uint2*>(a.dv + slot * kD * 2)[lane] = *reinterpret_cast<const uint2*>(vs);
-  } else {
-    Row4 xk = load_fp16x4(ks), xv = load_fp16x4(vs);
-    if (a.bal) {
-      const float4 bb = *reinterpret_cast<const float4*>(a.bal + unit * kD + lane * 4);
-      xk.x[0] = __fmul_rn(xk.x[0], bb.x);
-      xk.x[1] = __fmul_rn(xk.x[1], bb.y);
-      xk.x[2] = __fmul_rn(xk.x[2], bb.z);
-      xk.x[3] = __fmul_rn(xk.x[3], bb.w);
-    }
-    const int rb = kD * a.bits / 8;
-    uint32_t mk, mv;
-    const uint32_t pk = quantize4(xk, a.bits, mk);
-    const uint32_t pv = quantize4(xv, a.bits, mv);
-    store_codes(a.dk + slot * rb, lane, a.bits, pk);
-    store_codes(a.dv + slot * rb, lane, a.bits, pv);
-    store_meta(a.dkm + slot * 2, lane, mk);
-    store_meta(a.dvm + slot * 2, lane, mv);
-  }
-  if (lane == 0) {
-    a.dpos[slot] = src + a.pos_base;
-    if (a.dscores) a.dscores[slot] = a.src_scores ? a.src_scores[item] : 0.f;
-  }
+  append_item(a, item, lane);
 }
 
 __global__ void __launch_bounds__(256) demote_kernel(DemoteArgs a) {
@@ -112,13 +62,12 @@ using namespace mikv;
 
 namespace mikv {
 
-// Validate and launch an append of n_tokens source tokens into the HI or LO tier (counts
-// in *c are not changed here).  src_pos == nullptr means source token j goes to slot j.
-// ticket (optional): per-unit counters the kernel clears; after: the kernel launched just
-// before on `s` is one of ours and this launch may overlap its tail.
-int append_tokens(bool hi, const uint16_t* k, const uint16_t* v, int src_len, const int32_t* src_pos,
-                  int n_tokens, int pos_base, const float* src_scores, const mikv_cache* c,
-                  cudaStream_t s, unsigned* ticket, bool after) {
+// Validate an append of n_tokens source tokens into the HI or LO tier and fill its kernel
+// arguments (counts in *c are not changed).  src_pos == nullptr means source token j goes
+// to slot j.  ticket (optional): per-unit counters the kernel clears.
+int append_args(bool hi, const uint16_t* k, const uint16_t* v, int src_len, const int32_t* src_pos,
+                int n_tokens, int pos_base, const float* src_scores, const mikv_cache* c,
+                unsigned* ticket, AppendArgs& a) {
   const long units = static_cast<long>(c->B) * c->Hkv;
   const int bits = hi ? c->hi_bits : c->lo_bits;
   if ((!k || !v) && n_tokens > 0) return fail(MIKV_EINVAL, "quantize_append: null k/v");
@@ -128,7 +77,7 @@ int append_tokens(bool hi, const uint16_t* k, const uint16_t* v, int src_len, co
   if (base + n_tokens > cap)
     return fail(MIKV_ESHAPE, "quantize_append: tier capacity %d exceeded (%d + %d)", cap, base,
                 n_tokens);
-  AppendArgs a{};
+  a = AppendArgs{};
   a.k = reinterpret_cast<const __half*>(k);
   a.v = reinterpret_cast<const __half*>(v);
   a.src_pos = src_pos;
@@ -155,6 +104,17 @@ int append_tokens(bool hi, const uint16_t* k, const uint16_t* v, int src_len, co
     return fail(MIKV_EALIGN, "quantize_append: buffers must be 16-byte aligned");
   a.units_tokens = units * n_tokens;
   a.ticket = ticket;
+  return MIKV_OK;
+}
+
+// Validate and launch an append (see append_args); after: the kernel launched just before on
+// `s` is one of ours and this launch may overlap its tail.
+int append_tokens(bool hi, const uint16_t* k, const uint16_t* v, int src_len, const int32_t* src_pos,
+                  int n_tokens, int pos_base, const float* src_scores, const mikv_cache* c,
+                  cudaStream_t s, unsigned* ticket, bool after) {
+  AppendArgs a;
+  if (int e = append_args(hi, k, v, src_len, src_pos, n_tokens, pos_base, src_scores, c, ticket, a))
+    return e;
   if (n_tokens > 0) {
     const long blocks = (a.units_tokens + 7) / 8;
     if (after) {
