@@ -85,12 +85,38 @@ __device__ __forceinline__ Row4 dequant_int8x4(const uint8_t* row, const __half2
 }
 
 // Move important slot `vslot` of `unit` into the low tier (re-quantised) and the last
-// important slot into its place.  One warp; lanes own 4 channels each.
+// important slot into its place.  One warp; lanes own 4 channels each.  The last slot's
+// contents are loaded first: they do not depend on the victim, so both loads overlap.
 __device__ __forceinline__ void demote_one(const DemoteArgs& a, long unit, int vslot, int lane) {
   if (vslot < 0 || vslot >= a.n_hi) return;  // invalid victim: nothing moves
   const long hs = unit * a.cap_hi + vslot;
   const long last = unit * a.cap_hi + (a.n_hi - 1);
   const long ls = unit * a.cap_lo + a.n_lo;
+  const bool move = hs != last;
+  const int hrb = a.hi_bits == 16 ? kD * 2 : kD;  // bytes per important row
+  const int words = hrb / 4;                        // 64 or 32: lane owns words lane, lane + 32
+  uint32_t lk0 = 0, lk1 = 0, lv0 = 0, lv1 = 0;
+  __half2 lkm = {}, lvm = {};
+  int lpos = 0;
+  float lsc = 0.f;
+  if (move) {
+    const uint32_t* sk = reinterpret_cast<const uint32_t*>(a.k_hi + last * hrb);
+    const uint32_t* sv = reinterpret_cast<const uint32_t*>(a.v_hi + last * hrb);
+    lk0 = sk[lane];
+    lv0 = sv[lane];
+    if (words > 32) {
+      lk1 = sk[lane + 32];
+      lv1 = sv[lane + 32];
+    }
+    if (a.hi_bits == 8 && lane < 2) {
+      lkm = a.k_hi_meta[last * 2 + lane];
+      lvm = a.v_hi_meta[last * 2 + lane];
+    }
+    if (lane == 0) {
+      lpos = a.pos_hi[last];
+      lsc = __ldcg(a.scores + last);  // may have been updated by another CTA
+    }
+  }
   Row4 xk, xv;
   if (a.hi_bits == 16) {
     xk = load_fp16x4(reinterpret_cast<const __half*>(a.k_hi) + hs * kD + lane * 4);
@@ -106,6 +132,7 @@ __device__ __forceinline__ void demote_one(const DemoteArgs& a, long unit, int v
     xk = dequant_int8x4(a.k_hi + hs * kD, a.k_hi_meta + hs * 2, lane);
     xv = dequant_int8x4(a.v_hi + hs * kD, a.v_hi_meta + hs * 2, lane);
   }
+  const int vpos = lane == 0 ? a.pos_hi[hs] : 0;
   const int rb = kD * a.lo_bits / 8;
   uint32_t mk, mv;
   const uint32_t pk = quantize4(xk, a.lo_bits, mk);
@@ -114,25 +141,25 @@ __device__ __forceinline__ void demote_one(const DemoteArgs& a, long unit, int v
   store_codes(a.v_lo + ls * rb, lane, a.lo_bits, pv);
   store_meta(a.k_lo_meta + ls * 2, lane, mk);
   store_meta(a.v_lo_meta + ls * 2, lane, mv);
-  if (lane == 0) a.pos_lo[ls] = a.pos_hi[hs];
+  if (lane == 0) a.pos_lo[ls] = vpos;
   __syncwarp();
   // swap-remove: the last important slot moves into the freed one
-  if (hs != last) {
-    const int hrb = a.hi_bits == 16 ? kD * 2 : kD;
-    const int words = hrb / 4;
-    for (int i = lane; i < words; i += 32) {
-      reinterpret_cast<uint32_t*>(a.k_hi + hs * hrb)[i] =
-          reinterpret_cast<const uint32_t*>(a.k_hi + last * hrb)[i];
-      reinterpret_cast<uint32_t*>(a.v_hi + hs * hrb)[i] =
-          reinterpret_cast<const uint32_t*>(a.v_hi + last * hrb)[i];
+  if (move) {
+    uint32_t* dk = reinterpret_cast<uint32_t*>(a.k_hi + hs * hrb);
+    uint32_t* dv = reinterpret_cast<uint32_t*>(a.v_hi + hs * hrb);
+    dk[lane] = lk0;
+    dv[lane] = lv0;
+    if (words > 32) {
+      dk[lane + 32] = lk1;
+      dv[lane + 32] = lv1;
     }
     if (a.hi_bits == 8 && lane < 2) {
-      a.k_hi_meta[hs * 2 + lane] = a.k_hi_meta[last * 2 + lane];
-      a.v_hi_meta[hs * 2 + lane] = a.v_hi_meta[last * 2 + lane];
+      a.k_hi_meta[hs * 2 + lane] = lkm;
+      a.v_hi_meta[hs * 2 + lane] = lvm;
     }
     if (lane == 0) {
-      a.pos_hi[hs] = a.pos_hi[last];
-      a.scores[hs] = __ldcg(a.scores + last);  // may have been updated by another CTA
+      a.pos_hi[hs] = lpos;
+      a.scores[hs] = lsc;
     }
   }
 }
