@@ -43,6 +43,8 @@ def parse():
     p.add_argument("--workload", default="llama31_8b_full")
     p.add_argument("--layers", type=int, default=None)
     p.add_argument("--lo-bits", type=int, default=None)
+    p.add_argument("--hi-bits", type=int, default=None)
+    p.add_argument("--window", type=int, default=None)
     p.add_argument("--budget", type=int, default=None)
     p.add_argument("--batch", type=int, default=None)
     p.add_argument("--no-e2e", action="store_true")
@@ -61,6 +63,10 @@ def workload(args):
         kw["layers"] = args.layers
     if args.lo_bits:
         kw["lo_bits"] = args.lo_bits
+    if args.hi_bits:
+        kw["hi_bits"] = args.hi_bits
+    if args.window is not None:
+        kw["window"] = args.window
     if args.budget is not None:
         kw["budget_pct"] = args.budget
     if args.batch:

@@ -74,8 +74,11 @@ extern "C" {
  *
  * Slot layouts (all per [B][Hkv][capacity]):
  *   hi_bits == 16: k_hi, v_hi fp16 [B][Hkv][cap_hi][D]; hi meta unused (NULL).
- *   hi_bits ==  8: k_hi, v_hi uint8 codes [B][Hkv][cap_hi][D];
- *                  k_hi_meta, v_hi_meta [B][Hkv][cap_hi][D/64][2] fp16 (scale, zero).
+ *   hi_bits == 8 or 4: k_hi, v_hi uint8 codes [B][Hkv][cap_hi][D*hi_bits/8],
+ *                  packed as the lo tier below; k_hi_meta, v_hi_meta
+ *                  [B][Hkv][cap_hi][D/64][2] fp16 (scale, zero).  An INT4 important
+ *                  tier with an INT2 low tier is the INT4/INT2 split of the pages'
+ *                  precision sweeps ([notes] "3)", [paperlayer] 4.1).
  *   lo tier:       k_lo, v_lo uint8 [B][Hkv][cap_lo][D*lo_bits/8] packed codes:
  *                  channel c sits in bits [(c*lo_bits) % 8, +lo_bits) of byte
  *                  (c*lo_bits)/8, least significant bits first;
@@ -83,13 +86,13 @@ extern "C" {
  *   pos_hi, pos_lo int32: original sequence position of each slot.
  *   scores         fp32 [B][Hkv][cap_hi]: accumulated H2O importance of each hi slot.
  *   balancer       fp32 [B][Hkv][D] or NULL (identity).
- * Quantised keys (INT8 hi tier and the lo tier) hold I(k*b); the FP16 tier holds
+ * lo_bits <= hi_bits.  Quantised keys (INT8/INT4 hi tier and the lo tier) hold I(k*b); the FP16 tier holds
  * the original k.  Values are never balanced.
  * Code and meta buffers must be 16-byte aligned.
  */
 typedef struct mikv_cache {
   int32_t B, Hkv, Hq, D;
-  int32_t hi_bits, lo_bits; /* hi in {16, 8}; lo in {2, 4, 8} */
+  int32_t hi_bits, lo_bits; /* hi in {16, 8, 4}; lo in {2, 4, 8}, lo <= hi */
   int32_t cap_hi, cap_lo;
   int32_t n_hi, n_lo; /* current counts; updated on the host by the calls that change them */
   void* k_hi;

@@ -42,7 +42,7 @@ class MikvCache:
             self.v_hi = torch.zeros_like(self.k_hi)
             self.k_hi_meta = self.v_hi_meta = None
         else:
-            self.k_hi = torch.zeros(B, Hkv, cap_hi, D, dtype=torch.uint8, device=dev)
+            self.k_hi = torch.zeros(B, Hkv, cap_hi, D * hi_bits // 8, dtype=torch.uint8, device=dev)
             self.v_hi = torch.zeros_like(self.k_hi)
             self.k_hi_meta = torch.zeros(B, Hkv, cap_hi, ng, 2, dtype=torch.float16, device=dev)
             self.v_hi_meta = torch.zeros_like(self.k_hi_meta)

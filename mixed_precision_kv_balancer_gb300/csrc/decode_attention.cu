@@ -1075,7 +1075,7 @@ namespace {
 int prepare_decode(const uint16_t* q, const mikv_cache* c, float* hi_logits, void* ws,
                    size_t ws_bytes, Params& P, int& nsplit, const char* who) {
   if (c->n_hi + c->n_lo < 1) return fail(MIKV_ESHAPE, "%s: empty cache", who);
-  if (c->n_hi > 0 && (!c->k_hi || !c->v_hi || (c->hi_bits == 8 && (!c->k_hi_meta || !c->v_hi_meta))))
+  if (c->n_hi > 0 && (!c->k_hi || !c->v_hi || (c->hi_bits != 16 && (!c->k_hi_meta || !c->v_hi_meta))))
     return fail(MIKV_EINVAL, "%s: null hi-tier buffer", who);
   if (c->n_lo > 0 && (!c->k_lo || !c->v_lo || !c->k_lo_meta || !c->v_lo_meta))
     return fail(MIKV_EINVAL, "%s: null lo-tier buffer", who);
@@ -1111,9 +1111,9 @@ int prepare_decode(const uint16_t* q, const mikv_cache* c, float* hi_logits, voi
                                          align_up(rows * 2 * sizeof(float), 256));
   P.qf = P.qf_out;
   nsplit = P.nsplit_hi + nsplit_lo;
-  if (c->hi_bits * 100 + c->lo_bits != 1602 && c->hi_bits * 100 + c->lo_bits != 1604 &&
-      c->hi_bits * 100 + c->lo_bits != 1608 && c->hi_bits * 100 + c->lo_bits != 802 &&
-      c->hi_bits * 100 + c->lo_bits != 804 && c->hi_bits * 100 + c->lo_bits != 808)
+  const int fmt = c->hi_bits * 100 + c->lo_bits;
+  if (fmt != 1602 && fmt != 1604 && fmt != 1608 && fmt != 802 && fmt != 804 && fmt != 808 &&
+      fmt != 402 && fmt != 404)
     return fail(MIKV_EUNSUPPORTED, "%s: bits %d/%d", who, c->hi_bits, c->lo_bits);
   return MIKV_OK;
 }
@@ -1130,6 +1130,8 @@ int launch_partials(const Params& P, const mikv_cache* c, int nsplit, cudaStream
     case 1608: e = launch_nt<16, 8>(P, grid, s, after, step); break;
     case 802: e = launch_nt<8, 2>(P, grid, s, after, step); break;
     case 804: e = launch_nt<8, 4>(P, grid, s, after, step); break;
+    case 402: e = launch_nt<4, 2>(P, grid, s, after, step); break;
+    case 404: e = launch_nt<4, 4>(P, grid, s, after, step); break;
     default: e = launch_nt<8, 8>(P, grid, s, after, step); break;
   }
   return e;

@@ -73,6 +73,18 @@ struct DemoteArgs {
   float* scores;
 };
 
+// The 4 channels 4*lane.. of a 4-bit code row, dequantised as fl(fl(s*code) + z).
+__device__ __forceinline__ Row4 dequant_int4x4(const uint8_t* row, const __half2* meta, int lane) {
+  const uint32_t w = reinterpret_cast<const uint16_t*>(row)[lane];
+  const __half2 m = meta[lane >> 4];
+  const float sf = __low2float(m), zf = __high2float(m);
+  Row4 r;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    r.x[i] = __fadd_rn(__fmul_rn(sf, static_cast<float>((w >> (4 * i)) & 0xfu)), zf);
+  return r;
+}
+
 __device__ __forceinline__ Row4 dequant_int8x4(const uint8_t* row, const __half2* meta, int lane) {
   const uint32_t w = reinterpret_cast<const uint32_t*>(row)[lane];
   const __half2 m = meta[lane >> 4];
@@ -93,8 +105,8 @@ __device__ __forceinline__ void demote_one(const DemoteArgs& a, long unit, int v
   const long last = unit * a.cap_hi + (a.n_hi - 1);
   const long ls = unit * a.cap_lo + a.n_lo;
   const bool move = hs != last;
-  const int hrb = a.hi_bits == 16 ? kD * 2 : kD;  // bytes per important row
-  const int words = hrb / 4;                        // 64 or 32: lane owns words lane, lane + 32
+  const int hrb = kD * a.hi_bits / 8;  // bytes per important row
+  const int words = hrb / 4;           // 64, 32 or 16: lane owns words lane, lane + 32
   uint32_t lk0 = 0, lk1 = 0, lv0 = 0, lv1 = 0;
   __half2 lkm = {}, lvm = {};
   int lpos = 0;
@@ -102,13 +114,15 @@ __device__ __forceinline__ void demote_one(const DemoteArgs& a, long unit, int v
   if (move) {
     const uint32_t* sk = reinterpret_cast<const uint32_t*>(a.k_hi + last * hrb);
     const uint32_t* sv = reinterpret_cast<const uint32_t*>(a.v_hi + last * hrb);
-    lk0 = sk[lane];
-    lv0 = sv[lane];
+    if (lane < words) {
+      lk0 = sk[lane];
+      lv0 = sv[lane];
+    }
     if (words > 32) {
       lk1 = sk[lane + 32];
       lv1 = sv[lane + 32];
     }
-    if (a.hi_bits == 8 && lane < 2) {
+    if (a.hi_bits != 16 && lane < 2) {
       lkm = a.k_hi_meta[last * 2 + lane];
       lvm = a.v_hi_meta[last * 2 + lane];
     }
@@ -128,9 +142,12 @@ __device__ __forceinline__ void demote_one(const DemoteArgs& a, long unit, int v
       xk.x[2] = __fmul_rn(xk.x[2], bb.z);
       xk.x[3] = __fmul_rn(xk.x[3], bb.w);
     }
-  } else {  // INT8 tier holds balanced keys already
-    xk = dequant_int8x4(a.k_hi + hs * kD, a.k_hi_meta + hs * 2, lane);
-    xv = dequant_int8x4(a.v_hi + hs * kD, a.v_hi_meta + hs * 2, lane);
+  } else if (a.hi_bits == 8) {  // quantised tiers hold balanced keys already
+    xk = dequant_int8x4(a.k_hi + hs * hrb, a.k_hi_meta + hs * 2, lane);
+    xv = dequant_int8x4(a.v_hi + hs * hrb, a.v_hi_meta + hs * 2, lane);
+  } else {
+    xk = dequant_int4x4(a.k_hi + hs * hrb, a.k_hi_meta + hs * 2, lane);
+    xv = dequant_int4x4(a.v_hi + hs * hrb, a.v_hi_meta + hs * 2, lane);
   }
   const int vpos = lane == 0 ? a.pos_hi[hs] : 0;
   const int rb = kD * a.lo_bits / 8;
@@ -147,13 +164,15 @@ __device__ __forceinline__ void demote_one(const DemoteArgs& a, long unit, int v
   if (move) {
     uint32_t* dk = reinterpret_cast<uint32_t*>(a.k_hi + hs * hrb);
     uint32_t* dv = reinterpret_cast<uint32_t*>(a.v_hi + hs * hrb);
-    dk[lane] = lk0;
-    dv[lane] = lv0;
+    if (lane < words) {
+      dk[lane] = lk0;
+      dv[lane] = lv0;
+    }
     if (words > 32) {
       dk[lane + 32] = lk1;
       dv[lane + 32] = lv1;
     }
-    if (a.hi_bits == 8 && lane < 2) {
+    if (a.hi_bits != 16 && lane < 2) {
       a.k_hi_meta[hs * 2 + lane] = lkm;
       a.v_hi_meta[hs * 2 + lane] = lvm;
     }

@@ -39,10 +39,10 @@ __global__ void __launch_bounds__(256) demote_kernel(DemoteArgs a) {
 int validate_cache(const mikv_cache* c, const char* who) {
   if (!c) return fail(MIKV_EINVAL, "%s: null cache", who);
   if (c->D != kD) return fail(MIKV_EUNSUPPORTED, "%s: D=%d (only %d)", who, c->D, kD);
-  if (c->hi_bits != 16 && c->hi_bits != 8)
-    return fail(MIKV_EUNSUPPORTED, "%s: hi_bits=%d (16 or 8)", who, c->hi_bits);
-  if (c->lo_bits != 2 && c->lo_bits != 4 && c->lo_bits != 8)
-    return fail(MIKV_EUNSUPPORTED, "%s: lo_bits=%d (2, 4 or 8)", who, c->lo_bits);
+  if (c->hi_bits != 16 && c->hi_bits != 8 && c->hi_bits != 4)
+    return fail(MIKV_EUNSUPPORTED, "%s: hi_bits=%d (16, 8 or 4)", who, c->hi_bits);
+  if ((c->lo_bits != 2 && c->lo_bits != 4 && c->lo_bits != 8) || c->lo_bits > c->hi_bits)
+    return fail(MIKV_EUNSUPPORTED, "%s: lo_bits=%d (2, 4 or 8, at most hi_bits)", who, c->lo_bits);
   if (c->B < 1 || c->Hkv < 1 || c->Hq < c->Hkv || c->Hq % c->Hkv || c->Hq / c->Hkv > 8)
     return fail(MIKV_ESHAPE, "%s: bad heads B=%d Hq=%d Hkv=%d", who, c->B, c->Hq, c->Hkv);
   if (c->cap_hi < 0 || c->cap_lo < 0 || c->n_hi < 0 || c->n_lo < 0 || c->n_hi > c->cap_hi ||
@@ -156,7 +156,7 @@ int demote_args(const mikv_cache* c, const int32_t* victim, DemoteArgs& a) {
   a.pos_lo = c->pos_lo;
   a.scores = c->scores;
   if (!a.k_hi || !a.v_hi || !a.k_lo || !a.v_lo || !a.k_lo_meta || !a.v_lo_meta || !a.pos_hi ||
-      !a.pos_lo || !a.scores || (c->hi_bits == 8 && (!a.k_hi_meta || !a.v_hi_meta)))
+      !a.pos_lo || !a.scores || (c->hi_bits != 16 && (!a.k_hi_meta || !a.v_hi_meta)))
     return fail(MIKV_EINVAL, "demotion: null cache buffer");
   if (!aligned16(a.k_hi) || !aligned16(a.v_hi) || !aligned16(a.k_lo) || !aligned16(a.v_lo) ||
       !aligned16(a.k_lo_meta) || !aligned16(a.v_lo_meta))

@@ -56,7 +56,7 @@ def _positions(rng, B, Hkv, T, keep):
     return kp, ep
 
 
-@pytest.mark.parametrize("hi_bits,lo_bits", [(16, 2), (16, 4), (16, 8), (8, 2), (8, 4)])
+@pytest.mark.parametrize("hi_bits,lo_bits", [(16, 2), (16, 4), (16, 8), (8, 2), (8, 4), (4, 2), (4, 4)])
 def test_append_and_demote_bit_exact(hi_bits, lo_bits):
     wl = _wl(B=2, Hq=8, Hkv=2, T=257)
     x = inputs.make_prefill(wl, 2, "cpu")
@@ -123,6 +123,8 @@ ATTN_CASES = [
     (16, 2, 1, 8, 2, 300, 100, 8),      # 100% FP16: empty low tier
     (16, 4, 1, 8, 2, 300, 0, 0),        # empty important tier
     (8, 8, 1, 4, 1, 17, 50, 2),         # tiny ragged everything
+    (4, 2, 2, 32, 8, 800, 20, 32),      # INT4 important tier over INT2
+    (4, 4, 1, 40, 8, 500, 30, 16),      # INT4 / INT4, GQA 5
 ]
 
 
@@ -316,7 +318,10 @@ def test_vwo_norms(B, Hkv, rep, L, hidden):
 # ------------------------------------------------------------------ the composed path
 @pytest.mark.parametrize("name,scale", [("tiny", {}), ("llama31_8b", dict(B=2, T=700, steps=6)),
                                         ("qwen25_32b", dict(T=600, steps=4, hidden=640, Hq=10, Hkv=2)),
-                                        ("llama2_7b", dict(B=1, Hq=4, Hkv=4, T=400, steps=8))])
+                                        ("llama2_7b", dict(B=1, Hq=4, Hkv=4, T=400, steps=8)),
+                                        ("llama2_7b", dict(B=1, Hq=8, Hkv=2, T=300, steps=6, hi_bits=4)),
+                                        ("tiny", dict(budget_pct=0, window=0, steps=4)),     # uniform RTN
+                                        ("tiny", dict(budget_pct=100, steps=4))])            # all FP16
 def test_pipeline_matches_oracle(name, scale):
     """Prefill + decode steps through the library vs the oracle's composed path.
 
@@ -361,7 +366,8 @@ def test_pipeline_matches_oracle(name, scale):
 
 @pytest.mark.parametrize("name,scale", [("tiny", dict(steps=12)), ("llama31_8b", dict(B=2, T=600, steps=5)),
                                         ("llama2_7b", dict(B=2, Hq=8, Hkv=8, T=300, steps=6)),
-                                        ("qwen25_32b", dict(T=400, steps=3, Hq=10, Hkv=2))])
+                                        ("qwen25_32b", dict(T=400, steps=3, Hq=10, Hkv=2)),
+                                        ("tiny", dict(steps=6, hi_bits=4, lo_bits=2))])
 def test_fused_step_equals_separate_calls(name, scale):
     """mikv_decode_step (4 launches) leaves every buffer and output bit-identical to the
     five-call sequence."""
