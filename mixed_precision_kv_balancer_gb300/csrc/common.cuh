@@ -39,6 +39,11 @@ __device__ __forceinline__ void cp_async8(uint32_t dst, const void* src, bool va
   int n = valid ? 8 : 0;
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(dst), "l"(src), "r"(n));
 }
+// 4-byte async copy; zero-filled without reading when !valid.
+__device__ __forceinline__ void cp_async4_or_zero(uint32_t dst, const void* src, bool valid) {
+  int n = valid ? 4 : 0;
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(n));
+}
 // Hint: bring `bytes` (multiple of 16, 16-byte aligned) of global memory into L2.
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");

@@ -17,6 +17,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "tcgen05.cuh"
 
 namespace mikv {
 int validate_cache_public(const mikv_cache* c, const char* who);
@@ -242,6 +243,287 @@ __global__ void __launch_bounds__(kThr) col_sum_kernel(const __half* __restrict_
   }
 }
 
+// ---------------------------------------------------------------------------------
+// The same two passes on the 5th-generation tensor cores: 128 x 128 tiles, S = A . B^T
+// accumulated in TMEM by tcgen05.mma (fp16 in, fp32 accumulate), double-buffered in TMEM
+// so the next tile's MMA runs while the CTA exponentiates the current one.  256 threads:
+// row r of S (TMEM lane r) belongs to threads r and r + 128, which take columns 0..63 and
+// 64..127 and keep their own running state, combined once at the end.  The streamed
+// operand is double-buffered in shared memory by cp.async.  Per CTA: 3 tiles of 32 KB
+// (+ 1 KB of lse rows) and 256 TMEM columns, so two CTAs share an SM.
+constexpr int kTcTile = tc::kTileRows;
+constexpr int kTcThreads = 256;
+constexpr int kTcHalf = kTcTile / 2;                           // columns per thread
+constexpr int kTcCols = 2 * kTcTile;                           // two accumulators
+constexpr int kTcSmem = 3 * tc::kTileBytes + 2 * kTcTile * 4;  // + two lse rows (pass 2)
+constexpr uint32_t kTcIdesc = tc::idesc_f16(kTcTile, kTcTile);
+
+// Per-CTA set-up: mbarriers (one per TMEM accumulator) and the TMEM allocation.
+__device__ __forceinline__ uint32_t tc_setup(uint64_t* mbar, uint32_t* tslot) {
+  if (threadIdx.x == 0) {
+    tc::mbar_init(smem_u32(&mbar[0]), 1);
+    tc::mbar_init(smem_u32(&mbar[1]), 1);
+    tc::mbar_init_fence();
+  }
+  if (threadIdx.x < 32) tc::tmem_alloc(smem_u32(tslot), kTcCols);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  return *tslot;
+}
+__device__ __forceinline__ void tc_teardown(uint32_t tbase) {
+  tc::fence_before_sync();
+  __syncthreads();
+  if (threadIdx.x < 32) tc::tmem_dealloc(tbase, kTcCols);
+}
+// Stage a tile with all kTcThreads threads (two halves of the 128-thread copy loop).
+__device__ __forceinline__ void tc_load_tile(uint32_t s, const __half* g, long r0, int nrows) {
+  const int half = threadIdx.x >> 7;
+#pragma unroll 4
+  for (int i = (threadIdx.x & 127) + half * 1024; i < (half + 1) * 1024; i += 128) {
+    const int r = (i & 7) + ((i >> 7) << 3);
+    const int kc = ((i >> 3) & 15) * 8;
+    const bool ok = r < nrows;
+    const __half* src = ok ? g + (r0 + r) * kD + kc : g;
+    cp_async16(s + tc::tile_off(r, kc), src, ok);
+  }
+}
+
+// Pass 1 on tcgen05: lse2[b][h][t] for the 128 query rows of one block.
+__global__ void __launch_bounds__(kTcThreads, 2) row_lse_tc_kernel(const __half* __restrict__ q,
+                                                                   const __half* __restrict__ k, int Hq,
+                                                                   int Hkv, int T, float* __restrict__ lse2) {
+  extern __shared__ __align__(128) uint8_t sm[];  // Q tile, 2 K tiles
+  __shared__ __align__(8) uint64_t mbar[2];
+  __shared__ uint32_t tslot;
+  __shared__ float xm[kTcTile], xl[kTcTile];
+  const int nblk = (T + kTcTile - 1) / kTcTile;
+  const int rb = nblk - 1 - blockIdx.x;  // heaviest (last) row block first
+  const int bh = blockIdx.y, b = bh / Hq, h = bh % Hq;
+  const int g = h / (Hq / Hkv);
+  const int tid = threadIdx.x, warp = tid >> 5, row = tid & 127, half = tid >> 7;
+  const __half* qb = q + static_cast<long>(bh) * T * kD;
+  const __half* kb = k + (static_cast<long>(b) * Hkv + g) * T * kD;
+  const uint32_t sq = smem_u32(sm), sk0 = sq + tc::kTileBytes;
+  const int t0 = rb * kTcTile;
+  const uint32_t tbase = tc_setup(mbar, &tslot);
+  // prologue: Q and K tile 0, then K tile 1
+  tc_load_tile(sq, qb, t0, min(kTcTile, T - t0));
+  tc_load_tile(sk0, kb, 0, min(kTcTile, T));
+  cp_async_commit();
+  if (rb >= 1) tc_load_tile(sk0 + tc::kTileBytes, kb, kTcTile, min(kTcTile, T - kTcTile));
+  cp_async_commit();
+  cp_async_wait<1>();
+  tc::fence_proxy_async();
+  __syncthreads();
+  if (tid == 0) {
+    tc::fence_after_sync();
+    tc::mma_tile(tbase, sq, sk0, kTcIdesc);
+    tc::commit(smem_u32(&mbar[0]));
+  }
+  const int t = t0 + row;  // this thread's query row
+  float m = -INFINITY, l = 0.f, lc = 0.f;
+  bool ok = true;
+  for (int kt = 0; kt <= rb; ++kt) {
+    const int buf = kt & 1;
+    if (kt + 1 <= rb) {  // MMA of the next tile before this one is exponentiated
+      cp_async_wait<0>();
+      tc::fence_proxy_async();
+      tc::fence_before_sync();
+      __syncthreads();
+      if (tid == 0) {
+        tc::fence_after_sync();
+        tc::mma_tile(tbase + (buf ^ 1) * kTcTile, sq, sk0 + (buf ^ 1) * tc::kTileBytes, kTcIdesc);
+        tc::commit(smem_u32(&mbar[buf ^ 1]));
+      }
+    }
+    ok = tc::mbar_wait(smem_u32(&mbar[buf]), (kt >> 1) & 1) && ok;
+    tc::fence_after_sync();
+    if (kt + 2 <= rb)  // K tile kt's buffer is free once its MMA is done
+      tc_load_tile(sk0 + buf * tc::kTileBytes, kb, (kt + 2) * kTcTile, min(kTcTile, T - (kt + 2) * kTcTile));
+    cp_async_commit();
+    // this thread's 64 raw dot products: row t, keys kt*128 + half*64 ..
+    float s[kTcHalf];
+    const uint32_t lane_addr =
+        tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16) + buf * kTcTile + half * kTcHalf;
+    tc::tmem_ld32(lane_addr, *reinterpret_cast<float(*)[32]>(s));
+    tc::tmem_ld32(lane_addr + 32, *reinterpret_cast<float(*)[32]>(s + 32));
+    const int i0 = kt * kTcTile + half * kTcHalf;
+    const int lim = min(t - i0, T - 1 - i0);  // columns 0..lim are causal and in range
+    // 8 independent max / sum chains; masks only on the diagonal or last tile
+    float mx8[8], sm8[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mx8[j] = -INFINITY;
+    if (lim >= kTcHalf - 1) {
+#pragma unroll
+      for (int c = 0; c < kTcHalf; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+    } else {
+#pragma unroll
+      for (int c = 0; c < kTcHalf; ++c)
+        if (c <= lim) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+    }
+    const float mxr = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                            fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+    const float mn = fmaxf(m, mxr * kC);  // kC > 0: the max commutes with the scaling
+    if (mn != -INFINITY) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) sm8[j] = 0.f;
+      if (lim >= kTcHalf - 1) {
+#pragma unroll
+        for (int c = 0; c < kTcHalf; ++c) sm8[c & 7] += fast_exp2(fmaf(s[c], kC, -mn));
+      } else {
+#pragma unroll
+        for (int c = 0; c < kTcHalf; ++c)
+          if (c <= lim) sm8[c & 7] += fast_exp2(fmaf(s[c], kC, -mn));
+      }
+      const float sum = ((sm8[0] + sm8[1]) + (sm8[2] + sm8[3])) + ((sm8[4] + sm8[5]) + (sm8[6] + sm8[7]));
+      const float alpha = fast_exp2(m - mn);
+      l = __fmul_rn(l, alpha);
+      lc = __fmul_rn(lc, alpha);
+      const float y = sum - lc;
+      const float tt = l + y;
+      lc = (tt - l) - y;
+      l = tt;
+      m = mn;
+    }
+  }
+  cp_async_wait<0>();
+  // the two halves of each row: half 1 hands its (m, l) to half 0
+  if (half == 1) {
+    xm[row] = m;
+    xl[row] = l - lc;
+  }
+  tc_teardown(tbase);  // (its barrier also publishes xm / xl)
+  if (half == 0 && t < T) {
+    const float m1 = xm[row], l1 = xl[row], l0 = l - lc;
+    const float M = fmaxf(m, m1);
+    const float L = (m == -INFINITY ? 0.f : l0 * fast_exp2(m - M)) + (m1 == -INFINITY ? 0.f : l1 * fast_exp2(m1 - M));
+    lse2[static_cast<long>(bh) * T + t] = ok ? M + log2f(L) : __int_as_float(0x7fc00000);
+  }
+}
+
+// Pass 2 on tcgen05: S^h_i (and S_i) for 128 keys of one (b, key head).  S^T = K . Q^T per
+// query tile: TMEM lane = key, column = query; thread i and i + 128 take the query halves.
+__global__ void __launch_bounds__(kTcThreads, 2) col_sum_tc_kernel(const __half* __restrict__ q,
+                                                                   const __half* __restrict__ k,
+                                                                   const float* __restrict__ lse2, int Hq,
+                                                                   int Hkv, int T, float* __restrict__ s_full,
+                                                                   float* __restrict__ s_head) {
+  extern __shared__ __align__(128) uint8_t sm[];  // K tile, 2 Q tiles, 2 lse rows
+  __shared__ __align__(8) uint64_t mbar[2];
+  __shared__ uint32_t tslot;
+  __shared__ float xs[kTcTile];
+  float (*sl)[kTcTile] = reinterpret_cast<float (*)[kTcTile]>(sm + 3 * tc::kTileBytes);
+  const int nblk = (T + kTcTile - 1) / kTcTile;
+  const int kbi = blockIdx.x;  // key block 0 (heaviest) first
+  const int unit = blockIdx.y, b = unit / Hkv, g = unit % Hkv;
+  const int rep = Hq / Hkv;
+  const int tid = threadIdx.x, warp = tid >> 5, row = tid & 127, half = tid >> 7;
+  const __half* kbase = k + static_cast<long>(unit) * T * kD;
+  const uint32_t sk = smem_u32(sm), sq0 = sk + tc::kTileBytes;
+  const int i0 = kbi * kTcTile;
+  const int per = nblk - kbi;   // query tiles per head
+  const int ntile = rep * per;  // tiles of this CTA, head-major
+  const uint32_t tbase = tc_setup(mbar, &tslot);
+  // tile n: head hr = n / per, query tile qt = kbi + n % per
+  auto load_q = [&](int n, int buf) {
+    const int hr = n / per, qt = kbi + n % per;
+    const long bh = static_cast<long>(b) * Hq + g * rep + hr;
+    tc_load_tile(sq0 + buf * tc::kTileBytes, q + bh * T * kD, static_cast<long>(qt) * kTcTile,
+                 min(kTcTile, T - qt * kTcTile));
+    if (tid < kTcTile) {
+      const int tq = qt * kTcTile + tid;
+      cp_async4_or_zero(smem_u32(&sl[buf][tid]), lse2 + bh * T + min(tq, T - 1), tq < T);
+    }
+  };
+  tc_load_tile(sk, kbase, i0, min(kTcTile, T - i0));
+  load_q(0, 0);
+  cp_async_commit();
+  if (ntile > 1) load_q(1, 1);
+  cp_async_commit();
+  cp_async_wait<1>();
+  tc::fence_proxy_async();
+  __syncthreads();
+  if (tid == 0) {
+    tc::fence_after_sync();
+    tc::mma_tile(tbase, sk, sq0, kTcIdesc);
+    tc::commit(smem_u32(&mbar[0]));
+  }
+  const int i = i0 + row;  // this thread's key
+  float col = 0.f, colc = 0.f, tot = 0.f;
+  bool ok = true;
+  for (int n = 0; n < ntile; ++n) {
+    const int buf = n & 1;
+    if (n + 1 < ntile) {
+      cp_async_wait<0>();
+      tc::fence_proxy_async();
+      tc::fence_before_sync();
+      __syncthreads();
+      if (tid == 0) {
+        tc::fence_after_sync();
+        tc::mma_tile(tbase + (buf ^ 1) * kTcTile, sk, sq0 + (buf ^ 1) * tc::kTileBytes, kTcIdesc);
+        tc::commit(smem_u32(&mbar[buf ^ 1]));
+      }
+    }
+    ok = tc::mbar_wait(smem_u32(&mbar[buf]), (n >> 1) & 1) && ok;
+    tc::fence_after_sync();
+    // this thread's half of the lse row, before its buffer is refilled
+    float lt[kTcHalf];
+#pragma unroll
+    for (int c = 0; c < kTcHalf; c += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(&sl[buf][half * kTcHalf + c]);
+      lt[c] = v.x;
+      lt[c + 1] = v.y;
+      lt[c + 2] = v.z;
+      lt[c + 3] = v.w;
+    }
+    __syncthreads();  // every thread holds its lse values: the buffer may be refilled
+    if (n + 2 < ntile) load_q(n + 2, buf);
+    cp_async_commit();
+    const int qt = kbi + n % per;
+    const int cq = qt * kTcTile + half * kTcHalf;  // query of this thread's column 0
+    const int c0 = max(i - cq, 0);                  // first causal column (query >= key)
+    const int c1 = min(kTcHalf, T - cq);            // columns past T are padding
+    float p8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent chains
+    const bool full = c0 == 0 && c1 == kTcHalf;
+    const uint32_t lane_addr =
+        tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16) + buf * kTcTile + half * kTcHalf;
+#pragma unroll
+    for (int c = 0; c < kTcHalf; c += 32) {
+      float s[32];
+      tc::tmem_ld32(lane_addr + c, s);
+      if (full) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) p8[e & 7] += fast_exp2(fmaf(s[e], kC, -lt[c + e]));
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (c + e >= c0 && c + e < c1) p8[e & 7] += fast_exp2(fmaf(s[e], kC, -lt[c + e]));
+      }
+    }
+    const float part = ((p8[0] + p8[1]) + (p8[2] + p8[3])) + ((p8[4] + p8[5]) + (p8[6] + p8[7]));
+    const float y = part - colc;
+    const float tt = col + y;
+    colc = (tt - col) - y;
+    col = tt;
+    if (n % per == per - 1) {  // head done: the two query halves of each key, then the group
+      if (half == 1) xs[row] = col - colc;
+      __syncthreads();
+      if (half == 0) {
+        const int hr = n / per;
+        const float sh = ok ? (col - colc) + xs[row] : __int_as_float(0x7fc00000);
+        const long bh = static_cast<long>(b) * Hq + g * rep + hr;
+        if (i < T && s_head) s_head[bh * T + i] = sh;
+        tot = __fadd_rn(tot, sh);  // group sum in head order
+      }
+      col = colc = 0.f;
+    }
+  }
+  cp_async_wait<0>();
+  if (half == 0 && i < T) s_full[static_cast<long>(unit) * T + i] = tot;
+  tc_teardown(tbase);
+}
+
 // K4: S[b][g][j] += sum_h exp(logit[b][h][j] - lse[b][h]) for j < n_hi.
 __global__ void score_decode_kernel(const float* __restrict__ logits, const float* __restrict__ lse,
                                     float* __restrict__ scores, int Hq, int Hkv, int cap, int n) {
@@ -284,18 +566,18 @@ extern "C" int mikv_score_update(int mode, const uint16_t* q, const uint16_t* k,
     const size_t need = mikv_score_workspace_bytes(c->B, c->Hq, T);
     if (ws_bytes < need) return fail(MIKV_ESHAPE, "score_update: workspace %zu < %zu", ws_bytes, need);
     float* lse2 = static_cast<float*>(ws);
-    const int nblk = (T + kTile - 1) / kTile;
-    if (cudaFuncSetAttribute(row_lse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(col_sum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem) != cudaSuccess)
+    const int nblk = (T + kTcTile - 1) / kTcTile;
+    if (cudaFuncSetAttribute(row_lse_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(col_sum_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess)
       return check_launch("score kernels attribute");
-    row_lse_kernel<<<dim3(nblk, c->B * c->Hq), kThr, kScoreSmem, s>>>(
+    row_lse_tc_kernel<<<dim3(nblk, c->B * c->Hq), kTcThreads, kTcSmem, s>>>(
         reinterpret_cast<const __half*>(q), reinterpret_cast<const __half*>(k), c->Hq, c->Hkv, T,
         lse2);
-    if (int e = check_launch("row_lse_kernel")) return e;
-    col_sum_kernel<<<dim3(nblk, c->B * c->Hkv), kThr, kScoreSmem, s>>>(
+    if (int e = check_launch("row_lse_tc_kernel")) return e;
+    col_sum_tc_kernel<<<dim3(nblk, c->B * c->Hkv), kTcThreads, kTcSmem, s>>>(
         reinterpret_cast<const __half*>(q), reinterpret_cast<const __half*>(k), lse2, c->Hq, c->Hkv,
         T, scores_full, scores_head);
-    return check_launch("col_sum_kernel");
+    return check_launch("col_sum_tc_kernel");
   }
   if (mode == MIKV_DECODE) {
     if (int e = validate_cache_public(c, "score_update")) return e;

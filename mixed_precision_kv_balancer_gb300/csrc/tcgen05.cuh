@@ -1,0 +1,141 @@
+// 5th-generation tensor core (tcgen05) building blocks for sm_103a, as inline PTX.
+//
+// Operands live in shared memory in the K-major core-matrix layout without swizzle: a
+// core matrix is 8 rows x 16 bytes (8 fp16 of the reduction dimension), stored as 128
+// contiguous bytes; core matrices adjacent along K are kLbo bytes apart and 8-row groups
+// kSbo bytes apart.  A 128 x 128 fp16 tile is 32 KB.  Accumulators live in tensor memory
+// (TMEM): for M = 128 with one CTA, row i of D is TMEM lane i and column n is column
+// base + n, fp32.  One thread issues the MMAs; completion is signalled on an mbarrier by
+// tcgen05.commit; every wait on an mbarrier is bounded.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace mikv {
+namespace tc {
+
+constexpr int kTileRows = 128;                 // M = N = 128 rows per operand tile
+constexpr int kTileBytes = kTileRows * kD * 2; // 32 KB fp16
+constexpr uint32_t kLbo = 128;                 // K-direction core-matrix stride
+constexpr uint32_t kSbo = (kD / 8) * 128;      // 8-row-group stride (2048 B)
+
+// Byte offset of element (r, k) of a [128][kD] fp16 tile in the core-matrix layout.
+__host__ __device__ __forceinline__ uint32_t tile_off(int r, int k) {
+  return static_cast<uint32_t>(((r >> 3) * (kD / 8) + (k >> 3)) * 128 + (r & 7) * 16 + (k & 7) * 2);
+}
+
+// Shared-memory matrix descriptor: start address, K-direction and row-group strides, the
+// descriptor version of this architecture (bits 46-47 = 1), no swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+  uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((kLbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((kSbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
+// Instruction descriptor for kind::f16: D fp32, A and B fp16, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A . B^T over K = 16 (one fp16 MMA step).
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate ? 1u : 0u));
+}
+
+// D = A . B^T for two [128][kD] tiles at sa / sb (8 MMA steps along K).
+__device__ __forceinline__ void mma_tile(uint32_t tmem_d, uint32_t sa, uint32_t sb, uint32_t idesc) {
+#pragma unroll
+  for (int ks = 0; ks < kD / 16; ++ks)
+    mma_f16(tmem_d, smem_desc(sa + ks * 2 * kLbo), smem_desc(sb + ks * 2 * kLbo), idesc, ks > 0);
+}
+
+// The mbarrier at `mbar` completes when every tcgen05 op this thread issued so far is done.
+__device__ __forceinline__ void commit(uint32_t mbar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(mbar)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(mbar), "r"(count));
+}
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+
+// Wait for phase `parity` of the mbarrier, giving up after `limit` polls; true if it completed.
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, long limit = 1L << 22) {
+  uint32_t done = 0;
+  for (long it = 0; it < limit && !done; ++it) {
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+  }
+  return done != 0;
+}
+
+__device__ __forceinline__ void fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+// Shared-memory writes of the generic proxy (cp.async, st.shared) visible to the tensor core.
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+// TMEM allocation by one full warp: writes the base address to `slot` (shared memory).
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(slot), "r"(ncols));
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t base, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(base), "r"(ncols));
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes 32*(w%4)..).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Stage rows [r0, r0 + 128) of a row-major [rows][kD] fp16 matrix into the tile at `s`
+// with 16-byte cp.async copies (rows >= nrows zero-filled, not read).  Thread i of 128 takes
+// chunks i, i + 128, ...; eight consecutive threads fill one core matrix (8 rows x 16 B),
+// so a warp writes 512 contiguous bytes.
+__device__ __forceinline__ void load_tile_async(uint32_t s, const __half* g, long r0, int nrows) {
+#pragma unroll 4
+  for (int i = threadIdx.x; i < kTileRows * (kD / 8); i += 128) {
+    const int r = (i & 7) + ((i >> 7) << 3);  // row within the tile
+    const int kc = ((i >> 3) & 15) * 8;        // first channel of the 16-byte chunk
+    const bool ok = r < nrows;
+    const __half* src = ok ? g + (r0 + r) * kD + kc : g;
+    cp_async16(s + tile_off(r, kc), src, ok);
+  }
+}
+
+}  // namespace tc
+}  // namespace mikv
