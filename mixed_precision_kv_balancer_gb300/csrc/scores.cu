@@ -14,7 +14,11 @@
 //           every 64-query tile at or below the diagonal, exp2(s - lse_t) summed
 //           over the queries -> S^h_i, then S_i in head order.
 // Work is triangular, so CTAs are numbered heaviest first.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "tcgen05.cuh"
@@ -244,25 +248,42 @@ __global__ void __launch_bounds__(kThr) col_sum_kernel(const __half* __restrict_
 }
 
 // ---------------------------------------------------------------------------------
-// The same two passes on the 5th-generation tensor cores: 128 x 128 tiles, S = A . B^T
-// accumulated in TMEM by tcgen05.mma (fp16 in, fp32 accumulate), double-buffered in TMEM
-// so the next tile's MMA runs while the CTA exponentiates the current one.  256 threads:
-// row r of S (TMEM lane r) belongs to threads r and r + 128, which take columns 0..63 and
-// 64..127 and keep their own running state, combined once at the end.  The streamed
-// operand is double-buffered in shared memory by cp.async.  Per CTA: 3 tiles of 32 KB
-// (+ 1 KB of lse rows) and 256 TMEM columns, so two CTAs share an SM.
+// The two passes on the 5th-generation tensor cores.  128 x 128 tiles, S = A . B^T by
+// tcgen05.mma (fp16 in, fp32 accumulate in TMEM), two TMEM accumulators so the next tile's
+// MMA runs while the CTA exponentiates the current one.  Thread 0 is also the producer: it
+// streams the operand tiles with TMA (two shared-memory buffers) and issues the MMAs; every
+// hand-off is an mbarrier (tile loaded, MMA done, accumulator consumed by all 256 threads),
+// so no thread waits at a CTA barrier inside the loop.  Row r of S (TMEM lane r) belongs to
+// threads r and r + 128, which take columns 0..63 and 64..127 and keep their own running
+// state, combined once at the end.  Per CTA: 3 tiles of 32 KB plus 2 KB of lse rows and
+// 256 TMEM columns, so two CTAs share an SM.
 constexpr int kTcTile = tc::kTileRows;
 constexpr int kTcThreads = 256;
-constexpr int kTcHalf = kTcTile / 2;                           // columns per thread
-constexpr int kTcCols = 2 * kTcTile;                           // two accumulators
-constexpr int kTcSmem = 3 * tc::kTileBytes + 2 * kTcTile * 4;  // + two lse rows (pass 2)
+constexpr int kTcHalf = kTcTile / 2;                                    // columns per thread
+constexpr int kTcCols = 2 * kTcTile;                                    // two accumulators
+constexpr int kTcLseRing = 4;                                           // lse rows in flight
+constexpr int kTcSmem = 3 * tc::kTileBytes + kTcLseRing * kTcTile * 4 + 128;  // + alignment
 constexpr uint32_t kTcIdesc = tc::idesc_f16(kTcTile, kTcTile);
 
-// Per-CTA set-up: mbarriers (one per TMEM accumulator) and the TMEM allocation.
-__device__ __forceinline__ uint32_t tc_setup(uint64_t* mbar, uint32_t* tslot) {
+// lse rows are padded to whole tiles so one tile's 128 values are one aligned bulk copy.
+__host__ __device__ __forceinline__ int lse_stride(int T) { return (T + kTcTile - 1) / kTcTile * kTcTile; }
+
+struct TcBars {
+  uint64_t load[2];   // operand buffer b filled (TMA bytes)
+  uint64_t mma[2];    // accumulator b written (tcgen05.commit)
+  uint64_t freed[2];  // accumulator b read by all threads
+  uint64_t fixed;     // the resident operand tile filled
+};
+
+// Per-CTA set-up: mbarriers and the TMEM allocation; returns the TMEM base.
+__device__ __forceinline__ uint32_t tc_setup(TcBars& bar, uint32_t* tslot) {
   if (threadIdx.x == 0) {
-    tc::mbar_init(smem_u32(&mbar[0]), 1);
-    tc::mbar_init(smem_u32(&mbar[1]), 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(smem_u32(&bar.load[i]), 1);
+      tc::mbar_init(smem_u32(&bar.mma[i]), 1);
+      tc::mbar_init(smem_u32(&bar.freed[i]), kTcThreads);
+    }
+    tc::mbar_init(smem_u32(&bar.fixed), 1);
     tc::mbar_init_fence();
   }
   if (threadIdx.x < 32) tc::tmem_alloc(smem_u32(tslot), kTcCols);
@@ -276,25 +297,16 @@ __device__ __forceinline__ void tc_teardown(uint32_t tbase) {
   __syncthreads();
   if (threadIdx.x < 32) tc::tmem_dealloc(tbase, kTcCols);
 }
-// Stage a tile with all kTcThreads threads (two halves of the 128-thread copy loop).
-__device__ __forceinline__ void tc_load_tile(uint32_t s, const __half* g, long r0, int nrows) {
-  const int half = threadIdx.x >> 7;
-#pragma unroll 4
-  for (int i = (threadIdx.x & 127) + half * 1024; i < (half + 1) * 1024; i += 128) {
-    const int r = (i & 7) + ((i >> 7) << 3);
-    const int kc = ((i >> 3) & 15) * 8;
-    const bool ok = r < nrows;
-    const __half* src = ok ? g + (r0 + r) * kD + kc : g;
-    cp_async16(s + tc::tile_off(r, kc), src, ok);
-  }
-}
+// 128-byte aligned base of the dynamic shared memory (TMA destinations).
+__device__ __forceinline__ uint32_t tc_base(uint8_t* sm) { return (smem_u32(sm) + 127u) & ~127u; }
 
-// Pass 1 on tcgen05: lse2[b][h][t] for the 128 query rows of one block.
-__global__ void __launch_bounds__(kTcThreads, 2) row_lse_tc_kernel(const __half* __restrict__ q,
-                                                                   const __half* __restrict__ k, int Hq,
-                                                                   int Hkv, int T, float* __restrict__ lse2) {
+// Pass 1 on tcgen05: lse2[b][h][t] (row stride lse_stride(T)) for 128 query rows.
+__global__ void __launch_bounds__(kTcThreads, 2) row_lse_tc_kernel(const __grid_constant__ CUtensorMap tq,
+                                                                   const __grid_constant__ CUtensorMap tk,
+                                                                   int Hq, int Hkv, int T,
+                                                                   float* __restrict__ lse2) {
   extern __shared__ __align__(128) uint8_t sm[];  // Q tile, 2 K tiles
-  __shared__ __align__(8) uint64_t mbar[2];
+  __shared__ __align__(8) TcBars bar;
   __shared__ uint32_t tslot;
   __shared__ float xm[kTcTile], xl[kTcTile];
   const int nblk = (T + kTcTile - 1) / kTcTile;
@@ -302,52 +314,47 @@ __global__ void __launch_bounds__(kTcThreads, 2) row_lse_tc_kernel(const __half*
   const int bh = blockIdx.y, b = bh / Hq, h = bh % Hq;
   const int g = h / (Hq / Hkv);
   const int tid = threadIdx.x, warp = tid >> 5, row = tid & 127, half = tid >> 7;
-  const __half* qb = q + static_cast<long>(bh) * T * kD;
-  const __half* kb = k + (static_cast<long>(b) * Hkv + g) * T * kD;
-  const uint32_t sq = smem_u32(sm), sk0 = sq + tc::kTileBytes;
+  const int qrow0 = bh * T, krow0 = (b * Hkv + g) * T;  // first rows of this head in the maps
+  const uint32_t sq = tc_base(sm), sk0 = sq + tc::kTileBytes;
   const int t0 = rb * kTcTile;
-  const uint32_t tbase = tc_setup(mbar, &tslot);
-  // prologue: Q and K tile 0, then K tile 1
-  tc_load_tile(sq, qb, t0, min(kTcTile, T - t0));
-  tc_load_tile(sk0, kb, 0, min(kTcTile, T));
-  cp_async_commit();
-  if (rb >= 1) tc_load_tile(sk0 + tc::kTileBytes, kb, kTcTile, min(kTcTile, T - kTcTile));
-  cp_async_commit();
-  cp_async_wait<1>();
-  tc::fence_proxy_async();
-  __syncthreads();
+  const uint32_t tbase = tc_setup(bar, &tslot);
+  bool ok = true;
   if (tid == 0) {
-    tc::fence_after_sync();
+    tc::mbar_expect_tx(smem_u32(&bar.fixed), tc::kTileBytes);
+    tc::tma_tile(sq, &tq, qrow0 + t0, smem_u32(&bar.fixed));
+    for (int j = 0; j < 2 && j <= rb; ++j) {
+      tc::mbar_expect_tx(smem_u32(&bar.load[j]), tc::kTileBytes);
+      tc::tma_tile(sk0 + j * tc::kTileBytes, &tk, krow0 + j * kTcTile, smem_u32(&bar.load[j]));
+    }
+    ok = tc::mbar_wait(smem_u32(&bar.fixed), 0) && tc::mbar_wait(smem_u32(&bar.load[0]), 0);
     tc::mma_tile(tbase, sq, sk0, kTcIdesc);
-    tc::commit(smem_u32(&mbar[0]));
+    tc::commit(smem_u32(&bar.mma[0]));
   }
   const int t = t0 + row;  // this thread's query row
   float m = -INFINITY, l = 0.f, lc = 0.f;
-  bool ok = true;
   for (int kt = 0; kt <= rb; ++kt) {
     const int buf = kt & 1;
-    if (kt + 1 <= rb) {  // MMA of the next tile before this one is exponentiated
-      cp_async_wait<0>();
-      tc::fence_proxy_async();
-      tc::fence_before_sync();
-      __syncthreads();
-      if (tid == 0) {
-        tc::fence_after_sync();
-        tc::mma_tile(tbase + (buf ^ 1) * kTcTile, sq, sk0 + (buf ^ 1) * tc::kTileBytes, kTcIdesc);
-        tc::commit(smem_u32(&mbar[buf ^ 1]));
-      }
+    if (tid == 0 && kt + 1 <= rb) {  // the next tile's MMA before this one is exponentiated
+      ok = tc::mbar_wait(smem_u32(&bar.load[buf ^ 1]), ((kt + 1) >> 1) & 1) && ok;
+      if (kt >= 1) ok = tc::mbar_wait(smem_u32(&bar.freed[buf ^ 1]), ((kt - 1) >> 1) & 1) && ok;
+      tc::fence_after_sync();
+      tc::mma_tile(tbase + (buf ^ 1) * kTcTile, sq, sk0 + (buf ^ 1) * tc::kTileBytes, kTcIdesc);
+      tc::commit(smem_u32(&bar.mma[buf ^ 1]));
     }
-    ok = tc::mbar_wait(smem_u32(&mbar[buf]), (kt >> 1) & 1) && ok;
+    ok = tc::mbar_wait(smem_u32(&bar.mma[buf]), (kt >> 1) & 1) && ok;
     tc::fence_after_sync();
-    if (kt + 2 <= rb)  // K tile kt's buffer is free once its MMA is done
-      tc_load_tile(sk0 + buf * tc::kTileBytes, kb, (kt + 2) * kTcTile, min(kTcTile, T - (kt + 2) * kTcTile));
-    cp_async_commit();
+    if (tid == 0 && kt + 2 <= rb) {  // K tile kt's buffer is free once its MMA is done
+      tc::mbar_expect_tx(smem_u32(&bar.load[buf]), tc::kTileBytes);
+      tc::tma_tile(sk0 + buf * tc::kTileBytes, &tk, krow0 + (kt + 2) * kTcTile, smem_u32(&bar.load[buf]));
+    }
     // this thread's 64 raw dot products: row t, keys kt*128 + half*64 ..
     float s[kTcHalf];
     const uint32_t lane_addr =
         tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16) + buf * kTcTile + half * kTcHalf;
     tc::tmem_ld32(lane_addr, *reinterpret_cast<float(*)[32]>(s));
     tc::tmem_ld32(lane_addr + 32, *reinterpret_cast<float(*)[32]>(s + 32));
+    tc::fence_before_sync();
+    tc::mbar_arrive(smem_u32(&bar.freed[buf]));  // accumulator read: the MMA may reuse it
     const int i0 = kt * kTcTile + half * kTcHalf;
     const int lim = min(t - i0, T - 1 - i0);  // columns 0..lim are causal and in range
     // 8 independent max / sum chains; masks only on the diagonal or last tile
@@ -387,120 +394,111 @@ __global__ void __launch_bounds__(kTcThreads, 2) row_lse_tc_kernel(const __half*
       m = mn;
     }
   }
-  cp_async_wait<0>();
   // the two halves of each row: half 1 hands its (m, l) to half 0
   if (half == 1) {
     xm[row] = m;
     xl[row] = l - lc;
   }
   tc_teardown(tbase);  // (its barrier also publishes xm / xl)
+  if (tid == 0 && !ok) xm[0] = __int_as_float(0x7fc00000);
+  __syncthreads();
   if (half == 0 && t < T) {
     const float m1 = xm[row], l1 = xl[row], l0 = l - lc;
     const float M = fmaxf(m, m1);
     const float L = (m == -INFINITY ? 0.f : l0 * fast_exp2(m - M)) + (m1 == -INFINITY ? 0.f : l1 * fast_exp2(m1 - M));
-    lse2[static_cast<long>(bh) * T + t] = ok ? M + log2f(L) : __int_as_float(0x7fc00000);
+    const bool bad = !ok || isnan(xm[0]);
+    lse2[static_cast<long>(bh) * lse_stride(T) + t] = bad ? __int_as_float(0x7fc00000) : M + log2f(L);
   }
 }
 
 // Pass 2 on tcgen05: S^h_i (and S_i) for 128 keys of one (b, key head).  S^T = K . Q^T per
 // query tile: TMEM lane = key, column = query; thread i and i + 128 take the query halves.
-__global__ void __launch_bounds__(kTcThreads, 2) col_sum_tc_kernel(const __half* __restrict__ q,
-                                                                   const __half* __restrict__ k,
+__global__ void __launch_bounds__(kTcThreads, 2) col_sum_tc_kernel(const __grid_constant__ CUtensorMap tq,
+                                                                   const __grid_constant__ CUtensorMap tk,
                                                                    const float* __restrict__ lse2, int Hq,
                                                                    int Hkv, int T, float* __restrict__ s_full,
                                                                    float* __restrict__ s_head) {
-  extern __shared__ __align__(128) uint8_t sm[];  // K tile, 2 Q tiles, 2 lse rows
-  __shared__ __align__(8) uint64_t mbar[2];
+  extern __shared__ __align__(128) uint8_t sm[];  // K tile, 2 Q tiles, lse ring
+  __shared__ __align__(8) TcBars bar;
   __shared__ uint32_t tslot;
   __shared__ float xs[kTcTile];
-  float (*sl)[kTcTile] = reinterpret_cast<float (*)[kTcTile]>(sm + 3 * tc::kTileBytes);
+  __shared__ int bad;
   const int nblk = (T + kTcTile - 1) / kTcTile;
+  const int ls = lse_stride(T);
   const int kbi = blockIdx.x;  // key block 0 (heaviest) first
   const int unit = blockIdx.y, b = unit / Hkv, g = unit % Hkv;
   const int rep = Hq / Hkv;
   const int tid = threadIdx.x, warp = tid >> 5, row = tid & 127, half = tid >> 7;
-  const __half* kbase = k + static_cast<long>(unit) * T * kD;
-  const uint32_t sk = smem_u32(sm), sq0 = sk + tc::kTileBytes;
+  const uint32_t sk = tc_base(sm), sq0 = sk + tc::kTileBytes, sl0 = sk + 3 * tc::kTileBytes;
+  const float* sl = reinterpret_cast<const float*>(sm + (sl0 - smem_u32(sm)));
   const int i0 = kbi * kTcTile;
   const int per = nblk - kbi;   // query tiles per head
   const int ntile = rep * per;  // tiles of this CTA, head-major
-  const uint32_t tbase = tc_setup(mbar, &tslot);
-  // tile n: head hr = n / per, query tile qt = kbi + n % per
-  auto load_q = [&](int n, int buf) {
+  if (tid == 0) bad = 0;
+  const uint32_t tbase = tc_setup(bar, &tslot);
+  // tile n: head hr = n / per, query tile qt = kbi + n % per; Q into buffer n & 1, its lse
+  // row into ring slot n % kTcLseRing, one transaction on load[n & 1]
+  auto load_q = [&](int n) {
     const int hr = n / per, qt = kbi + n % per;
     const long bh = static_cast<long>(b) * Hq + g * rep + hr;
-    tc_load_tile(sq0 + buf * tc::kTileBytes, q + bh * T * kD, static_cast<long>(qt) * kTcTile,
-                 min(kTcTile, T - qt * kTcTile));
-    if (tid < kTcTile) {
-      const int tq = qt * kTcTile + tid;
-      cp_async4_or_zero(smem_u32(&sl[buf][tid]), lse2 + bh * T + min(tq, T - 1), tq < T);
-    }
+    const uint32_t mb = smem_u32(&bar.load[n & 1]);
+    tc::mbar_expect_tx(mb, tc::kTileBytes + kTcTile * 4);
+    tc::tma_tile(sq0 + (n & 1) * tc::kTileBytes, &tq, static_cast<int>(bh * T) + qt * kTcTile, mb);
+    tc::bulk_copy(sl0 + (n % kTcLseRing) * kTcTile * 4, lse2 + bh * ls + qt * kTcTile, kTcTile * 4, mb);
   };
-  tc_load_tile(sk, kbase, i0, min(kTcTile, T - i0));
-  load_q(0, 0);
-  cp_async_commit();
-  if (ntile > 1) load_q(1, 1);
-  cp_async_commit();
-  cp_async_wait<1>();
-  tc::fence_proxy_async();
-  __syncthreads();
+  bool ok = true;
   if (tid == 0) {
-    tc::fence_after_sync();
+    tc::mbar_expect_tx(smem_u32(&bar.fixed), tc::kTileBytes);
+    tc::tma_tile(sk, &tk, unit * T + i0, smem_u32(&bar.fixed));
+    load_q(0);
+    if (ntile > 1) load_q(1);
+    ok = tc::mbar_wait(smem_u32(&bar.fixed), 0) && tc::mbar_wait(smem_u32(&bar.load[0]), 0);
     tc::mma_tile(tbase, sk, sq0, kTcIdesc);
-    tc::commit(smem_u32(&mbar[0]));
+    tc::commit(smem_u32(&bar.mma[0]));
   }
   const int i = i0 + row;  // this thread's key
   float col = 0.f, colc = 0.f, tot = 0.f;
-  bool ok = true;
   for (int n = 0; n < ntile; ++n) {
     const int buf = n & 1;
-    if (n + 1 < ntile) {
-      cp_async_wait<0>();
-      tc::fence_proxy_async();
-      tc::fence_before_sync();
-      __syncthreads();
-      if (tid == 0) {
-        tc::fence_after_sync();
-        tc::mma_tile(tbase + (buf ^ 1) * kTcTile, sk, sq0 + (buf ^ 1) * tc::kTileBytes, kTcIdesc);
-        tc::commit(smem_u32(&mbar[buf ^ 1]));
-      }
+    if (tid == 0 && n + 1 < ntile) {
+      ok = tc::mbar_wait(smem_u32(&bar.load[buf ^ 1]), ((n + 1) >> 1) & 1) && ok;
+      if (n >= 1) ok = tc::mbar_wait(smem_u32(&bar.freed[buf ^ 1]), ((n - 1) >> 1) & 1) && ok;
+      tc::fence_after_sync();
+      tc::mma_tile(tbase + (buf ^ 1) * kTcTile, sk, sq0 + (buf ^ 1) * tc::kTileBytes, kTcIdesc);
+      tc::commit(smem_u32(&bar.mma[buf ^ 1]));
     }
-    ok = tc::mbar_wait(smem_u32(&mbar[buf]), (n >> 1) & 1) && ok;
+    ok = tc::mbar_wait(smem_u32(&bar.mma[buf]), (n >> 1) & 1) && ok;
     tc::fence_after_sync();
-    // this thread's half of the lse row, before its buffer is refilled
-    float lt[kTcHalf];
-#pragma unroll
-    for (int c = 0; c < kTcHalf; c += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(&sl[buf][half * kTcHalf + c]);
-      lt[c] = v.x;
-      lt[c + 1] = v.y;
-      lt[c + 2] = v.z;
-      lt[c + 3] = v.w;
-    }
-    __syncthreads();  // every thread holds its lse values: the buffer may be refilled
-    if (n + 2 < ntile) load_q(n + 2, buf);
-    cp_async_commit();
+    // Q buffer `buf` is free once MMA n is done; lse slot (n + 2) % 4 held tile n - 2, whose
+    // readers all passed freed[] before MMA n + 1 was issued
+    if (tid == 0 && n + 2 < ntile) load_q(n + 2);
     const int qt = kbi + n % per;
     const int cq = qt * kTcTile + half * kTcHalf;  // query of this thread's column 0
     const int c0 = max(i - cq, 0);                  // first causal column (query >= key)
     const int c1 = min(kTcHalf, T - cq);            // columns past T are padding
+    const float* lt = sl + (n % kTcLseRing) * kTcTile + half * kTcHalf;
     float p8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent chains
     const bool full = c0 == 0 && c1 == kTcHalf;
     const uint32_t lane_addr =
         tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16) + buf * kTcTile + half * kTcHalf;
+    float s0[32], s1[32];
+    tc::tmem_ld32(lane_addr, s0);
+    tc::tmem_ld32(lane_addr + 32, s1);
+    if (full) {
 #pragma unroll
-    for (int c = 0; c < kTcHalf; c += 32) {
-      float s[32];
-      tc::tmem_ld32(lane_addr + c, s);
-      if (full) {
+      for (int e = 0; e < 32; ++e) p8[e & 7] += fast_exp2(fmaf(s0[e], kC, -lt[e]));
 #pragma unroll
-        for (int e = 0; e < 32; ++e) p8[e & 7] += fast_exp2(fmaf(s[e], kC, -lt[c + e]));
-      } else {
+      for (int e = 0; e < 32; ++e) p8[e & 7] += fast_exp2(fmaf(s1[e], kC, -lt[32 + e]));
+    } else {
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (c + e >= c0 && c + e < c1) p8[e & 7] += fast_exp2(fmaf(s[e], kC, -lt[c + e]));
-      }
+      for (int e = 0; e < 32; ++e)
+        if (e >= c0 && e < c1) p8[e & 7] += fast_exp2(fmaf(s0[e], kC, -lt[e]));
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (32 + e >= c0 && 32 + e < c1) p8[e & 7] += fast_exp2(fmaf(s1[e], kC, -lt[32 + e]));
     }
+    tc::fence_before_sync();
+    tc::mbar_arrive(smem_u32(&bar.freed[buf]));  // accumulator and lse slot read
     const float part = ((p8[0] + p8[1]) + (p8[2] + p8[3])) + ((p8[4] + p8[5]) + (p8[6] + p8[7]));
     const float y = part - colc;
     const float tt = col + y;
@@ -511,17 +509,18 @@ __global__ void __launch_bounds__(kTcThreads, 2) col_sum_tc_kernel(const __half*
       __syncthreads();
       if (half == 0) {
         const int hr = n / per;
-        const float sh = ok ? (col - colc) + xs[row] : __int_as_float(0x7fc00000);
+        const float sh = (col - colc) + xs[row];
         const long bh = static_cast<long>(b) * Hq + g * rep + hr;
         if (i < T && s_head) s_head[bh * T + i] = sh;
         tot = __fadd_rn(tot, sh);  // group sum in head order
       }
       col = colc = 0.f;
+      __syncthreads();  // xs may be rewritten for the next head
     }
   }
-  cp_async_wait<0>();
-  if (half == 0 && i < T) s_full[static_cast<long>(unit) * T + i] = tot;
+  if (tid == 0 && !ok) bad = 1;
   tc_teardown(tbase);
+  if (half == 0 && i < T) s_full[static_cast<long>(unit) * T + i] = bad ? __int_as_float(0x7fc00000) : tot;
 }
 
 // K4: S[b][g][j] += sum_h exp(logit[b][h][j] - lse[b][h]) for j < n_hi.
@@ -542,11 +541,46 @@ __global__ void score_decode_kernel(const float* __restrict__ logits, const floa
 }  // namespace
 }  // namespace mikv
 
+namespace mikv {
+namespace {
+// The driver's tensor-map encoder, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    (void)cudaGetLastError();
+  });
+  return fn;
+}
+
+// 2-D map of a row-major [rows][kD] fp16 matrix with an 8-channel x 128-row box.
+int encode_rows(CUtensorMap* map, const void* base, long rows, const char* what) {
+  const auto enc = tensor_map_encoder();
+  if (!enc) return fail(MIKV_ECUDA, "score_update: cuTensorMapEncodeTiled unavailable");
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
+  const cuuint32_t box[2] = {8, static_cast<cuuint32_t>(kTcTile)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides,
+                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MIKV_ECUDA, "score_update: tensor map of %s (error %d)", what, static_cast<int>(r));
+  return MIKV_OK;
+}
+}  // namespace
+}  // namespace mikv
+
 using namespace mikv;
 
 extern "C" size_t mikv_score_workspace_bytes(int B, int Hq, int T) {
   if (B < 1 || Hq < 1 || T < 1) return 0;
-  return align_up(static_cast<size_t>(B) * Hq * T * sizeof(float), 256);
+  return align_up(static_cast<size_t>(B) * Hq * lse_stride(T) * sizeof(float), 256);
 }
 
 extern "C" int mikv_score_update(int mode, const uint16_t* q, const uint16_t* k, int T,
@@ -567,16 +601,16 @@ extern "C" int mikv_score_update(int mode, const uint16_t* q, const uint16_t* k,
     if (ws_bytes < need) return fail(MIKV_ESHAPE, "score_update: workspace %zu < %zu", ws_bytes, need);
     float* lse2 = static_cast<float*>(ws);
     const int nblk = (T + kTcTile - 1) / kTcTile;
+    CUtensorMap tq, tk;
+    if (int e = encode_rows(&tq, q, static_cast<long>(c->B) * c->Hq * T, "q")) return e;
+    if (int e = encode_rows(&tk, k, static_cast<long>(c->B) * c->Hkv * T, "k")) return e;
     if (cudaFuncSetAttribute(row_lse_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess ||
         cudaFuncSetAttribute(col_sum_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess)
       return check_launch("score kernels attribute");
-    row_lse_tc_kernel<<<dim3(nblk, c->B * c->Hq), kTcThreads, kTcSmem, s>>>(
-        reinterpret_cast<const __half*>(q), reinterpret_cast<const __half*>(k), c->Hq, c->Hkv, T,
-        lse2);
+    row_lse_tc_kernel<<<dim3(nblk, c->B * c->Hq), kTcThreads, kTcSmem, s>>>(tq, tk, c->Hq, c->Hkv, T, lse2);
     if (int e = check_launch("row_lse_tc_kernel")) return e;
-    col_sum_tc_kernel<<<dim3(nblk, c->B * c->Hkv), kTcThreads, kTcSmem, s>>>(
-        reinterpret_cast<const __half*>(q), reinterpret_cast<const __half*>(k), lse2, c->Hq, c->Hkv,
-        T, scores_full, scores_head);
+    col_sum_tc_kernel<<<dim3(nblk, c->B * c->Hkv), kTcThreads, kTcSmem, s>>>(tq, tk, lse2, c->Hq, c->Hkv, T,
+                                                                             scores_full, scores_head);
     return check_launch("col_sum_tc_kernel");
   }
   if (mode == MIKV_DECODE) {

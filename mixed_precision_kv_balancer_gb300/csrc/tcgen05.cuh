@@ -3,7 +3,9 @@
 // Operands live in shared memory in the K-major core-matrix layout without swizzle: a
 // core matrix is 8 rows x 16 bytes (8 fp16 of the reduction dimension), stored as 128
 // contiguous bytes; core matrices adjacent along K are kLbo bytes apart and 8-row groups
-// kSbo bytes apart.  A 128 x 128 fp16 tile is 32 KB.  Accumulators live in tensor memory
+// kSbo bytes apart.  A 128 x 128 fp16 tile is 32 KB, stored k-slice major: the 128 rows of
+// channels 8j..8j+7 are 2 KB at offset 2048 j, which is what one TMA box of 8 channels x
+// 128 rows writes.  Accumulators live in tensor memory
 // (TMEM): for M = 128 with one CTA, row i of D is TMEM lane i and column n is column
 // base + n, fp32.  One thread issues the MMAs; completion is signalled on an mbarrier by
 // tcgen05.commit; every wait on an mbarrier is bounded.
@@ -19,12 +21,13 @@ namespace tc {
 
 constexpr int kTileRows = 128;                 // M = N = 128 rows per operand tile
 constexpr int kTileBytes = kTileRows * kD * 2; // 32 KB fp16
-constexpr uint32_t kLbo = 128;                 // K-direction core-matrix stride
-constexpr uint32_t kSbo = (kD / 8) * 128;      // 8-row-group stride (2048 B)
+constexpr uint32_t kSlice = kTileRows * 16;    // one 8-channel k-slice of a tile (2 KB)
+constexpr uint32_t kLbo = kSlice;              // K-direction core-matrix stride
+constexpr uint32_t kSbo = 128;                 // 8-row-group stride
 
 // Byte offset of element (r, k) of a [128][kD] fp16 tile in the core-matrix layout.
 __host__ __device__ __forceinline__ uint32_t tile_off(int r, int k) {
-  return static_cast<uint32_t>(((r >> 3) * (kD / 8) + (k >> 3)) * 128 + (r & 7) * 16 + (k & 7) * 2);
+  return static_cast<uint32_t>((k >> 3) * kSlice + r * 16 + (k & 7) * 2);
 }
 
 // Shared-memory matrix descriptor: start address, K-direction and row-group strides, the
@@ -55,7 +58,7 @@ __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_
 __device__ __forceinline__ void mma_tile(uint32_t tmem_d, uint32_t sa, uint32_t sb, uint32_t idesc) {
 #pragma unroll
   for (int ks = 0; ks < kD / 16; ++ks)
-    mma_f16(tmem_d, smem_desc(sa + ks * 2 * kLbo), smem_desc(sb + ks * 2 * kLbo), idesc, ks > 0);
+    mma_f16(tmem_d, smem_desc(sa + ks * 2 * kSlice), smem_desc(sb + ks * 2 * kSlice), idesc, ks > 0);
 }
 
 // The mbarrier at `mbar` completes when every tcgen05 op this thread issued so far is done.
@@ -122,19 +125,35 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Stage rows [r0, r0 + 128) of a row-major [rows][kD] fp16 matrix into the tile at `s`
-// with 16-byte cp.async copies (rows >= nrows zero-filled, not read).  Thread i of 128 takes
-// chunks i, i + 128, ...; eight consecutive threads fill one core matrix (8 rows x 16 B),
-// so a warp writes 512 contiguous bytes.
-__device__ __forceinline__ void load_tile_async(uint32_t s, const __half* g, long r0, int nrows) {
-#pragma unroll 4
-  for (int i = threadIdx.x; i < kTileRows * (kD / 8); i += 128) {
-    const int r = (i & 7) + ((i >> 7) << 3);  // row within the tile
-    const int kc = ((i >> 3) & 15) * 8;        // first channel of the 16-byte chunk
-    const bool ok = r < nrows;
-    const __half* src = ok ? g + (r0 + r) * kD + kc : g;
-    cp_async16(s + tile_off(r, kc), src, ok);
-  }
+// One thread: expect `bytes` of asynchronous copies on the mbarrier (one arrival).
+__device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(mbar), "r"(bytes) : "memory");
+}
+// One arrival on the mbarrier.
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(mbar) : "memory");
+}
+
+// One thread: TMA-load rows [row0, row0 + 128) of a [rows][kD] fp16 matrix described by the
+// 2-D tensor map `tmap` (box 8 channels x 128 rows) into the tile at `s`: sixteen boxes,
+// one per 8-channel k-slice (x = 8j, a multiple of 16 bytes).  Rows past the end of the
+// matrix are zero-filled.  Completes `bytes` = 32 KB on the mbarrier.
+__device__ __forceinline__ void tma_tile(uint32_t s, const void* tmap, int row0, uint32_t mbar) {
+#pragma unroll
+  for (int j = 0; j < kD / 8; ++j)
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(s + j * kSlice),
+        "l"(tmap), "r"(j * 8), "r"(row0), "r"(mbar)
+        : "memory");
+}
+// One thread: bulk-copy `bytes` (multiple of 16, both addresses 16-byte aligned) into
+// shared memory, completing on the mbarrier.
+__device__ __forceinline__ void bulk_copy(uint32_t s, const void* g, uint32_t bytes, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(s),
+      "l"(g), "r"(bytes), "r"(mbar)
+      : "memory");
 }
 
 }  // namespace tc
