@@ -250,15 +250,16 @@ __global__ void __launch_bounds__(kThr) col_sum_kernel(const __half* __restrict_
 // ---------------------------------------------------------------------------------
 // The two passes on the 5th-generation tensor cores.  128 x 128 tiles, S = A . B^T by
 // tcgen05.mma (fp16 in, fp32 accumulate in TMEM), two TMEM accumulators so the next tile's
-// MMA runs while the CTA exponentiates the current one.  Thread 0 is also the producer: it
-// streams the operand tiles with TMA (two shared-memory buffers) and issues the MMAs; every
-// hand-off is an mbarrier (tile loaded, MMA done, accumulator consumed by all 256 threads),
-// so no thread waits at a CTA barrier inside the loop.  Row r of S (TMEM lane r) belongs to
+// MMA runs while the CTA exponentiates the current one.  A ninth warp is the producer: its
+// lane 0 streams the operand tiles with TMA (two shared-memory buffers) and issues the
+// MMAs; every hand-off is an mbarrier (tile loaded, MMA done, accumulator consumed by all
+// 256 consumer threads), so no thread waits at a CTA barrier inside the loop.  Row r of S (TMEM lane r) belongs to
 // threads r and r + 128, which take columns 0..63 and 64..127 and keep their own running
 // state, combined once at the end.  Per CTA: 3 tiles of 32 KB plus 2 KB of lse rows and
 // 256 TMEM columns, so two CTAs share an SM.
 constexpr int kTcTile = tc::kTileRows;
-constexpr int kTcThreads = 256;
+constexpr int kTcThreads = 256;                                        // consumers
+constexpr int kTcBlock = kTcThreads + 32;                              // + the producer warp
 constexpr int kTcHalf = kTcTile / 2;                                    // columns per thread
 constexpr int kTcCols = 2 * kTcTile;                                    // two accumulators
 constexpr int kTcLseRing = 4;                                           // lse rows in flight
@@ -301,123 +302,126 @@ __device__ __forceinline__ void tc_teardown(uint32_t tbase) {
 __device__ __forceinline__ uint32_t tc_base(uint8_t* sm) { return (smem_u32(sm) + 127u) & ~127u; }
 
 // Pass 1 on tcgen05: lse2[b][h][t] (row stride lse_stride(T)) for 128 query rows.
-__global__ void __launch_bounds__(kTcThreads, 2) row_lse_tc_kernel(const __grid_constant__ CUtensorMap tq,
-                                                                   const __grid_constant__ CUtensorMap tk,
-                                                                   int Hq, int Hkv, int T,
-                                                                   float* __restrict__ lse2) {
+__global__ void __launch_bounds__(kTcBlock, 2) row_lse_tc_kernel(const __grid_constant__ CUtensorMap tq,
+                                                                 const __grid_constant__ CUtensorMap tk,
+                                                                 int Hq, int Hkv, int T,
+                                                                 float* __restrict__ lse2) {
   extern __shared__ __align__(128) uint8_t sm[];  // Q tile, 2 K tiles
   __shared__ __align__(8) TcBars bar;
   __shared__ uint32_t tslot;
   __shared__ float xm[kTcTile], xl[kTcTile];
+  __shared__ int bad;
   const int nblk = (T + kTcTile - 1) / kTcTile;
   const int rb = nblk - 1 - blockIdx.x;  // heaviest (last) row block first
   const int bh = blockIdx.y, b = bh / Hq, h = bh % Hq;
   const int g = h / (Hq / Hkv);
-  const int tid = threadIdx.x, warp = tid >> 5, row = tid & 127, half = tid >> 7;
+  const int tid = threadIdx.x, warp = tid >> 5, row = tid & 127, half = (tid >> 7) & 1;
   const int qrow0 = bh * T, krow0 = (b * Hkv + g) * T;  // first rows of this head in the maps
   const uint32_t sq = tc_base(sm), sk0 = sq + tc::kTileBytes;
   const int t0 = rb * kTcTile;
+  if (tid == 0) bad = 0;
   const uint32_t tbase = tc_setup(bar, &tslot);
   bool ok = true;
-  if (tid == 0) {
+  float m = -INFINITY, l = 0.f, lc = 0.f;
+  const int t = t0 + row;  // a consumer's query row
+  if (tid == kTcThreads) {
+    // producer: Q once; K tiles through two buffers.  MMA kt as soon as its K tile is in
+    // and its accumulator's previous tile was read; K tile kt + 2 once MMA kt is done.
     tc::mbar_expect_tx(smem_u32(&bar.fixed), tc::kTileBytes);
     tc::tma_tile(sq, &tq, qrow0 + t0, smem_u32(&bar.fixed));
     for (int j = 0; j < 2 && j <= rb; ++j) {
       tc::mbar_expect_tx(smem_u32(&bar.load[j]), tc::kTileBytes);
       tc::tma_tile(sk0 + j * tc::kTileBytes, &tk, krow0 + j * kTcTile, smem_u32(&bar.load[j]));
     }
-    ok = tc::mbar_wait(smem_u32(&bar.fixed), 0) && tc::mbar_wait(smem_u32(&bar.load[0]), 0);
-    tc::mma_tile(tbase, sq, sk0, kTcIdesc);
-    tc::commit(smem_u32(&bar.mma[0]));
-  }
-  const int t = t0 + row;  // this thread's query row
-  float m = -INFINITY, l = 0.f, lc = 0.f;
-  for (int kt = 0; kt <= rb; ++kt) {
-    const int buf = kt & 1;
-    if (tid == 0 && kt + 1 <= rb) {  // the next tile's MMA before this one is exponentiated
-      ok = tc::mbar_wait(smem_u32(&bar.load[buf ^ 1]), ((kt + 1) >> 1) & 1) && ok;
-      if (kt >= 1) ok = tc::mbar_wait(smem_u32(&bar.freed[buf ^ 1]), ((kt - 1) >> 1) & 1) && ok;
+    ok = tc::mbar_wait(smem_u32(&bar.fixed), 0) && ok;
+    for (int kt = 0; kt <= rb; ++kt) {
+      const int buf = kt & 1;
+      ok = tc::mbar_wait(smem_u32(&bar.load[buf]), (kt >> 1) & 1) && ok;
+      if (kt >= 2) ok = tc::mbar_wait(smem_u32(&bar.freed[buf]), ((kt - 2) >> 1) & 1) && ok;
       tc::fence_after_sync();
-      tc::mma_tile(tbase + (buf ^ 1) * kTcTile, sq, sk0 + (buf ^ 1) * tc::kTileBytes, kTcIdesc);
-      tc::commit(smem_u32(&bar.mma[buf ^ 1]));
+      tc::mma_tile(tbase + buf * kTcTile, sq, sk0 + buf * tc::kTileBytes, kTcIdesc);
+      tc::commit(smem_u32(&bar.mma[buf]));
+      if (kt + 2 <= rb) {
+        ok = tc::mbar_wait(smem_u32(&bar.mma[buf]), (kt >> 1) & 1) && ok;
+        tc::mbar_expect_tx(smem_u32(&bar.load[buf]), tc::kTileBytes);
+        tc::tma_tile(sk0 + buf * tc::kTileBytes, &tk, krow0 + (kt + 2) * kTcTile, smem_u32(&bar.load[buf]));
+      }
     }
-    ok = tc::mbar_wait(smem_u32(&bar.mma[buf]), (kt >> 1) & 1) && ok;
-    tc::fence_after_sync();
-    if (tid == 0 && kt + 2 <= rb) {  // K tile kt's buffer is free once its MMA is done
-      tc::mbar_expect_tx(smem_u32(&bar.load[buf]), tc::kTileBytes);
-      tc::tma_tile(sk0 + buf * tc::kTileBytes, &tk, krow0 + (kt + 2) * kTcTile, smem_u32(&bar.load[buf]));
-    }
-    // this thread's 64 raw dot products: row t, keys kt*128 + half*64 ..
-    float s[kTcHalf];
-    const uint32_t lane_addr =
-        tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16) + buf * kTcTile + half * kTcHalf;
-    tc::tmem_ld32(lane_addr, *reinterpret_cast<float(*)[32]>(s));
-    tc::tmem_ld32(lane_addr + 32, *reinterpret_cast<float(*)[32]>(s + 32));
-    tc::fence_before_sync();
-    tc::mbar_arrive(smem_u32(&bar.freed[buf]));  // accumulator read: the MMA may reuse it
-    const int i0 = kt * kTcTile + half * kTcHalf;
-    const int lim = min(t - i0, T - 1 - i0);  // columns 0..lim are causal and in range
-    // 8 independent max / sum chains; masks only on the diagonal or last tile
-    float mx8[8], sm8[8];
+  } else if (tid < kTcThreads) {
+    for (int kt = 0; kt <= rb; ++kt) {
+      const int buf = kt & 1;
+      ok = tc::mbar_wait(smem_u32(&bar.mma[buf]), (kt >> 1) & 1) && ok;
+      tc::fence_after_sync();
+      // this thread's 64 raw dot products: row t, keys kt*128 + half*64 ..
+      float s[kTcHalf];
+      const uint32_t lane_addr =
+          tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16) + buf * kTcTile + half * kTcHalf;
+      tc::tmem_ld32(lane_addr, *reinterpret_cast<float(*)[32]>(s));
+      tc::tmem_ld32(lane_addr + 32, *reinterpret_cast<float(*)[32]>(s + 32));
+      tc::fence_before_sync();
+      tc::mbar_arrive(smem_u32(&bar.freed[buf]));  // accumulator read: the MMA may reuse it
+      const int i0 = kt * kTcTile + half * kTcHalf;
+      const int lim = min(t - i0, T - 1 - i0);  // columns 0..lim are causal and in range
+      // 8 independent max / sum chains; masks only on the diagonal or last tile
+      float mx8[8], sm8[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) mx8[j] = -INFINITY;
-    if (lim >= kTcHalf - 1) {
-#pragma unroll
-      for (int c = 0; c < kTcHalf; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-    } else {
-#pragma unroll
-      for (int c = 0; c < kTcHalf; ++c)
-        if (c <= lim) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-    }
-    const float mxr = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                            fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-    const float mn = fmaxf(m, mxr * kC);  // kC > 0: the max commutes with the scaling
-    if (mn != -INFINITY) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) sm8[j] = 0.f;
+      for (int j = 0; j < 8; ++j) mx8[j] = -INFINITY;
       if (lim >= kTcHalf - 1) {
 #pragma unroll
-        for (int c = 0; c < kTcHalf; ++c) sm8[c & 7] += fast_exp2(fmaf(s[c], kC, -mn));
+        for (int c = 0; c < kTcHalf; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
       } else {
 #pragma unroll
         for (int c = 0; c < kTcHalf; ++c)
-          if (c <= lim) sm8[c & 7] += fast_exp2(fmaf(s[c], kC, -mn));
+          if (c <= lim) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
       }
-      const float sum = ((sm8[0] + sm8[1]) + (sm8[2] + sm8[3])) + ((sm8[4] + sm8[5]) + (sm8[6] + sm8[7]));
-      const float alpha = fast_exp2(m - mn);
-      l = __fmul_rn(l, alpha);
-      lc = __fmul_rn(lc, alpha);
-      const float y = sum - lc;
-      const float tt = l + y;
-      lc = (tt - l) - y;
-      l = tt;
-      m = mn;
+      const float mxr = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float mn = fmaxf(m, mxr * kC);  // kC > 0: the max commutes with the scaling
+      if (mn != -INFINITY) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sm8[j] = 0.f;
+        if (lim >= kTcHalf - 1) {
+#pragma unroll
+          for (int c = 0; c < kTcHalf; ++c) sm8[c & 7] += fast_exp2(fmaf(s[c], kC, -mn));
+        } else {
+#pragma unroll
+          for (int c = 0; c < kTcHalf; ++c)
+            if (c <= lim) sm8[c & 7] += fast_exp2(fmaf(s[c], kC, -mn));
+        }
+        const float sum = ((sm8[0] + sm8[1]) + (sm8[2] + sm8[3])) + ((sm8[4] + sm8[5]) + (sm8[6] + sm8[7]));
+        const float alpha = fast_exp2(m - mn);
+        l = __fmul_rn(l, alpha);
+        lc = __fmul_rn(lc, alpha);
+        const float y = sum - lc;
+        const float tt = l + y;
+        lc = (tt - l) - y;
+        l = tt;
+        m = mn;
+      }
+    }
+    // the two halves of each row: half 1 hands its (m, l) to half 0
+    if (half == 1) {
+      xm[row] = m;
+      xl[row] = l - lc;
     }
   }
-  // the two halves of each row: half 1 hands its (m, l) to half 0
-  if (half == 1) {
-    xm[row] = m;
-    xl[row] = l - lc;
-  }
-  tc_teardown(tbase);  // (its barrier also publishes xm / xl)
-  if (tid == 0 && !ok) xm[0] = __int_as_float(0x7fc00000);
-  __syncthreads();
-  if (half == 0 && t < T) {
+  if (!ok) atomicExch(&bad, 1);
+  tc_teardown(tbase);  // (its barrier also publishes xm / xl / bad)
+  if (tid < kTcTile && t < T) {
     const float m1 = xm[row], l1 = xl[row], l0 = l - lc;
     const float M = fmaxf(m, m1);
     const float L = (m == -INFINITY ? 0.f : l0 * fast_exp2(m - M)) + (m1 == -INFINITY ? 0.f : l1 * fast_exp2(m1 - M));
-    const bool bad = !ok || isnan(xm[0]);
     lse2[static_cast<long>(bh) * lse_stride(T) + t] = bad ? __int_as_float(0x7fc00000) : M + log2f(L);
   }
 }
 
 // Pass 2 on tcgen05: S^h_i (and S_i) for 128 keys of one (b, key head).  S^T = K . Q^T per
 // query tile: TMEM lane = key, column = query; thread i and i + 128 take the query halves.
-__global__ void __launch_bounds__(kTcThreads, 2) col_sum_tc_kernel(const __grid_constant__ CUtensorMap tq,
-                                                                   const __grid_constant__ CUtensorMap tk,
-                                                                   const float* __restrict__ lse2, int Hq,
-                                                                   int Hkv, int T, float* __restrict__ s_full,
-                                                                   float* __restrict__ s_head) {
+__global__ void __launch_bounds__(kTcBlock, 2) col_sum_tc_kernel(const __grid_constant__ CUtensorMap tq,
+                                                                 const __grid_constant__ CUtensorMap tk,
+                                                                 const float* __restrict__ lse2, int Hq,
+                                                                 int Hkv, int T, float* __restrict__ s_full,
+                                                                 float* __restrict__ s_head) {
   extern __shared__ __align__(128) uint8_t sm[];  // K tile, 2 Q tiles, lse ring
   __shared__ __align__(8) TcBars bar;
   __shared__ uint32_t tslot;
@@ -428,7 +432,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) col_sum_tc_kernel(const __grid_
   const int kbi = blockIdx.x;  // key block 0 (heaviest) first
   const int unit = blockIdx.y, b = unit / Hkv, g = unit % Hkv;
   const int rep = Hq / Hkv;
-  const int tid = threadIdx.x, warp = tid >> 5, row = tid & 127, half = tid >> 7;
+  const int tid = threadIdx.x, warp = tid >> 5, row = tid & 127, half = (tid >> 7) & 1;
   const uint32_t sk = tc_base(sm), sq0 = sk + tc::kTileBytes, sl0 = sk + 3 * tc::kTileBytes;
   const float* sl = reinterpret_cast<const float*>(sm + (sl0 - smem_u32(sm)));
   const int i0 = kbi * kTcTile;
@@ -436,91 +440,95 @@ __global__ void __launch_bounds__(kTcThreads, 2) col_sum_tc_kernel(const __grid_
   const int ntile = rep * per;  // tiles of this CTA, head-major
   if (tid == 0) bad = 0;
   const uint32_t tbase = tc_setup(bar, &tslot);
-  // tile n: head hr = n / per, query tile qt = kbi + n % per; Q into buffer n & 1, its lse
-  // row into ring slot n % kTcLseRing, one transaction on load[n & 1]
-  auto load_q = [&](int n) {
-    const int hr = n / per, qt = kbi + n % per;
-    const long bh = static_cast<long>(b) * Hq + g * rep + hr;
-    const uint32_t mb = smem_u32(&bar.load[n & 1]);
-    tc::mbar_expect_tx(mb, tc::kTileBytes + kTcTile * 4);
-    tc::tma_tile(sq0 + (n & 1) * tc::kTileBytes, &tq, static_cast<int>(bh * T) + qt * kTcTile, mb);
-    tc::bulk_copy(sl0 + (n % kTcLseRing) * kTcTile * 4, lse2 + bh * ls + qt * kTcTile, kTcTile * 4, mb);
-  };
   bool ok = true;
-  if (tid == 0) {
+  const int i = i0 + row;  // a consumer's key
+  float tot = 0.f;
+  if (tid == kTcThreads) {
+    // producer.  Tile n: head hr = n / per, query tile qt = kbi + n % per; Q into buffer
+    // n & 1 and its lse row into ring slot n % kTcLseRing, one transaction on load[n & 1].
+    auto load_q = [&](int n) {
+      const int hr = n / per, qt = kbi + n % per;
+      const long bh = static_cast<long>(b) * Hq + g * rep + hr;
+      const uint32_t mb = smem_u32(&bar.load[n & 1]);
+      tc::mbar_expect_tx(mb, tc::kTileBytes + kTcTile * 4);
+      tc::tma_tile(sq0 + (n & 1) * tc::kTileBytes, &tq, static_cast<int>(bh * T) + qt * kTcTile, mb);
+      tc::bulk_copy(sl0 + (n % kTcLseRing) * kTcTile * 4, lse2 + bh * ls + qt * kTcTile, kTcTile * 4, mb);
+    };
     tc::mbar_expect_tx(smem_u32(&bar.fixed), tc::kTileBytes);
     tc::tma_tile(sk, &tk, unit * T + i0, smem_u32(&bar.fixed));
     load_q(0);
     if (ntile > 1) load_q(1);
-    ok = tc::mbar_wait(smem_u32(&bar.fixed), 0) && tc::mbar_wait(smem_u32(&bar.load[0]), 0);
-    tc::mma_tile(tbase, sk, sq0, kTcIdesc);
-    tc::commit(smem_u32(&bar.mma[0]));
-  }
-  const int i = i0 + row;  // this thread's key
-  float col = 0.f, colc = 0.f, tot = 0.f;
-  for (int n = 0; n < ntile; ++n) {
-    const int buf = n & 1;
-    if (tid == 0 && n + 1 < ntile) {
-      ok = tc::mbar_wait(smem_u32(&bar.load[buf ^ 1]), ((n + 1) >> 1) & 1) && ok;
-      if (n >= 1) ok = tc::mbar_wait(smem_u32(&bar.freed[buf ^ 1]), ((n - 1) >> 1) & 1) && ok;
+    ok = tc::mbar_wait(smem_u32(&bar.fixed), 0) && ok;
+    for (int n = 0; n < ntile; ++n) {
+      const int buf = n & 1;
+      ok = tc::mbar_wait(smem_u32(&bar.load[buf]), (n >> 1) & 1) && ok;
+      // accumulator buf and lse slot (n + 2) % 4 = (n - 2) % 4 both free once tile n - 2 is
+      // consumed
+      if (n >= 2) ok = tc::mbar_wait(smem_u32(&bar.freed[buf]), ((n - 2) >> 1) & 1) && ok;
       tc::fence_after_sync();
-      tc::mma_tile(tbase + (buf ^ 1) * kTcTile, sk, sq0 + (buf ^ 1) * tc::kTileBytes, kTcIdesc);
-      tc::commit(smem_u32(&bar.mma[buf ^ 1]));
-    }
-    ok = tc::mbar_wait(smem_u32(&bar.mma[buf]), (n >> 1) & 1) && ok;
-    tc::fence_after_sync();
-    // Q buffer `buf` is free once MMA n is done; lse slot (n + 2) % 4 held tile n - 2, whose
-    // readers all passed freed[] before MMA n + 1 was issued
-    if (tid == 0 && n + 2 < ntile) load_q(n + 2);
-    const int qt = kbi + n % per;
-    const int cq = qt * kTcTile + half * kTcHalf;  // query of this thread's column 0
-    const int c0 = max(i - cq, 0);                  // first causal column (query >= key)
-    const int c1 = min(kTcHalf, T - cq);            // columns past T are padding
-    const float* lt = sl + (n % kTcLseRing) * kTcTile + half * kTcHalf;
-    float p8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent chains
-    const bool full = c0 == 0 && c1 == kTcHalf;
-    const uint32_t lane_addr =
-        tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16) + buf * kTcTile + half * kTcHalf;
-    float s0[32], s1[32];
-    tc::tmem_ld32(lane_addr, s0);
-    tc::tmem_ld32(lane_addr + 32, s1);
-    if (full) {
-#pragma unroll
-      for (int e = 0; e < 32; ++e) p8[e & 7] += fast_exp2(fmaf(s0[e], kC, -lt[e]));
-#pragma unroll
-      for (int e = 0; e < 32; ++e) p8[e & 7] += fast_exp2(fmaf(s1[e], kC, -lt[32 + e]));
-    } else {
-#pragma unroll
-      for (int e = 0; e < 32; ++e)
-        if (e >= c0 && e < c1) p8[e & 7] += fast_exp2(fmaf(s0[e], kC, -lt[e]));
-#pragma unroll
-      for (int e = 0; e < 32; ++e)
-        if (32 + e >= c0 && 32 + e < c1) p8[e & 7] += fast_exp2(fmaf(s1[e], kC, -lt[32 + e]));
-    }
-    tc::fence_before_sync();
-    tc::mbar_arrive(smem_u32(&bar.freed[buf]));  // accumulator and lse slot read
-    const float part = ((p8[0] + p8[1]) + (p8[2] + p8[3])) + ((p8[4] + p8[5]) + (p8[6] + p8[7]));
-    const float y = part - colc;
-    const float tt = col + y;
-    colc = (tt - col) - y;
-    col = tt;
-    if (n % per == per - 1) {  // head done: the two query halves of each key, then the group
-      if (half == 1) xs[row] = col - colc;
-      __syncthreads();
-      if (half == 0) {
-        const int hr = n / per;
-        const float sh = (col - colc) + xs[row];
-        const long bh = static_cast<long>(b) * Hq + g * rep + hr;
-        if (i < T && s_head) s_head[bh * T + i] = sh;
-        tot = __fadd_rn(tot, sh);  // group sum in head order
+      tc::mma_tile(tbase + buf * kTcTile, sk, sq0 + buf * tc::kTileBytes, kTcIdesc);
+      tc::commit(smem_u32(&bar.mma[buf]));
+      if (n + 2 < ntile) {  // Q buffer buf is free once MMA n is done
+        ok = tc::mbar_wait(smem_u32(&bar.mma[buf]), (n >> 1) & 1) && ok;
+        load_q(n + 2);
       }
-      col = colc = 0.f;
-      __syncthreads();  // xs may be rewritten for the next head
+    }
+  } else if (tid < kTcThreads) {
+    float col = 0.f, colc = 0.f;
+    for (int n = 0; n < ntile; ++n) {
+      const int buf = n & 1;
+      ok = tc::mbar_wait(smem_u32(&bar.mma[buf]), (n >> 1) & 1) && ok;
+      tc::fence_after_sync();
+      const int qt = kbi + n % per;
+      const int cq = qt * kTcTile + half * kTcHalf;  // query of this thread's column 0
+      const int c0 = max(i - cq, 0);                  // first causal column (query >= key)
+      const int c1 = min(kTcHalf, T - cq);            // columns past T are padding
+      const float* lt = sl + (n % kTcLseRing) * kTcTile + half * kTcHalf;
+      float p8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent chains
+      const bool full = c0 == 0 && c1 == kTcHalf;
+      const uint32_t lane_addr =
+          tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16) + buf * kTcTile + half * kTcHalf;
+      float s0[32], s1[32];
+      tc::tmem_ld32(lane_addr, s0);
+      tc::tmem_ld32(lane_addr + 32, s1);
+      if (full) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) p8[e & 7] += fast_exp2(fmaf(s0[e], kC, -lt[e]));
+#pragma unroll
+        for (int e = 0; e < 32; ++e) p8[e & 7] += fast_exp2(fmaf(s1[e], kC, -lt[32 + e]));
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (e >= c0 && e < c1) p8[e & 7] += fast_exp2(fmaf(s0[e], kC, -lt[e]));
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (32 + e >= c0 && 32 + e < c1) p8[e & 7] += fast_exp2(fmaf(s1[e], kC, -lt[32 + e]));
+      }
+      tc::fence_before_sync();
+      tc::mbar_arrive(smem_u32(&bar.freed[buf]));  // accumulator and lse slot read
+      const float part = ((p8[0] + p8[1]) + (p8[2] + p8[3])) + ((p8[4] + p8[5]) + (p8[6] + p8[7]));
+      const float y = part - colc;
+      const float tt = col + y;
+      colc = (tt - col) - y;
+      col = tt;
+      if (n % per == per - 1) {  // head done: the two query halves of each key, then the group
+        if (half == 1) xs[row] = col - colc;
+        asm volatile("bar.sync 1, %0;\n" ::"n"(kTcThreads));  // consumers only
+        if (half == 0) {
+          const int hr = n / per;
+          const float sh = (col - colc) + xs[row];
+          const long bh = static_cast<long>(b) * Hq + g * rep + hr;
+          if (i < T && s_head) s_head[bh * T + i] = sh;
+          tot = __fadd_rn(tot, sh);  // group sum in head order
+        }
+        col = colc = 0.f;
+        asm volatile("bar.sync 1, %0;\n" ::"n"(kTcThreads));  // xs may be rewritten
+      }
     }
   }
-  if (tid == 0 && !ok) bad = 1;
+  if (!ok) atomicExch(&bad, 1);
   tc_teardown(tbase);
-  if (half == 0 && i < T) s_full[static_cast<long>(unit) * T + i] = bad ? __int_as_float(0x7fc00000) : tot;
+  if (tid < kTcTile && i < T) s_full[static_cast<long>(unit) * T + i] = bad ? __int_as_float(0x7fc00000) : tot;
 }
 
 // K4: S[b][g][j] += sum_h exp(logit[b][h][j] - lse[b][h]) for j < n_hi.
@@ -607,9 +615,9 @@ extern "C" int mikv_score_update(int mode, const uint16_t* q, const uint16_t* k,
     if (cudaFuncSetAttribute(row_lse_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess ||
         cudaFuncSetAttribute(col_sum_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess)
       return check_launch("score kernels attribute");
-    row_lse_tc_kernel<<<dim3(nblk, c->B * c->Hq), kTcThreads, kTcSmem, s>>>(tq, tk, c->Hq, c->Hkv, T, lse2);
+    row_lse_tc_kernel<<<dim3(nblk, c->B * c->Hq), kTcBlock, kTcSmem, s>>>(tq, tk, c->Hq, c->Hkv, T, lse2);
     if (int e = check_launch("row_lse_tc_kernel")) return e;
-    col_sum_tc_kernel<<<dim3(nblk, c->B * c->Hkv), kTcThreads, kTcSmem, s>>>(tq, tk, lse2, c->Hq, c->Hkv, T,
+    col_sum_tc_kernel<<<dim3(nblk, c->B * c->Hkv), kTcBlock, kTcSmem, s>>>(tq, tk, lse2, c->Hq, c->Hkv, T,
                                                                              scores_full, scores_head);
     return check_launch("col_sum_tc_kernel");
   }
