@@ -263,7 +263,7 @@ constexpr int kTcBlock = kTcThreads + 32;                              // + the 
 constexpr int kTcHalf = kTcTile / 2;                                    // columns per thread
 constexpr int kTcCols = 2 * kTcTile;                                    // two accumulators
 constexpr int kTcLseRing = 4;                                           // lse rows in flight
-constexpr int kTcSmem = 3 * tc::kTileBytes + kTcLseRing * kTcTile * 4 + 128;  // + alignment
+constexpr int kTcSmem = 3 * tc::kTileBytes + kTcLseRing * kTcTile * 4 + 1024;  // + alignment
 constexpr uint32_t kTcIdesc = tc::idesc_f16(kTcTile, kTcTile);
 
 // lse rows are padded to whole tiles so one tile's 128 values are one aligned bulk copy.
@@ -298,8 +298,8 @@ __device__ __forceinline__ void tc_teardown(uint32_t tbase) {
   __syncthreads();
   if (threadIdx.x < 32) tc::tmem_dealloc(tbase, kTcCols);
 }
-// 128-byte aligned base of the dynamic shared memory (TMA destinations).
-__device__ __forceinline__ uint32_t tc_base(uint8_t* sm) { return (smem_u32(sm) + 127u) & ~127u; }
+// 1024-byte aligned base of the dynamic shared memory (swizzled TMA destinations).
+__device__ __forceinline__ uint32_t tc_base(uint8_t* sm) { return (smem_u32(sm) + 1023u) & ~1023u; }
 
 // Pass 1 on tcgen05: lse2[b][h][t] (row stride lse_stride(T)) for 128 query rows.
 __global__ void __launch_bounds__(kTcBlock, 2) row_lse_tc_kernel(const __grid_constant__ CUtensorMap tq,
@@ -567,16 +567,17 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 2-D map of a row-major [rows][kD] fp16 matrix with an 8-channel x 128-row box.
+// 2-D map of a row-major [rows][kD] fp16 matrix with a 64-channel x 128-row box and
+// 128-byte swizzle.
 int encode_rows(CUtensorMap* map, const void* base, long rows, const char* what) {
   const auto enc = tensor_map_encoder();
   if (!enc) return fail(MIKV_ECUDA, "score_update: cuTensorMapEncodeTiled unavailable");
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
-  const cuuint32_t box[2] = {8, static_cast<cuuint32_t>(kTcTile)};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTcTile)};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides,
-                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(MIKV_ECUDA, "score_update: tensor map of %s (error %d)", what, static_cast<int>(r));
   return MIKV_OK;

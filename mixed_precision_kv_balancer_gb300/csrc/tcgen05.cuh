@@ -1,14 +1,14 @@
 // 5th-generation tensor core (tcgen05) building blocks for sm_103a, as inline PTX.
 //
-// Operands live in shared memory in the K-major core-matrix layout without swizzle: a
-// core matrix is 8 rows x 16 bytes (8 fp16 of the reduction dimension), stored as 128
-// contiguous bytes; core matrices adjacent along K are kLbo bytes apart and 8-row groups
-// kSbo bytes apart.  A 128 x 128 fp16 tile is 32 KB, stored k-slice major: the 128 rows of
-// channels 8j..8j+7 are 2 KB at offset 2048 j, which is what one TMA box of 8 channels x
-// 128 rows writes.  Accumulators live in tensor memory
-// (TMEM): for M = 128 with one CTA, row i of D is TMEM lane i and column n is column
-// base + n, fp32.  One thread issues the MMAs; completion is signalled on an mbarrier by
-// tcgen05.commit; every wait on an mbarrier is bounded.
+// Operands live in shared memory in the K-major layout with 128-byte swizzle, as TMA
+// writes it: a [128][kD] fp16 tile is two k-blocks of 64 channels, each [128 rows][128 B]
+// (16 KB, 1024-byte aligned); inside each 1024-byte group of 8 rows, 16-byte chunk c of row
+// r sits at chunk c ^ (r % 8).  The MMA descriptor names that layout (type 2), the 8-row
+// group stride (1024 B), and a start address that advances 32 B per 16-channel K step
+// inside a k-block.  Accumulators live in tensor memory (TMEM): for M = 128 with one CTA,
+// row i of D is TMEM lane i and column n is column base + n, fp32.  One thread issues the
+// MMAs; completion is signalled on an mbarrier by tcgen05.commit; every wait on an
+// mbarrier is bounded.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -21,22 +21,22 @@ namespace tc {
 
 constexpr int kTileRows = 128;                 // M = N = 128 rows per operand tile
 constexpr int kTileBytes = kTileRows * kD * 2; // 32 KB fp16
-constexpr uint32_t kSlice = kTileRows * 16;    // one 8-channel k-slice of a tile (2 KB)
-constexpr uint32_t kLbo = kSlice;              // K-direction core-matrix stride
-constexpr uint32_t kSbo = 128;                 // 8-row-group stride
+constexpr uint32_t kKBlock = kTileRows * 128;  // one 64-channel k-block of a tile (16 KB)
 
-// Byte offset of element (r, k) of a [128][kD] fp16 tile in the core-matrix layout.
+// Byte offset of element (r, k) of a [128][kD] fp16 tile in the swizzled layout.
 __host__ __device__ __forceinline__ uint32_t tile_off(int r, int k) {
-  return static_cast<uint32_t>((k >> 3) * kSlice + r * 16 + (k & 7) * 2);
+  return static_cast<uint32_t>((k >> 6) * kKBlock + r * 128 + ((((k & 63) >> 3) ^ (r & 7)) << 4) + (k & 7) * 2);
 }
 
-// Shared-memory matrix descriptor: start address, K-direction and row-group strides, the
-// descriptor version of this architecture (bits 46-47 = 1), no swizzle.
+// Shared-memory matrix descriptor for the swizzled K-major layout: start address, the
+// (unused) leading offset, 8-row group stride 1024 B, descriptor version of this
+// architecture (bits 46-47 = 1), layout type 128-byte swizzle.
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
   uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>((kLbo >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((kSbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 16;                  // leading offset (16 B, unused)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;          // 8-row group stride
   d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;                  // 128-byte swizzle
   return d;
 }
 
@@ -54,11 +54,13 @@ __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate ? 1u : 0u));
 }
 
-// D = A . B^T for two [128][kD] tiles at sa / sb (8 MMA steps along K).
+// D = A . B^T for two [128][kD] tiles at sa / sb (8 MMA steps along K: 4 per k-block).
 __device__ __forceinline__ void mma_tile(uint32_t tmem_d, uint32_t sa, uint32_t sb, uint32_t idesc) {
 #pragma unroll
-  for (int ks = 0; ks < kD / 16; ++ks)
-    mma_f16(tmem_d, smem_desc(sa + ks * 2 * kSlice), smem_desc(sb + ks * 2 * kSlice), idesc, ks > 0);
+  for (int ks = 0; ks < kD / 16; ++ks) {
+    const uint32_t off = (ks >> 2) * kKBlock + (ks & 3) * 32;
+    mma_f16(tmem_d, smem_desc(sa + off), smem_desc(sb + off), idesc, ks > 0);
+  }
 }
 
 // The mbarrier at `mbar` completes when every tcgen05 op this thread issued so far is done.
@@ -135,18 +137,19 @@ __device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
 }
 
 // One thread: TMA-load rows [row0, row0 + 128) of a [rows][kD] fp16 matrix described by the
-// 2-D tensor map `tmap` (box 8 channels x 128 rows) into the tile at `s`: sixteen boxes,
-// one per 8-channel k-slice (x = 8j, a multiple of 16 bytes).  Rows past the end of the
-// matrix are zero-filled.  Completes `bytes` = 32 KB on the mbarrier.
+// 2-D tensor map `tmap` (box 64 channels x 128 rows, 128-byte swizzle) into the tile at `s`
+// (1024-byte aligned): two boxes, one per k-block (x = 0 and 64).  Rows past the end of the
+// matrix are zero-filled.  Completes 32 KB on the mbarrier.
 __device__ __forceinline__ void tma_tile(uint32_t s, const void* tmap, int row0, uint32_t mbar) {
 #pragma unroll
-  for (int j = 0; j < kD / 8; ++j)
+  for (int j = 0; j < kD / 64; ++j)
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(s + j * kSlice),
-        "l"(tmap), "r"(j * 8), "r"(row0), "r"(mbar)
+        " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(s + j * kKBlock),
+        "l"(tmap), "r"(j * 64), "r"(row0), "r"(mbar)
         : "memory");
 }
+
 // One thread: bulk-copy `bytes` (multiple of 16, both addresses 16-byte aligned) into
 // shared memory, completing on the mbarrier.
 __device__ __forceinline__ void bulk_copy(uint32_t s, const void* g, uint32_t bytes, uint32_t mbar) {
