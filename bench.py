@@ -232,7 +232,9 @@ def run_gpu(args, wl, rank, world):
         x = inputs.make_prefill(rank_seed(wl, rank), l, dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        c.prefill(x["q"], x["k"], x["v"], wl.budget_pct, wl.window)
+        w_o = inputs.make_w_o(rank_seed(wl, rank), l, dev) if wl.policy == "criticalkv" else None
+        c.prefill(x["q"], x["k"], x["v"], wl.budget_pct, wl.window, policy=wl.policy, alpha=wl.alpha,
+                  w_o=w_o)
         e1.record()
         torch.cuda.synchronize()
         prefill_ms.append(e0.elapsed_time(e1))
@@ -271,7 +273,7 @@ def run_gpu(args, wl, rank, world):
                 # tiers as attended (after the append)
                 attn_pairs.append((a0, a1, cache_bytes(wl, c.n_hi + 1, c.n_lo)))
                 _lib.mikv_set_attention_events(a0, a1)
-            c.decode_step(t["q"], t["k"], t["v"], L_before, wl.budget_pct, wl.window)
+            c.decode_step(t["q"], t["k"], t["v"], L_before, wl.budget_pct, wl.window, policy=wl.policy)
             if mode == "step":
                 e1.record()
         return 4 * len(layers)   # append, split-K attention, merge, score update/demotion
@@ -337,7 +339,7 @@ def run_gpu(args, wl, rank, world):
                 for n in ("q", "k", "v"):
                     dev_in[l][n].copy_(host_in[i][l][n], non_blocking=True)
                 out, _ = c.decode_step(dev_in[l]["q"], dev_in[l]["k"], dev_in[l]["v"], L_before,
-                                       wl.budget_pct, wl.window)
+                                       wl.budget_pct, wl.window, policy=wl.policy)
                 host_out[l].copy_(out, non_blocking=True)
             e2e_tokens += wl.B * (L_before + 1) * wl.layers
         e1.record()

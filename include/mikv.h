@@ -192,9 +192,11 @@ size_t mikv_score_workspace_bytes(int B, int Hq, int T);
  *   pos < L - window picks the minimum of (score ascending, position descending)
  *   and writes its slot index to evict_pos [B][Hkv]; L is the current length.
  *   Requires c->n_hi > window.
- * ws >= mikv_select_workspace_bytes(policy, B, Hkv, Hq, L, hidden).
+ * ws >= mikv_select_workspace_bytes(policy, B, Hkv, Hq, L, hidden), 16-byte aligned;
+ *   CRITICALKV keeps the stage-2 keys there and, when w_o != NULL, a transposed copy of
+ *   w_o ([hidden][Hq*D] fp16, so both tensor-core operands are channel-contiguous).
  * Errors: EINVAL (null, policy, alpha outside [0,1]), ESHAPE (L, budget, window,
- * hidden), EUNSUPPORTED, ECUDA.
+ * hidden, B*Hkv*L >= 2^31), EALIGN (v, w_o, ws), EUNSUPPORTED, ECUDA.
  */
 int mikv_select(int policy, const mikv_cache* c, int L, int budget_pct, int window, float alpha,
                 const float* scores, const float* scores_head, const uint16_t* v,

@@ -14,11 +14,7 @@
 //           every 64-query tile at or below the diagonal, exp2(s - lse_t) summed
 //           over the queries -> S^h_i, then S_i in head order.
 // Work is triangular, so CTAs are numbered heaviest first.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <algorithm>
-#include <mutex>
 
 #include "common.cuh"
 #include "tcgen05.cuh"
@@ -269,45 +265,13 @@ constexpr uint32_t kTcIdesc = tc::idesc_f16(kTcTile, kTcTile);
 // lse rows are padded to whole tiles so one tile's 128 values are one aligned bulk copy.
 __host__ __device__ __forceinline__ int lse_stride(int T) { return (T + kTcTile - 1) / kTcTile * kTcTile; }
 
-struct TcBars {
-  uint64_t load[2];   // operand buffer b filled (TMA bytes)
-  uint64_t mma[2];    // accumulator b written (tcgen05.commit)
-  uint64_t freed[2];  // accumulator b read by all threads
-  uint64_t fixed;     // the resident operand tile filled
-};
-
-// Per-CTA set-up: mbarriers and the TMEM allocation; returns the TMEM base.
-__device__ __forceinline__ uint32_t tc_setup(TcBars& bar, uint32_t* tslot) {
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(smem_u32(&bar.load[i]), 1);
-      tc::mbar_init(smem_u32(&bar.mma[i]), 1);
-      tc::mbar_init(smem_u32(&bar.freed[i]), kTcThreads);
-    }
-    tc::mbar_init(smem_u32(&bar.fixed), 1);
-    tc::mbar_init_fence();
-  }
-  if (threadIdx.x < 32) tc::tmem_alloc(smem_u32(tslot), kTcCols);
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  return *tslot;
-}
-__device__ __forceinline__ void tc_teardown(uint32_t tbase) {
-  tc::fence_before_sync();
-  __syncthreads();
-  if (threadIdx.x < 32) tc::tmem_dealloc(tbase, kTcCols);
-}
-// 1024-byte aligned base of the dynamic shared memory (swizzled TMA destinations).
-__device__ __forceinline__ uint32_t tc_base(uint8_t* sm) { return (smem_u32(sm) + 1023u) & ~1023u; }
-
 // Pass 1 on tcgen05: lse2[b][h][t] (row stride lse_stride(T)) for 128 query rows.
 __global__ void __launch_bounds__(kTcBlock, 2) row_lse_tc_kernel(const __grid_constant__ CUtensorMap tq,
                                                                  const __grid_constant__ CUtensorMap tk,
                                                                  int Hq, int Hkv, int T,
                                                                  float* __restrict__ lse2) {
   extern __shared__ __align__(128) uint8_t sm[];  // Q tile, 2 K tiles
-  __shared__ __align__(8) TcBars bar;
+  __shared__ __align__(8) tc::Bars bar;
   __shared__ uint32_t tslot;
   __shared__ float xm[kTcTile], xl[kTcTile];
   __shared__ int bad;
@@ -317,10 +281,10 @@ __global__ void __launch_bounds__(kTcBlock, 2) row_lse_tc_kernel(const __grid_co
   const int g = h / (Hq / Hkv);
   const int tid = threadIdx.x, warp = tid >> 5, row = tid & 127, half = (tid >> 7) & 1;
   const int qrow0 = bh * T, krow0 = (b * Hkv + g) * T;  // first rows of this head in the maps
-  const uint32_t sq = tc_base(sm), sk0 = sq + tc::kTileBytes;
+  const uint32_t sq = tc::smem_base(sm), sk0 = sq + tc::kTileBytes;
   const int t0 = rb * kTcTile;
   if (tid == 0) bad = 0;
-  const uint32_t tbase = tc_setup(bar, &tslot);
+  const uint32_t tbase = tc::cta_setup(bar, &tslot, kTcThreads, kTcCols);
   bool ok = true;
   float m = -INFINITY, l = 0.f, lc = 0.f;
   const int t = t0 + row;  // a consumer's query row
@@ -406,7 +370,7 @@ __global__ void __launch_bounds__(kTcBlock, 2) row_lse_tc_kernel(const __grid_co
     }
   }
   if (!ok) atomicExch(&bad, 1);
-  tc_teardown(tbase);  // (its barrier also publishes xm / xl / bad)
+  tc::cta_teardown(tbase, kTcCols);  // (its barrier also publishes xm / xl / bad)
   if (tid < kTcTile && t < T) {
     const float m1 = xm[row], l1 = xl[row], l0 = l - lc;
     const float M = fmaxf(m, m1);
@@ -423,7 +387,7 @@ __global__ void __launch_bounds__(kTcBlock, 2) col_sum_tc_kernel(const __grid_co
                                                                  int Hkv, int T, float* __restrict__ s_full,
                                                                  float* __restrict__ s_head) {
   extern __shared__ __align__(128) uint8_t sm[];  // K tile, 2 Q tiles, lse ring
-  __shared__ __align__(8) TcBars bar;
+  __shared__ __align__(8) tc::Bars bar;
   __shared__ uint32_t tslot;
   __shared__ float xs[kTcTile];
   __shared__ int bad;
@@ -433,13 +397,13 @@ __global__ void __launch_bounds__(kTcBlock, 2) col_sum_tc_kernel(const __grid_co
   const int unit = blockIdx.y, b = unit / Hkv, g = unit % Hkv;
   const int rep = Hq / Hkv;
   const int tid = threadIdx.x, warp = tid >> 5, row = tid & 127, half = (tid >> 7) & 1;
-  const uint32_t sk = tc_base(sm), sq0 = sk + tc::kTileBytes, sl0 = sk + 3 * tc::kTileBytes;
+  const uint32_t sk = tc::smem_base(sm), sq0 = sk + tc::kTileBytes, sl0 = sk + 3 * tc::kTileBytes;
   const float* sl = reinterpret_cast<const float*>(sm + (sl0 - smem_u32(sm)));
   const int i0 = kbi * kTcTile;
   const int per = nblk - kbi;   // query tiles per head
   const int ntile = rep * per;  // tiles of this CTA, head-major
   if (tid == 0) bad = 0;
-  const uint32_t tbase = tc_setup(bar, &tslot);
+  const uint32_t tbase = tc::cta_setup(bar, &tslot, kTcThreads, kTcCols);
   bool ok = true;
   const int i = i0 + row;  // a consumer's key
   float tot = 0.f;
@@ -527,7 +491,7 @@ __global__ void __launch_bounds__(kTcBlock, 2) col_sum_tc_kernel(const __grid_co
     }
   }
   if (!ok) atomicExch(&bad, 1);
-  tc_teardown(tbase);
+  tc::cta_teardown(tbase, kTcCols);
   if (tid < kTcTile && i < T) s_full[static_cast<long>(unit) * T + i] = bad ? __int_as_float(0x7fc00000) : tot;
 }
 
@@ -551,37 +515,6 @@ __global__ void score_decode_kernel(const float* __restrict__ logits, const floa
 
 namespace mikv {
 namespace {
-// The driver's tensor-map encoder, looked up once through the runtime.
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    (void)cudaGetLastError();
-  });
-  return fn;
-}
-
-// 2-D map of a row-major [rows][kD] fp16 matrix with a 64-channel x 128-row box and
-// 128-byte swizzle.
-int encode_rows(CUtensorMap* map, const void* base, long rows, const char* what) {
-  const auto enc = tensor_map_encoder();
-  if (!enc) return fail(MIKV_ECUDA, "score_update: cuTensorMapEncodeTiled unavailable");
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTcTile)};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides,
-                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(MIKV_ECUDA, "score_update: tensor map of %s (error %d)", what, static_cast<int>(r));
-  return MIKV_OK;
-}
 }  // namespace
 }  // namespace mikv
 
@@ -611,8 +544,8 @@ extern "C" int mikv_score_update(int mode, const uint16_t* q, const uint16_t* k,
     float* lse2 = static_cast<float*>(ws);
     const int nblk = (T + kTcTile - 1) / kTcTile;
     CUtensorMap tq, tk;
-    if (int e = encode_rows(&tq, q, static_cast<long>(c->B) * c->Hq * T, "q")) return e;
-    if (int e = encode_rows(&tk, k, static_cast<long>(c->B) * c->Hkv * T, "k")) return e;
+    if (int e = tc::encode_rows(&tq, q, static_cast<long>(c->B) * c->Hq * T, "score_update: q")) return e;
+    if (int e = tc::encode_rows(&tk, k, static_cast<long>(c->B) * c->Hkv * T, "score_update: k")) return e;
     if (cudaFuncSetAttribute(row_lse_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess ||
         cudaFuncSetAttribute(col_sum_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess)
       return check_launch("score kernels attribute");

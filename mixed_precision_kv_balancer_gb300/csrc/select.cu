@@ -24,6 +24,7 @@
 #include <cmath>
 
 #include "common.cuh"
+#include "tcgen05.cuh"
 
 namespace mikv {
 int validate_cache_public(const mikv_cache* c, const char* who);
@@ -218,91 +219,124 @@ __global__ void ckey_kernel(const float* __restrict__ s_head, const float* __res
 }
 
 // ---------------------------------------------------------------------------------
-// K6: projected-value L1 norms on tensor cores.
-constexpr int kVwoThreads = 256;  // 8 warps x 16 tokens
-constexpr int kVwoM = 128;
-constexpr int kVwoN = 128;
+// K6: projected-value L1 norms on the 5th-generation tensor cores.
+// N[b][h][i] = sum_col | v_i^g . W_O[hD:(h+1)D, col] |.  W_O [Hq*D][hidden] is first
+// transposed into the workspace, so both operands are K-major (channels contiguous): per CTA
+// the V tile of 128 tokens of one (b, key head) stays resident; for each query head of the
+// group the 128-column blocks of W_O^T stream through TMA into two buffers, C = V . W^T
+// (128 x 128, fp32 in TMEM) by tcgen05.mma, and the consumers (two threads per token, 64
+// columns each) add |C|.  The same producer / consumer pipeline as the prefill scores.
+constexpr int kVwoThreads = 256;                        // consumers
+constexpr int kVwoBlock = kVwoThreads + 32;             // + the producer warp
+constexpr int kVwoN = tc::kTileRows;                    // hidden columns per tile
+constexpr int kVwoCols = 2 * kVwoN;                     // two TMEM accumulators
+constexpr int kVwoSmem = 3 * tc::kTileBytes + 1024;
+constexpr uint32_t kVwoIdesc = tc::idesc_f16(tc::kTileRows, kVwoN);
 
-__global__ void __launch_bounds__(kVwoThreads) vwo_norm_kernel(const __half* __restrict__ v,
-                                                               const __half* __restrict__ w,
-                                                               int Hq, int Hkv, int L, int hidden,
-                                                               float* __restrict__ out) {
-  extern __shared__ __align__(128) uint8_t sm[];
-  const uint32_t sv = smem_u32(sm);                 // [128 tokens][128 ch] swizzled
-  const uint32_t sw0 = sv + kVwoM * 256;            // 2 x [128 k][128 n] swizzled
-  const int bh = blockIdx.y, b = bh / Hq, h = bh % Hq;
-  const int g = h / (Hq / Hkv);
-  const int i0 = blockIdx.x * kVwoM;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gid = lane >> 2, tig = lane & 3;
-  const __half* vb = v + (static_cast<long>(b) * Hkv + g) * L * kD;
-  const __half* wb = w + static_cast<long>(h) * kD * hidden;
-  const int nrows = min(kVwoM, L - i0);
-  for (int i = threadIdx.x; i < kVwoM * 16; i += kVwoThreads) {
-    const int r = i >> 4, cc = i & 15;
-    const bool ok = r < nrows;
-    cp_async16(sv + r * 256 + ((cc ^ (r & 7)) << 4), ok ? vb + (static_cast<long>(i0) + r) * kD + cc * 8 : vb, ok);
-  }
-  auto load_w = [&](int step, int buf) {
-    const int n0 = step * kVwoN;
-    const uint32_t s = sw0 + buf * (kD * 256);
-    for (int i = threadIdx.x; i < kD * 16; i += kVwoThreads) {
-      const int r = i >> 4, cc = i & 15;
-      cp_async16(s + r * 256 + ((cc ^ (r & 7)) << 4), wb + static_cast<long>(r) * hidden + n0 + cc * 8, true);
-    }
-  };
-  const int nsteps = hidden / kVwoN;
-  load_w(0, 0);
-  cp_async_commit();
-  uint32_t a[8][4];
-  float run[2] = {0.f, 0.f}, comp[2] = {0.f, 0.f};
-  for (int st = 0; st < nsteps; ++st) {
-    if (st + 1 < nsteps) load_w(st + 1, (st + 1) & 1);
-    cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();
-    if (st == 0) {
+// W^T[c][r] = W[r][c] for a [rows][cols] fp16 matrix, 32 x 32 tiles through shared memory.
+__global__ void __launch_bounds__(256) transpose_kernel(const __half* __restrict__ w, int rows, int cols,
+                                                        __half* __restrict__ wt) {
+  __shared__ __half tile[32][33];
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  for (int j = ty; j < 32; j += 8)
+    if (r0 + j < rows && c0 + tx < cols) tile[j][tx] = w[static_cast<long>(r0 + j) * cols + c0 + tx];
+  __syncthreads();
+  for (int j = ty; j < 32; j += 8)
+    if (c0 + j < cols && r0 + tx < rows) wt[static_cast<long>(c0 + j) * rows + r0 + tx] = tile[tx][j];
+}
+
+__global__ void __launch_bounds__(kVwoBlock, 2) vwo_norm_tc_kernel(const __grid_constant__ CUtensorMap tv,
+                                                                   const __grid_constant__ CUtensorMap twt,
+                                                                   int Hq, int Hkv, int L, int hidden,
+                                                                   float* __restrict__ out) {
+  extern __shared__ __align__(128) uint8_t sm[];  // V tile, 2 W tiles
+  __shared__ __align__(8) tc::Bars bar;
+  __shared__ uint32_t tslot;
+  __shared__ float xs[tc::kTileRows];
+  __shared__ int bad;
+  const int unit = blockIdx.y, b = unit / Hkv, g = unit % Hkv;
+  const int rep = Hq / Hkv;
+  const int i0 = blockIdx.x * tc::kTileRows;
+  const int tid = threadIdx.x, warp = tid >> 5, row = tid & 127, half = (tid >> 7) & 1;
+  const uint32_t sv = tc::smem_base(sm), sw0 = sv + tc::kTileBytes;
+  const int per = hidden / kVwoN;  // column blocks per head
+  const int ntile = rep * per;     // tiles of this CTA, head-major
+  if (tid == 0) bad = 0;
+  const uint32_t tbase = tc::cta_setup(bar, &tslot, kVwoThreads, kVwoCols);
+  bool ok = true;
+  const int i = i0 + row;  // a consumer's token
+  if (tid == kVwoThreads) {
+    // producer.  Tile n: head g*rep + n / per, columns (n % per) * 128 ..: rows of W^T, the
+    // head's 128 channels at x = h * 128
+    auto load_w = [&](int n) {
+      const int h = g * rep + n / per, cb = n % per;
+      const uint32_t mb = smem_u32(&bar.load[n & 1]);
+      tc::mbar_expect_tx(mb, tc::kTileBytes);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int row = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int chunk = 2 * k + (lane >> 4);
-        ldsm_x4(sv + row * 256 + ((chunk ^ (row & 7)) << 4), a[k][0], a[k][1], a[k][2], a[k][3]);
+      for (int j = 0; j < kD / 64; ++j)
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(sw0 + (n & 1) * tc::kTileBytes + j * tc::kKBlock),
+            "l"(&twt), "r"(h * kD + j * 64), "r"(cb * kVwoN), "r"(mb)
+            : "memory");
+    };
+    tc::mbar_expect_tx(smem_u32(&bar.fixed), tc::kTileBytes);
+    tc::tma_tile(sv, &tv, unit * L + i0, smem_u32(&bar.fixed));
+    load_w(0);
+    if (ntile > 1) load_w(1);
+    ok = tc::mbar_wait(smem_u32(&bar.fixed), 0) && ok;
+    for (int n = 0; n < ntile; ++n) {
+      const int buf = n & 1;
+      ok = tc::mbar_wait(smem_u32(&bar.load[buf]), (n >> 1) & 1) && ok;
+      if (n >= 2) ok = tc::mbar_wait(smem_u32(&bar.freed[buf]), ((n - 2) >> 1) & 1) && ok;
+      tc::fence_after_sync();
+      tc::mma_tile(tbase + buf * kVwoN, sv, sw0 + buf * tc::kTileBytes, kVwoIdesc);
+      tc::commit(smem_u32(&bar.mma[buf]));
+      if (n + 2 < ntile) {  // W buffer buf is free once MMA n is done
+        ok = tc::mbar_wait(smem_u32(&bar.mma[buf]), (n >> 1) & 1) && ok;
+        load_w(n + 2);
       }
     }
-    const uint32_t s = sw0 + (st & 1) * (kD * 256);
-    float part[2] = {0.f, 0.f};
+  } else if (tid < kVwoThreads) {
+    float run = 0.f, comp = 0.f;
+    for (int n = 0; n < ntile; ++n) {
+      const int buf = n & 1;
+      ok = tc::mbar_wait(smem_u32(&bar.mma[buf]), (n >> 1) & 1) && ok;
+      tc::fence_after_sync();
+      float c0[32], c1[32];
+      const uint32_t lane_addr =
+          tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16) + buf * kVwoN + half * (kVwoN / 2);
+      tc::tmem_ld32(lane_addr, c0);
+      tc::tmem_ld32(lane_addr + 32, c1);
+      tc::fence_before_sync();
+      tc::mbar_arrive(smem_u32(&bar.freed[buf]));  // accumulator read
+      float p8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int np = 0; np < 8; ++np) {
-      float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int e = 0; e < 32; ++e) p8[e & 7] += fabsf(c0[e]);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int krow = 16 * k + (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int chunk = 2 * np + (lane >> 4);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(s + krow * 256 + ((chunk ^ (krow & 7)) << 4), b0, b1, b2, b3);
-        mma16816(acc0, a[k][0], a[k][1], a[k][2], a[k][3], b0, b1);
-        mma16816(acc1, a[k][0], a[k][1], a[k][2], a[k][3], b2, b3);
+      for (int e = 0; e < 32; ++e) p8[e & 7] += fabsf(c1[e]);
+      const float part = ((p8[0] + p8[1]) + (p8[2] + p8[3])) + ((p8[4] + p8[5]) + (p8[6] + p8[7]));
+      const float y = part - comp;
+      const float t = run + y;
+      comp = (t - run) - y;
+      run = t;
+      if (n % per == per - 1) {  // head done: the two column halves of each token
+        if (half == 1) xs[row] = run - comp;
+        asm volatile("bar.sync 1, %0;\n" ::"n"(kVwoThreads));  // consumers only
+        if (half == 0 && i < L) {
+          const int h = g * rep + n / per;
+          out[(static_cast<long>(b) * Hq + h) * L + i] = (run - comp) + xs[row];
+        }
+        run = comp = 0.f;
+        asm volatile("bar.sync 1, %0;\n" ::"n"(kVwoThreads));  // xs may be rewritten
       }
-      part[0] += fabsf(acc0[0]) + fabsf(acc0[1]) + fabsf(acc1[0]) + fabsf(acc1[1]);
-      part[1] += fabsf(acc0[2]) + fabsf(acc0[3]) + fabsf(acc1[2]) + fabsf(acc1[3]);
     }
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const float y = part[hh] - comp[hh];
-      const float t = run[hh] + y;
-      comp[hh] = (t - run[hh]) - y;
-      run[hh] = t;
-    }
-    __syncthreads();
   }
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    float x = run[hh] - comp[hh];
-    x += __shfl_xor_sync(0xffffffffu, x, 1);
-    x += __shfl_xor_sync(0xffffffffu, x, 2);
-    const int i = i0 + warp * 16 + gid + 8 * hh;
-    if (tig == 0 && i < L) out[static_cast<long>(bh) * L + i] = x;
-  }
+  if (!ok) atomicExch(&bad, 1);
+  tc::cta_teardown(tbase, kVwoCols);
+  if (bad && tid < tc::kTileRows && i < L)  // a wait gave up: mark the unit's rows
+    for (int hr = 0; hr < rep; ++hr) out[(static_cast<long>(b) * Hq + g * rep + hr) * L + i] = __int_as_float(0x7fc00000);
 }
 
 }  // namespace
@@ -316,10 +350,10 @@ static int n_keep_of(int L, int pct, int window) {
 }
 
 extern "C" size_t mikv_select_workspace_bytes(int policy, int B, int Hkv, int Hq, int L, int hidden) {
-  (void)Hq;
-  (void)hidden;
   if (policy != MIKV_CRITICALKV || B < 1 || Hkv < 1 || L < 1) return 0;
-  return align_up(static_cast<size_t>(B) * Hkv * L * sizeof(float), 256);
+  // the stage-2 keys, then the transpose of W_O (when hidden > 0)
+  return align_up(static_cast<size_t>(B) * Hkv * L * sizeof(float), 256) +
+         align_up(static_cast<size_t>(std::max(hidden, 0)) * std::max(Hq, 0) * kD * 2, 256);
 }
 
 extern "C" int mikv_select(int policy, const mikv_cache* c, int L, int budget_pct, int window,
@@ -358,21 +392,30 @@ extern "C" int mikv_select(int policy, const mikv_cache* c, int L, int budget_pc
     if (!scores_head || !vwo_norm || !ws) return fail(MIKV_EINVAL, "select(CRITICALKV): null pointer");
     const size_t need = mikv_select_workspace_bytes(policy, c->B, c->Hkv, c->Hq, L, hidden);
     if (ws_bytes < need) return fail(MIKV_ESHAPE, "select: workspace %zu < %zu", ws_bytes, need);
+    if (!aligned16(ws)) return fail(MIKV_EALIGN, "select: workspace alignment");
     take1 = static_cast<int>(std::floor(static_cast<double>(alpha) * bud));
     take2 = bud - take1;
     if (w_o) {
       if (!v) return fail(MIKV_EINVAL, "select(CRITICALKV): null v");
       if (c->D != kD) return fail(MIKV_EUNSUPPORTED, "select: D=%d", c->D);
       if (hidden < kVwoN || hidden % kVwoN) return fail(MIKV_ESHAPE, "select: hidden=%d (multiple of %d)", hidden, kVwoN);
+      if (static_cast<long>(c->B) * c->Hkv * L > (1L << 31) - 1) return fail(MIKV_ESHAPE, "select: B*Hkv*L too large");
       if (!aligned16(v) || !aligned16(w_o)) return fail(MIKV_EALIGN, "select: v/w_o alignment");
-      const int smem = kVwoM * 256 + 2 * kD * 256;
-      if (cudaFuncSetAttribute(vwo_norm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-        return check_launch("vwo_norm_kernel attribute");
-      dim3 grid((L + kVwoM - 1) / kVwoM, c->B * c->Hq);
-      vwo_norm_kernel<<<grid, kVwoThreads, smem, s>>>(reinterpret_cast<const __half*>(v),
-                                                       reinterpret_cast<const __half*>(w_o), c->Hq,
-                                                       c->Hkv, L, hidden, vwo_norm);
-      if (int e = check_launch("vwo_norm_kernel")) return e;
+      // W_O^T into the workspace after the stage-2 keys
+      __half* wt = reinterpret_cast<__half*>(static_cast<char*>(ws) +
+                                             align_up(static_cast<size_t>(c->B) * c->Hkv * L * sizeof(float), 256));
+      const int wrows = c->Hq * kD;
+      transpose_kernel<<<dim3((hidden + 31) / 32, (wrows + 31) / 32), 256, 0, s>>>(
+          reinterpret_cast<const __half*>(w_o), wrows, hidden, wt);
+      if (int e = check_launch("transpose_kernel")) return e;
+      CUtensorMap tv, twt;
+      if (int e = tc::encode_rows(&tv, v, static_cast<long>(c->B) * c->Hkv * L, "select: v")) return e;
+      if (int e = tc::encode_rows(&twt, wt, hidden, "select: w_o^T", wrows)) return e;
+      if (cudaFuncSetAttribute(vwo_norm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kVwoSmem) != cudaSuccess)
+        return check_launch("vwo_norm_tc_kernel attribute");
+      vwo_norm_tc_kernel<<<dim3((L + tc::kTileRows - 1) / tc::kTileRows, units), kVwoBlock, kVwoSmem, s>>>(
+          tv, twt, c->Hq, c->Hkv, L, hidden, vwo_norm);
+      if (int e = check_launch("vwo_norm_tc_kernel")) return e;
     }
     float* ckey = static_cast<float*>(ws);
     ckey_kernel<<<dim3((L + 255) / 256, units), 256, 0, s>>>(scores_head, vwo_norm, c->Hq, c->Hkv, L, ckey);

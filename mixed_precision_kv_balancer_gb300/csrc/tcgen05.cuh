@@ -11,8 +11,12 @@
 // mbarrier is bounded.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
+
+#include <mutex>
 
 #include "common.cuh"
 
@@ -157,6 +161,75 @@ __device__ __forceinline__ void bulk_copy(uint32_t s, const void* g, uint32_t by
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(s),
       "l"(g), "r"(bytes), "r"(mbar)
       : "memory");
+}
+
+// ---------------------------------------------------------------------------------
+// CTA scaffolding of the warp-specialised tile pipelines: one producer lane (TMA + MMA
+// issue) and `consumers` threads that read the accumulators.
+struct Bars {
+  uint64_t load[2];   // operand buffer b filled (TMA bytes)
+  uint64_t mma[2];    // accumulator b written (tcgen05.commit)
+  uint64_t freed[2];  // accumulator b read by all consumer threads
+  uint64_t fixed;     // the resident operand tile filled
+};
+
+// mbarriers and the TMEM allocation (`cols` columns); returns the TMEM base.  Every thread
+// of the CTA calls it (it holds a barrier).
+__device__ __forceinline__ uint32_t cta_setup(Bars& bar, uint32_t* tslot, int consumers, uint32_t cols) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bar.load[i]), 1);
+      mbar_init(smem_u32(&bar.mma[i]), 1);
+      mbar_init(smem_u32(&bar.freed[i]), consumers);
+    }
+    mbar_init(smem_u32(&bar.fixed), 1);
+    mbar_init_fence();
+  }
+  if (threadIdx.x < 32) tmem_alloc(smem_u32(tslot), cols);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  return *tslot;
+}
+// Every thread of the CTA calls it after its last TMEM access.
+__device__ __forceinline__ void cta_teardown(uint32_t tbase, uint32_t cols) {
+  fence_before_sync();
+  __syncthreads();
+  if (threadIdx.x < 32) tmem_dealloc(tbase, cols);
+}
+// 1024-byte aligned base of the dynamic shared memory (swizzled TMA destinations).
+__device__ __forceinline__ uint32_t smem_base(uint8_t* sm) { return (smem_u32(sm) + 1023u) & ~1023u; }
+
+// ---------------------------------------------------------------------------------
+// Host: 2-D tensor map of a row-major [rows][cols] fp16 matrix (cols a multiple of 64)
+// with a 64-column x 128-row box and 128-byte swizzle, through the driver's encoder
+// (looked up once).  `what` names the caller in the error message.
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    (void)cudaGetLastError();
+  });
+  return fn;
+}
+inline int encode_rows(CUtensorMap* map, const void* base, long rows, const char* what, long cols = kD) {
+  const auto enc = tensor_map_encoder();
+  if (!enc) return fail(MIKV_ECUDA, "%s: cuTensorMapEncodeTiled unavailable", what);
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTileRows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides,
+                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MIKV_ECUDA, "%s: tensor map (error %d)", what, static_cast<int>(r));
+  return MIKV_OK;
 }
 
 }  // namespace tc
