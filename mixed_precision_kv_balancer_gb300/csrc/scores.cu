@@ -7,11 +7,11 @@
 //            S_i   = sum over the key head's query heads, h ascending, fp32
 //   decode   S_j  += sum_h exp(logit_{h,j} - lse_h) for important-tier slots.
 //
-// K3 is a dense causal QK^T: two tensor-core passes (mma.sync m16n8k16, fp16 in,
-// fp32 accumulate) over 64x64 tiles staged by cp.async:
-//   pass 1  per (b, h, 64 query rows): online row max/sum -> lse_t (base 2),
-//   pass 2  per (b, key head, 64 keys): for every query head of the group and
-//           every 64-query tile at or below the diagonal, exp2(s - lse_t) summed
+// K3 is a dense causal QK^T: two tensor-core passes (tcgen05, fp16 in, fp32 accumulate)
+// over 128x128 tiles:
+//   pass 1  per (b, h, 128 query rows): online row max/sum -> lse_t (base 2),
+//   pass 2  per (b, key head, 128 keys): for every query head of the group and
+//           every query tile at or below the diagonal, exp2(s - lse_t) summed
 //           over the queries -> S^h_i, then S_i in head order.
 // Work is triangular, so CTAs are numbered heaviest first.
 #include <algorithm>
@@ -24,9 +24,6 @@ int validate_cache_public(const mikv_cache* c, const char* who);
 
 namespace {
 
-constexpr int kTile = 64;
-constexpr int kThr = 128;   // 4 warps x 16 rows
-constexpr int kScoreSmem = 3 * kTile * 256 + 2 * kTile * 4;
 // log2(e)/sqrt(128): logits in base 2, one rounding shared by both passes
 constexpr float kC = 0.12751743082459868f;
 
@@ -37,210 +34,11 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// Stage a [64][128] fp16 tile (rows r0.., rows >= nrows zero-filled) into 128B-swizzled smem.
-__device__ __forceinline__ void load_tile(uint32_t s, const __half* g, long r0, int nrows) {
-  for (int i = threadIdx.x; i < kTile * 16; i += kThr) {
-    const int r = i >> 4, cc = i & 15;
-    const bool ok = r < nrows;
-    const __half* src = ok ? g + (r0 + r) * kD + cc * 8 : g;
-    cp_async16(s + r * 256 + ((cc ^ (r & 7)) << 4), src, ok);
-  }
-}
-
-// A fragments (16 rows x 128 ch) of a swizzled [64][128] tile for warp rows w*16..
-__device__ __forceinline__ void load_a_frags(uint32_t s, int w, int lane, uint32_t (&a)[8][4]) {
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int row = w * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-    const int chunk = 2 * k + (lane >> 4);
-    ldsm_x4(s + row * 256 + ((chunk ^ (row & 7)) << 4), a[k][0], a[k][1], a[k][2], a[k][3]);
-  }
-}
-
-// acc[n][4] = A(16 x 128) . Tile^T for the 64 rows of the tile as 8 n-tiles of 8.
-__device__ __forceinline__ void qk_tile(uint32_t s, const uint32_t (&a)[8][4], int lane,
-                                        float (&acc)[8][4]) {
-#pragma unroll
-  for (int n = 0; n < 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-#pragma unroll
-    for (int np = 0; np < 4; ++np) {  // pairs of n-tiles: rows np*16 .. +16 of the tile
-      const int row = np * 16 + (lane & 7) + ((lane >> 4) << 3);
-      const int chunk = 2 * k + ((lane >> 3) & 1);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(s + row * 256 + ((chunk ^ (row & 7)) << 4), b0, b1, b2, b3);
-      mma16816(acc[2 * np], a[k][0], a[k][1], a[k][2], a[k][3], b0, b1);
-      mma16816(acc[2 * np + 1], a[k][0], a[k][1], a[k][2], a[k][3], b2, b3);
-    }
-  }
-}
-
-// Pass 1: lse2[b][h][t] = log2 sum_{i <= t} exp2(s2_ti).
-__global__ void __launch_bounds__(kThr) row_lse_kernel(const __half* __restrict__ q,
-                                                       const __half* __restrict__ k, int Hq,
-                                                       int Hkv, int T, float* __restrict__ lse2) {
-  extern __shared__ __align__(128) uint8_t sm[];  // Q tile + 2 K tiles (kScoreSmem)
-  const int nblk = (T + kTile - 1) / kTile;
-  const int rb = nblk - 1 - blockIdx.x;  // heaviest (last) row block first
-  const int bh = blockIdx.y, b = bh / Hq, h = bh % Hq;
-  const int g = h / (Hq / Hkv);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gid = lane >> 2, tig = lane & 3;
-  const __half* qb = q + static_cast<long>(bh) * T * kD;
-  const __half* kb = k + (static_cast<long>(b) * Hkv + g) * T * kD;
-  const uint32_t sq = smem_u32(sm), sk0 = sq + kTile * 256;
-  const int t0 = rb * kTile;
-  load_tile(sq, qb, t0, min(kTile, T - t0));
-  load_tile(sk0, kb, 0, min(kTile, T));
-  cp_async_commit();
-  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f}, lc[2] = {0.f, 0.f};  // lc: compensation
-  uint32_t a[8][4];
-  const int row0 = t0 + warp * 16 + gid;  // rows row0, row0 + 8
-  for (int kt = 0; kt <= rb; ++kt) {
-    if (kt + 1 <= rb) {
-      load_tile(sk0 + ((kt + 1) & 1) * kTile * 256, kb, (kt + 1) * kTile,
-                min(kTile, T - (kt + 1) * kTile));
-    }
-    cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();
-    if (kt == 0) load_a_frags(sq, warp, lane, a);
-    float acc[8][4];
-    qk_tile(sk0 + (kt & 1) * kTile * 256, a, lane, acc);
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int t = row0 + 8 * hh;
-      float mx = -INFINITY;
-      float x[8][2];
-#pragma unroll
-      for (int n = 0; n < 8; ++n)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int i = kt * kTile + n * 8 + 2 * tig + e;
-          const float v = (i <= t && i < T) ? acc[n][2 * hh + e] * kC : -INFINITY;
-          x[n][e] = v;
-          mx = fmaxf(mx, v);
-        }
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float mn = fmaxf(m[hh], mx);
-      float sum = 0.f;
-      if (mn != -INFINITY) {
-        // exponent acc*kC - m with a single rounding (fused), so the dominant terms
-        // (exponent near 0) carry no rounding error of the ~40-sized logit itself
-#pragma unroll
-        for (int n = 0; n < 8; ++n)
-#pragma unroll
-          for (int e = 0; e < 2; ++e)
-            if (x[n][e] != -INFINITY) sum += fast_exp2(fmaf(acc[n][2 * hh + e], kC, -mn));
-        const float alpha = fast_exp2(m[hh] - mn);
-        // compensated (Kahan) running sum, rescaled with the running max
-        l[hh] = __fmul_rn(l[hh], alpha);
-        lc[hh] = __fmul_rn(lc[hh], alpha);
-        const float y = sum - lc[hh];
-        const float tt = l[hh] + y;
-        lc[hh] = (tt - l[hh]) - y;
-        l[hh] = tt;
-        m[hh] = mn;
-      }
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    float s = l[hh] - lc[hh];
-    s += __shfl_xor_sync(0xffffffffu, s, 1);
-    s += __shfl_xor_sync(0xffffffffu, s, 2);
-    const int t = row0 + 8 * hh;
-    if (tig == 0 && t < T) lse2[static_cast<long>(bh) * T + t] = m[hh] + log2f(s);
-  }
-}
-
-// Pass 2: S^h_i for 64 keys of one (b, key head), all query heads of the group.
-__global__ void __launch_bounds__(kThr) col_sum_kernel(const __half* __restrict__ q,
-                                                       const __half* __restrict__ k,
-                                                       const float* __restrict__ lse2, int Hq,
-                                                       int Hkv, int T, float* __restrict__ s_full,
-                                                       float* __restrict__ s_head) {
-  extern __shared__ __align__(128) uint8_t sm[];  // K tile + 2 Q tiles + 2 lse rows
-  float (*sl)[kTile] = reinterpret_cast<float (*)[kTile]>(sm + 3 * kTile * 256);
-  const int nblk = (T + kTile - 1) / kTile;
-  const int kb_i = blockIdx.x;  // key block 0 (heaviest) first
-  const int unit = blockIdx.y, b = unit / Hkv, g = unit % Hkv;
-  const int rep = Hq / Hkv;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gid = lane >> 2, tig = lane & 3;
-  const __half* kbase = k + static_cast<long>(unit) * T * kD;
-  const uint32_t sk = smem_u32(sm), sq0 = sk + kTile * 256;
-  const int i0 = kb_i * kTile;
-  load_tile(sk, kbase, i0, min(kTile, T - i0));
-  cp_async_commit();
-  uint32_t a[8][4];
-  const int key0 = i0 + warp * 16 + gid;  // keys key0, key0 + 8
-  float tot[2] = {0.f, 0.f};
-  for (int hr = 0; hr < rep; ++hr) {
-    const int h = g * rep + hr;
-    const long bh = static_cast<long>(b) * Hq + h;
-    const __half* qb = q + bh * T * kD;
-    const float* lb = lse2 + bh * T;
-    float col[2] = {0.f, 0.f}, colc[2] = {0.f, 0.f};  // colc: Kahan compensation
-    // first query tile is the diagonal one
-    load_tile(sq0, qb, i0, min(kTile, T - i0));
-    for (int j = threadIdx.x; j < kTile; j += kThr) sl[0][j] = (i0 + j < T) ? lb[i0 + j] : 0.f;
-    cp_async_commit();
-    for (int qt = kb_i; qt < nblk; ++qt) {
-      const int buf = (qt - kb_i) & 1;
-      if (qt + 1 < nblk) {
-        const int nt0 = (qt + 1) * kTile;
-        load_tile(sq0 + (buf ^ 1) * kTile * 256, qb, nt0, min(kTile, T - nt0));
-        for (int j = threadIdx.x; j < kTile; j += kThr)
-          sl[buf ^ 1][j] = (nt0 + j < T) ? lb[nt0 + j] : 0.f;
-      }
-      cp_async_commit();
-      cp_async_wait<1>();
-      __syncthreads();
-      if (hr == 0 && qt == kb_i) load_a_frags(sk, warp, lane, a);
-      float acc[8][4];
-      qk_tile(sq0 + buf * kTile * 256, a, lane, acc);
-      float part[2] = {0.f, 0.f};
-#pragma unroll
-      for (int n = 0; n < 8; ++n)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int jq = n * 8 + 2 * tig + e;
-          const int t = qt * kTile + jq;
-          const float lt = sl[buf][jq];
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int i = key0 + 8 * hh;
-            if (t >= i && t < T) part[hh] += fast_exp2(fmaf(acc[n][2 * hh + e], kC, -lt));
-          }
-        }
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const float y = part[hh] - colc[hh];
-        const float tt = col[hh] + y;
-        colc[hh] = (tt - col[hh]) - y;
-        col[hh] = tt;
-      }
-      __syncthreads();
-    }
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      float s = col[hh] - colc[hh];
-      s += __shfl_xor_sync(0xffffffffu, s, 1);
-      s += __shfl_xor_sync(0xffffffffu, s, 2);
-      const int i = key0 + 8 * hh;
-      if (tig == 0 && i < T && s_head) s_head[bh * T + i] = s;
-      tot[hh] = __fadd_rn(tot[hh], s);  // group sum in head order
-    }
-  }
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    const int i = key0 + 8 * hh;
-    if (tig == 0 && i < T) s_full[static_cast<long>(unit) * T + i] = tot[hh];
-  }
+// max(a, b, c) in one instruction (exact, like two fmaxf).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 // ---------------------------------------------------------------------------------
@@ -265,11 +63,12 @@ constexpr uint32_t kTcIdesc = tc::idesc_f16(kTcTile, kTcTile);
 // lse rows are padded to whole tiles so one tile's 128 values are one aligned bulk copy.
 __host__ __device__ __forceinline__ int lse_stride(int T) { return (T + kTcTile - 1) / kTcTile * kTcTile; }
 
-// Pass 1 on tcgen05: lse2[b][h][t] (row stride lse_stride(T)) for 128 query rows.
+// Pass 1 on tcgen05: nlse2[b][h][t] = -lse_t in base 2 (row stride lse_stride(T)) for 128
+// query rows (negated, so pass 2 forms s * kC - lse_t with one fma).
 __global__ void __launch_bounds__(kTcBlock, 2) row_lse_tc_kernel(const __grid_constant__ CUtensorMap tq,
                                                                  const __grid_constant__ CUtensorMap tk,
                                                                  int Hq, int Hkv, int T,
-                                                                 float* __restrict__ lse2) {
+                                                                 float* __restrict__ nlse2) {
   extern __shared__ __align__(128) uint8_t sm[];  // Q tile, 2 K tiles
   __shared__ __align__(8) tc::Bars bar;
   __shared__ uint32_t tslot;
@@ -326,33 +125,49 @@ __global__ void __launch_bounds__(kTcBlock, 2) row_lse_tc_kernel(const __grid_co
       tc::mbar_arrive(smem_u32(&bar.freed[buf]));  // accumulator read: the MMA may reuse it
       const int i0 = kt * kTcTile + half * kTcHalf;
       const int lim = min(t - i0, T - 1 - i0);  // columns 0..lim are causal and in range
-      // 8 independent max / sum chains; masks only on the diagonal or last tile
-      float mx8[8], sm8[8];
+      // 8 independent max / sum chains (chain c % 8); masks only on the diagonal or last
+      // tile.  Unmasked tiles take three-input max and packed f32x2 fma / add: the same
+      // chains, in the same order, in fewer instructions.
+      const bool full = lim >= kTcHalf - 1;
+      float mx8[8];
+      if (full) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) mx8[j] = -INFINITY;
-      if (lim >= kTcHalf - 1) {
-#pragma unroll
-        for (int c = 0; c < kTcHalf; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+        for (int j = 0; j < 8; ++j) {
+          float x = max3(s[j], s[8 + j], s[16 + j]);
+          x = max3(x, s[24 + j], s[32 + j]);
+          x = max3(x, s[40 + j], s[48 + j]);
+          mx8[j] = fmaxf(x, s[56 + j]);
+        }
       } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mx8[j] = -INFINITY;
 #pragma unroll
         for (int c = 0; c < kTcHalf; ++c)
           if (c <= lim) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
       }
-      const float mxr = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float mxr = fmaxf(max3(mx8[0], mx8[1], mx8[2]), max3(max3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
       const float mn = fmaxf(m, mxr * kC);  // kC > 0: the max commutes with the scaling
       if (mn != -INFINITY) {
+        float2 sm4[4];  // chains 2j, 2j + 1
 #pragma unroll
-        for (int j = 0; j < 8; ++j) sm8[j] = 0.f;
-        if (lim >= kTcHalf - 1) {
+        for (int j = 0; j < 4; ++j) sm4[j] = make_float2(0.f, 0.f);
+        if (full) {
+          const float2 k2 = make_float2(kC, kC), nm = make_float2(-mn, -mn);
 #pragma unroll
-          for (int c = 0; c < kTcHalf; ++c) sm8[c & 7] += fast_exp2(fmaf(s[c], kC, -mn));
+          for (int c = 0; c < kTcHalf; c += 2) {
+            const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), k2, nm);
+            sm4[(c >> 1) & 3] = __fadd2_rn(sm4[(c >> 1) & 3], make_float2(fast_exp2(x.x), fast_exp2(x.y)));
+          }
         } else {
 #pragma unroll
           for (int c = 0; c < kTcHalf; ++c)
-            if (c <= lim) sm8[c & 7] += fast_exp2(fmaf(s[c], kC, -mn));
+            if (c <= lim) {
+              const float e = fast_exp2(fmaf(s[c], kC, -mn));
+              if (c & 1) sm4[(c >> 1) & 3].y += e;
+              else sm4[(c >> 1) & 3].x += e;
+            }
         }
-        const float sum = ((sm8[0] + sm8[1]) + (sm8[2] + sm8[3])) + ((sm8[4] + sm8[5]) + (sm8[6] + sm8[7]));
+        const float sum = ((sm4[0].x + sm4[0].y) + (sm4[1].x + sm4[1].y)) + ((sm4[2].x + sm4[2].y) + (sm4[3].x + sm4[3].y));
         const float alpha = fast_exp2(m - mn);
         l = __fmul_rn(l, alpha);
         lc = __fmul_rn(lc, alpha);
@@ -375,7 +190,7 @@ __global__ void __launch_bounds__(kTcBlock, 2) row_lse_tc_kernel(const __grid_co
     const float m1 = xm[row], l1 = xl[row], l0 = l - lc;
     const float M = fmaxf(m, m1);
     const float L = (m == -INFINITY ? 0.f : l0 * fast_exp2(m - M)) + (m1 == -INFINITY ? 0.f : l1 * fast_exp2(m1 - M));
-    lse2[static_cast<long>(bh) * lse_stride(T) + t] = bad ? __int_as_float(0x7fc00000) : M + log2f(L);
+    nlse2[static_cast<long>(bh) * lse_stride(T) + t] = bad ? __int_as_float(0x7fc00000) : -(M + log2f(L));
   }
 }
 
@@ -383,7 +198,7 @@ __global__ void __launch_bounds__(kTcBlock, 2) row_lse_tc_kernel(const __grid_co
 // query tile: TMEM lane = key, column = query; thread i and i + 128 take the query halves.
 __global__ void __launch_bounds__(kTcBlock, 2) col_sum_tc_kernel(const __grid_constant__ CUtensorMap tq,
                                                                  const __grid_constant__ CUtensorMap tk,
-                                                                 const float* __restrict__ lse2, int Hq,
+                                                                 const float* __restrict__ nlse2, int Hq,
                                                                  int Hkv, int T, float* __restrict__ s_full,
                                                                  float* __restrict__ s_head) {
   extern __shared__ __align__(128) uint8_t sm[];  // K tile, 2 Q tiles, lse ring
@@ -416,7 +231,7 @@ __global__ void __launch_bounds__(kTcBlock, 2) col_sum_tc_kernel(const __grid_co
       const uint32_t mb = smem_u32(&bar.load[n & 1]);
       tc::mbar_expect_tx(mb, tc::kTileBytes + kTcTile * 4);
       tc::tma_tile(sq0 + (n & 1) * tc::kTileBytes, &tq, static_cast<int>(bh * T) + qt * kTcTile, mb);
-      tc::bulk_copy(sl0 + (n % kTcLseRing) * kTcTile * 4, lse2 + bh * ls + qt * kTcTile, kTcTile * 4, mb);
+      tc::bulk_copy(sl0 + (n % kTcLseRing) * kTcTile * 4, nlse2 + bh * ls + qt * kTcTile, kTcTile * 4, mb);
     };
     tc::mbar_expect_tx(smem_u32(&bar.fixed), tc::kTileBytes);
     tc::tma_tile(sk, &tk, unit * T + i0, smem_u32(&bar.fixed));
@@ -447,30 +262,41 @@ __global__ void __launch_bounds__(kTcBlock, 2) col_sum_tc_kernel(const __grid_co
       const int cq = qt * kTcTile + half * kTcHalf;  // query of this thread's column 0
       const int c0 = max(i - cq, 0);                  // first causal column (query >= key)
       const int c1 = min(kTcHalf, T - cq);            // columns past T are padding
-      const float* lt = sl + (n % kTcLseRing) * kTcTile + half * kTcHalf;
-      float p8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent chains
+      const float* lt = sl + (n % kTcLseRing) * kTcTile + half * kTcHalf;  // -lse of the columns
+      float2 p4[4];  // independent chains e % 8 = 2j, 2j + 1
+#pragma unroll
+      for (int j = 0; j < 4; ++j) p4[j] = make_float2(0.f, 0.f);
       const bool full = c0 == 0 && c1 == kTcHalf;
       const uint32_t lane_addr =
           tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16) + buf * kTcTile + half * kTcHalf;
       float s0[32], s1[32];
       tc::tmem_ld32(lane_addr, s0);
       tc::tmem_ld32(lane_addr + 32, s1);
-      if (full) {
+      if (full) {  // packed f32x2 fma / add, -lse read four at a time
+        const float4* l4 = reinterpret_cast<const float4*>(lt);
+        const float2 k2 = make_float2(kC, kC);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) p8[e & 7] += fast_exp2(fmaf(s0[e], kC, -lt[e]));
-#pragma unroll
-        for (int e = 0; e < 32; ++e) p8[e & 7] += fast_exp2(fmaf(s1[e], kC, -lt[32 + e]));
+        for (int e = 0; e < 64; e += 4) {
+          const float4 a = l4[e >> 2];
+          const float* sv = e < 32 ? s0 + e : s1 + (e - 32);
+          const float2 x0 = __ffma2_rn(make_float2(sv[0], sv[1]), k2, make_float2(a.x, a.y));
+          const float2 x1 = __ffma2_rn(make_float2(sv[2], sv[3]), k2, make_float2(a.z, a.w));
+          p4[(e >> 1) & 3] = __fadd2_rn(p4[(e >> 1) & 3], make_float2(fast_exp2(x0.x), fast_exp2(x0.y)));
+          p4[((e >> 1) + 1) & 3] =
+              __fadd2_rn(p4[((e >> 1) + 1) & 3], make_float2(fast_exp2(x1.x), fast_exp2(x1.y)));
+        }
       } else {
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (e >= c0 && e < c1) p8[e & 7] += fast_exp2(fmaf(s0[e], kC, -lt[e]));
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (32 + e >= c0 && 32 + e < c1) p8[e & 7] += fast_exp2(fmaf(s1[e], kC, -lt[32 + e]));
+        for (int e = 0; e < 64; ++e)
+          if (e >= c0 && e < c1) {
+            const float x = fast_exp2(fmaf(e < 32 ? s0[e] : s1[e - 32], kC, lt[e]));
+            if (e & 1) p4[(e >> 1) & 3].y += x;
+            else p4[(e >> 1) & 3].x += x;
+          }
       }
       tc::fence_before_sync();
       tc::mbar_arrive(smem_u32(&bar.freed[buf]));  // accumulator and lse slot read
-      const float part = ((p8[0] + p8[1]) + (p8[2] + p8[3])) + ((p8[4] + p8[5]) + (p8[6] + p8[7]));
+      const float part = ((p4[0].x + p4[0].y) + (p4[1].x + p4[1].y)) + ((p4[2].x + p4[2].y) + (p4[3].x + p4[3].y));
       const float y = part - colc;
       const float tt = col + y;
       colc = (tt - col) - y;
@@ -538,10 +364,11 @@ extern "C" int mikv_score_update(int mode, const uint16_t* q, const uint16_t* k,
   if (mode == MIKV_PREFILL) {
     if (!q || !k || !scores_full || !ws) return fail(MIKV_EINVAL, "score_update: null pointer");
     if (T < 1) return fail(MIKV_ESHAPE, "score_update: T=%d", T);
+    if (static_cast<long>(c->B) * c->Hq * T > (1L << 31) - 1) return fail(MIKV_ESHAPE, "score_update: B*Hq*T too large");
     if (!aligned16(q) || !aligned16(k)) return fail(MIKV_EALIGN, "score_update: q/k alignment");
     const size_t need = mikv_score_workspace_bytes(c->B, c->Hq, T);
     if (ws_bytes < need) return fail(MIKV_ESHAPE, "score_update: workspace %zu < %zu", ws_bytes, need);
-    float* lse2 = static_cast<float*>(ws);
+    float* nlse2 = static_cast<float*>(ws);
     const int nblk = (T + kTcTile - 1) / kTcTile;
     CUtensorMap tq, tk;
     if (int e = tc::encode_rows(&tq, q, static_cast<long>(c->B) * c->Hq * T, "score_update: q")) return e;
@@ -549,9 +376,9 @@ extern "C" int mikv_score_update(int mode, const uint16_t* q, const uint16_t* k,
     if (cudaFuncSetAttribute(row_lse_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess ||
         cudaFuncSetAttribute(col_sum_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess)
       return check_launch("score kernels attribute");
-    row_lse_tc_kernel<<<dim3(nblk, c->B * c->Hq), kTcBlock, kTcSmem, s>>>(tq, tk, c->Hq, c->Hkv, T, lse2);
+    row_lse_tc_kernel<<<dim3(nblk, c->B * c->Hq), kTcBlock, kTcSmem, s>>>(tq, tk, c->Hq, c->Hkv, T, nlse2);
     if (int e = check_launch("row_lse_tc_kernel")) return e;
-    col_sum_tc_kernel<<<dim3(nblk, c->B * c->Hkv), kTcBlock, kTcSmem, s>>>(tq, tk, lse2, c->Hq, c->Hkv, T,
+    col_sum_tc_kernel<<<dim3(nblk, c->B * c->Hkv), kTcBlock, kTcSmem, s>>>(tq, tk, nlse2, c->Hq, c->Hkv, T,
                                                                              scores_full, scores_head);
     return check_launch("col_sum_tc_kernel");
   }
