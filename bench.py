@@ -51,6 +51,8 @@ def parse():
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-attn-events", action="store_true",
                    help="do not time the attention kernel alone (roofline from the whole step)")
+    p.add_argument("--no-perturbation", action="store_true",
+                   help="skip the timing of the step after attention (o . W_O and the perturbation)")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     return p.parse_args()
 
@@ -346,6 +348,34 @@ def run_gpu(args, wl, rank, world):
         torch.cuda.synchronize()
         e2e_ms = max(e0.elapsed_time(e1), (time.perf_counter() - t0) * 1e3)
         res.update(e2e_ms=e2e_ms, e2e_tokens=e2e_tokens * world, h2d=h2d, d2h=d2h)
+
+    # ---- the step after attention: y = o . W_O and the per-head perturbation between two
+    # attention outputs of the workload's shape, one call (3 launches) timed alone with the L2
+    # flushed before each call (W_O fits in L2)
+    if not args.no_perturbation:
+        g = torch.Generator(device=dev).manual_seed(rank_seed(wl, rank).seed + 91)
+        o = 0.3 * torch.randn(wl.B, wl.Hq, wl.D, device=dev, generator=g)
+        oh = o + 0.01 * torch.randn(wl.B, wl.Hq, wl.D, device=dev, generator=g)
+        w_t = inputs.make_w_o(rank_seed(wl, rank), 0, dev).t().contiguous()   # [hidden][Hq*D]
+        hidden = w_t.shape[0]
+        y = torch.empty(wl.B, hidden, device=dev)
+        pert = torch.empty(wl.B, wl.Hq, device=dev)
+        ws = torch.empty(_lib.load().mikv_output_perturbation_workspace_bytes(wl.B, wl.Hq, hidden),
+                         dtype=torch.uint8, device=dev)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+        for i in range(3 + len(pev)):
+            flush.zero_()
+            if i >= 3:
+                pev[i - 3][0].record()
+            _lib.mikv_output_perturbation(o, oh, w_t, y=y, pert=pert, ws=ws)
+            if i >= 3:
+                pev[i - 3][1].record()
+        torch.cuda.synchronize()
+        p_ms = statistics.mean(a.elapsed_time(b) for a, b in pev)
+        p_bytes = hidden * wl.Hq * wl.D * 2 + 2 * wl.B * wl.Hq * wl.D * 4 + wl.B * hidden * 4 + wl.B * wl.Hq * 4
+        res.update(pert_ms=p_ms, pert_bytes=p_bytes, pert_hidden=hidden)
+        del flush, ws
     return res
 
 
@@ -444,6 +474,14 @@ def main():
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
     }
+    if "pert_ms" in res:
+        gbs = res["pert_bytes"] / (res["pert_ms"] / 1e3) / 1e9
+        line["output_perturbation"] = {
+            "what": "y = o . W_O and per-head ||(o - o_hat) . W_O^(h)||_1 (prep, tcgen05 product, reduce)",
+            "shape": {"batch": wl.B, "q_heads": wl.Hq, "head_dim": wl.D, "hidden": res["pert_hidden"]},
+            "us_per_call": res["pert_ms"] * 1e3, "launches_per_call": 3,
+            "bytes_per_call": res["pert_bytes"], "gbs": gbs, "frac_of_hbm_peak": gbs / peak,
+            "timing": "CUDA events around each of 20 calls, L2 flushed (256 MB write) before each"}
     if "e2e_ms" in res:
         line["e2e"] = {"value": res["e2e_tokens"] / (res["e2e_ms"] / 1e3), "unit": "KV-tokens/s",
                        "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]}

@@ -273,6 +273,30 @@ int mikv_decode_step(const uint16_t* q, const uint16_t* k_new, const uint16_t* v
 size_t mikv_decode_step_workspace_bytes(const mikv_cache* c);
 
 /*
+ * K9: the step after attention ([criticalkv] "Theoretical framework": the output
+ * perturbation L = ||o - o^||_1 of replacing the full cache, bounded through the value
+ * states projected by W_O; "Experimental results": reported per attention head).
+ * Head h reaches the hidden state through rows h*D .. h*D + D - 1 of W_O:
+ *   y[b][:]  = sum_h o[b][h][:] . W_O^(h)                      (the output projection)
+ *   pert[b][h] = || (o[b][h][:] - o_hat[b][h][:]) . W_O^(h) ||_1  (sum over hidden)
+ * o, o_hat fp32 [B][Hq][D] (D = 128): e.g. decode attention over the full cache and over
+ * the mixed-precision (or evicted) cache.  w_o_t fp16 [hidden][Hq*D], row-major: W_O
+ * transposed, the layout nn.Linear stores; hidden % 64 == 0; 16-byte aligned.
+ * y fp32 [B][hidden] (16-byte aligned) is written if not NULL; pert fp32 [B][Hq] if not
+ * NULL (needs o_hat).  With w_o_t == NULL, pert[b][h] = || o - o_hat ||_1 over D (y must
+ * be NULL).  Products are formed from fp16 (hi, lo) splits of o and o - o_hat with fp32
+ * accumulation (relative error ~1e-6).
+ * ws >= mikv_output_perturbation_workspace_bytes(B, Hq, hidden), 16-byte aligned
+ * (operand tiles and per-column partial sums).  Stream-ordered; no synchronisation.
+ * Errors: EINVAL (null o, pert without o_hat, y without w_o_t, null ws), EUNSUPPORTED (D),
+ * ESHAPE (B < 1, Hq outside 1..128, hidden, workspace), EALIGN, ECUDA.
+ */
+int mikv_output_perturbation(const float* o, const float* o_hat, const uint16_t* w_o_t, int B, int Hq,
+                             int D, int hidden, float* y, float* pert, void* ws, size_t ws_bytes,
+                             void* stream);
+size_t mikv_output_perturbation_workspace_bytes(int B, int Hq, int hidden);
+
+/*
  * Measurement hook (no counterpart in the papers): while set, every
  * mikv_decode_attention and mikv_decode_step call made by this thread records
  * `begin` (a cudaEvent_t) on its stream just before the split-K attention

@@ -24,6 +24,7 @@ EXPORTS = (
     "mikv_quantize_append",
     "mikv_decode_attention", "mikv_decode_workspace_bytes",
     "mikv_decode_step", "mikv_decode_step_workspace_bytes",
+    "mikv_output_perturbation", "mikv_output_perturbation_workspace_bytes",
     "mikv_set_attention_events", "mikv_last_error",
 )
 
@@ -76,6 +77,8 @@ def load() -> ctypes.CDLL:
         "mikv_decode_workspace_bytes": (S, [CP]),
         "mikv_decode_step": (I, [P, P, P, I, I, I, I, CP, P, P, P, S, P]),
         "mikv_decode_step_workspace_bytes": (S, [CP]),
+        "mikv_output_perturbation": (I, [P, P, P, I, I, I, I, P, P, P, S, P]),
+        "mikv_output_perturbation_workspace_bytes": (S, [I, I, I]),
         "mikv_set_attention_events": (I, [P, P]),
         "mikv_last_error": (ctypes.c_char_p, []),
     }
@@ -183,6 +186,19 @@ def mikv_decode_step(q, k_new, v_new, pos, budget_pct, window, policy, cache, ou
     _check("mikv_decode_step", lib.mikv_decode_step(
         _ptr(q), _ptr(k_new), _ptr(v_new), pos, budget_pct, window, policy, ctypes.byref(c),
         _ptr(out), _ptr(lse), _ptr(w), nb, _stream(stream)))
+
+
+def mikv_output_perturbation(o, o_hat=None, w_o_t=None, y=None, pert=None, ws=None, stream=None):
+    """o, o_hat fp32 [B][Hq][D]; w_o_t fp16 [hidden][Hq*D] (W_O transposed, nn.Linear layout);
+    y fp32 [B][hidden] and / or pert fp32 [B][Hq] are written."""
+    lib = load()
+    B, Hq, D = o.shape
+    hidden = 0 if w_o_t is None else w_o_t.shape[0]
+    w, nb = (None, 0) if w_o_t is None else _ws(lib.mikv_output_perturbation_workspace_bytes(B, Hq, hidden),
+                                                o.device, ws)
+    _check("mikv_output_perturbation", lib.mikv_output_perturbation(
+        _ptr(o), _ptr(o_hat), _ptr(w_o_t), B, Hq, D, hidden, _ptr(y), _ptr(pert), _ptr(w), nb,
+        _stream(stream)))
 
 
 def mikv_set_attention_events(begin=None, end=None):

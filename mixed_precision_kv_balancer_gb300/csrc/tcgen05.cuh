@@ -191,6 +191,89 @@ __device__ __forceinline__ uint32_t cta_setup(Bars& bar, uint32_t* tslot, int co
   fence_after_sync();
   return *tslot;
 }
+// ---------------------------------------------------------------------------------
+// Ring pipeline of the warp-specialised kernels: resident operand tiles plus a stream of
+// operand tiles through R shared-memory buffers, and NACC TMEM accumulators.  One producer
+// lane issues the TMA copies and the MMAs; step s reads buffer s % R and writes accumulator
+// s % NACC; consumer threads read each accumulator and release it.
+//   full[b]   buffer b landed (TMA transaction bytes)
+//   empty[b]  the MMAs that read buffer b are done (tcgen05.commit)
+//   mma[a]    accumulator a written (tcgen05.commit)
+//   freed[a]  accumulator a read by its consumers (`consumers` arrivals)
+//   fixed     the resident tiles landed
+template <int R, int NACC>
+struct Ring {
+  uint64_t full[R], empty[R], mma[NACC], freed[NACC], fixed;
+};
+
+// mbarriers and the TMEM allocation (`cols` columns); returns the TMEM base.  Every thread
+// of the CTA calls it (it holds a barrier).
+template <int R, int NACC>
+__device__ __forceinline__ uint32_t ring_setup(Ring<R, NACC>& r, uint32_t* tslot, int consumers, uint32_t cols) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < R; ++i) {
+      mbar_init(smem_u32(&r.full[i]), 1);
+      mbar_init(smem_u32(&r.empty[i]), 1);
+    }
+    for (int i = 0; i < NACC; ++i) {
+      mbar_init(smem_u32(&r.mma[i]), 1);
+      mbar_init(smem_u32(&r.freed[i]), consumers);
+    }
+    mbar_init(smem_u32(&r.fixed), 1);
+    mbar_init_fence();
+  }
+  if (threadIdx.x < 32) tmem_alloc(smem_u32(tslot), cols);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  return *tslot;
+}
+
+// The producer lane, steps 0 .. nsteps-1.  load(s, b, mbar) issues step s's copies into
+// buffer b with their expect_tx on mbar; mma(s, b, a) issues its MMAs from buffer b into
+// accumulator a.  Step s's MMAs go out once its buffer landed and its accumulator's
+// previous step (s - NACC) was released; then the buffer of step s - 1 is refilled with step
+// s - 1 + R as soon as step s - 1's MMAs are done (step s's already queue behind them), so a
+// copy has R - 1 MMA durations to land.  The resident tiles are awaited on `fixed` before
+// the first MMA, and the last MMAs before returning, so no arrival is left in flight when
+// the CTA retires.  False if a wait gave up.
+template <int R, int NACC, class Load, class Mma>
+__device__ __forceinline__ bool ring_produce(Ring<R, NACC>& r, int nsteps, Load load, Mma mma) {
+  bool ok = true;
+  for (int s = 0; s < nsteps && s < R; ++s) load(s, s, smem_u32(&r.full[s]));
+  ok = mbar_wait(smem_u32(&r.fixed), 0) && ok;
+  for (int s = 0; s < nsteps; ++s) {
+    const int b = s % R, a = s % NACC;
+    ok = mbar_wait(smem_u32(&r.full[b]), (s / R) & 1) && ok;
+    if (s >= NACC) ok = mbar_wait(smem_u32(&r.freed[a]), (s / NACC - 1) & 1) && ok;
+    fence_after_sync();
+    mma(s, b, a);
+    commit(smem_u32(&r.mma[a]));
+    commit(smem_u32(&r.empty[b]));
+    const int p = s - 1;
+    if (p >= 0 && p + R < nsteps) {
+      ok = mbar_wait(smem_u32(&r.empty[p % R]), (p / R) & 1) && ok;
+      load(p + R, p % R, smem_u32(&r.full[p % R]));
+    }
+  }
+  for (int s = nsteps > R ? nsteps - R : 0; s < nsteps; ++s)  // buffers never refilled
+    ok = mbar_wait(smem_u32(&r.empty[s % R]), (s / R) & 1) && ok;
+  return ok;
+}
+
+// Consumer side of step s: wait for its accumulator; release it after the last tcgen05.ld.
+template <int R, int NACC>
+__device__ __forceinline__ bool ring_acquire(Ring<R, NACC>& r, int s) {
+  const bool ok = mbar_wait(smem_u32(&r.mma[s % NACC]), (s / NACC) & 1);
+  fence_after_sync();
+  return ok;
+}
+template <int R, int NACC>
+__device__ __forceinline__ void ring_release(Ring<R, NACC>& r, int s) {
+  fence_before_sync();
+  mbar_arrive(smem_u32(&r.freed[s % NACC]));
+}
+
 // Every thread of the CTA calls it after its last TMEM access.
 __device__ __forceinline__ void cta_teardown(uint32_t tbase, uint32_t cols) {
   fence_before_sync();
@@ -202,7 +285,7 @@ __device__ __forceinline__ uint32_t smem_base(uint8_t* sm) { return (smem_u32(sm
 
 // ---------------------------------------------------------------------------------
 // Host: 2-D tensor map of a row-major [rows][cols] fp16 matrix (cols a multiple of 64)
-// with a 64-column x 128-row box and 128-byte swizzle, through the driver's encoder
+// with a 64-column x box_rows box (128 by default) and 128-byte swizzle, through the driver's encoder
 // (looked up once).  `what` names the caller in the error message.
 inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -218,12 +301,13 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   });
   return fn;
 }
-inline int encode_rows(CUtensorMap* map, const void* base, long rows, const char* what, long cols = kD) {
+inline int encode_rows(CUtensorMap* map, const void* base, long rows, const char* what, long cols = kD,
+                       int box_rows = kTileRows) {
   const auto enc = tensor_map_encoder();
   if (!enc) return fail(MIKV_ECUDA, "%s: cuTensorMapEncodeTiled unavailable", what);
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTileRows)};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides,
                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -53,6 +53,10 @@ def test_workspace_queries(lib):
     assert lib.mikv_score_workspace_bytes(1, 4, 100) >= 4 * 100 * 4
     assert lib.mikv_select_workspace_bytes(0, 1, 8, 40, 1000, 5120) == 0      # H2O needs none
     assert lib.mikv_select_workspace_bytes(1, 1, 8, 40, 1000, 5120) >= 8 * 1000 * 4
+    # operand tiles (32 KB per head and 32-row batch block) + per-column partial sums
+    assert lib.mikv_output_perturbation_workspace_bytes(64, 32, 4096) >= 32 * 2 * 32768 + 64 * 32 * 128 * 4
+    assert lib.mikv_output_perturbation_workspace_bytes(1, 40, 5120) >= 40 * 32768 + 40 * 160 * 4
+    assert lib.mikv_output_perturbation_workspace_bytes(1, 4, 32) == 0        # hidden below one column block
     c = _cache(cap_hi=1000, cap_lo=4000)
     assert lib.mikv_decode_workspace_bytes(ctypes.byref(c)) > 0
     bad = _cache(D=64)
@@ -94,6 +98,17 @@ def test_host_side_rejections(lib):
                            None, fake, None, None, 0, None) == ESHAPE     # n_hi <= window
     assert lib.mikv_score_update(9, None, None, 0, None, None, ctypes.byref(_cache()), None, None,
                                  None, 0, None) == EINVAL
+    # the step after attention
+    op = lib.mikv_output_perturbation
+    assert op(None, None, None, 1, 4, 128, 128, None, fake, None, 0, None) == EINVAL      # null o
+    assert op(fake, None, fake, 1, 4, 128, 128, None, fake, fake, 1 << 20, None) == EINVAL  # pert needs o_hat
+    assert op(fake, fake, None, 1, 4, 128, 128, fake, None, None, 0, None) == EINVAL      # y needs w_o_t
+    assert op(fake, fake, fake, 1, 4, 64, 128, fake, fake, fake, 1 << 20, None) == EUNSUP
+    assert op(fake, fake, fake, 0, 4, 128, 128, fake, fake, fake, 1 << 20, None) == ESHAPE
+    assert op(fake, fake, fake, 1, 4, 128, 96, fake, fake, fake, 1 << 20, None) == ESHAPE  # hidden % 64
+    assert op(fake, fake, fake, 1, 4, 128, 128, fake, fake, fake, 64, None) == ESHAPE      # workspace
+    assert op(fake, fake, ctypes.c_void_p(4098), 1, 4, 128, 128, fake, fake, fake, 1 << 20, None) == EALIGN
+    assert op(fake, fake, fake, 1, 4, 128, 128, None, None, None, 0, None) == 0            # nothing asked
     # the attention timing hook takes both events or neither
     assert lib.mikv_set_attention_events(fake, None) == EINVAL
     assert lib.mikv_set_attention_events(None, fake) == EINVAL
