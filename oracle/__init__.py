@@ -23,7 +23,7 @@ balance    channel balancer b = sqrt(max|q| / max|k|) (MiKV notes, "Outlier-awar
 quant      per-token asymmetric group quantizer, bit packing
 scores     H2O accumulated attention (prefill column sums, decode update)
 select     H2O top-k with recent window, CriticalKV two-stage, demotion victim
-attention  decode attention over the two-tier cache (float64)
+attention  decode attention over the two-tier cache (float64); post-attention top-k ("oracle eviction")
 perturbation  the step after attention: o . W_O and the CriticalKV per-head perturbation
 pipeline   prefill + decode steps composed into one cache, the whole path
 

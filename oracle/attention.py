@@ -60,3 +60,35 @@ def decode_attention_unit(q: np.ndarray, hi: dict, lo: dict, b: np.ndarray | Non
     out = (p @ np.concatenate([v_hi, v_lo], axis=0)) / s
     lse = (m + np.log(s))[:, 0]
     return out, lse, l_hi
+
+
+def topk_count(L: int, budget_pct: int) -> int:
+    """Tokens kept per query head by the post-attention top-k: max(1, floor(p * L / 100))."""
+    return max(1, budget_pct * L // 100)
+
+
+def topk_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, keep: int, select_logits=None):
+    """Post-attention top-k over a full-precision cache, one query head.
+
+    Source: MiKV reading notes (velog), "1-4) Quantitative analysis": the oracle-eviction
+    simulation computes the attention map over the full cache first and applies top-k
+    sparsity after the attention, an upper-bound proxy for knowing which past KV pairs
+    matter for the token being generated.
+    Reading: the kept tokens are the `keep` largest attention weights of this query head
+    (equivalently the largest logits), ties to the lower index; the output is attention
+    over the kept tokens alone (softmax renormalised over them, as if the rest had been
+    evicted).  `select_logits` (default: this function's own float64 logits) is what the
+    selection ranks, so a test can take the decision in the kernel's precision.
+
+    q [D], k [L][D], v [L][D] (fp16 or float) -> (out [D], lse, kept indices ascending), float64.
+    """
+    D = q.shape[0]
+    logits = (k.astype(np.float64) @ q.astype(np.float64)) / np.sqrt(D)
+    key = logits if select_logits is None else np.asarray(select_logits)
+    order = sorted(range(len(key)), key=lambda i: (-float(key[i]), i))
+    kept = np.array(sorted(order[:keep]), dtype=np.int64)
+    lk = logits[kept]
+    m = lk.max()
+    w = np.exp(lk - m)
+    out = (w @ v.astype(np.float64)[kept]) / w.sum()
+    return out, m + np.log(w.sum()), kept
