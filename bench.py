@@ -19,6 +19,7 @@ the same workload (the slow, obviously-correct restatement the parity tests use)
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import math
 import os
@@ -53,6 +54,8 @@ def parse():
                    help="do not time the attention kernel alone (roofline from the whole step)")
     p.add_argument("--no-perturbation", action="store_true",
                    help="skip the timing of the step after attention (o . W_O and the perturbation)")
+    p.add_argument("--no-topk", action="store_true",
+                   help="skip the timing of the post-attention top-k over a full FP16 cache")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     return p.parse_args()
 
@@ -376,6 +379,38 @@ def run_gpu(args, wl, rank, world):
         p_bytes = hidden * wl.Hq * wl.D * 2 + 2 * wl.B * wl.Hq * wl.D * 4 + wl.B * hidden * 4 + wl.B * wl.Hq * 4
         res.update(pert_ms=p_ms, pert_bytes=p_bytes, pert_hidden=hidden)
         del flush, ws
+
+    # ---- post-attention top-k (the pages' oracle-eviction simulation) over one layer of the
+    # workload kept whole in FP16: decode attention for every logit, per-head top-k at the
+    # workload's budget, attention over the kept slots; 20 calls timed alone (the cache is
+    # larger than L2)
+    if not args.no_topk:
+        full = MikvCache(wl.B, wl.Hq, wl.Hkv, wl.D, 16, wl.lo_bits, wl.T + 1, 1, dev)
+        x = inputs.make_prefill(rank_seed(wl, rank), 0, dev)
+        full.prefill(x["q"], x["k"], x["v"], 100, 0)
+        del x
+        torch.cuda.empty_cache()
+        qf = toks[0][0]["q"]
+        k_keep = max(1, wl.budget_pct * wl.T // 100)
+        out_t = torch.empty(wl.B, wl.Hq, wl.D, device=dev)
+        lse_t = torch.empty(wl.B, wl.Hq, device=dev)
+        ws = torch.empty(_lib.load().mikv_topk_attention_workspace_bytes(ctypes.byref(full.struct), wl.budget_pct),
+                         dtype=torch.uint8, device=dev)
+        tev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+        for i in range(3 + len(tev)):
+            if i >= 3:
+                tev[i - 3][0].record()
+            _lib.mikv_topk_attention(qf, full, wl.budget_pct, out_t, lse=lse_t, ws=ws)
+            if i >= 3:
+                tev[i - 3][1].record()
+        torch.cuda.synchronize()
+        t_ms = statistics.mean(a.elapsed_time(b) for a, b in tev)
+        # K and V once, every logit written and read back by the selection, the kept V rows
+        t_bytes = (wl.B * wl.Hkv * wl.T * wl.D * 2 * 2 + 2 * wl.B * wl.Hq * wl.T * 4
+                   + wl.B * wl.Hq * k_keep * wl.D * 2)
+        res.update(topk_ms=t_ms, topk_bytes=t_bytes, topk_k=k_keep)
+        del full, ws
+        torch.cuda.empty_cache()
     return res
 
 
@@ -482,6 +517,14 @@ def main():
             "us_per_call": res["pert_ms"] * 1e3, "launches_per_call": 3,
             "bytes_per_call": res["pert_bytes"], "gbs": gbs, "frac_of_hbm_peak": gbs / peak,
             "timing": "CUDA events around each of 20 calls, L2 flushed (256 MB write) before each"}
+    if "topk_ms" in res:
+        gbs = res["topk_bytes"] / (res["topk_ms"] / 1e3) / 1e9
+        line["topk_attention"] = {
+            "what": "post-attention top-k over one layer kept whole in FP16 (decode attention for all "
+                    "logits, per-head radix select, attention over the kept slots)",
+            "kept_per_head": res["topk_k"], "us_per_call": res["topk_ms"] * 1e3, "launches_per_call": 5,
+            "bytes_per_call": res["topk_bytes"], "gbs": gbs, "frac_of_hbm_peak": gbs / peak,
+            "timing": "CUDA events around each of 20 calls (cache larger than L2)"}
     if "e2e_ms" in res:
         line["e2e"] = {"value": res["e2e_tokens"] / (res["e2e_ms"] / 1e3), "unit": "KV-tokens/s",
                        "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]}

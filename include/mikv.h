@@ -297,6 +297,26 @@ int mikv_output_perturbation(const float* o, const float* o_hat, const uint16_t*
 size_t mikv_output_perturbation_workspace_bytes(int B, int Hq, int hidden);
 
 /*
+ * Post-attention top-k over the full cache ([notes] "1-4) Quantitative analysis": the
+ * oracle-eviction simulation computes the attention map over the full cache first and
+ * applies top-k sparsity after the attention, an upper-bound proxy for eviction).
+ * c must hold the full cache in its FP16 tier (hi_bits 16, n_lo 0, n_hi = L >= 1 tokens,
+ * e.g. a prefill at budget 100).  Per (batch, query head) the k = max(1, floor(p*L/100))
+ * largest logits q.k/sqrt(D) are kept (ties to the lower slot) and
+ *   out[b][h] = sum_{i kept} exp(l_i - m) v_i / sum_{i kept} exp(l_i - m),
+ *   lse[b][h] = log sum_{i kept} exp(l_i)            (natural log; written if not NULL),
+ *   keep_idx [B][Hq][k] int32 = the kept slots, ascending (written if not NULL).
+ * q fp16 [B][Hq][D]; out fp32 [B][Hq][D].  Three stages, stream-ordered: the decode attention
+ * of this cache (all logits), a radix select per head, attention over the kept slots.
+ * ws >= mikv_topk_attention_workspace_bytes(c, budget_pct), 16-byte aligned.
+ * Errors: EINVAL (null), EUNSUPPORTED (not a full FP16 cache), ESHAPE (budget, heads,
+ * n_hi outside 1..131072, workspace), and those of mikv_decode_attention.
+ */
+int mikv_topk_attention(const uint16_t* q, const mikv_cache* c, int budget_pct, float* out, float* lse,
+                        int32_t* keep_idx, void* ws, size_t ws_bytes, void* stream);
+size_t mikv_topk_attention_workspace_bytes(const mikv_cache* c, int budget_pct);
+
+/*
  * Measurement hook (no counterpart in the papers): while set, every
  * mikv_decode_attention and mikv_decode_step call made by this thread records
  * `begin` (a cudaEvent_t) on its stream just before the split-K attention

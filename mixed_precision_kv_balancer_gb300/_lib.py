@@ -25,6 +25,7 @@ EXPORTS = (
     "mikv_decode_attention", "mikv_decode_workspace_bytes",
     "mikv_decode_step", "mikv_decode_step_workspace_bytes",
     "mikv_output_perturbation", "mikv_output_perturbation_workspace_bytes",
+    "mikv_topk_attention", "mikv_topk_attention_workspace_bytes",
     "mikv_set_attention_events", "mikv_last_error",
 )
 
@@ -79,6 +80,8 @@ def load() -> ctypes.CDLL:
         "mikv_decode_step_workspace_bytes": (S, [CP]),
         "mikv_output_perturbation": (I, [P, P, P, I, I, I, I, P, P, P, S, P]),
         "mikv_output_perturbation_workspace_bytes": (S, [I, I, I]),
+        "mikv_topk_attention": (I, [P, CP, I, P, P, P, P, S, P]),
+        "mikv_topk_attention_workspace_bytes": (S, [CP, I]),
         "mikv_set_attention_events": (I, [P, P]),
         "mikv_last_error": (ctypes.c_char_p, []),
     }
@@ -198,6 +201,16 @@ def mikv_output_perturbation(o, o_hat=None, w_o_t=None, y=None, pert=None, ws=No
                                                 o.device, ws)
     _check("mikv_output_perturbation", lib.mikv_output_perturbation(
         _ptr(o), _ptr(o_hat), _ptr(w_o_t), B, Hq, D, hidden, _ptr(y), _ptr(pert), _ptr(w), nb,
+        _stream(stream)))
+
+
+def mikv_topk_attention(q, cache, budget_pct, out, lse=None, keep_idx=None, ws=None, stream=None):
+    """Post-attention top-k over a full FP16 cache (all tokens in the important tier)."""
+    lib = load()
+    c = cache.struct if hasattr(cache, "struct") else cache
+    w, nb = _ws(lib.mikv_topk_attention_workspace_bytes(ctypes.byref(c), budget_pct), q.device, ws)
+    _check("mikv_topk_attention", lib.mikv_topk_attention(
+        _ptr(q), ctypes.byref(c), budget_pct, _ptr(out), _ptr(lse), _ptr(keep_idx), _ptr(w), nb,
         _stream(stream)))
 
 

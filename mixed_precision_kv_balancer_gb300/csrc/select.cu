@@ -122,15 +122,16 @@ __device__ void topk_mark(const float* __restrict__ key, int L, int take, uint8_
 }
 
 // One CTA per (batch, key head).  flag: 0 evicted, 1 taken by a stage, 2 recent window.
+// key1 rows are `stride1` floats apart (L for the score arrays, the slot capacity for logits).
 __global__ void __launch_bounds__(kSelThreads) select_kernel(
-    const float* __restrict__ key1, const float* __restrict__ key2, int L, int window, int take1,
-    int take2, int n_keep, int32_t* __restrict__ keep_pos, int32_t* __restrict__ evict_pos,
+    const float* __restrict__ key1, long stride1, const float* __restrict__ key2, int L, int window,
+    int take1, int take2, int n_keep, int32_t* __restrict__ keep_pos, int32_t* __restrict__ evict_pos,
     float* __restrict__ keep_scores) {
   extern __shared__ uint8_t flag[];
   __shared__ unsigned hist[256];
   __shared__ int scratch[2 + 32];
   const long unit = blockIdx.x;
-  const float* k1 = key1 + unit * L;
+  const float* k1 = key1 + unit * stride1;
   const int w = min(window, L);
   for (int i = threadIdx.x; i < L; i += blockDim.x) flag[i] = (i >= L - w) ? 2 : 0;
   __syncthreads();
@@ -339,6 +340,83 @@ __global__ void __launch_bounds__(kVwoBlock, 2) vwo_norm_tc_kernel(const __grid_
     for (int hr = 0; hr < rep; ++hr) out[(static_cast<long>(b) * Hq + g * rep + hr) * L + i] = __int_as_float(0x7fc00000);
 }
 
+// ---------------------------------------------------------------------------------
+// Post-attention top-k over the full cache (MiKV reading notes, "1-4) Quantitative
+// analysis": the oracle-eviction simulation computes the attention map over the full cache
+// first and applies top-k sparsity after it, an upper-bound proxy).  Reading: per query head
+// the k = max(1, floor(p * L / 100)) largest logits (ties to the lower slot) are kept and the
+// output is attention over them alone, the softmax renormalised over the kept set.
+// topk_attend_kernel: one CTA per (batch, query head), one thread per channel: the max of
+// the kept logits, then the kept tokens in chunks (weights exp(l - m) and slot indices in
+// shared memory; each thread adds w * v[slot][d], one coalesced 256-byte row per token).
+constexpr int kTkChunk = 1024;
+
+__global__ void __launch_bounds__(kD) topk_attend_kernel(const float* __restrict__ logits, int cap,
+                                                        const int32_t* __restrict__ keep, int k,
+                                                        const __half* __restrict__ v, int Hq, int Hkv,
+                                                        float* __restrict__ out, float* __restrict__ lse) {
+  __shared__ float w[kTkChunk];
+  __shared__ int idx[kTkChunk];
+  __shared__ float red[kD / 32];
+  const int bh = blockIdx.x, b = bh / Hq, h = bh % Hq, g = h / (Hq / Hkv);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float* lg = logits + static_cast<long>(bh) * cap;
+  const int32_t* kp = keep + static_cast<long>(bh) * k;
+  const __half* vb = v + static_cast<long>(b * Hkv + g) * cap * kD;
+  float m = -INFINITY;
+  for (int j = tid; j < k; j += kD) m = fmaxf(m, lg[kp[j]]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  m = red[0];
+#pragma unroll
+  for (int i = 1; i < kD / 32; ++i) m = fmaxf(m, red[i]);
+  __syncthreads();
+  float acc = 0.f, tsum = 0.f;
+  for (int c0 = 0; c0 < k; c0 += kTkChunk) {
+    const int n = min(kTkChunk, k - c0);
+    for (int j = tid; j < n; j += kD) {
+      const int i = kp[c0 + j];
+      const float e = expf(lg[i] - m);
+      w[j] = e;
+      idx[j] = i;
+      tsum += e;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int j = 0; j < n; ++j) acc = fmaf(w[j], __half2float(vb[static_cast<long>(idx[j]) * kD + tid]), acc);
+    __syncthreads();
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) tsum += __shfl_xor_sync(0xffffffffu, tsum, off);
+  if (lane == 0) red[warp] = tsum;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int i = 0; i < kD / 32; ++i) tot += red[i];
+  out[static_cast<long>(bh) * kD + tid] = acc / tot;
+  if (tid == 0 && lse) lse[bh] = m + logf(tot);
+}
+
+int topk_count(int L, int budget_pct) { return std::max(1, static_cast<int>(static_cast<long>(budget_pct) * L / 100)); }
+
+struct TopkWs {
+  size_t dec, out, lse, logits, keep, evict, total;
+};
+TopkWs topk_ws_layout(const mikv_cache* c, int k) {
+  const size_t bh = static_cast<size_t>(c->B) * c->Hq;
+  TopkWs t;
+  t.dec = 0;
+  t.out = align_up(mikv_decode_workspace_bytes(c), 256);
+  t.lse = t.out + align_up(bh * kD * sizeof(float), 256);
+  t.logits = t.lse + align_up(bh * sizeof(float), 256);
+  t.keep = t.logits + align_up(bh * c->cap_hi * sizeof(float), 256);
+  t.evict = t.keep + align_up(bh * k * sizeof(int32_t), 256);
+  t.total = t.evict + align_up(bh * (c->n_hi - k) * sizeof(int32_t), 256);
+  return t;
+}
+
 }  // namespace
 }  // namespace mikv
 
@@ -424,7 +502,47 @@ extern "C" int mikv_select(int policy, const mikv_cache* c, int L, int budget_pc
   }
   if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L) != cudaSuccess)
     return check_launch("select_kernel attribute");
-  select_kernel<<<units, kSelThreads, L, s>>>(scores, key2, L, window, take1, take2, n_keep,
+  select_kernel<<<units, kSelThreads, L, s>>>(scores, L, key2, L, window, take1, take2, n_keep,
                                                keep_pos, evict_pos, keep_scores);
   return check_launch("select_kernel");
+}
+
+extern "C" size_t mikv_topk_attention_workspace_bytes(const mikv_cache* c, int budget_pct) {
+  if (!c || c->n_hi < 1 || c->B < 1 || c->Hq < 1 || budget_pct < 0 || budget_pct > 100) return 0;
+  return topk_ws_layout(c, topk_count(c->n_hi, budget_pct)).total;
+}
+
+extern "C" int mikv_topk_attention(const uint16_t* q, const mikv_cache* c, int budget_pct, float* out, float* lse,
+                                   int32_t* keep_idx, void* ws, size_t ws_bytes, void* stream) {
+  clear_error();
+  if (!c) return fail(MIKV_EINVAL, "topk_attention: null cache");
+  if (!q || !out || !ws) return fail(MIKV_EINVAL, "topk_attention: null pointer");
+  if (c->hi_bits != 16 || c->n_lo != 0)
+    return fail(MIKV_EUNSUPPORTED, "topk_attention: needs the full FP16 cache (hi_bits=%d, n_lo=%d)", c->hi_bits, c->n_lo);
+  if (budget_pct < 0 || budget_pct > 100) return fail(MIKV_ESHAPE, "topk_attention: budget_pct=%d", budget_pct);
+  const int L = c->n_hi;
+  if (L < 1 || L > kMaxSelectL) return fail(MIKV_ESHAPE, "topk_attention: n_hi=%d (1..%d)", L, kMaxSelectL);
+  if (c->B < 1 || c->Hkv < 1 || c->Hq < c->Hkv || c->Hq % c->Hkv) return fail(MIKV_ESHAPE, "topk_attention: bad heads");
+  const int k = topk_count(L, budget_pct);
+  const TopkWs t = topk_ws_layout(c, k);
+  if (ws_bytes < t.total) return fail(MIKV_ESHAPE, "topk_attention: workspace %zu < %zu", ws_bytes, t.total);
+  char* w = static_cast<char*>(ws);
+  float* full_out = reinterpret_cast<float*>(w + t.out);
+  float* full_lse = reinterpret_cast<float*>(w + t.lse);
+  float* logits = reinterpret_cast<float*>(w + t.logits);
+  int32_t* keep = keep_idx ? keep_idx : reinterpret_cast<int32_t*>(w + t.keep);
+  int32_t* evict = reinterpret_cast<int32_t*>(w + t.evict);
+  // 1. the full attention map: every logit of the cache (and the full-cache output)
+  if (int e = mikv_decode_attention(q, c, full_out, full_lse, logits, w + t.dec, t.out, stream)) return e;
+  cudaStream_t s = as_stream(stream);
+  const int units = c->B * c->Hq;
+  // 2. per query head, the k largest logits (ties to the lower slot), slots ascending
+  if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L) != cudaSuccess)
+    return check_launch("select_kernel attribute");
+  select_kernel<<<units, kSelThreads, L, s>>>(logits, c->cap_hi, nullptr, L, 0, k, 0, k, keep, evict, nullptr);
+  if (int e = check_launch("select_kernel")) return e;
+  // 3. attention over the kept tokens alone
+  topk_attend_kernel<<<units, kD, 0, s>>>(logits, c->cap_hi, keep, k, reinterpret_cast<const __half*>(c->v_hi),
+                                          c->Hq, c->Hkv, out, lse);
+  return check_launch("topk_attend_kernel");
 }

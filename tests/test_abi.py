@@ -109,6 +109,17 @@ def test_host_side_rejections(lib):
     assert op(fake, fake, fake, 1, 4, 128, 128, fake, fake, fake, 64, None) == ESHAPE      # workspace
     assert op(fake, fake, ctypes.c_void_p(4098), 1, 4, 128, 128, fake, fake, fake, 1 << 20, None) == EALIGN
     assert op(fake, fake, fake, 1, 4, 128, 128, None, None, None, 0, None) == 0            # nothing asked
+    # post-attention top-k needs the full FP16 cache
+    tk = lib.mikv_topk_attention
+    c = _cache(n_hi=4)
+    assert tk(None, ctypes.byref(c), 20, fake, None, None, fake, 1 << 20, None) == EINVAL
+    assert tk(fake, ctypes.byref(_cache(n_hi=4, n_lo=2)), 20, fake, None, None, fake, 1 << 20, None) == EUNSUP
+    assert tk(fake, ctypes.byref(_cache(n_hi=4, hi_bits=8)), 20, fake, None, None, fake, 1 << 20, None) == EUNSUP
+    assert tk(fake, ctypes.byref(c), 101, fake, None, None, fake, 1 << 20, None) == ESHAPE
+    assert tk(fake, ctypes.byref(_cache()), 20, fake, None, None, fake, 1 << 20, None) == ESHAPE   # n_hi 0
+    assert tk(fake, ctypes.byref(c), 20, fake, None, None, fake, 16, None) == ESHAPE             # workspace
+    assert lib.mikv_topk_attention_workspace_bytes(ctypes.byref(c), 20) > 0
+    assert lib.mikv_topk_attention_workspace_bytes(ctypes.byref(_cache()), 20) == 0
     # the attention timing hook takes both events or neither
     assert lib.mikv_set_attention_events(fake, None) == EINVAL
     assert lib.mikv_set_attention_events(None, fake) == EINVAL
