@@ -83,14 +83,37 @@ __device__ void topk_mark(const float* __restrict__ key, int L, int take, uint8_
       if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
     }
     __syncthreads();
-    if (tid == 0) {
-      int above = 0, d = 255;
-      for (; d > 0; --d) {
-        if (above + static_cast<int>(hist[d]) >= remaining) break;
-        above += hist[d];
+    // the digit d where the count of candidates in bins above d first reaches `remaining`
+    // (scanning 255 -> 0): one warp, lane l holding bins 255 - 8l .. 248 - 8l; if every bin
+    // together holds fewer than `remaining`, d = 0 with the count above it
+    if (tid < 32) {
+      int c[8], sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = static_cast<int>(hist[255 - 8 * tid - j]);
+        sum += c[j];
       }
-      scratch[0] = d;
-      scratch[1] = remaining - above;
+      int incl = sum;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (tid >= off) incl += y;
+      }
+      int above = incl - sum;  // candidates in the bins above this lane's first one
+      if (above < remaining && remaining <= incl) {
+        int d = 255 - 8 * tid;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          d = 255 - 8 * tid - j;
+          if (above + c[j] >= remaining) break;
+          above += c[j];
+        }
+        scratch[0] = d;
+        scratch[1] = remaining - above;
+      } else if (tid == 31 && incl < remaining) {
+        scratch[0] = 0;
+        scratch[1] = remaining - (incl - c[7]);
+      }
     }
     __syncthreads();
     prefix |= static_cast<uint32_t>(scratch[0]) << shift;
@@ -346,37 +369,43 @@ __global__ void __launch_bounds__(kVwoBlock, 2) vwo_norm_tc_kernel(const __grid_
 // first and applies top-k sparsity after it, an upper-bound proxy).  Reading: per query head
 // the k = max(1, floor(p * L / 100)) largest logits (ties to the lower slot) are kept and the
 // output is attention over them alone, the softmax renormalised over the kept set.
-// topk_attend_kernel: one CTA per (batch, query head), one thread per channel: the max of
-// the kept logits, then the kept tokens in chunks (weights exp(l - m) and slot indices in
-// shared memory; each thread adds w * v[slot][d], one coalesced 256-byte row per token).
+// topk_attend_kernel: one CTA per (batch, query head), four row groups of one thread per
+// channel: the max of the kept logits, then the kept tokens in chunks (weights exp(l - m) and
+// slot indices in shared memory); group r adds w * v[slot][d] over the chunk's tokens
+// j = r (mod 4), one coalesced 256-byte row per token, four rows in flight per channel; the
+// groups' sums are added at the end.
 constexpr int kTkChunk = 1024;
+constexpr int kTkGroups = 4;
+constexpr int kTkThreads = kTkGroups * kD;
 
-__global__ void __launch_bounds__(kD) topk_attend_kernel(const float* __restrict__ logits, int cap,
-                                                        const int32_t* __restrict__ keep, int k,
-                                                        const __half* __restrict__ v, int Hq, int Hkv,
-                                                        float* __restrict__ out, float* __restrict__ lse) {
+__global__ void __launch_bounds__(kTkThreads) topk_attend_kernel(const float* __restrict__ logits, int cap,
+                                                                const int32_t* __restrict__ keep, int k,
+                                                                const __half* __restrict__ v, int Hq, int Hkv,
+                                                                float* __restrict__ out, float* __restrict__ lse) {
   __shared__ float w[kTkChunk];
   __shared__ int idx[kTkChunk];
-  __shared__ float red[kD / 32];
+  __shared__ float red[kTkThreads / 32];
+  __shared__ float part[kTkGroups - 1][kD];
   const int bh = blockIdx.x, b = bh / Hq, h = bh % Hq, g = h / (Hq / Hkv);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int d = tid % kD, grp = tid / kD;
   const float* lg = logits + static_cast<long>(bh) * cap;
   const int32_t* kp = keep + static_cast<long>(bh) * k;
   const __half* vb = v + static_cast<long>(b * Hkv + g) * cap * kD;
   float m = -INFINITY;
-  for (int j = tid; j < k; j += kD) m = fmaxf(m, lg[kp[j]]);
+  for (int j = tid; j < k; j += kTkThreads) m = fmaxf(m, lg[kp[j]]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
   if (lane == 0) red[warp] = m;
   __syncthreads();
   m = red[0];
 #pragma unroll
-  for (int i = 1; i < kD / 32; ++i) m = fmaxf(m, red[i]);
+  for (int i = 1; i < kTkThreads / 32; ++i) m = fmaxf(m, red[i]);
   __syncthreads();
   float acc = 0.f, tsum = 0.f;
   for (int c0 = 0; c0 < k; c0 += kTkChunk) {
     const int n = min(kTkChunk, k - c0);
-    for (int j = tid; j < n; j += kD) {
+    for (int j = tid; j < n; j += kTkThreads) {
       const int i = kp[c0 + j];
       const float e = expf(lg[i] - m);
       w[j] = e;
@@ -384,19 +413,24 @@ __global__ void __launch_bounds__(kD) topk_attend_kernel(const float* __restrict
       tsum += e;
     }
     __syncthreads();
-#pragma unroll 8
-    for (int j = 0; j < n; ++j) acc = fmaf(w[j], __half2float(vb[static_cast<long>(idx[j]) * kD + tid]), acc);
+#pragma unroll 4
+    for (int j = grp; j < n; j += kTkGroups) acc = fmaf(w[j], __half2float(vb[static_cast<long>(idx[j]) * kD + d]), acc);
     __syncthreads();
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) tsum += __shfl_xor_sync(0xffffffffu, tsum, off);
   if (lane == 0) red[warp] = tsum;
+  if (grp > 0) part[grp - 1][d] = acc;
   __syncthreads();
-  float tot = 0.f;
+  if (grp == 0) {
+    float tot = 0.f;
 #pragma unroll
-  for (int i = 0; i < kD / 32; ++i) tot += red[i];
-  out[static_cast<long>(bh) * kD + tid] = acc / tot;
-  if (tid == 0 && lse) lse[bh] = m + logf(tot);
+    for (int i = 0; i < kTkThreads / 32; ++i) tot += red[i];
+#pragma unroll
+    for (int r = 0; r < kTkGroups - 1; ++r) acc += part[r][d];
+    out[static_cast<long>(bh) * kD + d] = acc / tot;
+    if (d == 0 && lse) lse[bh] = m + logf(tot);
+  }
 }
 
 int topk_count(int L, int budget_pct) { return std::max(1, static_cast<int>(static_cast<long>(budget_pct) * L / 100)); }
@@ -542,7 +576,7 @@ extern "C" int mikv_topk_attention(const uint16_t* q, const mikv_cache* c, int b
   select_kernel<<<units, kSelThreads, L, s>>>(logits, c->cap_hi, nullptr, L, 0, k, 0, k, keep, evict, nullptr);
   if (int e = check_launch("select_kernel")) return e;
   // 3. attention over the kept tokens alone
-  topk_attend_kernel<<<units, kD, 0, s>>>(logits, c->cap_hi, keep, k, reinterpret_cast<const __half*>(c->v_hi),
+  topk_attend_kernel<<<units, kTkThreads, 0, s>>>(logits, c->cap_hi, keep, k, reinterpret_cast<const __half*>(c->v_hi),
                                           c->Hq, c->Hkv, out, lse);
   return check_launch("topk_attend_kernel");
 }
