@@ -56,7 +56,7 @@ constexpr int kTcThreads = 256;                                        // consum
 constexpr int kTcBlock = kTcThreads + 32;                              // + the producer warp
 constexpr int kTcHalf = kTcTile / 2;                                    // columns per thread
 constexpr int kTcCols = 2 * kTcTile;                                    // two accumulators
-constexpr int kTcLseRing = 4;                                           // lse rows in flight
+constexpr int kTcLseRing = 8;                                           // lse rows in flight
 constexpr int kTcSmem = 3 * tc::kTileBytes + kTcLseRing * kTcTile * 4 + 1024;  // + alignment
 constexpr uint32_t kTcIdesc = tc::idesc_f16(kTcTile, kTcTile);
 
@@ -225,6 +225,8 @@ __global__ void __launch_bounds__(kTcBlock, 2) col_sum_tc_kernel(const __grid_co
   if (tid == kTcThreads) {
     // producer.  Tile n: head hr = n / per, query tile qt = kbi + n % per; Q into buffer
     // n & 1 and its lse row into ring slot n % kTcLseRing, one transaction on load[n & 1].
+    // When tile n + 2 is loaded (after MMA n), every consumer is at tile n - 2 or later, so
+    // the slots of tiles n - 2 .. n + 1 may still be read and slot (n + 2) % 8 is not one.
     auto load_q = [&](int n) {
       const int hr = n / per, qt = kbi + n % per;
       const long bh = static_cast<long>(b) * Hq + g * rep + hr;
@@ -241,8 +243,7 @@ __global__ void __launch_bounds__(kTcBlock, 2) col_sum_tc_kernel(const __grid_co
     for (int n = 0; n < ntile; ++n) {
       const int buf = n & 1;
       ok = tc::mbar_wait(smem_u32(&bar.load[buf]), (n >> 1) & 1) && ok;
-      // accumulator buf and lse slot (n + 2) % 4 = (n - 2) % 4 both free once tile n - 2 is
-      // consumed
+      // accumulator buf is free once every consumer has read tile n - 2 from TMEM
       if (n >= 2) ok = tc::mbar_wait(smem_u32(&bar.freed[buf]), ((n - 2) >> 1) & 1) && ok;
       tc::fence_after_sync();
       tc::mma_tile(tbase + buf * kTcTile, sk, sq0 + buf * tc::kTileBytes, kTcIdesc);
@@ -272,6 +273,11 @@ __global__ void __launch_bounds__(kTcBlock, 2) col_sum_tc_kernel(const __grid_co
       float s0[32], s1[32];
       tc::tmem_ld32(lane_addr, s0);
       tc::tmem_ld32(lane_addr + 32, s1);
+      // accumulator read: the MMA may reuse it.  Its lse slot stays valid: tile n + 2's row
+      // (slot (n + 2) % 8) is loaded only after MMA n, and tiles n - 2 .. n + 1 hold the
+      // slots that consumers may still be reading.
+      tc::fence_before_sync();
+      tc::mbar_arrive(smem_u32(&bar.freed[buf]));
       if (full) {  // packed f32x2 fma / add, -lse read four at a time
         const float4* l4 = reinterpret_cast<const float4*>(lt);
         const float2 k2 = make_float2(kC, kC);
@@ -294,8 +300,6 @@ __global__ void __launch_bounds__(kTcBlock, 2) col_sum_tc_kernel(const __grid_co
             else p4[(e >> 1) & 3].x += x;
           }
       }
-      tc::fence_before_sync();
-      tc::mbar_arrive(smem_u32(&bar.freed[buf]));  // accumulator and lse slot read
       const float part = ((p4[0].x + p4[0].y) + (p4[1].x + p4[1].y)) + ((p4[2].x + p4[2].y) + (p4[3].x + p4[3].y));
       const float y = part - colc;
       const float tt = col + y;
