@@ -125,6 +125,7 @@ ATTN_CASES = [
     (8, 8, 1, 4, 1, 17, 50, 2),         # tiny ragged everything
     (4, 2, 2, 32, 8, 800, 20, 32),      # INT4 important tier over INT2
     (4, 4, 1, 40, 8, 500, 30, 16),      # INT4 / INT4, GQA 5
+    (16, 2, 2, 8, 2, 1, 100, 1),        # a one-token context
 ]
 
 
@@ -180,7 +181,8 @@ def test_decode_attention_slot_permutation_invariant():
 
 
 # ------------------------------------------------------------------ prefill scores (K3)
-@pytest.mark.parametrize("B,Hq,Hkv,T", [(1, 4, 4, 512), (2, 8, 2, 300), (1, 10, 2, 130), (1, 4, 1, 64), (1, 2, 1, 5)])
+@pytest.mark.parametrize("B,Hq,Hkv,T", [(1, 4, 4, 512), (2, 8, 2, 300), (1, 10, 2, 130), (1, 4, 1, 64), (1, 2, 1, 5),
+                                         (2, 4, 2, 1)])
 def test_prefill_scores(B, Hq, Hkv, T):
     wl = _wl(B=B, Hq=Hq, Hkv=Hkv, T=T, n_outlier=8)
     x = inputs.make_prefill(wl, 6, "cpu")
@@ -226,6 +228,8 @@ def test_decode_score_update():
 
 # ------------------------------------------------------------------ selection (K5) and V.W_O (K6)
 def _score_tensor(rng, B, Hkv, L, ties):
+    if ties == "const":          # one value everywhere: the whole ranking is the position rule
+        return np.full((B, Hkv, L), 2.5, dtype=np.float32)
     if ties:
         return rng.integers(0, 6, size=(B, Hkv, L)).astype(np.float32)
     return rng.random((B, Hkv, L)).astype(np.float32) * 10
@@ -233,7 +237,8 @@ def _score_tensor(rng, B, Hkv, L, ties):
 
 @pytest.mark.parametrize("L,p,W,ties", [(512, 20, 32, False), (512, 20, 32, True), (4097, 25, 32, True),
                                         (33, 50, 40, False), (1000, 0, 0, True), (1000, 100, 5, False),
-                                        (32768, 40, 32, False)])
+                                        (32768, 40, 32, False), (131072, 20, 64, True), (1, 20, 0, False),
+                                        (2048, 30, 16, "const")])
 def test_select_h2o_bit_exact(L, p, W, ties):
     rng = np.random.default_rng(L + p)
     B, Hkv = 2, 3
