@@ -281,8 +281,8 @@ size_t mikv_decode_step_workspace_bytes(const mikv_cache* c);
  *   pert[b][h] = || (o[b][h][:] - o_hat[b][h][:]) . W_O^(h) ||_1  (sum over hidden)
  * o, o_hat fp32 [B][Hq][D] (D = 128): e.g. decode attention over the full cache and over
  * the mixed-precision (or evicted) cache.  w_o_t fp16 [hidden][Hq*D], row-major: W_O
- * transposed, the layout nn.Linear stores; hidden % 64 == 0; 16-byte aligned.
- * y fp32 [B][hidden] (16-byte aligned) is written if not NULL; pert fp32 [B][Hq] if not
+ * transposed, the layout nn.Linear stores; hidden % 128 == 0; 16-byte aligned.
+ * y fp32 [B][hidden] is written if not NULL; pert fp32 [B][Hq] if not
  * NULL (needs o_hat).  With w_o_t == NULL, pert[b][h] = || o - o_hat ||_1 over D (y must
  * be NULL).  Products are formed from fp16 (hi, lo) splits of o and o - o_hat with fp32
  * accumulation (relative error ~1e-6).

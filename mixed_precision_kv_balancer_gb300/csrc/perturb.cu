@@ -29,28 +29,39 @@
 namespace mikv {
 namespace {
 
-constexpr int kPtRows = tc::kTileRows;           // operand rows per batch block
-constexpr int kPtBatch = 32;                     // batch rows per block (hi, lo) x (o, d)
-constexpr int kPtN = 64;                         // hidden columns per CTA
+constexpr int kPtM = tc::kTileRows;              // hidden columns per CTA (the MMA's M)
+constexpr int kPtBatch = 64;                     // batch rows per block
+constexpr int kPtN = 4 * kPtBatch;               // operand rows: (o, d) x (hi, lo) per batch row
 constexpr int kPtThreads = 256;                  // consumers
 constexpr int kPtBlock = kPtThreads + 32;        // + the producer warp
-constexpr int kPtABytes = kPtRows * kD * 2;      // 32 KB
-constexpr int kPtWBytes = kPtN * kD * 2;         // 16 KB
-constexpr int kPtStage = kPtABytes + kPtWBytes;  // 48 KB
-constexpr int kPtRing = 4;                       // stages in flight
-constexpr int kPtAcc = 4;                        // 64-column TMEM accumulators
-constexpr int kPtSmem = kPtRing * kPtStage + 1024;  // + the row scales of the block (Hq * 64 floats)
+constexpr int kPtWBytes = kPtM * kD * 2;         // 32 KB
+constexpr int kPtOBytes = kPtN * kD * 2;         // 64 KB
+constexpr int kPtStage = kPtWBytes + kPtOBytes;  // 96 KB
+constexpr int kPtRing = 2;
+constexpr int kPtSmem = kPtRing * kPtStage + 1024;  // + the chunk's row scales
 constexpr int kPtMaxHq = 128;
-using PtRing = tc::Ring<kPtRing, kPtAcc>;
-constexpr uint32_t kPtIdesc = tc::idesc_f16(kPtRows, kPtN);
+constexpr uint32_t kPtIdesc = tc::idesc_f16(kPtM, kPtN);
+using PtRing = tc::Ring<kPtRing, 2>;
 
 __host__ __device__ constexpr int pt_blocks(int B) { return (B + kPtBatch - 1) / kPtBatch; }
+// Head chunks per (column block, batch block): as many as fill one wave of CTAs (one per SM of
+// the current device), at most one head each, and enough that a chunk's row scales (512 B a
+// head) fit beside the ring in shared memory (at most kPtMaxChunkHeads heads).
+constexpr int kPtMaxChunkHeads = 48;
+inline int pt_chunks(int Hq, int ncb, int nbb) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 148;
+  const int fill = std::max(1, std::min(Hq, sms / std::max(1, ncb * nbb)));
+  return std::max(fill, (Hq + kPtMaxChunkHeads - 1) / kPtMaxChunkHeads);
+}
+__host__ __device__ inline int pt_chunk_begin(int Hq, int nch, int c) { return static_cast<int>(static_cast<long>(Hq) * c / nch); }
 
-// One warp per (head h, batch row b < 32 * nbb): the four operand rows of (b, h) in the tile
-// of (h, b / 32): r = (b % 32) * 2 + {0: hi, 1: lo} for o, the same + 64 for d = o - o_hat.
-// Each row (b, h, o | d) is first scaled by a power of two that brings its largest magnitude
-// into [2^13, 2^14), exactly, so that neither part falls into fp16's subnormal range;
-// invs[(h * 32 * nbb + b) * 2 + {0: o, 1: d}] receives the inverse.  Rows b >= B are zero.
+// One warp per (head h, batch row b < 64 * nbb): the four operand rows of (b, h) in the tile
+// of (h, b / 64): r = 4 * (b % 64) + 2 * {0: o, 1: d} + {0: hi, 1: lo}, d = o - o_hat.  Each
+// row (b, h, o | d) is first scaled by a power of two that brings its largest magnitude into
+// [2^13, 2^14), exactly, so that neither part falls into fp16's subnormal range;
+// invs[(h * 64 * nbb + b) * 2 + {0: o, 1: d}] receives the inverse.  Rows b >= B are zero.
 __global__ void perturb_prep_kernel(const float* __restrict__ o, const float* __restrict__ o_hat, int B, int Hq,
                                     __half* __restrict__ a, float* __restrict__ invs) {
   const int nbb = pt_blocks(B), Bp = nbb * kPtBatch;
@@ -81,8 +92,8 @@ __global__ void perturb_prep_kernel(const float* __restrict__ o, const float* __
     return min(max(14 - E, -100), 100);
   };
   const int eo = scale_exp(mo), ed = scale_exp(md);
-  __half* tile = a + static_cast<long>(h * nbb + bb) * kPtRows * kD;
-  const int r0 = (b % kPtBatch) * 2;
+  __half* tile = a + static_cast<long>(h * nbb + bb) * kPtN * kD;
+  const int r0 = 4 * (b % kPtBatch);
 #pragma unroll
   for (int part = 0; part < 2; ++part) {
     const float* x = part ? xd : xo;
@@ -94,8 +105,8 @@ __global__ void perturb_prep_kernel(const float* __restrict__ o, const float* __
       hi[j] = __half2float(__float2half_rn(xs));
       lo[j] = xs - hi[j];
     }
-    __half2* rh = reinterpret_cast<__half2*>(tile + (part * 64 + r0) * kD + 4 * lane);
-    __half2* rl = reinterpret_cast<__half2*>(tile + (part * 64 + r0 + 1) * kD + 4 * lane);
+    __half2* rh = reinterpret_cast<__half2*>(tile + (r0 + 2 * part) * kD + 4 * lane);
+    __half2* rl = reinterpret_cast<__half2*>(tile + (r0 + 2 * part + 1) * kD + 4 * lane);
     rh[0] = __floats2half2_rn(hi[0], hi[1]);
     rh[1] = __floats2half2_rn(hi[2], hi[3]);
     rl[0] = __floats2half2_rn(lo[0], lo[1]);
@@ -107,108 +118,154 @@ __global__ void perturb_prep_kernel(const float* __restrict__ o, const float* __
   }
 }
 
-// D (TMEM, 128 x 64) = A (128 x kD, 32 KB tile) . W^T (64 x kD, 16 KB tile): 8 K steps; the
-// W tile's k-blocks are 8 KB apart.
-__device__ __forceinline__ void mma_a_w(uint32_t tmem_d, uint32_t sa, uint32_t sw) {
+// D (TMEM, 128 hidden columns x 256 operand rows) = W^T tile (128 x kD, 32 KB) . operand
+// tile^T (256 x kD, 64 KB): 8 K steps; the operand tile's k-blocks are 32 KB apart.
+__device__ __forceinline__ void mma_w_o(uint32_t tmem_d, uint32_t sw, uint32_t so) {
 #pragma unroll
   for (int ks = 0; ks < kD / 16; ++ks) {
-    const uint32_t a_off = (ks >> 2) * tc::kKBlock + (ks & 3) * 32;
-    const uint32_t w_off = (ks >> 2) * (kPtN * 128) + (ks & 3) * 32;
-    tc::mma_f16(tmem_d, tc::smem_desc(sa + a_off), tc::smem_desc(sw + w_off), kPtIdesc, ks > 0);
+    const uint32_t w_off = (ks >> 2) * tc::kKBlock + (ks & 3) * 32;
+    const uint32_t o_off = (ks >> 2) * (kPtN * 128) + (ks & 3) * 32;
+    tc::mma_f16(tmem_d, tc::smem_desc(sw + w_off), tc::smem_desc(so + o_off), kPtIdesc, ks > 0);
   }
 }
 
-__global__ void __launch_bounds__(kPtBlock, 1) perturb_tc_kernel(const __grid_constant__ CUtensorMap ta,
-                                                                 const __grid_constant__ CUtensorMap tw, int B,
+// Lane l of the warp ends with the sum over the 32 lanes of v[l] (butterfly reduce-scatter:
+// at offset r each lane keeps the half of its values selected by bit r of its index).
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int r = 16, n = 16; r >= 1; r >>= 1, n >>= 1) {
+    const bool up = (lane & r) != 0;
+#pragma unroll
+    for (int j = 0; j < n; ++j) {
+      const float send = up ? v[j] : v[j + n];
+      const float keep = up ? v[j + n] : v[j];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, r);
+    }
+  }
+  return v[0];
+}
+
+// CTA (column block cb of 128 hidden columns, head chunk hc, batch block bb).  Step s = head
+// h0 + s of the chunk: the 128 x 128 block of W^T at rows cb*128, channels h*128, and the
+// operand tile of (h, bb), through a two-stage TMA ring; tcgen05.mma into one of two
+// 256-column TMEM accumulators (TMEM lane = hidden column, column = operand row).
+// Consumer thread (lane = hidden column c, half) reads the 128 columns of batch rows
+// 32 * half .. + 32: y[b] += (o_hi + o_lo) * 2^-eo for the chunk's heads (written once as the
+// chunk's partial), |z| = |d_hi + d_lo| * 2^-ed summed over the 128 columns per (b, h) by a
+// warp reduce-scatter and a shared-memory add over the four lane quarters.
+__global__ void __launch_bounds__(kPtBlock, 1) perturb_tc_kernel(const __grid_constant__ CUtensorMap tw,
+                                                                 const __grid_constant__ CUtensorMap to, int B,
                                                                  int Hq, int hidden,
                                                                  const float* __restrict__ invs,
-                                                                 float* __restrict__ y, float* __restrict__ part) {
-  extern __shared__ __align__(128) uint8_t sm[];  // kPtRing stages of (A tile, W tile), row scales
+                                                                 float* __restrict__ ypart, float* __restrict__ part) {
+  extern __shared__ __align__(128) uint8_t sm[];  // kPtRing stages of (W tile, operand tile), row scales
   __shared__ __align__(8) PtRing ring;
   __shared__ uint32_t tslot;
+  __shared__ float red[2][8][32];
   __shared__ int bad;
-  const int cb = blockIdx.x, bb = blockIdx.y, nbb = gridDim.y, Bp = nbb * kPtBatch;
-  const int ncb = hidden / kPtN;
-  const int tid = threadIdx.x, warp = tid >> 5, row = tid & 127, half = (tid >> 7) & 1;
-  const int b = bb * kPtBatch + ((row & 63) >> 1);
-  const bool drow = row >= 64, hirow = (row & 1) == 0;
+  const int cb = blockIdx.x, hc = blockIdx.y, bb = blockIdx.z, nbb = gridDim.z, Bp = nbb * kPtBatch;
+  const int ncb = hidden / kPtM;
+  const int nch = gridDim.y;
+  const int h0 = pt_chunk_begin(Hq, nch, hc), nh = pt_chunk_begin(Hq, nch, hc + 1) - h0;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, half = (tid >> 7) & 1;
+  const int col = cb * kPtM + (warp & 3) * 32 + lane;  // a consumer's hidden column
   const uint32_t s0 = tc::smem_base(sm);
-  // inverse row scales of this batch block for every head, [h][64] (read each step)
-  float* sinv = reinterpret_cast<float*>(sm + (s0 - smem_u32(sm)) + kPtRing * kPtStage);
-  for (int j = tid; j < Hq * 2 * kPtBatch; j += kPtBlock)
-    sinv[j] = invs[(static_cast<long>(j / (2 * kPtBatch)) * Bp + bb * kPtBatch) * 2 + j % (2 * kPtBatch)];
+  float* sinv = reinterpret_cast<float*>(sm + (s0 - smem_u32(sm)) + kPtRing * kPtStage);  // [nh][64][2]
+  for (int j = tid; j < nh * 2 * kPtBatch; j += kPtBlock)
+    sinv[j] = invs[(static_cast<long>(h0 + j / (2 * kPtBatch)) * Bp + bb * kPtBatch) * 2 + j % (2 * kPtBatch)];
   if (tid == 0) bad = 0;
-  const uint32_t tbase = tc::ring_setup(ring, &tslot, kPtThreads, kPtAcc * kPtN);  // (its barrier publishes sinv)
+  const uint32_t tbase = tc::ring_setup(ring, &tslot, kPtThreads, 2 * kPtN);  // (its barrier publishes sinv)
   bool ok = true;
   if (tid == kPtThreads) {
-    // producer.  Step s takes head h = (s + cb) % Hq: the operand tile of (h, bb) and the
-    // 64 x 128 block of W^T at rows cb*64, channels h*128; nothing is resident.  The head
-    // order is rotated per column block so that the CTAs running at one time read different
-    // operand tiles (all reading the same tile at once concentrates them on a few L2 slices).
-    tc::mbar_arrive(smem_u32(&ring.fixed));
+    tc::mbar_arrive(smem_u32(&ring.fixed));  // nothing resident
     ok = tc::ring_produce(
-        ring, Hq,
+        ring, nh,
         [&](int s, int st, uint32_t mb) {
-          const int h = (s + cb) % Hq;
-          const uint32_t sa = s0 + st * kPtStage;
+          const int h = h0 + s;
+          const uint32_t sw = s0 + st * kPtStage, so = sw + kPtWBytes;
           tc::mbar_expect_tx(mb, kPtStage);
-          tc::tma_tile(sa, &ta, (h * nbb + bb) * kPtRows, mb);
 #pragma unroll
-          for (int j = 0; j < kD / 64; ++j)
+          for (int j = 0; j < kD / 64; ++j) {
             asm volatile(
                 "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(sa + kPtABytes + j * (kPtN * 128)),
-                "l"(&tw), "r"(h * kD + j * 64), "r"(cb * kPtN), "r"(mb)
+                " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(sw + j * tc::kKBlock),
+                "l"(&tw), "r"(h * kD + j * 64), "r"(cb * kPtM), "r"(mb)
                 : "memory");
+            asm volatile(
+                "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(so + j * (kPtN * 128)),
+                "l"(&to), "r"(j * 64), "r"((h * nbb + bb) * kPtN), "r"(mb)
+                : "memory");
+          }
         },
         [&](int, int st, int acc) {
-          const uint32_t sa = s0 + st * kPtStage;
-          mma_a_w(tbase + acc * kPtN, sa, sa + kPtABytes);
+          const uint32_t sw = s0 + st * kPtStage;
+          mma_w_o(tbase + acc * kPtN, sw, sw + kPtWBytes);
         });
   } else if (tid < kPtThreads) {
-    float yacc[32];
+    float y[32];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) yacc[e] = 0.f;
-    for (int st = 0; st < Hq; ++st) {
-      const int h = (st + cb) % Hq;
-      ok = tc::ring_acquire(ring, st) && ok;
-      float v[32];
-      tc::tmem_ld32(tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16) + (st % kPtAcc) * kPtN + half * 32, v);
-      tc::ring_release(ring, st);  // accumulator read
+    for (int i = 0; i < 32; ++i) y[i] = 0.f;
+    for (int s = 0; s < nh; ++s) {
+      ok = tc::ring_acquire(ring, s) && ok;
+      const float* si = sinv + s * 2 * kPtBatch + half * 64;  // (b_local, o | d) of this half
+      float za[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) v[e] += __shfl_xor_sync(0xffffffffu, v[e], 1);  // hi + lo row
-      if (hirow && b < B) {
-        const float is = sinv[h * 2 * kPtBatch + (b - bb * kPtBatch) * 2 + (drow ? 1 : 0)];  // undo the row scale
+      for (int q = 0; q < 4; ++q) {  // 8 batch rows per 32 columns
+        float v[32];
+        tc::tmem_ld32(tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16) + (s & 1) * kPtN + half * 128 + q * 32, v);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] *= is;
-        if (!drow) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) yacc[e] += v[e];
-        } else {
-          float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int e = 0; e < 32; ++e) s4[e & 3] += fabsf(v[e]);
-          part[(static_cast<long>(b) * Hq + h) * (2 * ncb) + 2 * cb + half] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        for (int i = 0; i < 8; ++i) {
+          const int bi = q * 8 + i;
+          y[bi] = fmaf(v[4 * i] + v[4 * i + 1], si[2 * bi], y[bi]);
+          za[bi] = fabsf((v[4 * i + 2] + v[4 * i + 3]) * si[2 * bi + 1]);
         }
       }
+      tc::ring_release(ring, s);  // accumulator read
+      const float zs = reduce_scatter32(za, lane);  // lane l: batch row 32 * half + l
+      red[s & 1][warp][lane] = zs;
+      tc::consumer_sync<kPtThreads>();
+      if (tid < 64) {  // (half, l) = (tid / 32, tid % 32): add the four lane quarters
+        const int hf = tid >> 5, l = tid & 31;
+        const float t = (red[s & 1][4 * hf][l] + red[s & 1][4 * hf + 1][l]) +
+                        (red[s & 1][4 * hf + 2][l] + red[s & 1][4 * hf + 3][l]);
+        const int b = bb * kPtBatch + 32 * hf + l;
+        if (b < B) part[(static_cast<long>(b) * Hq + h0 + s) * ncb + cb] = t;
+      }
     }
-    if (y && hirow && !drow && b < B) {
-      float4* dst = reinterpret_cast<float4*>(y + static_cast<long>(b) * hidden + cb * kPtN + half * 32);
+    if (ypart) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) dst[e] = make_float4(yacc[4 * e], yacc[4 * e + 1], yacc[4 * e + 2], yacc[4 * e + 3]);
+      for (int i = 0; i < 32; ++i) {
+        const int b = bb * kPtBatch + 32 * half + i;
+        if (b < B) ypart[(static_cast<long>(hc) * B + b) * hidden + col] = y[i];
+      }
     }
   }
   if (!ok) atomicExch(&bad, 1);
-  tc::cta_teardown(tbase, kPtAcc * kPtN);
-  if (bad && tid < kPtThreads && hirow && b < B) {  // a wait gave up: mark this CTA's outputs
-    if (y && !drow)
-      for (int e = 0; e < 32; ++e) y[static_cast<long>(b) * hidden + cb * kPtN + half * 32 + e] = __int_as_float(0x7fc00000);
-    if (drow)
-      for (int h = 0; h < Hq; ++h) part[(static_cast<long>(b) * Hq + h) * (2 * ncb) + 2 * cb + half] = __int_as_float(0x7fc00000);
+  tc::cta_teardown(tbase, 2 * kPtN);
+  if (bad && tid < 64) {  // a wait gave up: mark this CTA's perturbation outputs
+    const int b = bb * kPtBatch + tid;
+    if (b < B)
+      for (int s = 0; s < nh; ++s) part[(static_cast<long>(b) * Hq + h0 + s) * ncb + cb] = __int_as_float(0x7fc00000);
+  }
+  if (bad && ypart && tid < kPtThreads)
+    for (int i = 0; i < 32; ++i) {
+      const int b = bb * kPtBatch + 32 * half + i;
+      if (b < B) ypart[(static_cast<long>(hc) * B + b) * hidden + col] = __int_as_float(0x7fc00000);
+    }
+}
+
+// y[b][c] = sum over the head chunks of their partials, in chunk order.
+__global__ void perturb_yreduce_kernel(const float* __restrict__ ypart, int nchunk, long n, float* __restrict__ y) {
+  for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long>(gridDim.x) * blockDim.x) {
+    float t = 0.f;
+    for (int c = 0; c < nchunk; ++c) t += ypart[c * n + i];
+    y[i] = t;
   }
 }
 
-// pert[b][h] = sum of the 2 * ncb partial sums, in column order.  One warp per (b, h).
+// pert[b][h] = sum of the ncb column-block partial sums, in column order.  One warp per (b, h).
 __global__ void perturb_reduce_kernel(const float* __restrict__ part, int n, int nparts, float* __restrict__ pert) {
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (w >= n) return;
@@ -231,9 +288,18 @@ __global__ void perturb_raw_kernel(const float* __restrict__ o, const float* __r
   if (lane == 0) pert[w] = s;
 }
 
-size_t a_bytes(int B, int Hq) { return align_up(static_cast<size_t>(Hq) * pt_blocks(B) * kPtABytes, 256); }
-size_t invs_bytes(int B, int Hq) {
-  return align_up(static_cast<size_t>(Hq) * pt_blocks(B) * kPtBatch * 2 * sizeof(float), 256);
+struct PtWs {
+  size_t a, invs, part, ypart, total;
+};
+PtWs pt_ws_layout(int B, int Hq, int hidden) {  // y partials sized for one chunk per head (the most)
+  const int nbb = pt_blocks(B);
+  PtWs w;
+  w.a = 0;
+  w.invs = align_up(static_cast<size_t>(Hq) * nbb * kPtOBytes, 256);
+  w.part = w.invs + align_up(static_cast<size_t>(Hq) * nbb * kPtBatch * 2 * sizeof(float), 256);
+  w.ypart = w.part + align_up(static_cast<size_t>(B) * Hq * (hidden / kPtM) * sizeof(float), 256);
+  w.total = w.ypart + align_up(static_cast<size_t>(Hq) * B * hidden * sizeof(float), 256);
+  return w;
 }
 
 }  // namespace
@@ -242,9 +308,8 @@ size_t invs_bytes(int B, int Hq) {
 using namespace mikv;
 
 extern "C" size_t mikv_output_perturbation_workspace_bytes(int B, int Hq, int hidden) {
-  if (B < 1 || Hq < 1 || hidden < kPtN) return 0;
-  return a_bytes(B, Hq) + invs_bytes(B, Hq) +
-         align_up(static_cast<size_t>(B) * Hq * 2 * (hidden / kPtN) * sizeof(float), 256);
+  if (B < 1 || Hq < 1 || hidden < kPtM) return 0;
+  return pt_ws_layout(B, Hq, hidden).total;
 }
 
 extern "C" int mikv_output_perturbation(const float* o, const float* o_hat, const uint16_t* w_o_t, int B, int Hq,
@@ -263,33 +328,41 @@ extern "C" int mikv_output_perturbation(const float* o, const float* o_hat, cons
     perturb_raw_kernel<<<(n + 7) / 8, 256, 0, s>>>(o, o_hat, n, pert);
     return check_launch("perturb_raw_kernel");
   }
-  if (hidden < kPtN || hidden % kPtN)
-    return fail(MIKV_ESHAPE, "output_perturbation: hidden=%d (multiple of %d)", hidden, kPtN);
-  if (static_cast<long>(Hq) * pt_blocks(B) * kPtRows > (1L << 31) - 1 || static_cast<long>(Hq) * kD > (1L << 31) - 1)
+  if (hidden < kPtM || hidden % kPtM)
+    return fail(MIKV_ESHAPE, "output_perturbation: hidden=%d (multiple of %d)", hidden, kPtM);
+  if (static_cast<long>(Hq) * pt_blocks(B) * kPtN > (1L << 31) - 1 || static_cast<long>(B) * hidden * Hq > (1L << 31) - 1)
     return fail(MIKV_ESHAPE, "output_perturbation: too large");
   if (!ws) return fail(MIKV_EINVAL, "output_perturbation: null workspace");
-  const size_t need = mikv_output_perturbation_workspace_bytes(B, Hq, hidden);
-  if (ws_bytes < need) return fail(MIKV_ESHAPE, "output_perturbation: workspace %zu < %zu", ws_bytes, need);
-  if (!aligned16(o) || (o_hat && !aligned16(o_hat)) || !aligned16(w_o_t) || !aligned16(ws) || (y && !aligned16(y)))
-    return fail(MIKV_EALIGN, "output_perturbation: o / o_hat / w_o_t / ws / y alignment");
-  const int nbb = pt_blocks(B), ncb = hidden / kPtN;
-  __half* a = static_cast<__half*>(ws);
-  float* invs = reinterpret_cast<float*>(static_cast<char*>(ws) + a_bytes(B, Hq));
-  float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + a_bytes(B, Hq) + invs_bytes(B, Hq));
+  const PtWs L = pt_ws_layout(B, Hq, hidden);
+  if (ws_bytes < L.total) return fail(MIKV_ESHAPE, "output_perturbation: workspace %zu < %zu", ws_bytes, L.total);
+  if (!aligned16(o) || (o_hat && !aligned16(o_hat)) || !aligned16(w_o_t) || !aligned16(ws))
+    return fail(MIKV_EALIGN, "output_perturbation: o / o_hat / w_o_t / ws alignment");
+  const int nbb = pt_blocks(B), ncb = hidden / kPtM, nch = pt_chunks(Hq, ncb, nbb);
+  char* w = static_cast<char*>(ws);
+  __half* a = reinterpret_cast<__half*>(w + L.a);
+  float* invs = reinterpret_cast<float*>(w + L.invs);
+  float* part = reinterpret_cast<float*>(w + L.part);
+  float* ypart = y ? reinterpret_cast<float*>(w + L.ypart) : nullptr;
   const int nwarp = Hq * nbb * kPtBatch;
   perturb_prep_kernel<<<(nwarp + 7) / 8, 256, 0, s>>>(o, o_hat, B, Hq, a, invs);
   if (int e = check_launch("perturb_prep_kernel")) return e;
-  CUtensorMap ta, tw;
-  if (int e = tc::encode_rows(&ta, a, static_cast<long>(Hq) * nbb * kPtRows, "output_perturbation: operand")) return e;
-  if (int e = tc::encode_rows(&tw, w_o_t, hidden, "output_perturbation: w_o_t", static_cast<long>(Hq) * kD, kPtN))
+  CUtensorMap tw, to;
+  if (int e = tc::encode_rows(&tw, w_o_t, hidden, "output_perturbation: w_o_t", static_cast<long>(Hq) * kD)) return e;
+  if (int e = tc::encode_rows(&to, a, static_cast<long>(Hq) * nbb * kPtN, "output_perturbation: operand", kD, kPtN))
     return e;
-  const int smem = kPtSmem + Hq * 2 * kPtBatch * static_cast<int>(sizeof(float));
+  const int hmax = (Hq + nch - 1) / nch;  // heads of the largest chunk
+  const int smem = kPtSmem + hmax * 2 * kPtBatch * static_cast<int>(sizeof(float));
   if (cudaFuncSetAttribute(perturb_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return check_launch("perturb_tc_kernel attribute");
-  perturb_tc_kernel<<<dim3(ncb, nbb), kPtBlock, smem, s>>>(ta, tw, B, Hq, hidden, invs, y, part);
+  perturb_tc_kernel<<<dim3(ncb, nch, nbb), kPtBlock, smem, s>>>(tw, to, B, Hq, hidden, invs, ypart, part);
   if (int e = check_launch("perturb_tc_kernel")) return e;
+  if (y) {
+    const long n = static_cast<long>(B) * hidden;
+    perturb_yreduce_kernel<<<static_cast<int>(std::min<long>((n + 255) / 256, 152L * 8)), 256, 0, s>>>(ypart, nch, n, y);
+    if (int e = check_launch("perturb_yreduce_kernel")) return e;
+  }
   if (!pert) return MIKV_OK;
   const int n = B * Hq;
-  perturb_reduce_kernel<<<(n + 7) / 8, 256, 0, s>>>(part, n, 2 * ncb, pert);
+  perturb_reduce_kernel<<<(n + 7) / 8, 256, 0, s>>>(part, n, ncb, pert);
   return check_launch("perturb_reduce_kernel");
 }

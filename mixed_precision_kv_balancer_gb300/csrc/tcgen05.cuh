@@ -274,6 +274,12 @@ __device__ __forceinline__ void ring_release(Ring<R, NACC>& r, int s) {
   mbar_arrive(smem_u32(&r.freed[s % NACC]));
 }
 
+// Consumer-only barrier (named barrier 1; the producer warp does not take part).
+template <int N>
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;\n" ::"n"(N) : "memory");
+}
+
 // Every thread of the CTA calls it after its last TMEM access.
 __device__ __forceinline__ void cta_teardown(uint32_t tbase, uint32_t cols) {
   fence_before_sync();

@@ -105,7 +105,7 @@ def test_host_side_rejections(lib):
     assert op(fake, fake, None, 1, 4, 128, 128, fake, None, None, 0, None) == EINVAL      # y needs w_o_t
     assert op(fake, fake, fake, 1, 4, 64, 128, fake, fake, fake, 1 << 20, None) == EUNSUP
     assert op(fake, fake, fake, 0, 4, 128, 128, fake, fake, fake, 1 << 20, None) == ESHAPE
-    assert op(fake, fake, fake, 1, 4, 128, 96, fake, fake, fake, 1 << 20, None) == ESHAPE  # hidden % 64
+    assert op(fake, fake, fake, 1, 4, 128, 192, fake, fake, fake, 1 << 20, None) == ESHAPE  # hidden % 128
     assert op(fake, fake, fake, 1, 4, 128, 128, fake, fake, fake, 64, None) == ESHAPE      # workspace
     assert op(fake, fake, ctypes.c_void_p(4098), 1, 4, 128, 128, fake, fake, fake, 1 << 20, None) == EALIGN
     assert op(fake, fake, fake, 1, 4, 128, 128, None, None, None, 0, None) == 0            # nothing asked

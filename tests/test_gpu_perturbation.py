@@ -46,7 +46,8 @@ def _assert_y(got, want):
     assert err.max() <= 1e-5, f"y normwise error {err.max():.3e}"
 
 
-@pytest.mark.parametrize("B,Hq,hidden", [(1, 4, 64), (3, 5, 640), (33, 8, 128), (2, 10, 256), (7, 28, 3584)])
+@pytest.mark.parametrize("B,Hq,hidden", [(1, 4, 128), (3, 5, 640), (33, 8, 128), (2, 10, 256), (7, 28, 3584),
+                                         (70, 6, 384), (5, 2, 256)])
 def test_output_perturbation_matches_oracle(B, Hq, hidden):
     o, oh, w = _case(B, Hq, hidden, seed=B * 100 + Hq)
     y, pert = _run(o, oh, w)
@@ -70,7 +71,7 @@ def test_identical_outputs_give_exactly_zero():
 
 
 def test_projection_only_and_raw_distance():
-    o, oh, w = _case(4, 6, 192, seed=4)
+    o, oh, w = _case(4, 6, 384, seed=4)
     y, _ = _run(o, None, w, want_pert=False)                 # y alone needs no o^
     _assert_y(y, opt.output_projection(o.numpy(), w.numpy()))
     pert = torch.empty(4, 6, device=dev())                   # no W_O: ||o - o^||_1 over D
