@@ -256,12 +256,11 @@ def run_gpu(args, wl, rank, world):
         e.record()              # creates the CUDA event; the library records it again later
         return e
 
-    # events per (step, layer): the whole layer step in the timed steps; the split-K attention
-    # kernel alone in the attention pass (recorded by the library on the launching stream
-    # around that one launch).  Events between the step's kernels stop them from overlapping
-    # one another's launch, so the timed steps run without them.
+    # events per (step, layer) of the attention pass: the split-K attention kernel alone
+    # (recorded by the library on the launching stream around that one launch).  The timed
+    # steps carry no events inside: events between kernels stop their launches from
+    # overlapping.
     n_ev = args.steps * wl.layers
-    step_ev = [(new_event(), new_event()) for _ in range(n_ev)]
     attn_ev = [(new_event(), new_event()) for _ in range(n_ev if attn_steps else 0)]
     torch.cuda.synchronize()
 
@@ -269,21 +268,15 @@ def run_gpu(args, wl, rank, world):
         L_before = wl.T + s
         for l, c in enumerate(layers):
             t = toks[s][l]
-            if mode == "step":
-                e0, e1 = step_ev[len(step_pairs)]
-                step_pairs.append((e0, e1))
-                e0.record()
-            elif mode == "attn":
+            if mode == "attn":
                 a0, a1 = attn_ev[len(attn_pairs)]
                 # tiers as attended (after the append)
                 attn_pairs.append((a0, a1, cache_bytes(wl, c.n_hi + 1, c.n_lo)))
                 _lib.mikv_set_attention_events(a0, a1)
             c.decode_step(t["q"], t["k"], t["v"], L_before, wl.budget_pct, wl.window, policy=wl.policy)
-            if mode == "step":
-                e1.record()
         return 4 * len(layers)   # append, split-K attention, merge, score update/demotion
 
-    step_pairs, attn_pairs = [], []
+    attn_pairs = []
     for s in range(args.warmup):
         step(s)
     torch.cuda.synchronize()
@@ -302,7 +295,7 @@ def run_gpu(args, wl, rank, world):
         L = wl.T + s + 1
         kv_tokens += wl.B * L * wl.layers
         read_bytes += [cache_bytes(wl, c.n_hi + 1, c.n_lo) for c in layers]
-        launches += step(s, mode="step")
+        launches += step(s)
     end.record()
     torch.cuda.synchronize()
     ms = start.elapsed_time(end)
@@ -313,7 +306,8 @@ def run_gpu(args, wl, rank, world):
     _lib.mikv_set_attention_events(None, None)
     clk = clocks.stop()
     ms = reduce_over_ranks(ms, world, dev)
-    step_ms = [e0.elapsed_time(e1) for e0, e1 in step_pairs]
+    # per layer-step: the timed region over its layer steps (no events inside the region)
+    step_ms = [ms / (args.steps * wl.layers)]
     if attn_pairs:
         attn_ms = [a0.elapsed_time(a1) for a0, a1, _ in attn_pairs]
         attn_bytes = [nb for *_, nb in attn_pairs]
@@ -332,7 +326,18 @@ def run_gpu(args, wl, rank, world):
         host_out = [torch.empty(wl.B, wl.Hq, wl.D, dtype=torch.float32).pin_memory() for _ in range(wl.layers)]
         h2d = sum(t.numel() * t.element_size() for t in host_in[0][0].values()) * wl.layers
         d2h = sum(t.numel() * t.element_size() for t in host_out)
-        dev_in = [{n: torch.empty_like(t, device=dev) for n, t in host_in[0][l].items()} for l in range(wl.layers)]
+        # device staging per (layer, parity of the step): the copies run on their own stream and
+        # overlap the other layers' attention; events order each copy against its consumer
+        dev_in = [[{n: torch.empty_like(t, device=dev) for n, t in host_in[0][l].items()} for l in range(wl.layers)]
+                  for _ in range(2)]
+        dev_out = [[torch.empty(wl.B, wl.Hq, wl.D, dtype=torch.float32, device=dev) for _ in range(wl.layers)]
+                   for _ in range(2)]
+        copy_s = torch.cuda.Stream(device=dev)
+        comp_s = torch.cuda.current_stream(dev)
+        in_ready = [[torch.cuda.Event() for _ in range(wl.layers)] for _ in range(2)]
+        out_ready = [[torch.cuda.Event() for _ in range(wl.layers)] for _ in range(2)]
+        out_taken = [[torch.cuda.Event() for _ in range(wl.layers)] for _ in range(2)]
+        in_used = [[torch.cuda.Event() for _ in range(wl.layers)] for _ in range(2)]
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0 = time.perf_counter()
@@ -340,13 +345,28 @@ def run_gpu(args, wl, rank, world):
         e2e_tokens = 0
         for i, s in enumerate(range(e2e_first, e2e_first + args.steps)):
             L_before = wl.T + s
+            par = i & 1
+            with torch.cuda.stream(copy_s):  # this step's inputs, all layers
+                for l in range(wl.layers):
+                    if i >= 2:
+                        copy_s.wait_event(in_used[par][l])      # step i - 2 has read this buffer
+                    for n in ("q", "k", "v"):
+                        dev_in[par][l][n].copy_(host_in[i][l][n], non_blocking=True)
+                    in_ready[par][l].record(copy_s)
             for l, c in enumerate(layers):
-                for n in ("q", "k", "v"):
-                    dev_in[l][n].copy_(host_in[i][l][n], non_blocking=True)
-                out, _ = c.decode_step(dev_in[l]["q"], dev_in[l]["k"], dev_in[l]["v"], L_before,
-                                       wl.budget_pct, wl.window, policy=wl.policy)
-                host_out[l].copy_(out, non_blocking=True)
+                comp_s.wait_event(in_ready[par][l])
+                if i >= 2:
+                    comp_s.wait_event(out_taken[par][l])        # step i - 2's output was copied out
+                c.decode_step(dev_in[par][l]["q"], dev_in[par][l]["k"], dev_in[par][l]["v"], L_before,
+                              wl.budget_pct, wl.window, policy=wl.policy, out=dev_out[par][l])
+                in_used[par][l].record(comp_s)
+                out_ready[par][l].record(comp_s)
+                with torch.cuda.stream(copy_s):
+                    copy_s.wait_event(out_ready[par][l])
+                    host_out[l].copy_(dev_out[par][l], non_blocking=True)
+                    out_taken[par][l].record(copy_s)
             e2e_tokens += wl.B * (L_before + 1) * wl.layers
+        comp_s.wait_stream(copy_s)
         e1.record()
         torch.cuda.synchronize()
         e2e_ms = max(e0.elapsed_time(e1), (time.perf_counter() - t0) * 1e3)

@@ -124,13 +124,16 @@ class MikvCache:
         _lib.mikv_quantize_append(_lib.MIKV_TIER_LO, self, k, v, evict_pos, evict_pos.shape[2], 0)
 
     # --- decode --------------------------------------------------------------------
-    def decode_step(self, q, k, v, L_before, budget_pct, window, policy="h2o"):
+    def decode_step(self, q, k, v, L_before, budget_pct, window, policy="h2o", out=None, lse=None):
         """One decode step through mikv_decode_step (append, attention, merge, score update +
-        demotion); q [B,Hq,D], k/v [B,Hkv,D] fp16.  Returns (out, lse) views."""
+        demotion); q [B,Hq,D], k/v [B,Hkv,D] fp16.  Writes out fp32 [B,Hq,D] and lse fp32 [B,Hq]
+        (the cache's own buffers unless given) and returns them."""
         pol = _lib.MIKV_H2O if policy == "h2o" else _lib.MIKV_CRITICALKV
-        _lib.mikv_decode_step(q, k, v, L_before, budget_pct, window, pol, self, self.out, self.lse,
+        out = self.out if out is None else out
+        lse = self.lse if lse is None else lse
+        _lib.mikv_decode_step(q, k, v, L_before, budget_pct, window, pol, self, out, lse,
                               ws=self.ws_decode)
-        return self.out, self.lse
+        return out, lse
 
     def decode_step_calls(self, q, k, v, L_before, budget_pct, window, policy="h2o"):
         """The same step as the sequence of the five separate calls."""
