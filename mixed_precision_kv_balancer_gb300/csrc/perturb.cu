@@ -34,10 +34,11 @@ constexpr int kPtBatch = 64;                     // batch rows per block
 constexpr int kPtN = 4 * kPtBatch;               // operand rows: (o, d) x (hi, lo) per batch row
 constexpr int kPtThreads = 256;                  // consumers
 constexpr int kPtBlock = kPtThreads + 32;        // + the producer warp
-constexpr int kPtWBytes = kPtM * kD * 2;         // 32 KB
-constexpr int kPtOBytes = kPtN * kD * 2;         // 64 KB
-constexpr int kPtStage = kPtWBytes + kPtOBytes;  // 96 KB
-constexpr int kPtRing = 2;
+constexpr int kPtWBytes = kPtM * 64 * 2;         // one 64-channel k-block of the W^T block: 16 KB
+constexpr int kPtOBytes = kPtN * 64 * 2;         // one k-block of the operand tile: 32 KB
+constexpr int kPtStage = kPtWBytes + kPtOBytes;  // 48 KB
+constexpr long kPtOTile = static_cast<long>(kPtN) * kD * 2;  // a whole operand tile in global memory: 64 KB
+constexpr int kPtRing = 4;                       // stages: two per head, three in flight
 constexpr int kPtSmem = kPtRing * kPtStage + 1024;  // + the chunk's row scales
 constexpr int kPtMaxHq = 128;
 constexpr uint32_t kPtIdesc = tc::idesc_f16(kPtM, kPtN);
@@ -47,7 +48,7 @@ __host__ __device__ constexpr int pt_blocks(int B) { return (B + kPtBatch - 1) /
 // Head chunks per (column block, batch block): as many as fill one wave of CTAs (one per SM of
 // the current device), at most one head each, and enough that a chunk's row scales (512 B a
 // head) fit beside the ring in shared memory (at most kPtMaxChunkHeads heads).
-constexpr int kPtMaxChunkHeads = 48;
+constexpr int kPtMaxChunkHeads = 48;  // 24 KB of row scales beside the 193 KB ring
 inline int pt_chunks(int Hq, int ncb, int nbb) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -118,15 +119,12 @@ __global__ void perturb_prep_kernel(const float* __restrict__ o, const float* __
   }
 }
 
-// D (TMEM, 128 hidden columns x 256 operand rows) = W^T tile (128 x kD, 32 KB) . operand
-// tile^T (256 x kD, 64 KB): 8 K steps; the operand tile's k-blocks are 32 KB apart.
-__device__ __forceinline__ void mma_w_o(uint32_t tmem_d, uint32_t sw, uint32_t so) {
+// D (TMEM, 128 hidden columns x 256 operand rows) (+)= one 64-channel k-block: the W^T
+// k-block (128 rows x 128 B) times the operand k-block (256 rows x 128 B), 4 K steps of 16.
+__device__ __forceinline__ void mma_w_o_kblock(uint32_t tmem_d, uint32_t sw, uint32_t so, bool accumulate) {
 #pragma unroll
-  for (int ks = 0; ks < kD / 16; ++ks) {
-    const uint32_t w_off = (ks >> 2) * tc::kKBlock + (ks & 3) * 32;
-    const uint32_t o_off = (ks >> 2) * (kPtN * 128) + (ks & 3) * 32;
-    tc::mma_f16(tmem_d, tc::smem_desc(sw + w_off), tc::smem_desc(so + o_off), kPtIdesc, ks > 0);
-  }
+  for (int kk = 0; kk < 4; ++kk)
+    tc::mma_f16(tmem_d, tc::smem_desc(sw + kk * 32), tc::smem_desc(so + kk * 32), kPtIdesc, accumulate || kk > 0);
 }
 
 // Lane l of the warp ends with the sum over the 32 lanes of v[l] (butterfly reduce-scatter:
@@ -145,10 +143,11 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
   return v[0];
 }
 
-// CTA (column block cb of 128 hidden columns, head chunk hc, batch block bb).  Step s = head
-// h0 + s of the chunk: the 128 x 128 block of W^T at rows cb*128, channels h*128, and the
-// operand tile of (h, bb), through a two-stage TMA ring; tcgen05.mma into one of two
-// 256-column TMEM accumulators (TMEM lane = hidden column, column = operand row).
+// CTA (column block cb of 128 hidden columns, head chunk hc, batch block bb).  For each head
+// h of the chunk, its two 64-channel k-blocks of the W^T block (rows cb*128) and of the operand
+// tile of (h, bb) go through a four-stage TMA ring (48 KB a stage); tcgen05.mma accumulates
+// them into one of two 256-column TMEM accumulators (TMEM lane = hidden column, column =
+// operand row).
 // Consumer thread (lane = hidden column c, half) reads the 128 columns of batch rows
 // 32 * half .. + 32: y[b] += (o_hi + o_lo) * 2^-eo for the chunk's heads (written once as the
 // chunk's partial), |z| = |d_hi + d_lo| * 2^-ed summed over the 128 columns per (b, h) by a
@@ -177,31 +176,43 @@ __global__ void __launch_bounds__(kPtBlock, 1) perturb_tc_kernel(const __grid_co
   const uint32_t tbase = tc::ring_setup(ring, &tslot, kPtThreads, 2 * kPtN);  // (its barrier publishes sinv)
   bool ok = true;
   if (tid == kPtThreads) {
-    tc::mbar_arrive(smem_u32(&ring.fixed));  // nothing resident
-    ok = tc::ring_produce(
-        ring, nh,
-        [&](int s, int st, uint32_t mb) {
-          const int h = h0 + s;
-          const uint32_t sw = s0 + st * kPtStage, so = sw + kPtWBytes;
-          tc::mbar_expect_tx(mb, kPtStage);
-#pragma unroll
-          for (int j = 0; j < kD / 64; ++j) {
-            asm volatile(
-                "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(sw + j * tc::kKBlock),
-                "l"(&tw), "r"(h * kD + j * 64), "r"(cb * kPtM), "r"(mb)
-                : "memory");
-            asm volatile(
-                "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(so + j * (kPtN * 128)),
-                "l"(&to), "r"(j * 64), "r"((h * nbb + bb) * kPtN), "r"(mb)
-                : "memory");
-          }
-        },
-        [&](int, int st, int acc) {
-          const uint32_t sw = s0 + st * kPtStage;
-          mma_w_o(tbase + acc * kPtN, sw, sw + kPtWBytes);
-        });
+    // producer.  Step s = k-block s % 2 of head h0 + s / 2: the W^T k-block at rows cb*128,
+    // channels h*128 + 64*(s % 2), and the operand tile's k-block, into stage s % kPtRing.
+    // The head's accumulator (h & 1) is committed after its second k-block; the first waits
+    // until head h - 2 was read from it.  A stage is refilled (step s - 1 + kPtRing) once the
+    // MMAs of step s - 1 are done, while step s's queue behind them.
+    const int nsteps = 2 * nh;
+    auto load = [&](int s, int st) {
+      const int h = h0 + s / 2, kb = s % 2;
+      const uint32_t sw = s0 + st * kPtStage, so = sw + kPtWBytes, mb = smem_u32(&ring.full[st]);
+      tc::mbar_expect_tx(mb, kPtStage);
+      asm volatile(
+          "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+          " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(sw), "l"(&tw), "r"(h * kD + kb * 64), "r"(cb * kPtM), "r"(mb)
+          : "memory");
+      asm volatile(
+          "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+          " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(so), "l"(&to), "r"(kb * 64), "r"((h * nbb + bb) * kPtN), "r"(mb)
+          : "memory");
+    };
+    for (int st = 0; st < nsteps && st < kPtRing; ++st) load(st, st);
+    for (int st = 0; st < nsteps; ++st) {
+      const int b = st % kPtRing, hl = st / 2, a = hl & 1;
+      ok = tc::mbar_wait(smem_u32(&ring.full[b]), (st / kPtRing) & 1) && ok;
+      if (st % 2 == 0 && hl >= 2) ok = tc::mbar_wait(smem_u32(&ring.freed[a]), ((hl - 2) / 2) & 1) && ok;
+      tc::fence_after_sync();
+      const uint32_t sw = s0 + b * kPtStage;
+      mma_w_o_kblock(tbase + a * kPtN, sw, sw + kPtWBytes, st % 2 == 1);
+      tc::commit(smem_u32(&ring.empty[b]));
+      if (st % 2 == 1) tc::commit(smem_u32(&ring.mma[a]));
+      const int p = st - 1;
+      if (p >= 0 && p + kPtRing < nsteps) {
+        ok = tc::mbar_wait(smem_u32(&ring.empty[p % kPtRing]), (p / kPtRing) & 1) && ok;
+        load(p + kPtRing, p % kPtRing);
+      }
+    }
+    for (int st = nsteps > kPtRing ? nsteps - kPtRing : 0; st < nsteps; ++st)  // stages never refilled
+      ok = tc::mbar_wait(smem_u32(&ring.empty[st % kPtRing]), (st / kPtRing) & 1) && ok;
   } else if (tid < kPtThreads) {
     float y[32];
 #pragma unroll
@@ -295,7 +306,7 @@ PtWs pt_ws_layout(int B, int Hq, int hidden) {  // y partials sized for one chun
   const int nbb = pt_blocks(B);
   PtWs w;
   w.a = 0;
-  w.invs = align_up(static_cast<size_t>(Hq) * nbb * kPtOBytes, 256);
+  w.invs = align_up(static_cast<size_t>(Hq) * nbb * kPtOTile, 256);
   w.part = w.invs + align_up(static_cast<size_t>(Hq) * nbb * kPtBatch * 2 * sizeof(float), 256);
   w.ypart = w.part + align_up(static_cast<size_t>(B) * Hq * (hidden / kPtM) * sizeof(float), 256);
   w.total = w.ypart + align_up(static_cast<size_t>(Hq) * B * hidden * sizeof(float), 256);
