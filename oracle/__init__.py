@@ -25,6 +25,7 @@ scores     H2O accumulated attention (prefill column sums, decode update)
 select     H2O top-k with recent window, CriticalKV two-stage, demotion victim
 attention  decode attention over the two-tier cache (float64); post-attention top-k ("oracle eviction")
 perturbation  the step after attention: o . W_O and the CriticalKV per-head perturbation
+channel_quant  per-channel key quantisation with pending-token buffering (Appendix C alternative)
 pipeline   prefill + decode steps composed into one cache, the whole path
 
 Parity pins for every function live in ``tests/test_oracle_*.py``.
