@@ -317,6 +317,23 @@ int mikv_topk_attention(const uint16_t* q, const mikv_cache* c, int budget_pct, 
 size_t mikv_topk_attention_workspace_bytes(const mikv_cache* c, int budget_pct);
 
 /*
+ * Per-channel group quantisation of retained-tier keys ([notes] Appendix C remarks;
+ * [paperlayer] C: group size 64, keys quantised per channel): the first stage of the
+ * per-channel key alternative, whose cache integration is not built.
+ * k fp16 [units][n][D] (D = 128): each unit's keys in slot order.  The floor(n / 64) full
+ * groups are quantised; the n mod 64 keys after them are left alone (they wait in FP16 until
+ * a group is full).  Per (group, channel c), over the group's 64 values of channel c:
+ *   s = fp16(fl(fl(mx - mn) / qmax)), z = fp16(mn),
+ *   code = clamp(rint_even(fl(fl(x - z) / s)), 0, qmax), 0 where s == 0.
+ * codes uint8 [units][n][D*bits/8]: per-token rows (channel c at bits (c*bits) mod 8 of byte
+ * c*bits/8, LSB first), rows of full groups written; meta fp16 [units][n/64][D][2] =
+ * (scale, zero).  bits in {2, 4, 8}.  Stream-ordered.
+ * Errors: EINVAL (null), EUNSUPPORTED (D, bits), ESHAPE (units outside 1..65535, n < 0).
+ */
+int mikv_channel_quantize(const uint16_t* k, int units, int n, int D, int bits, uint8_t* codes,
+                          uint16_t* meta, void* stream);
+
+/*
  * Measurement hook (no counterpart in the papers): while set, every
  * mikv_decode_attention and mikv_decode_step call made by this thread records
  * `begin` (a cudaEvent_t) on its stream just before the split-K attention

@@ -26,6 +26,7 @@ EXPORTS = (
     "mikv_decode_step", "mikv_decode_step_workspace_bytes",
     "mikv_output_perturbation", "mikv_output_perturbation_workspace_bytes",
     "mikv_topk_attention", "mikv_topk_attention_workspace_bytes",
+    "mikv_channel_quantize",
     "mikv_set_attention_events", "mikv_last_error",
 )
 
@@ -82,6 +83,7 @@ def load() -> ctypes.CDLL:
         "mikv_output_perturbation_workspace_bytes": (S, [I, I, I]),
         "mikv_topk_attention": (I, [P, CP, I, P, P, P, P, S, P]),
         "mikv_topk_attention_workspace_bytes": (S, [CP, I]),
+        "mikv_channel_quantize": (I, [P, I, I, I, I, P, P, P]),
         "mikv_set_attention_events": (I, [P, P]),
         "mikv_last_error": (ctypes.c_char_p, []),
     }
@@ -212,6 +214,13 @@ def mikv_topk_attention(q, cache, budget_pct, out, lse=None, keep_idx=None, ws=N
     _check("mikv_topk_attention", lib.mikv_topk_attention(
         _ptr(q), ctypes.byref(c), budget_pct, _ptr(out), _ptr(lse), _ptr(keep_idx), _ptr(w), nb,
         _stream(stream)))
+
+
+def mikv_channel_quantize(k, bits, codes, meta, stream=None):
+    """k fp16 [units, n, D]; codes uint8 [units, n, D*bits/8]; meta fp16 [units, n//64, D, 2]."""
+    units, n, D = k.shape
+    _check("mikv_channel_quantize", load().mikv_channel_quantize(
+        _ptr(k), units, n, D, bits, _ptr(codes), _ptr(meta), _stream(stream)))
 
 
 def mikv_set_attention_events(begin=None, end=None):

@@ -120,6 +120,13 @@ def test_host_side_rejections(lib):
     assert tk(fake, ctypes.byref(c), 20, fake, None, None, fake, 16, None) == ESHAPE             # workspace
     assert lib.mikv_topk_attention_workspace_bytes(ctypes.byref(c), 20) > 0
     assert lib.mikv_topk_attention_workspace_bytes(ctypes.byref(_cache()), 20) == 0
+    # per-channel group quantisation
+    cqz = lib.mikv_channel_quantize
+    assert cqz(None, 1, 64, 128, 2, fake, fake, None) == EINVAL
+    assert cqz(fake, 1, 64, 64, 2, fake, fake, None) == EUNSUP
+    assert cqz(fake, 1, 64, 128, 3, fake, fake, None) == EUNSUP
+    assert cqz(fake, 0, 64, 128, 2, fake, fake, None) == ESHAPE
+    assert cqz(fake, 1, 63, 128, 2, fake, fake, None) == 0          # no full group: nothing to do
     # the attention timing hook takes both events or neither
     assert lib.mikv_set_attention_events(fake, None) == EINVAL
     assert lib.mikv_set_attention_events(None, fake) == EINVAL
