@@ -73,3 +73,24 @@ class RetainedKeys:
         if self.pending:
             parts.append(np.stack(self.pending).astype(np.float64))
         return np.concatenate(parts, axis=0) if parts else np.zeros((0, self.D))
+
+
+def decode_attention_channel_keys(q: np.ndarray, k_hi: np.ndarray, v_hi: np.ndarray, retained: RetainedKeys,
+                                  v_lo: np.ndarray):
+    """Decode attention of one key head's query heads over an FP16 important tier and a
+    retained tier with per-channel keys, float64.
+
+    q [rep][D] (fp16); k_hi, v_hi [n_hi][D] fp16 (the important tier, attended as stored);
+    retained: the retained tier's keys (groups and pending, slot order); v_lo [n_lo][D] the
+    retained values as attended (float, e.g. dequantised per token).  Softmax over the union
+    of both tiers, logits q.k / sqrt(D).  Returns out [rep][D], lse [rep]."""
+    D = q.shape[1]
+    qf = q.astype(np.float64)
+    k = np.concatenate([k_hi.astype(np.float64), retained.keys_f64()], axis=0)
+    v = np.concatenate([v_hi.astype(np.float64), np.asarray(v_lo, dtype=np.float64)], axis=0)
+    assert k.shape[0] == v.shape[0]
+    logits = (qf @ k.T) / np.sqrt(D)
+    m = logits.max(axis=1, keepdims=True)
+    p = np.exp(logits - m)
+    s = p.sum(axis=1, keepdims=True)
+    return (p @ v) / s, (m + np.log(s))[:, 0]

@@ -80,3 +80,55 @@ def test_pending_buffer(n):
     for gi in range(n // 64):
         c, m = cq.quantize_channel_group(rows[64 * gi:64 * gi + 64], 2)
         np.testing.assert_array_equal(keys[64 * gi:64 * gi + 64], cq.dequantize_channel_group(c, m))
+
+
+def _exact(q, k, v):
+    l = (q.astype(np.float64) @ k.astype(np.float64).T) / np.sqrt(q.shape[1])
+    p = np.exp(l - l.max(axis=1, keepdims=True))
+    return (p @ v.astype(np.float64)) / p.sum(axis=1, keepdims=True)
+
+
+def test_attention_with_only_pending_keys_is_exact():
+    """Fewer than 64 retained keys: all pending in FP16, so attention is exact attention."""
+    rng = np.random.default_rng(21)
+    q = rng.standard_normal((4, 128)).astype(np.float16)
+    k = rng.standard_normal((90, 128)).astype(np.float16)
+    v = rng.standard_normal((90, 128)).astype(np.float16)
+    r = cq.RetainedKeys(128, 2)
+    for row in k[30:]:
+        r.append(row)
+    assert len(r.groups) == 0
+    out, _ = cq.decode_attention_channel_keys(q, k[:30], v[:30], r, v[30:])
+    np.testing.assert_allclose(out, _exact(q, k, v), rtol=1e-12, atol=1e-12)
+
+
+def test_attention_error_shrinks_with_bits():
+    rng = np.random.default_rng(22)
+    q = rng.standard_normal((4, 128)).astype(np.float16)
+    k = rng.standard_normal((1000, 128)).astype(np.float16)
+    v = rng.standard_normal((1000, 128)).astype(np.float16)
+    want = _exact(q, k, v)
+    errs = []
+    for bits in (2, 4, 8):
+        r = cq.RetainedKeys(128, bits)
+        for row in k[200:]:
+            r.append(row)
+        out, _ = cq.decode_attention_channel_keys(q, k[:200], v[:200], r, v[200:])
+        errs.append(np.abs(out - want).max())
+    assert errs[0] > errs[1] > errs[2] and errs[2] < 1e-2
+
+
+def test_per_channel_keys_beat_per_token_on_outlier_channels():
+    """The pages' observation (Appendix C): with channel-aligned key outliers, per-channel
+    INT2 keys reconstruct the keys better than per-token INT2 keys without the balancer."""
+    rng = np.random.default_rng(23)
+    k = rng.standard_normal((256, 128)).astype(np.float32)
+    k[:, [3, 40, 77, 100]] *= 16.0                       # systematic outlier channels
+    k = k.astype(np.float16)
+    r = cq.RetainedKeys(128, 2)
+    for row in k:
+        r.append(row)
+    err_channel = np.abs(r.keys_f64() - k.astype(np.float64)).mean()
+    codes, meta = oq.quantize_groups(k.astype(np.float32), 2, 64)
+    err_token = np.abs(oq.dequantize(codes, meta, 64) - k.astype(np.float64)).mean()
+    assert err_channel < 0.5 * err_token
