@@ -136,8 +136,10 @@ size_t mikv_balance_workspace_bytes(int B, int Hkv, int D);
  *   Limit: B * Hkv <= 1024 (the array holds 2 x 1024 x 128 floats, 1 MiB, on
  *   every device that loads the library, until the process exits); larger
  *   shapes return MIKV_ESHAPE.
- *   The first call on a device looks up that array's device address (with the
- *   device current); make that first call before any stream capture.
+ *   Every call looks up that array's device address in the context current on
+ *   the calling thread (a lookup, not an allocation), so the address stays right
+ *   after cudaDeviceReset or under another context.  The first call on a device
+ *   may load the library's device code there; make it before any stream capture.
  *   All calls share the one array and each clears it first: calls whose kernels
  *   can overlap on the GPU (different streams, without ordering) race and
  *   return wrong results.  Calls allocate nothing.

@@ -13,7 +13,6 @@
 // depend on the order).  A second kernel forms b in fp32, RN division then RN
 // square root.
 #include <algorithm>
-#include <mutex>
 
 #include "common.cuh"
 
@@ -155,26 +154,17 @@ constexpr int kNoAllocMaxUnits = 1024;
 constexpr int kNoAllocFloats = 2 * kNoAllocMaxUnits * kD;  // Mq then Mk
 static __device__ __align__(256) float g_balance_scratch[kNoAllocFloats];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-float* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of g_balance_scratch on the current device, looked up once per device.
-// (In host code the symbol is only a host-side stand-in, never a device address.)
-int scratch_for_current_device(float** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail(MIKV_ECUDA, "balance_prefill_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
-  if (dev < 0 || dev >= kMaxDevices) return fail(MIKV_ECUDA, "balance_prefill_noalloc: device %d", dev);
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_balance_scratch);
-    if (e != cudaSuccess || !p)
-      return fail(MIKV_ECUDA, "balance_prefill_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-    g_scratch_ptr[dev] = static_cast<float*>(p);
-  }
-  *out = g_scratch_ptr[dev];
+// Device address of g_balance_scratch in the context current on this thread, looked up on
+// every call.  (In host code the symbol is only a host-side stand-in, never a device
+// address.)  The lookup is not cached: after cudaDeviceReset, or under another context on
+// the same device, the array lives at a different address, and a cached one would point at
+// memory that no longer belongs to it.  The lookup allocates nothing.
+int scratch_for_current_context(float** out) {
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_balance_scratch);
+  if (e != cudaSuccess || !p)
+    return fail(MIKV_ECUDA, "balance_prefill_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+  *out = static_cast<float*>(p);
   return MIKV_OK;
 }
 
@@ -196,7 +186,7 @@ extern "C" int mikv_balance_prefill_noalloc(const uint16_t* q, const uint16_t* k
   if (!aligned16(q) || !aligned16(k))
     return fail(MIKV_EALIGN, "balance_prefill_noalloc: q and k must be 16-byte aligned");
   float* scratch = nullptr;
-  if (int e = scratch_for_current_device(&scratch)) return e;
+  if (int e = scratch_for_current_context(&scratch)) return e;
   cudaStream_t s = as_stream(stream);
   const int units = B * Hkv;
   float* ws_q = scratch;
