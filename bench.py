@@ -56,6 +56,10 @@ def parse():
                    help="skip the timing of the step after attention (o . W_O and the perturbation)")
     p.add_argument("--no-topk", action="store_true",
                    help="skip the timing of the post-attention top-k over a full FP16 cache")
+    p.add_argument("--no-sweep", action="store_true",
+                   help="skip the low-tier width x budget sweep of the full-depth workload")
+    p.add_argument("--sweep-layers", type=int, default=8)
+    p.add_argument("--sweep-steps", type=int, default=8)
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     return p.parse_args()
 
@@ -213,21 +217,20 @@ def oracle_sample(wl, seconds: float):
 
 
 # ------------------------------------------------------------------------------ GPU leg
-def run_gpu(args, wl, rank, world):
+def decode_run(wl, rank, world, dev, warmup, steps, attn_steps, extra_steps=0):
+    """Prefill every layer of `wl` (untimed), then `warmup` untimed decode steps, `steps` timed
+    steps (CUDA events around the whole region, none inside it) and `attn_steps` further steps
+    with the split-K attention launch of every layer timed alone by library-recorded events.
+    The caches hold room for `extra_steps` more steps, whose decode tokens are also drawn.
+    Returns (result dict, layers, toks, index of the first unused step)."""
     import torch
 
     from mixed_precision_kv_balancer_gb300 import _lib, inputs
     from mixed_precision_kv_balancer_gb300.cache import MikvCache, n_keep
 
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    _lib.load()
-    total_steps = args.warmup + args.steps
-    # after the timed steps: K steps with the attention kernel timed alone, then K e2e steps
-    attn_steps = 0 if args.no_attn_events else args.steps
-    e2e_steps = 0 if args.no_e2e else args.steps
+    total_steps = warmup + steps
     keep0 = n_keep(wl.T, wl.budget_pct, wl.window)
-    extra = attn_steps + e2e_steps
+    extra = attn_steps + extra_steps
     cap_hi = keep0 + total_steps + extra + 1
     cap_lo = (wl.T - keep0) + total_steps + extra + 1
     layers = []
@@ -260,8 +263,7 @@ def run_gpu(args, wl, rank, world):
     # (recorded by the library on the launching stream around that one launch).  The timed
     # steps carry no events inside: events between kernels stop their launches from
     # overlapping.
-    n_ev = args.steps * wl.layers
-    attn_ev = [(new_event(), new_event()) for _ in range(n_ev if attn_steps else 0)]
+    attn_ev = [(new_event(), new_event()) for _ in range(attn_steps * wl.layers)]
     torch.cuda.synchronize()
 
     def step(s, mode=None):
@@ -277,7 +279,7 @@ def run_gpu(args, wl, rank, world):
         return 4 * len(layers)   # append, split-K attention, merge, score update/demotion
 
     attn_pairs = []
-    for s in range(args.warmup):
+    for s in range(warmup):
         step(s)
     torch.cuda.synchronize()
     if world > 1:
@@ -291,7 +293,7 @@ def run_gpu(args, wl, rank, world):
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record()
-    for s in range(args.warmup, total_steps):
+    for s in range(warmup, total_steps):
         L = wl.T + s + 1
         kv_tokens += wl.B * L * wl.layers
         read_bytes += [cache_bytes(wl, c.n_hi + 1, c.n_lo) for c in layers]
@@ -307,7 +309,7 @@ def run_gpu(args, wl, rank, world):
     clk = clocks.stop()
     ms = reduce_over_ranks(ms, world, dev)
     # per layer-step: the timed region over its layer steps (no events inside the region)
-    step_ms = [ms / (args.steps * wl.layers)]
+    step_ms = [ms / (steps * wl.layers)]
     if attn_pairs:
         attn_ms = [a0.elapsed_time(a1) for a0, a1, _ in attn_pairs]
         attn_bytes = [nb for *_, nb in attn_pairs]
@@ -317,7 +319,46 @@ def run_gpu(args, wl, rank, world):
                attn_ms_mean=statistics.mean(attn_ms), attn_bytes_mean=statistics.mean(attn_bytes),
                step_ms_mean=statistics.mean(step_ms), step_bytes_mean=statistics.mean(read_bytes),
                prefill_ms_per_layer=statistics.mean(prefill_ms))
-    e2e_first = total_steps + attn_steps
+    return res, layers, toks, total_steps + attn_steps
+
+
+# The full-depth workload's stated sweep: low-tier width x budget.
+SWEEP = [(lo, p) for lo in (2, 4) for p in (10, 20, 40)]
+
+
+def sweep_points(wl, rank, world, dev, layers, steps, warmup, peak):
+    """Each point of the sweep on `layers` layers of the workload: KV-tokens/s of the whole
+    step, and the attention kernel timed alone against the HBM peak."""
+    import torch
+    out = []
+    for lo, p in SWEEP:
+        pw = wl.scaled(lo_bits=lo, budget_pct=p, layers=layers)
+        r, ls, tk, _ = decode_run(pw, rank, world, dev, warmup, steps, steps)
+        del ls, tk
+        torch.cuda.empty_cache()
+        gbs = r["attn_bytes_mean"] / (r["attn_ms_mean"] / 1e3) / 1e9
+        out.append({"lo_bits": lo, "budget_pct": p, "layers": layers, "steps": steps,
+                    "kv_tokens_per_s": r["kv_tokens"] / (r["ms"] / 1e3),
+                    "decode_step_us_per_layer": r["step_ms_mean"] * 1e3,
+                    "attn_us_per_launch": r["attn_ms_mean"] * 1e3,
+                    "attn_bytes_per_launch": r["attn_bytes_mean"],
+                    "attn_gbs": gbs, "frac": gbs / peak, "clocks": r["clocks"]})
+    return out
+
+
+def run_gpu(args, wl, rank, world):
+    import torch
+
+    from mixed_precision_kv_balancer_gb300 import _lib, inputs
+    from mixed_precision_kv_balancer_gb300.cache import MikvCache
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    _lib.load()
+    attn_steps = 0 if args.no_attn_events else args.steps
+    e2e_steps = 0 if args.no_e2e else args.steps
+    res, layers, toks, e2e_first = decode_run(wl, rank, world, dev, args.warmup, args.steps,
+                                              attn_steps, e2e_steps)
 
     # ---- end to end through the public API with host buffers
     if not args.no_e2e:
@@ -431,6 +472,14 @@ def run_gpu(args, wl, rank, world):
         res.update(topk_ms=t_ms, topk_bytes=t_bytes, topk_k=k_keep)
         del full, ws
         torch.cuda.empty_cache()
+
+    # ---- the stated sweep of the full-depth workload (low-tier width x budget), each point
+    # on fewer layers so that the default run stays within minutes
+    if not args.no_sweep and wl.name == "llama31_8b_full":
+        del layers, toks
+        torch.cuda.empty_cache()
+        res["sweep"] = sweep_points(wl, rank, world, dev, args.sweep_layers, args.sweep_steps,
+                                    args.warmup, peaks()[0])
     return res
 
 
@@ -483,7 +532,10 @@ def main():
         ms = (wl.B * (wl.T + 1) * wl.layers) / v * 1e3
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": v, "unit": "KV-tokens/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "ms_per_step_kind": "derived, not timed: B*(T+1)*layers / value, the rate measured on a "
+                                "bounded sample of whole units scaled to the whole step",
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config,
             "cpu_baseline": {"value": v, "unit": "KV-tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
@@ -545,6 +597,13 @@ def main():
             "kept_per_head": res["topk_k"], "us_per_call": res["topk_ms"] * 1e3, "launches_per_call": 5,
             "bytes_per_call": res["topk_bytes"], "gbs": gbs, "frac_of_hbm_peak": gbs / peak,
             "timing": "CUDA events around each of 20 calls (cache larger than L2)"}
+    if "sweep" in res:
+        line["sweep"] = {
+            "what": "the full-depth workload's stated sweep, low-tier width {2, 4} x budget {10, 20, "
+                    "40}%%, FP16 important tier, each point on %d layers: KV-tokens/s of the whole "
+                    "step, and the split-K attention launch timed alone against the HBM peak"
+                    % args.sweep_layers,
+            "points": res["sweep"]}
     if "e2e_ms" in res:
         line["e2e"] = {"value": res["e2e_tokens"] / (res["e2e_ms"] / 1e3), "unit": "KV-tokens/s",
                        "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]}

@@ -143,3 +143,96 @@ def test_demoted_int8_token_requantised_from_its_int8_value():
     cache.demote(np.array([[j]], np.int32))
     np.testing.assert_array_equal(quant.unpack_codes(cache.k_lo[0, 0, n_lo], 2, 128), want)
     np.testing.assert_array_equal(cache.k_lo_meta[0, 0, n_lo], want_m)
+
+
+def test_budget_zero_is_uniform_rtn():
+    """Budget 0 with no window: every token is in the low tier, in position order, each slot
+    holding the per-token quantisation of its own (balanced) key and value, and attention is
+    softmax attention (torch's) over the dequantised keys s*code + z with q / b."""
+    rng = np.random.default_rng(6)
+    B, Hq, Hkv, T, D = 1, 4, 2, 80, 128
+    q, k, v = _inputs(rng, B, Hq, Hkv, T, D)
+    cache, info = pipeline.prefill(q, k, v, hi_bits=16, lo_bits=4, budget_pct=0, window=0)
+    assert cache.n_hi == 0 and cache.n_lo == T
+    b = info["balancer"]
+    qd = q[:, :, -1]
+    out, _, _ = cache.attend(qd)
+    for g in range(Hkv):
+        np.testing.assert_array_equal(cache.pos_lo[0, g, :T], np.arange(T))
+        for t in (0, 17, T - 1):
+            xk = k[0, g, t].astype(np.float32) * b[0, g]
+            kc, km = quant.quantize_groups(xk.astype(np.float32), 4, 64)
+            vc, vm = quant.quantize_groups(v[0, g, t].astype(np.float32), 4, 64)
+            np.testing.assert_array_equal(cache.k_lo[0, g, t], quant.pack_codes(kc, 4))
+            np.testing.assert_array_equal(cache.k_lo_meta[0, g, t], km)
+            np.testing.assert_array_equal(cache.v_lo[0, g, t], quant.pack_codes(vc, 4))
+            np.testing.assert_array_equal(cache.v_lo_meta[0, g, t], vm)
+        # dequantised rows by hand: fp16 scale and zero per 64-channel group
+        codes_k = np.unpackbits(cache.k_lo[0, g, :T, :, None], axis=2, bitorder="little")
+        codes_k = codes_k.reshape(T, D, 4) @ (1 << np.arange(4))
+        codes_v = np.unpackbits(cache.v_lo[0, g, :T, :, None], axis=2, bitorder="little")
+        codes_v = codes_v.reshape(T, D, 4) @ (1 << np.arange(4))
+        mk = cache.k_lo_meta[0, g, :T].view(np.float16).astype(np.float64)      # [T, 2, 2]
+        mv = cache.v_lo_meta[0, g, :T].view(np.float16).astype(np.float64)
+        grp = np.arange(D) // 64
+        kt = mk[:, grp, 0] * codes_k + mk[:, grp, 1]
+        vt = mv[:, grp, 0] * codes_v + mv[:, grp, 1]
+        for h in range(g * 2, g * 2 + 2):
+            qb = qd[0, h].astype(np.float64) / b[0, g].astype(np.float64)
+            ref = _textbook(qb[None], kt, vt)[0]
+            np.testing.assert_allclose(out[0, h], ref, rtol=1e-10, atol=1e-12)
+
+
+def test_two_demotions_traced_by_hand():
+    """Two decode steps with a zero query (every logit 0, so each step adds 1/L to every
+    important score and leaves their order alone), traced by hand.
+
+    Prompt of 10 tokens; important slots hold positions [0, 3, 5, 7, 9] with scores
+    [2, 0.5, 0.5, 1, 0.25]; budget 48 %, window 2.
+    Step 1 (L = 11): token 10 joins at slot 5 with score 0, every score gains a = 1/11;
+      n_keep(11) = 5 < 6, so one demotion.  Candidates are positions < 9: slots 0-3.  The
+      lowest score, 0.5 + a, is shared by positions 3 and 5; the later one, 5 (slot 2), is
+      the victim.  Slot 5 (position 10, score a) moves into slot 2: positions
+      [0, 3, 10, 7, 9]; the low tier's slot 5 takes position 5.
+    Step 2 (L = 12): token 11 joins at slot 5 with score 0, every score gains b = 1/12;
+      n_keep(12) = 5 < 6.  Candidates are positions < 10: slots 0, 1, 3, 4 (position 10 in
+      slot 2 is in the window).  Lowest: slot 4 (position 9, 0.25 + a + b).  Slot 5
+      (position 11, score b) moves into slot 4: positions [0, 3, 10, 7, 11], scores
+      [2+a+b, 0.5+a+b, a+b, 1+a+b, b]; the low tier's slot 6 takes position 9.
+    With a zero query the output is the plain mean of the attended values."""
+    rng = np.random.default_rng(9)
+    D = 128
+    k = rng.standard_normal((1, 1, 12, D)).astype(np.float16)
+    v = rng.standard_normal((1, 1, 12, D)).astype(np.float16)
+    cache = pipeline.OracleCache(1, 1, 1, D, 64, 16, 4, 8, 8, None)
+    hi_pos = np.array([[[0, 3, 5, 7, 9]]], np.int32)
+    cache.append("hi", k, v, hi_pos, 0, np.array([[[2.0, 0.5, 0.5, 1.0, 0.25]]]))
+    cache.append("lo", k, v, np.array([[[1, 2, 4, 6, 8]]], np.int32), 0)
+    q0 = np.zeros((1, 1, D), np.float16)
+    a, b_ = 1.0 / 11, 1.0 / 12
+    row = lambda t: k[0, 0, t].view(np.uint16)
+
+    out, _, vic = pipeline.decode_step(cache, q0, k[:, :, 10], v[:, :, 10], 10, budget_pct=48, window=2)
+    assert vic[0, 0] == 2
+    np.testing.assert_array_equal(cache.pos_hi[0, 0, :5], [0, 3, 10, 7, 9])
+    np.testing.assert_allclose(cache.scores[0, 0, :5], [2 + a, 0.5 + a, a, 1 + a, 0.25 + a], rtol=1e-15)
+    np.testing.assert_array_equal(cache.k_hi[0, 0, 2], row(10))
+    np.testing.assert_array_equal(cache.pos_lo[0, 0, :6], [1, 2, 4, 6, 8, 5])
+    kc, km = quant.quantize_groups(k[0, 0, 5].astype(np.float32), 4, 64)
+    np.testing.assert_array_equal(cache.k_lo[0, 0, 5], quant.pack_codes(kc, 4))
+    np.testing.assert_array_equal(cache.k_lo_meta[0, 0, 5], km)
+
+    out, _, vic = pipeline.decode_step(cache, q0, k[:, :, 11], v[:, :, 11], 11, budget_pct=48, window=2)
+    assert vic[0, 0] == 4
+    np.testing.assert_array_equal(cache.pos_hi[0, 0, :5], [0, 3, 10, 7, 11])
+    np.testing.assert_allclose(cache.scores[0, 0, :5], [2 + a + b_, 0.5 + a + b_, a + b_, 1 + a + b_, b_],
+                               rtol=1e-15)
+    np.testing.assert_array_equal(cache.k_hi[0, 0, 4], row(11))
+    np.testing.assert_array_equal(cache.pos_lo[0, 0, :7], [1, 2, 4, 6, 8, 5, 9])
+    assert (cache.n_hi, cache.n_lo) == (5, 7)
+    # the second step attended 6 important rows (FP16) and 6 low rows (dequantised), weight 1/12 each
+    hi_v = v[0, 0, [0, 3, 10, 7, 9, 11]].astype(np.float64)
+    lo_v = [quant.dequantize(*quant.quantize_groups(v[0, 0, t].astype(np.float32), 4, 64), 64)
+            for t in (1, 2, 4, 6, 8, 5)]
+    want = (hi_v.sum(axis=0) + np.sum(lo_v, axis=0)) / 12
+    np.testing.assert_allclose(out[0, 0], want, rtol=1e-12, atol=1e-14)

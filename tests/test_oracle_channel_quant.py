@@ -132,3 +132,39 @@ def test_per_channel_keys_beat_per_token_on_outlier_channels():
     codes, meta = oq.quantize_groups(k.astype(np.float32), 2, 64)
     err_token = np.abs(oq.dequantize(codes, meta, 64) - k.astype(np.float64)).mean()
     assert err_channel < 0.5 * err_token
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_full_groups_on_an_exact_grid_give_exact_attention(bits):
+    """Keys whose every channel, within each group of 64, lies on a grid z_c + j * s_c with
+    s_c a power of two and both ends j = 0 and j = qmax present: the quantiser finds
+    s = (max - min) / qmax = s_c and z = min exactly, every code is the grid index, and the
+    dequantised keys are the keys themselves.  Attention over two full groups and 20 pending
+    keys is then exactly softmax attention over the original keys (scipy's softmax here)."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(40 + bits)
+    qmax = 2 ** bits - 1
+    D, n_groups, n_pending = 128, 2, 20
+    rows = []
+    for _ in range(n_groups):
+        s_c = 2.0 ** -rng.integers(2, 6, size=D)                 # per channel, exact in fp16
+        z_c = rng.integers(-40, 40, size=D) * s_c
+        j = rng.integers(0, qmax + 1, size=(64, D))
+        j[0], j[1] = 0, qmax                                       # both ends in every channel
+        x = z_c + j * s_c
+        assert np.array_equal(x.astype(np.float16).astype(np.float64), x)   # exact in fp16
+        rows.append(x.astype(np.float16))
+    pend = rng.standard_normal((n_pending, D)).astype(np.float16)
+    k_lo = np.concatenate(rows + [pend])
+    r = cq.RetainedKeys(D, bits)
+    for row in k_lo:
+        r.append(row)
+    assert len(r.groups) == n_groups and len(r.pending) == n_pending
+    np.testing.assert_array_equal(r.keys_f64(), k_lo.astype(np.float64))
+    q = rng.standard_normal((4, D)).astype(np.float16)
+    k_hi = rng.standard_normal((30, D)).astype(np.float16)
+    v = rng.standard_normal((30 + len(k_lo), D)).astype(np.float16)
+    out, lse = cq.decode_attention_channel_keys(q, k_hi, v[:30], r, v[30:])
+    k_all = np.concatenate([k_hi, k_lo]).astype(np.float64)
+    w = softmax(q.astype(np.float64) @ k_all.T / np.sqrt(D), axis=1)
+    np.testing.assert_allclose(out, w @ v.astype(np.float64), rtol=1e-12, atol=1e-13)

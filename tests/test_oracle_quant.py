@@ -126,11 +126,21 @@ def test_balanced_keys_are_float32_products():
 
 
 def test_dequantize_f32_order():
-    """fl(fl(s*code) + z): a case where a fused multiply-add would round differently."""
-    s = np.float16(0.333251953125)
-    z = np.float16(-0.0999755859375)
-    meta = np.array([[[s.view(np.uint16), z.view(np.uint16)]]], np.uint16)
-    codes = np.full((1, 4), 3, np.uint8)
-    got = quant.dequantize_f32(codes, meta, 4)[0, 0]
-    want = np.float32(np.float32(np.float32(s) * np.float32(3)) + np.float32(z))
-    assert got == want
+    """fl32(s * code + z), rounded once to float32, against bit patterns derived by hand.
+
+    s = fp16 0x3C01 = 1025/1024, z = fp16 0x8401 = -(1025/1024) * 2^-14, code 255:
+    s*code = 261375/1024 = 255.2490234375 (exact: 19 significant bits), and
+    s*code + z = 255.24896234273910522...; float32 spacing at 2^7 is 2^-16, and the sum is
+    16727995 + 255/256 spacings, so it rounds up to 16727996 * 2^-16 = 255.24896240234375,
+    bits 0x437F3FBC.
+    s = 0x3C01, z = fp16 0x0001 = 2^-24, code 3: 3075/1024 + 2^-24 = 3.00292974710464...;
+    spacing at 2^1 is 2^-22, the sum is 12595200 + 1/4 spacings, rounds down to
+    3.0029296875, bits 0x40403000."""
+    def one(s_bits, z_bits, code):
+        meta = np.array([[[s_bits, z_bits]]], np.uint16)
+        codes = np.full((1, 4), code, np.uint8)
+        got = quant.dequantize_f32(codes, meta, 4)
+        assert got.dtype == np.float32
+        return got[0].view(np.uint32)
+    np.testing.assert_array_equal(one(0x3C01, 0x8401, 255), np.full(4, 0x437F3FBC, np.uint32))
+    np.testing.assert_array_equal(one(0x3C01, 0x0001, 3), np.full(4, 0x40403000, np.uint32))
