@@ -346,6 +346,26 @@ int mikv_channel_quantize(const uint16_t* k, int units, int n, int D, int bits, 
  */
 int mikv_set_attention_events(void* begin, void* end);
 
+/*
+ * Wait status of the tensor-core kernels (no counterpart in the papers; a failure report).
+ * The tcgen05 kernels (K3's two prefill score passes in mikv_score_update(MIKV_PREFILL),
+ * K6's V.W_O norms in mikv_select(MIKV_CRITICALKV) with w_o, K9 in
+ * mikv_output_perturbation) hand tiles between a TMA/MMA thread and their consumer warps
+ * through mbarriers, and every wait there gives up after ~4 million polls instead of
+ * spinning for ever.  No wait is expected to run out; if one does, the kernel keeps the
+ * hand-off order (so that every copy and MMA it issued still completes before it exits),
+ * writes NaN into the outputs of the affected CTA (prefill scores and -lse rows, V.W_O
+ * norms, perturbation and y partial sums), and sets a bit in a device-side status word.
+ * The call that launched it has already returned MIKV_OK (launches are asynchronous).
+ * mikv_wait_status stores the OR of the bits set since the last clear in *bits:
+ *   1 = K3 pass 1 (row log-sum-exp), 2 = K3 pass 2 (column sums), 4 = K6 (V.W_O norms),
+ *   8 = K9 (output perturbation)
+ * and clears them if `clear` is non-zero.  It copies synchronously: call it after the work
+ * in question has completed (e.g. after synchronising its stream).
+ * Errors: EINVAL (null bits), ECUDA (the copy failed).
+ */
+int mikv_wait_status(unsigned* bits, int clear);
+
 /* Message of the last failed call on this thread ("" if none). */
 const char* mikv_last_error(void);
 

@@ -27,7 +27,7 @@ EXPORTS = (
     "mikv_output_perturbation", "mikv_output_perturbation_workspace_bytes",
     "mikv_topk_attention", "mikv_topk_attention_workspace_bytes",
     "mikv_channel_quantize",
-    "mikv_set_attention_events", "mikv_last_error",
+    "mikv_set_attention_events", "mikv_wait_status", "mikv_last_error",
 )
 
 
@@ -85,6 +85,7 @@ def load() -> ctypes.CDLL:
         "mikv_topk_attention_workspace_bytes": (S, [CP, I]),
         "mikv_channel_quantize": (I, [P, I, I, I, I, P, P, P]),
         "mikv_set_attention_events": (I, [P, P]),
+        "mikv_wait_status": (I, [ctypes.POINTER(ctypes.c_uint), I]),
         "mikv_last_error": (ctypes.c_char_p, []),
     }
     for name, (res, args) in sig.items():
@@ -230,3 +231,15 @@ def mikv_set_attention_events(begin=None, end=None):
     lib = load()
     h = lambda e: None if e is None else e.cuda_event
     _check("mikv_set_attention_events", lib.mikv_set_attention_events(h(begin), h(end)))
+
+
+WAIT_BITS = {1: "K3 pass 1 (row log-sum-exp)", 2: "K3 pass 2 (column sums)", 4: "K6 (V.W_O norms)",
+             8: "K9 (output perturbation)"}
+
+
+def mikv_wait_status(clear=True) -> int:
+    """OR of the wait-status bits the tensor-core kernels set since the last clear (0 when no
+    bounded mbarrier wait gave up).  Synchronous: call after the work has completed."""
+    v = ctypes.c_uint(0)
+    _check("mikv_wait_status", load().mikv_wait_status(ctypes.byref(v), int(bool(clear))))
+    return v.value

@@ -19,6 +19,10 @@ constexpr int kNumSMs = 152;
 int fail(int code, const char* fmt, ...);
 int check_launch(const char* what);
 void clear_error();
+// Wait-status words of the source files whose tensor-core kernels poll mbarriers.
+int scores_wait_giveups(unsigned* out, bool clear);
+int select_wait_giveups(unsigned* out, bool clear);
+int perturb_wait_giveups(unsigned* out, bool clear);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }

@@ -252,7 +252,10 @@ __global__ void __launch_bounds__(kPtBlock, 1) perturb_tc_kernel(const __grid_co
       }
     }
   }
-  if (!ok) atomicExch(&bad, 1);
+  if (!ok) {
+    atomicExch(&bad, 1);
+    tc::report_giveup(tc::kGiveupPerturb);
+  }
   tc::cta_teardown(tbase, 2 * kPtN);
   if (bad && tid < 64) {  // a wait gave up: mark this CTA's perturbation outputs
     const int b = bb * kPtBatch + tid;
@@ -377,3 +380,8 @@ extern "C" int mikv_output_perturbation(const float* o, const float* o_hat, cons
   perturb_reduce_kernel<<<(n + 7) / 8, 256, 0, s>>>(part, n, ncb, pert);
   return check_launch("perturb_reduce_kernel");
 }
+
+namespace mikv {
+// This file's wait-status word (see tc::wait_giveups), for mikv_wait_status.
+int perturb_wait_giveups(unsigned* out, bool clear) { return tc::wait_giveups(out, clear); }
+}  // namespace mikv

@@ -184,7 +184,10 @@ __global__ void __launch_bounds__(kTcBlock, 2) row_lse_tc_kernel(const __grid_co
       xl[row] = l - lc;
     }
   }
-  if (!ok) atomicExch(&bad, 1);
+  if (!ok) {
+    atomicExch(&bad, 1);
+    tc::report_giveup(tc::kGiveupRowLse);
+  }
   tc::cta_teardown(tbase, kTcCols);  // (its barrier also publishes xm / xl / bad)
   if (tid < kTcTile && t < T) {
     const float m1 = xm[row], l1 = xl[row], l0 = l - lc;
@@ -320,7 +323,10 @@ __global__ void __launch_bounds__(kTcBlock, 2) col_sum_tc_kernel(const __grid_co
       }
     }
   }
-  if (!ok) atomicExch(&bad, 1);
+  if (!ok) {
+    atomicExch(&bad, 1);
+    tc::report_giveup(tc::kGiveupColSum);
+  }
   tc::cta_teardown(tbase, kTcCols);
   if (tid < kTcTile && i < T) s_full[static_cast<long>(unit) * T + i] = bad ? __int_as_float(0x7fc00000) : tot;
 }
@@ -397,3 +403,8 @@ extern "C" int mikv_score_update(int mode, const uint16_t* q, const uint16_t* k,
   }
   return fail(MIKV_EINVAL, "score_update: bad mode %d", mode);
 }
+
+namespace mikv {
+// This file's wait-status word (see tc::wait_giveups), for mikv_wait_status.
+int scores_wait_giveups(unsigned* out, bool clear) { return tc::wait_giveups(out, clear); }
+}  // namespace mikv

@@ -357,7 +357,10 @@ __global__ void __launch_bounds__(kVwoBlock, 2) vwo_norm_tc_kernel(const __grid_
       }
     }
   }
-  if (!ok) atomicExch(&bad, 1);
+  if (!ok) {
+    atomicExch(&bad, 1);
+    tc::report_giveup(tc::kGiveupVwo);
+  }
   tc::cta_teardown(tbase, kVwoCols);
   if (bad && tid < tc::kTileRows && i < L)  // a wait gave up: mark the unit's rows
     for (int hr = 0; hr < rep; ++hr) out[(static_cast<long>(b) * Hq + g * rep + hr) * L + i] = __int_as_float(0x7fc00000);
@@ -580,3 +583,8 @@ extern "C" int mikv_topk_attention(const uint16_t* q, const mikv_cache* c, int b
                                           c->Hq, c->Hkv, out, lse);
   return check_launch("topk_attend_kernel");
 }
+
+namespace mikv {
+// This file's wait-status word (see tc::wait_giveups), for mikv_wait_status.
+int select_wait_giveups(unsigned* out, bool clear) { return tc::wait_giveups(out, clear); }
+}  // namespace mikv

@@ -27,3 +27,14 @@ int check_launch(const char* what) {
 }  // namespace mikv
 
 extern "C" const char* mikv_last_error(void) { return mikv::g_msg; }
+
+extern "C" int mikv_wait_status(unsigned* bits, int clear) {
+  mikv::clear_error();
+  if (!bits) return mikv::fail(MIKV_EINVAL, "wait_status: null pointer");
+  unsigned v = 0;
+  if (int e = mikv::scores_wait_giveups(&v, clear != 0)) return e;
+  if (int e = mikv::select_wait_giveups(&v, clear != 0)) return e;
+  if (int e = mikv::perturb_wait_giveups(&v, clear != 0)) return e;
+  *bits = v;
+  return MIKV_OK;
+}

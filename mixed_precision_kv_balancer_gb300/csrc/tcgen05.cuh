@@ -80,6 +80,32 @@ __device__ __forceinline__ void mbar_init_fence() {
   asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
 }
 
+// Wait-status bits (mikv_wait_status): the kernel in which a bounded mbarrier wait gave up.
+constexpr unsigned kGiveupRowLse = 1u;   // K3 pass 1, row_lse_tc_kernel
+constexpr unsigned kGiveupColSum = 2u;   // K3 pass 2, col_sum_tc_kernel
+constexpr unsigned kGiveupVwo = 4u;      // K6, vwo_norm_tc_kernel
+constexpr unsigned kGiveupPerturb = 8u;  // K9, perturb_tc_kernel
+
+// The wait-status word of the translation unit that includes this header (internal
+// linkage: one word per source file, each read by that file's wait_giveups()).
+static __device__ unsigned g_wait_giveups = 0;
+
+// Called by a thread whose bounded wait gave up: records `bit` in the status word.
+__device__ __forceinline__ void report_giveup(unsigned bit) { atomicOr(&g_wait_giveups, bit); }
+
+// Host side: this source file's status word, cleared if `clear`.  Synchronous copies.
+static inline int wait_giveups(unsigned* out, bool clear) {
+  unsigned v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_wait_giveups, sizeof(v));
+  if (e == cudaSuccess && clear && v) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_wait_giveups, &zero, sizeof(zero));
+  }
+  if (e != cudaSuccess) return fail(MIKV_ECUDA, "wait_status: %s", cudaGetErrorString(e));
+  *out |= v;
+  return MIKV_OK;
+}
+
 // Wait for phase `parity` of the mbarrier, giving up after `limit` polls; true if it completed.
 __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, long limit = 1L << 22) {
   uint32_t done = 0;

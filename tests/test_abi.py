@@ -131,3 +131,5 @@ def test_host_side_rejections(lib):
     assert lib.mikv_set_attention_events(fake, None) == EINVAL
     assert lib.mikv_set_attention_events(None, fake) == EINVAL
     assert lib.mikv_set_attention_events(None, None) == 0
+    # the wait-status query needs somewhere to write
+    assert lib.mikv_wait_status(None, 0) == EINVAL

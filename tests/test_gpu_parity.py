@@ -400,3 +400,24 @@ def test_fused_step_equals_separate_calls(name, scale):
             n = fused.n_hi if "hi" in name_ else fused.n_lo
             assert torch.equal(a[:, :, :n], b[:, :, :n]), name_
         assert torch.equal(fused.scores[:, :, :fused.n_hi], calls.scores[:, :, :calls.n_hi])
+
+
+# ------------------------------------------------------------------ wait status
+def test_tensor_core_kernels_report_no_wait_giveup():
+    """After K3 (both prefill score passes), K6 (V.W_O norms) and K9 (output perturbation)
+    have run, the wait-status word is clear: no bounded mbarrier wait ran out.  (No test
+    forces a give-up on the GPU: a CTA must not retire with copies still in flight.)"""
+    _lib.mikv_wait_status(clear=True)
+    wl = inputs.WORKLOADS["qwen25_32b"].scaled(T=300, steps=1, hidden=256, Hq=10, Hkv=2)
+    x = {k: v.to(dev()) for k, v in inputs.make_prefill(wl, 3, "cpu").items()}
+    w_o = inputs.make_w_o(wl, 3, "cpu").to(dev())
+    gc = MikvCache(wl.B, wl.Hq, wl.Hkv, 128, wl.hi_bits, wl.lo_bits, wl.T, wl.T, dev())
+    gc.prefill(x["q"], x["k"], x["v"], wl.budget_pct, wl.window, policy="criticalkv", alpha=wl.alpha,
+               w_o=w_o)
+    o = torch.randn(2, wl.Hq, 128, device=dev())
+    y = torch.empty(2, 256, device=dev())
+    pert = torch.empty(2, wl.Hq, device=dev())
+    _lib.mikv_output_perturbation(o, o + 0.01, w_o.t().contiguous(), y=y, pert=pert)
+    torch.cuda.synchronize()
+    assert _lib.mikv_wait_status(clear=True) == 0
+    assert torch.isfinite(y).all() and torch.isfinite(pert).all()
