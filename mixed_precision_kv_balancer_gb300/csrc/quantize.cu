@@ -6,27 +6,297 @@
 // quantised as I(k*b); group size = half the head dimension), "3)" (INT8
 // important tier).
 //
-// One warp per (token, key head): lane l owns channels 4l..4l+3, so a 64-channel
-// group is one half-warp and its min/max are two 4-step shuffle reductions.  Every
-// step uses explicit round-to-nearest intrinsics in the order the format fixes:
+// Appends of many tokens (prefill) run append_tile_kernel below: 32 tokens of one (batch, key
+// head) per CTA, one thread per (tensor, 64-channel group, token).  The one-token paths
+// (demotion, and the decode step's own append) keep one warp per (token, key head): lane l
+// owns channels 4l..4l+3, so a group is one half-warp and its min/max are two 4-step shuffle
+// reductions.  Every step takes round-to-nearest in the order the format fixes:
 //   x = fl(k*b) (keys of a quantised tier) or v
 //   s = fp16(fl(fl(mx - mn) / qmax)), z = fp16(mn)
 //   code = clamp(rint_even(fl(fl(x - z) / s)), 0, qmax); 0 where s == 0.
 // Codes are packed LSB-first (channel c at bit c*bits of the row), meta is the
 // fp16 pair (scale, zero) per group.  HBM-bound: 512 B read per token-head,
 // 80/144/272/512 B written.
+#include <algorithm>
+
 #include "quant_device.cuh"
 
 namespace mikv {
 namespace {
 
-__global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
-  pdl_wait();
-  pdl_trigger();
-  const int lane = threadIdx.x & 31;
-  const long item = static_cast<long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  if (item >= a.units_tokens) return;
-  append_item(a, item, lane);
+// Appends of many tokens (prefill): one CTA of 128 threads per (32 consecutive tokens of the
+// append, unit).  The 32 source rows of K and V are gathered with coalesced 16-byte loads into
+// shared memory (16-byte chunk c of row r at chunk c ^ (r % 8), so that the eight rows a
+// quarter-warp reads next sit in different banks); then thread (tensor, group, row) quantises
+// one 64-channel group of one row from there and stores its codes with 16-byte stores:
+// 16 / 32 / 64 bytes for INT2 / INT4 / INT8.  An FP16 tier is a plain 16-byte copy.
+constexpr int kTileTok = 32;
+constexpr int kTileThreads = 128;
+
+// Packed fp32 pairs (explicit round-to-nearest PTX) for the steps after the balancer product.
+__device__ __forceinline__ uint64_t f2_bits(float2 a) {
+  return static_cast<uint64_t>(__float_as_uint(a.x)) | (static_cast<uint64_t>(__float_as_uint(a.y)) << 32);
+}
+__device__ __forceinline__ float2 bits_f2(uint64_t u) {
+  return make_float2(__uint_as_float(static_cast<uint32_t>(u)), __uint_as_float(static_cast<uint32_t>(u >> 32)));
+}
+__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(d);
+}
+__device__ __forceinline__ float2 add2_rn(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(d);
+}
+
+// Chunk `chunk` (8 channels) of a shared-memory row as 4 fp32 pairs, times the per-channel
+// factors `mul` (the balancer for keys, ones for values: x * 1 is exact).  The product is
+// taken with scalar __fmul_rn, which is never merged into a fused multiply-add: fl(k * b) - z
+// must be rounded twice, as the format states.  A packed multiply whose only use was the
+// packed subtraction of z came out fused on sm_103a (one rounding of k * b - z), which moved
+// exact ties such as d / s = 139.5 to 139.49998 and changed their codes.
+__device__ __forceinline__ void chunk_f32x2(const uint8_t* row, int chunk, int r, const float* mul, float2 (&x)[4]) {
+  const uint4 w = *reinterpret_cast<const uint4*>(row + ((chunk ^ (r & 7)) * 16));
+  const __half2* h = reinterpret_cast<const __half2*>(&w);
+  const float4 b0 = reinterpret_cast<const float4*>(mul)[2 * chunk];
+  const float4 b1 = reinterpret_cast<const float4*>(mul)[2 * chunk + 1];
+  const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __half22float2(h[e]);
+    x[e] = make_float2(__fmul_rn(f.x, bb[2 * e]), __fmul_rn(f.y, bb[2 * e + 1]));
+  }
+}
+
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// rint_even(fl(d / s)) with the correctly rounded division, for values near a tie.
+__device__ __noinline__ float rint_div(float d, float s) { return rintf(__fdiv_rn(d, s)); }
+
+// Codes and meta of one 64-channel group of one row (8 swizzled 16-byte chunks in shared
+// memory).  code = clamp(rint_even(fl(d / s)), 0, qmax), d = fl(x - z), is computed from
+// r = fl(1/s), taken once per group (__frcp_rn is correctly rounded), as q0 = fl(d * r).  q0 is
+// within a relative 2^-23 (1 + 2^-24) of d / s: below |d/s| = 257 that is less than 2^-14
+// absolute, and fl(d / s) is within 2^-16 of d / s, so rint(q0) and rint(fl(d / s)) can only
+// differ when d / s lies within ~2^-13 of a half-integer.  A value whose q0 comes within
+// 2^-12 of one (|q0 - rint(q0)| > 1/2 - 2^-12) takes the correctly rounded __fdiv_rn quotient
+// instead.  The codes therefore equal the rounding of fl(d / s) in every case.
+//   d and q0 are monotone in x, so when the group's extremes give q0 inside
+// (-1/2, qmax + 1/2) with a 2^-10 margin, no value needs the clamp: that common case runs on
+// packed fp32 pairs, rounds with 1.5 * 2^23 (q + 1.5*2^23 lands on the integer grid, ties to
+// even, for |q| < 2^22) and packs the codes of 16-bit fields as exact fp32 sums
+// sum c_i 2^(BITS i) < 2^16.  Otherwise every value is clamped one by one.
+constexpr float kTieGuard = 1.f / 4096.f;
+constexpr float kRangeGuard = 1.f / 1024.f;
+constexpr float kRoundMagic = 12582912.f;  // 1.5 * 2^23
+
+template <int BITS>
+__device__ __forceinline__ uint32_t quantize_group64(const uint8_t* row, int g, int r, const float* mul,
+                                                     bool scaled, uint32_t (&out)[64 * BITS / 32]) {
+  constexpr int kWords = 64 * BITS / 32;
+  constexpr int qmax = (1 << BITS) - 1;
+  float mn, mx;
+  if (scaled) {  // keys of a balanced tier: the extremes of fl(k * b)
+    mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float2 x[4];
+      chunk_f32x2(row, g * 8 + i, r, mul, x);
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        mn = min3f(mn, x[p].x, x[p].y);
+        mx = max3f(mx, x[p].x, x[p].y);
+      }
+    }
+  } else {  // fp16 values as they are: min / max of fp16 numbers are exact in half2 arithmetic
+    __half2 m0 = __float2half2_rn(INFINITY), m1 = __float2half2_rn(-INFINITY);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint4 w = *reinterpret_cast<const uint4*>(row + (((g * 8 + i) ^ (r & 7)) * 16));
+      const __half2* h = reinterpret_cast<const __half2*>(&w);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        m0 = __hmin2(m0, h[e]);
+        m1 = __hmax2(m1, h[e]);
+      }
+    }
+    mn = fminf(__low2float(m0), __high2float(m0));
+    mx = fmaxf(__low2float(m1), __high2float(m1));
+  }
+  const float s32 = __fdiv_rn(__fsub_rn(mx, mn), static_cast<float>(qmax));
+  const __half sh = __float2half_rn(s32), zh = __float2half_rn(mn);
+  const float sf = __half2float(sh), zf = __half2float(zh);
+#pragma unroll
+  for (int k = 0; k < kWords; ++k) out[k] = 0u;
+  if (sf == 0.f) return pack_half2(sh, zh);
+  const float rf = __frcp_rn(sf);
+  const float q_lo = __fmul_rn(__fsub_rn(mn, zf), rf), q_hi = __fmul_rn(__fsub_rn(mx, zf), rf);
+  if (q_lo > -0.5f + kRangeGuard && q_hi < qmax + 0.5f - kRangeGuard) {
+    const float2 nz = make_float2(-zf, -zf), r2 = make_float2(rf, rf);
+    const float2 mg = make_float2(kRoundMagic, kRoundMagic), nmg = make_float2(-kRoundMagic, -kRoundMagic);
+    const float2 m1 = make_float2(-1.f, -1.f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float2 x[4], d[4], qi[4];
+      chunk_f32x2(row, g * 8 + i, r, mul, x);
+      float emax = 0.f;  // largest |q0 - rint(q0)| of the chunk
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        d[p] = add2_rn(x[p], nz);
+        const float2 q = mul2_rn(d[p], r2);
+        qi[p] = add2_rn(add2_rn(q, mg), nmg);
+        const float2 e = __ffma2_rn(qi[p], m1, q);  // q - qi, exact
+        emax = max3f(emax, fabsf(e.x), fabsf(e.y));
+      }
+      if (emax > 0.5f - kTieGuard) {  // rare: a value of this chunk is near a tie
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          if (fabsf(__fmul_rn(d[p].x, rf) - qi[p].x) > 0.5f - kTieGuard) qi[p].x = rint_div(d[p].x, sf);
+          if (fabsf(__fmul_rn(d[p].y, rf) - qi[p].y) > 0.5f - kTieGuard) qi[p].y = rint_div(d[p].y, sf);
+        }
+      }
+      // 16-bit fields of kPack codes each, summed exactly as fp32 pairs
+      constexpr int kPack = 16 / BITS;
+#pragma unroll
+      for (int f = 0; f < 8 / kPack; ++f) {
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int p = f * kPack / 2; p < (f + 1) * kPack / 2; ++p) {
+          const int e0 = 2 * p - f * kPack;  // index of qi[p].x within the field
+          acc = __ffma2_rn(qi[p], make_float2(static_cast<float>(1 << (BITS * e0)),
+                                              static_cast<float>(1 << (BITS * (e0 + 1)))), acc);
+        }
+        const int bit = (i * 8 + f * kPack) * BITS;  // first bit of the field in the group
+        out[bit / 32] |= (__float_as_uint((acc.x + acc.y) + 8388608.f) & 0xffffu) << (bit % 32);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float2 x[4];
+      chunk_f32x2(row, g * 8 + i, r, mul, x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float xe = e & 1 ? x[e >> 1].y : x[e >> 1].x;
+        const float d = __fsub_rn(xe, zf);
+        const float q = __fmul_rn(d, rf);
+        float qi = rintf(q);
+        if (fabsf(q - qi) > 0.5f - kTieGuard) qi = rint_div(d, sf);
+        const int ch = i * 8 + e;
+        out[ch * BITS / 32] |= static_cast<uint32_t>(fminf(fmaxf(qi, 0.f), static_cast<float>(qmax)))
+                               << ((ch * BITS) % 32);
+      }
+    }
+  }
+  return pack_half2(sh, zh);
+}
+
+// Tile of 32 consecutive tokens of one unit: 2 tensors x 32 rows x 16 chunks of 16 bytes,
+// kPer chunks per thread (rows (t / 16) + 8 m, chunk t % 16).
+constexpr int kPer = 2 * kTileTok * 16 / kTileThreads;
+
+struct TileAt {
+  long unit;
+  int j0, nt;
+};
+__device__ __forceinline__ TileAt tile_at(const AppendArgs& a, long tile, int tiles_per_unit) {
+  TileAt p;
+  p.unit = tile / tiles_per_unit;
+  p.j0 = static_cast<int>(tile % tiles_per_unit) * kTileTok;
+  p.nt = min(kTileTok, a.n_tokens - p.j0);
+  return p;
+}
+// Source row of token j0 + r of the tile, or -1 (past the end, or out of range: left unchanged).
+__device__ __forceinline__ int tile_src(const AppendArgs& a, const TileAt& p, int r) {
+  if (r >= p.nt) return -1;
+  const int src = a.src_pos ? a.src_pos[p.unit * a.n_tokens + p.j0 + r] : p.j0 + r;
+  return (src < 0 || src >= a.src_len) ? -1 : src;
+}
+
+// FP16 tier: a plain copy, all of a thread's 16-byte loads issued before its stores.
+__global__ void __launch_bounds__(kTileThreads) append_copy_kernel(AppendArgs a, int tiles_per_unit) {
+  const TileAt p = tile_at(a, blockIdx.x, tiles_per_unit);
+  const int t = threadIdx.x, c = t & 15;
+  int src[kPer / 2];
+  uint4 w[kPer];
+#pragma unroll
+  for (int m = 0; m < kPer / 2; ++m) src[m] = tile_src(a, p, (t >> 4) + 8 * m);
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int m = k % (kPer / 2), tensor = k / (kPer / 2);
+    if (src[m] >= 0) w[k] = __ldg(reinterpret_cast<const uint4*>((tensor ? a.v : a.k) + (p.unit * a.src_len + src[m]) * kD) + c);
+  }
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int m = k % (kPer / 2), tensor = k / (kPer / 2), r = (t >> 4) + 8 * m;
+    if (src[m] >= 0)
+      reinterpret_cast<uint4*>((tensor ? a.dv : a.dk) + (p.unit * a.cap + a.base_slot + p.j0 + r) * (kD * 2))[c] = w[k];
+  }
+  if (t < kTileTok) {
+    const int sr = tile_src(a, p, t);
+    if (sr >= 0) {
+      const long slot = p.unit * a.cap + a.base_slot + p.j0 + t;
+      a.dpos[slot] = sr + a.pos_base;
+      if (a.dscores) a.dscores[slot] = a.src_scores ? a.src_scores[p.unit * a.n_tokens + p.j0 + t] : 0.f;
+    }
+  }
+}
+
+// Quantised tiers: one CTA per tile.  Its rows (and the unit's balancer) are copied into
+// shared memory with cp.async, all of a thread's copies in flight at once; then thread
+// (tensor, group, row) quantises one group.  Several CTAs per SM overlap one tile's copies
+// with another's arithmetic.
+template <int BITS>
+__global__ void __launch_bounds__(kTileThreads) append_tile_kernel(AppendArgs a, int tiles_per_unit) {
+  __shared__ __align__(16) uint8_t rows[2][kTileTok][kD * 2];
+  __shared__ __align__(16) float smul[2][kD];  // keys: the balancer (or ones); values: ones
+  __shared__ int ssrc[kTileTok];
+  const int t = threadIdx.x, c = t & 15;
+  const TileAt p = tile_at(a, blockIdx.x, tiles_per_unit);
+#pragma unroll
+  for (int m = 0; m < kPer / 2; ++m) {
+    const int r = (t >> 4) + 8 * m;
+    const int src = tile_src(a, p, r);
+    if (c == 0) ssrc[r] = src;
+#pragma unroll
+    for (int tensor = 0; tensor < 2; ++tensor) {
+      const __half* row = (tensor ? a.v : a.k) + (p.unit * a.src_len + (src >= 0 ? src : 0)) * kD;
+      cp_async16(smem_u32(&rows[tensor][r][(c ^ (r & 7)) * 16]), row + c * 8, src >= 0);
+    }
+  }
+  if (a.bal && t < kD / 4) cp_async16(smem_u32(&smul[0][4 * t]), a.bal + p.unit * kD + 4 * t, true);
+  if (!a.bal) smul[0][t] = 1.f;
+  smul[1][t] = 1.f;
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+  if (t < kTileTok && ssrc[t] >= 0) {
+    const long slot = p.unit * a.cap + a.base_slot + p.j0 + t;
+    a.dpos[slot] = ssrc[t] + a.pos_base;
+    if (a.dscores) a.dscores[slot] = a.src_scores ? a.src_scores[p.unit * a.n_tokens + p.j0 + t] : 0.f;
+  }
+  const int tensor = t >> 6, g = (t >> 5) & 1, r = t & 31;
+  if (ssrc[r] < 0) return;
+  uint32_t out[64 * BITS / 32];
+  const uint32_t meta = quantize_group64<BITS>(rows[tensor][r], g, r, smul[tensor], tensor == 0 && a.bal != nullptr, out);
+  const long slot = p.unit * a.cap + a.base_slot + p.j0 + r;
+  constexpr int kRB = kD * BITS / 8;
+  uint8_t* dst = (tensor ? a.dv : a.dk) + slot * kRB + g * (kRB / 2);
+#pragma unroll
+  for (int k = 0; k < 64 * BITS / 128; ++k)
+    reinterpret_cast<uint4*>(dst)[k] = make_uint4(out[4 * k], out[4 * k + 1], out[4 * k + 2], out[4 * k + 3]);
+  reinterpret_cast<uint32_t*>(tensor ? a.dvm : a.dkm)[slot * 2 + g] = meta;
 }
 
 __global__ void __launch_bounds__(256) demote_kernel(DemoteArgs a) {
@@ -107,27 +377,27 @@ int append_args(bool hi, const uint16_t* k, const uint16_t* v, int src_len, cons
   return MIKV_OK;
 }
 
-// Validate and launch an append (see append_args); after: the kernel launched just before on
-// `s` is one of ours and this launch may overlap its tail.
+// Validate and launch an append (see append_args).
 int append_tokens(bool hi, const uint16_t* k, const uint16_t* v, int src_len, const int32_t* src_pos,
                   int n_tokens, int pos_base, const float* src_scores, const mikv_cache* c,
-                  cudaStream_t s, unsigned* ticket, bool after) {
+                  cudaStream_t s) {
   AppendArgs a;
-  if (int e = append_args(hi, k, v, src_len, src_pos, n_tokens, pos_base, src_scores, c, ticket, a))
+  if (int e = append_args(hi, k, v, src_len, src_pos, n_tokens, pos_base, src_scores, c, nullptr, a))
     return e;
-  if (n_tokens > 0) {
-    const long blocks = (a.units_tokens + 7) / 8;
-    if (after) {
-      if (int e = check_launch_after(
-              launch_after(append_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, a),
-              "append_kernel"))
-        return e;
-    } else {
-      append_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
-      if (int e = check_launch("append_kernel")) return e;
-    }
+  if (n_tokens == 0) return MIKV_OK;
+  const long units = static_cast<long>(c->B) * c->Hkv;
+  const int tiles_per_unit = (n_tokens + kTileTok - 1) / kTileTok;
+  const long ntiles = units * tiles_per_unit;
+  if (a.bits == 16) {
+    if (ntiles > 0x7fffffffL) return fail(MIKV_ESHAPE, "quantize_append: %ld tiles", ntiles);
+    append_copy_kernel<<<static_cast<unsigned>(ntiles), kTileThreads, 0, s>>>(a, tiles_per_unit);
+    return check_launch("append_copy_kernel");
   }
-  return MIKV_OK;
+  if (ntiles > 0x7fffffffL) return fail(MIKV_ESHAPE, "quantize_append: %ld tiles", ntiles);
+  void (*kern)(AppendArgs, int) = a.bits == 8 ? append_tile_kernel<8>
+                                  : a.bits == 4 ? append_tile_kernel<4> : append_tile_kernel<2>;
+  kern<<<static_cast<unsigned>(ntiles), kTileThreads, 0, s>>>(a, tiles_per_unit);
+  return check_launch("append_tile_kernel");
 }
 
 // Demotion arguments for the current counts of *c (victim list: [B*Hkv] hi slots).
@@ -175,8 +445,7 @@ extern "C" int mikv_quantize_append(int tier, const uint16_t* k, const uint16_t*
   cudaStream_t s = as_stream(stream);
   if (tier == MIKV_TIER_HI || tier == MIKV_TIER_LO) {
     const bool hi = tier == MIKV_TIER_HI;
-    if (int e = append_tokens(hi, k, v, src_len, src_pos, n_tokens, pos_base, src_scores, c, s,
-                              nullptr, false))
+    if (int e = append_tokens(hi, k, v, src_len, src_pos, n_tokens, pos_base, src_scores, c, s))
       return e;
     if (hi) c->n_hi += n_tokens;
     else c->n_lo += n_tokens;

@@ -14,6 +14,7 @@ from mixed_precision_kv_balancer_gb300 import _lib, inputs
 from mixed_precision_kv_balancer_gb300.cache import MikvCache
 from oracle import balance as obal
 from oracle import pipeline as opipe
+from oracle import quant as oquant
 from oracle import scores as oscores
 from oracle import select as osel
 
@@ -108,6 +109,88 @@ def test_append_without_balancer_and_ragged_counts():
     compare_tiers(gc, oc)
     with pytest.raises(_lib.MikvError):   # full tier: rejected on the host, nothing launched
         _lib.mikv_quantize_append(_lib.MIKV_TIER_LO, gc, d["k"], d["v"], torch.from_numpy(ep[:, :, :1]).to(dev()), 1)
+
+
+def _tie_rows(rng, T, qmax):
+    """fp16 rows whose 64-channel groups put values exactly on, and one fp16 step next to, the
+    half-integer points z + (k + 1/2) s of their own quantisation grid (s with few mantissa
+    bits, the group's ends at z and z + qmax s), so that (x - z) / s meets rounding ties."""
+    rows = np.zeros((T, 128), np.float16)
+    for t in range(T):
+        for g in range(2):
+            s = np.float32(rng.choice([1, 3, 5, 7]) * 2.0 ** -int(rng.integers(2, 7)))
+            z = np.float32(int(rng.integers(-40, 40)) * s / 2)
+            k = rng.integers(0, qmax, size=64)
+            x = (z + (k + 0.5) * s).astype(np.float16)
+            step = rng.integers(-1, 2, size=64)      # -1, 0, +1 fp16 steps away from the tie
+            away = np.nextafter(x, np.where(step > 0, np.float16(np.inf), np.float16(-np.inf)))
+            x = np.where((step != 0) & (np.abs(x) > 1e-2), away, x)
+            x[0], x[1] = z, z + qmax * s
+            rows[t, g * 64:(g + 1) * 64] = x.astype(np.float16)
+    return rows
+
+
+@pytest.mark.parametrize("hi_bits,lo_bits", [(16, 2), (16, 4), (8, 8)])
+def test_append_near_tie_codes_bit_exact(hi_bits, lo_bits):
+    """The prefill append's quotient fast path (reciprocal, product, exact division near a
+    half-integer) against the oracle's fl(d / s) on values placed at rounding ties."""
+    rng = np.random.default_rng(70 + lo_bits)
+    T, keep = 96, 16
+    qmax = 2 ** lo_bits - 1
+    k = _tie_rows(rng, T, qmax)[None, None]
+    v = _tie_rows(rng, T, qmax)[None, None]
+    kp = np.sort(rng.choice(T, keep, replace=False)).astype(np.int32)[None, None]
+    ep = np.setdiff1d(np.arange(T), kp[0, 0]).astype(np.int32)[None, None]
+    oc = opipe.OracleCache(1, 1, 1, 128, 64, hi_bits, lo_bits, keep, T - keep, None)
+    oc.append("hi", k, v, kp, 0)
+    oc.append("lo", k, v, ep, 0)
+    gc = MikvCache(1, 1, 1, 128, hi_bits, lo_bits, keep, T - keep, dev(), use_balancer=False)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+    gc.append_positions(t(k), t(v), t(kp), t(ep))
+    torch.cuda.synchronize()
+    compare_tiers(gc, oc)
+
+
+# (fp16 key bits, fp32 balancer bits, group zero z, group scale s): fl(fl(k b) - z) / s is
+# exactly a half-integer (an INT8 rounding tie, resolved to even), while the once-rounded
+# fused value k b - z lies just beside it; found on the seeded Llama-3.1-8B-shaped workload.
+_BALANCED_TIES = [(0xb0a5, 0x4062c927, -11.5234375, 0.07891846), (0x3c69, 0x3ff2dea7, -12.3046875, 0.07678223),
+                  (0x4095, 0x4064ff5c, -42.9375, 0.20251465), (0xb820, 0x407efb29, -6.5820312, 0.06707764),
+                  (0x3a36, 0x407cbcb0, -5.8671875, 0.06793213), (0x3d97, 0x406b60c5, -19.546875, 0.10394287),
+                  (0xbdbd, 0x3f874748, -8.9921875, 0.062561035)]
+
+
+def test_append_balanced_key_exact_ties():
+    """Balanced keys whose quotient fl(fl(k b) - z) / s is exactly k + 1/2: fl(k b) must be
+    rounded before z is subtracted, as the format states (a fused k b - z gives the neighbouring
+    code).  One unit per case: channel 0 is the group minimum z, channel 1 the maximum z + 255 s
+    (so the group's scale is s), channel 2 carries (k, b); the second group repeats the first."""
+    n = len(_BALANCED_TIES)
+    k = np.zeros((n, 1, 1, 128), np.float16)
+    bal = np.ones((n, 1, 128), np.float32)
+    for u, (kb, bb, z, s) in enumerate(_BALANCED_TIES):
+        k[u, 0, 0, 0] = np.float16(z)
+        k[u, 0, 0, 1] = np.float16(float(np.float16(z)) + 255 * float(np.float16(s)))
+        k[u, 0, 0, 2] = np.array([kb], np.uint16).view(np.float16)[0]
+        bal[u, 0, 2] = np.array([bb], np.uint32).view(np.float32)[0]
+    k[..., 64:] = k[..., :64]
+    bal[..., 64:] = bal[..., :64]
+    v = k.copy()
+    for u in range(n):
+        xk = oquant.balance_keys(k[u, 0, 0], bal[u, 0])
+        _, meta = oquant.quantize_groups(xk, 8, 64)
+        s, z = (np.float32(np.uint16(m).view(np.float16)) for m in meta[0])
+        q = np.float32(np.float32(xk[2] - z) / s)
+        assert q - np.floor(q) == 0.5                                   # the tie is there
+    pos = np.zeros((n, 1, 1), np.int32)
+    oc = opipe.OracleCache(n, 1, 1, 128, 64, 8, 4, 1, 1, bal)
+    oc.append("hi", k, v, pos, 0)
+    gc = MikvCache(n, 1, 1, 128, 8, 4, 1, 1, dev())
+    gc.balancer.copy_(torch.from_numpy(bal))
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+    _lib.mikv_quantize_append(_lib.MIKV_TIER_HI, gc, t(k), t(v), t(pos), 1, 0)
+    torch.cuda.synchronize()
+    compare_tiers(gc, oc, what=("hi",))
 
 
 # ------------------------------------------------------------------ decode attention (K7/K8)
