@@ -168,3 +168,98 @@ def test_full_groups_on_an_exact_grid_give_exact_attention(bits):
     k_all = np.concatenate([k_hi, k_lo]).astype(np.float64)
     w = softmax(q.astype(np.float64) @ k_all.T / np.sqrt(D), axis=1)
     np.testing.assert_allclose(out, w @ v.astype(np.float64), rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------------------------------ the composed cache
+def _textbook(q, k, v):
+    """float64 softmax attention by torch's scaled_dot_product_attention (an independent routine)."""
+    import torch
+    qt = torch.from_numpy(q.astype(np.float64))[None, :, None, :]
+    kt = torch.from_numpy(k.astype(np.float64))[None, None].expand(1, q.shape[0], -1, -1)
+    vt = torch.from_numpy(v.astype(np.float64))[None, None].expand(1, q.shape[0], -1, -1)
+    return torch.nn.functional.scaled_dot_product_attention(qt, kt, vt)[0, :, 0].numpy()
+
+
+def _binary_inputs(rng, B, Hkv, L, D, bits):
+    """Keys that take two values per (key head, channel), z_c and z_c + qmax s_c, and values
+    that take two values per (token, 64-channel group), a and a + qmax sigma, with power-of-two
+    steps: any group of them quantises exactly (both ends present, or a constant channel /
+    group with scale 0), per channel or per token, so the whole cache reconstructs K and V."""
+    qmax = 2 ** bits - 1
+    s = 2.0 ** -rng.integers(3, 6, size=(B, Hkv, 1, D))
+    z = rng.integers(-8, 8, size=(B, Hkv, 1, D)) * s
+    k = (z + qmax * s * rng.integers(0, 2, size=(B, Hkv, L, D))).astype(np.float16)
+    sig = 2.0 ** -rng.integers(3, 6, size=(B, Hkv, L, 2, 1))
+    a = rng.integers(-8, 8, size=(B, Hkv, L, 2, 1)) * sig
+    v = (a + qmax * sig * rng.integers(0, 2, size=(B, Hkv, L, 2, 64))).reshape(B, Hkv, L, D).astype(np.float16)
+    assert np.array_equal(k.astype(np.float64), z + qmax * s * (k.astype(np.float64) != z))
+    return k, v
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_channel_cache_on_binary_inputs_is_exact_attention(bits):
+    """Prefill (H2O selection, 2 full groups + 32 waiting pairs per unit) and 45 decode steps
+    (a pair demoted on 4 steps of 5; the third group closes on the way): every step's output
+    equals softmax attention over all L tokens' original keys and values, since every pair is
+    kept (FP16 or quantised exactly) and none is lost or duplicated.  The positions of both
+    tiers partition 0 .. L - 1 at every step."""
+    rng = np.random.default_rng(60 + bits)
+    B, Hq, Hkv, T, D, steps = 1, 4, 2, 200, 128, 45
+    k, v = _binary_inputs(rng, B, Hkv, T + steps, D, bits)
+    q = rng.standard_normal((B, Hq, T + steps, D)).astype(np.float16)
+    cache, _ = cq.prefill_channel(q[:, :, :T], k[:, :, :T], v[:, :, :T], lo_bits=bits, budget_pct=20,
+                                  window=8, extra_steps=steps)
+    assert (cache.n_hi, cache.n_lo, cache.n_pending) == (40, 160, 32)
+    closed = False
+    for s in range(steps):
+        L = T + s + 1
+        out, _, _ = cq.decode_step_channel(cache, q[:, :, L - 1], k[:, :, L - 1], v[:, :, L - 1], L - 1,
+                                           budget_pct=20, window=8)
+        for g in range(Hkv):
+            pos = sorted(cache.pos_hi[0, g, :cache.n_hi].tolist() + cache.pos_lo[0, g, :cache.n_lo].tolist())
+            assert pos == list(range(L))
+            hs = slice(g * 2, g * 2 + 2)
+            want = _textbook(q[0, hs, L - 1], k[0, g, :L], v[0, g, :L])
+            np.testing.assert_allclose(out[0, hs], want, rtol=1e-11, atol=1e-12)
+        closed |= cache.n_lo >= 192
+    assert closed and cache.n_lo // 64 == 3
+
+
+def test_the_64th_pair_closes_the_group():
+    """Counts and slot order: 160 evicted tokens give two groups and 32 waiting pairs in
+    position order; demoted pairs wait in order of arrival; the 32nd demotion closes the third
+    group, whose slots 128 .. 191 hold the 32 waiting evicted positions then the 32 victims,
+    and whose keys dequantise to the original keys of those tokens (binary inputs)."""
+    rng = np.random.default_rng(70)
+    B, Hq, Hkv, T, D = 1, 2, 1, 200, 128
+    k, v = _binary_inputs(rng, B, Hkv, T, D, 2)
+    q = rng.standard_normal((B, Hq, T, D)).astype(np.float16)
+    cache, info = cq.prefill_channel(q, k, v, lo_bits=2, budget_pct=40, window=8, extra_steps=0)
+    assert (cache.n_hi, cache.n_lo, cache.n_pending) == (80, 120, 56)
+    # demote 8 times by hand: important slot 0 each time (swap-remove keeps the tier dense)
+    victims = []
+    for i in range(8):
+        victims.append(int(cache.pos_hi[0, 0, 0]))
+        cache.demote(np.zeros((1, 1), np.int32))
+        assert cache.n_pending == (57 + i) % 64
+    assert cache.n_lo == 128 and cache.n_pending == 0
+    np.testing.assert_array_equal(cache.pos_lo[0, 0, 64:128],
+                                  np.concatenate([info["evict_pos"][0, 0, 64:120], victims]))
+    r, _ = cache.retained(0, 0)
+    assert len(r.groups) == 2 and not r.pending
+    np.testing.assert_array_equal(r.keys_f64()[64:], k[0, 0, cache.pos_lo[0, 0, 64:128]].astype(np.float64))
+
+
+def test_channel_cache_with_only_waiting_pairs_is_exact():
+    """Fewer than 64 retained tokens: every retained pair waits in FP16, so attention over the
+    cache is exact attention over the prompt, whatever the inputs."""
+    rng = np.random.default_rng(71)
+    q = rng.standard_normal((1, 4, 80, 128)).astype(np.float16)
+    k = rng.standard_normal((1, 2, 80, 128)).astype(np.float16)
+    v = rng.standard_normal((1, 2, 80, 128)).astype(np.float16)
+    cache, _ = cq.prefill_channel(q, k, v, lo_bits=2, budget_pct=40, window=8)
+    assert cache.n_lo == 48 and cache.n_pending == 48
+    out, _, _ = cache.attend(q[:, :, -1])
+    for g in range(2):
+        want = _textbook(q[0, 2 * g:2 * g + 2, -1], k[0, g], v[0, g])
+        np.testing.assert_allclose(out[0, 2 * g:2 * g + 2], want, rtol=1e-11, atol=1e-12)
