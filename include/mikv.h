@@ -65,6 +65,10 @@ extern "C" {
 #define MIKV_TIER_LO 1
 #define MIKV_TIER_DEMOTE 2
 
+/* mikv_cache.key_mode: how the low tier stores keys */
+#define MIKV_KEYS_PER_TOKEN 0   /* per-token asymmetric groups of 64 channels (MiKV) */
+#define MIKV_KEYS_PER_CHANNEL 1 /* per-channel groups of 64 slots (the Appendix C alternative) */
+
 /*
  * One layer's two-tier cache ([notes] "Key contributions 1)" and "3)": tokens
  * an eviction policy would drop are kept in low precision next to the important
@@ -89,6 +93,21 @@ extern "C" {
  * lo_bits <= hi_bits.  Quantised keys (INT8/INT4 hi tier and the lo tier) hold I(k*b); the FP16 tier holds
  * the original k.  Values are never balanced.
  * Code and meta buffers must be 16-byte aligned.
+ *
+ * key_mode == MIKV_KEYS_PER_CHANNEL ([notes] Appendix C remarks: per-channel quantisation
+ * isolates outlier channels, but a cache then has to hold KV pairs in a buffer until enough
+ * have accumulated; [paperlayer] C: group size 64, keys per channel, 20 % FP16 / 80 % INTx):
+ *   hi_bits must be 16 and lo_bits 2 or 4; cap_lo a multiple of 64; the balancer is not used.
+ *   The low tier's slots [0, n_lo - n_lo % 64) form closed groups of 64 slots: k_lo holds
+ *   per-token code rows as above, but their scale and zero are per (group, channel):
+ *   k_lo_meta [B][Hkv][cap_lo/64][D][2] fp16 (scale, zero), the per-token quantizer's rule
+ *   applied to each channel's 64 values; v_lo and v_lo_meta stay per token.
+ *   The last n_lo % 64 retained pairs wait unquantised:
+ *   k_pend, v_pend fp16 [B][Hkv][64][D], row p = slot n_lo - n_lo % 64 + p (pos_lo holds their
+ *   positions).  The pair that brings them to 64 closes the group: its keys are quantised per
+ *   channel and its values per token into the group's slots.  Attention reads closed groups
+ *   and waiting pairs (as stored); waiting pairs are attended with the original q.
+ * key_mode == MIKV_KEYS_PER_TOKEN (0): k_pend, v_pend unused (NULL).
  */
 typedef struct mikv_cache {
   int32_t B, Hkv, Hq, D;
@@ -107,6 +126,9 @@ typedef struct mikv_cache {
   int32_t* pos_lo;
   const float* balancer;
   float* scores;
+  int32_t key_mode; /* MIKV_KEYS_PER_TOKEN or MIKV_KEYS_PER_CHANNEL */
+  void* k_pend;     /* per-channel keys: waiting pairs, fp16 [B][Hkv][64][D] */
+  void* v_pend;
 } mikv_cache;
 
 /*

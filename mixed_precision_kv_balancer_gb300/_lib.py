@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(_HERE, "libmikv.so")
 MIKV_PREFILL, MIKV_DECODE = 0, 1
 MIKV_H2O, MIKV_CRITICALKV, MIKV_DEMOTE = 0, 1, 2
 MIKV_TIER_HI, MIKV_TIER_LO, MIKV_TIER_DEMOTE = 0, 1, 2
+MIKV_KEYS_PER_TOKEN, MIKV_KEYS_PER_CHANNEL = 0, 1
 
 EXPORTS = (
     "mikv_balance_prefill", "mikv_balance_workspace_bytes", "mikv_balance_prefill_noalloc",
@@ -49,6 +50,7 @@ class mikv_cache(ctypes.Structure):
         ("k_lo_meta", ctypes.c_void_p), ("v_lo_meta", ctypes.c_void_p),
         ("pos_hi", ctypes.c_void_p), ("pos_lo", ctypes.c_void_p),
         ("balancer", ctypes.c_void_p), ("scores", ctypes.c_void_p),
+        ("key_mode", ctypes.c_int32), ("k_pend", ctypes.c_void_p), ("v_pend", ctypes.c_void_p),
     ]
 
 

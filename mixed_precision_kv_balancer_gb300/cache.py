@@ -30,10 +30,18 @@ class MikvCache:
     """One layer's cache: tiers, metadata, positions, scores, balancer, plus reusable workspaces."""
 
     def __init__(self, B, Hq, Hkv, D, hi_bits, lo_bits, cap_hi, cap_lo, device="cuda",
-                 use_balancer=True):
+                 use_balancer=True, key_mode=_lib.MIKV_KEYS_PER_TOKEN):
+        """key_mode MIKV_KEYS_PER_CHANNEL: the low tier keeps per-channel keys in closed groups of
+        64 slots and the last n_lo % 64 retained pairs in FP16 (cap_lo is rounded up to a
+        multiple of 64; no balancer)."""
         assert D == 128 and Hq % Hkv == 0
         self.B, self.Hq, self.Hkv, self.D = B, Hq, Hkv, D
         self.hi_bits, self.lo_bits = hi_bits, lo_bits
+        self.key_mode = key_mode
+        per_channel = key_mode == _lib.MIKV_KEYS_PER_CHANNEL
+        if per_channel:
+            cap_lo = -(-cap_lo // 64) * 64
+            use_balancer = False
         self.device = torch.device(device)
         dev = self.device
         ng = D // 64
@@ -49,8 +57,14 @@ class MikvCache:
         rb = D * lo_bits // 8
         self.k_lo = torch.zeros(B, Hkv, cap_lo, rb, dtype=torch.uint8, device=dev)
         self.v_lo = torch.zeros_like(self.k_lo)
-        self.k_lo_meta = torch.zeros(B, Hkv, cap_lo, ng, 2, dtype=torch.float16, device=dev)
-        self.v_lo_meta = torch.zeros_like(self.k_lo_meta)
+        self.v_lo_meta = torch.zeros(B, Hkv, cap_lo, ng, 2, dtype=torch.float16, device=dev)
+        if per_channel:
+            self.k_lo_meta = torch.zeros(B, Hkv, cap_lo // 64, D, 2, dtype=torch.float16, device=dev)
+            self.k_pend = torch.zeros(B, Hkv, 64, D, dtype=torch.float16, device=dev)
+            self.v_pend = torch.zeros_like(self.k_pend)
+        else:
+            self.k_lo_meta = torch.zeros_like(self.v_lo_meta)
+            self.k_pend = self.v_pend = None
         self.pos_hi = torch.zeros(B, Hkv, cap_hi, dtype=torch.int32, device=dev)
         self.pos_lo = torch.zeros(B, Hkv, cap_lo, dtype=torch.int32, device=dev)
         self.scores = torch.zeros(B, Hkv, cap_hi, dtype=torch.float32, device=dev)
@@ -63,6 +77,7 @@ class MikvCache:
         s.k_hi, s.v_hi, s.k_hi_meta, s.v_hi_meta = p(self.k_hi), p(self.v_hi), p(self.k_hi_meta), p(self.v_hi_meta)
         s.k_lo, s.v_lo, s.k_lo_meta, s.v_lo_meta = p(self.k_lo), p(self.v_lo), p(self.k_lo_meta), p(self.v_lo_meta)
         s.pos_hi, s.pos_lo, s.balancer, s.scores = p(self.pos_hi), p(self.pos_lo), p(self.balancer), p(self.scores)
+        s.key_mode, s.k_pend, s.v_pend = key_mode, p(self.k_pend), p(self.v_pend)
         self.struct = s
         lib = _lib.load()
         import ctypes

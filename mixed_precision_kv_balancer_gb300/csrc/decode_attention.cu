@@ -50,17 +50,20 @@ constexpr float kLogitScale = 0.12751743082459868f;  // log2(e) / sqrt(128)
 // rows, so that 4 warps x 2 stages of any format pairing fit 3 CTAs per SM.
 __host__ __device__ constexpr int stage_tokens(int bits) { return bits == 16 ? 16 : (bits == 2 ? 64 : 32); }
 
-template <int BITS>
+// CH: keys quantised per channel (groups of 64 slots); a stage then carries its group's key
+// meta row (D x (scale, zero), 512 bytes) instead of per-token key meta.
+template <int BITS, bool CH = false>
 struct Fmt {
   static constexpr bool kQuant = BITS != 16;
   static constexpr int kRB = kD * BITS / 8;                            // bytes per token row
   static constexpr int kRS = kQuant ? kRB : kRB + 16;                  // smem row stride (FP16 padded)
   static constexpr int kST = stage_tokens(BITS);                      // tokens per stage
   static constexpr int kMetaB = kQuant ? 8 : 0;                        // (scale, zero) x 2 groups
+  static constexpr int kMetaKB = CH ? kD * 4 : kST * kMetaB;           // key meta bytes per stage
   static constexpr int kOffV = kST * kRS;
   static constexpr int kOffKM = 2 * kST * kRS;
-  static constexpr int kOffVM = kOffKM + kST * kMetaB;
-  static constexpr int kStageBytes = 2 * kST * kRS + 2 * kST * kMetaB;
+  static constexpr int kOffVM = kOffKM + kMetaKB;
+  static constexpr int kStageBytes = 2 * kST * kRS + kMetaKB + kST * kMetaB;
   static constexpr int kCPR = kRB / 16;          // 16-byte chunks per row
   static constexpr int kRowsPerIt = 32 / kCPR;   // rows one warp-wide copy covers
   static constexpr int kGB = 64 * BITS / 8;      // bytes of one 64-channel group
@@ -87,7 +90,13 @@ struct Params {
   float* ws_ml;            // [B*Hq][smax][2]
   const uint32_t* qf;      // query fragments, [B*Hkv][2][32][kQW]
   uint32_t* qf_out;        // the same buffer, written by the prep kernel
+  // per-channel keys: the low tier's closed groups, then the waiting pairs (FP16) as a third
+  // tier; qc = the query in the lane order of the low tier's fragments, fp32 [B*Hkv][32][kQC]
+  TierPtrs pend;
+  int nsplit_lo;
+  float* qc;
 };
+constexpr int kQC = 64;
 
 // ---------------------------------------------------------------------------------
 // Shared-memory tiles.  FP16 rows are padded to 272 B, which puts the 8 rows of an
@@ -130,11 +139,11 @@ struct CopyLane {
 // One warp copies a stage: gk/gv point at this lane's first chunk of the stage (stage rows
 // are contiguous), gkm/gvm at the stage's first meta row.  FULL: all kST rows valid; else
 // rows at or past `nvalid` are zero-filled without being read.
-template <int BITS, bool FULL>
+template <int BITS, bool FULL, bool CH = false>
 __device__ __forceinline__ void load_stage(uint32_t sb, const uint8_t* gk, const uint8_t* gv,
                                            const uint8_t* gkm, const uint8_t* gvm, int nvalid,
                                            int lane, const CopyLane<BITS>& cl) {
-  using F = Fmt<BITS>;
+  using F = Fmt<BITS, CH>;
 #pragma unroll
   for (int it = 0; it < F::kST / F::kRowsPerIt; ++it) {
     const bool ok = FULL || cl.rl + it * F::kRowsPerIt < nvalid;
@@ -144,12 +153,13 @@ __device__ __forceinline__ void load_stage(uint32_t sb, const uint8_t* gk, const
     cp_async16(sb + F::kOffV + dst, ok ? gv + it * 512 : gv - lane * 16, ok);
   }
   if constexpr (F::kQuant) {
+    if constexpr (CH) cp_async16(sb + F::kOffKM + lane * 16, gkm + lane * 16, true);  // the group's key meta
 #pragma unroll
     for (int it = 0; it < (F::kST + 31) / 32; ++it) {
       const int r = lane + 32 * it;
       if (F::kST % 32 == 0 || r < F::kST) {
         const bool ok = FULL || r < nvalid;
-        cp_async8(sb + F::kOffKM + r * 8, ok ? gkm + r * 8 : gkm, ok);
+        if constexpr (!CH) cp_async8(sb + F::kOffKM + r * 8, ok ? gkm + r * 8 : gkm, ok);
         cp_async8(sb + F::kOffVM + r * 8, ok ? gvm + r * 8 : gvm, ok);
       }
     }
@@ -307,12 +317,14 @@ __device__ __forceinline__ FragOffs frag_offsets(int lane) {
 
 // One stage of BITS-format tokens for one warp.  The query fragments are pre-scaled by
 // log2(e)/sqrt(D), so the accumulators hold base-2 logits.  FULL: all kST rows valid.
-template <int BITS, int NT, bool FULL>
+// CH: keys quantised per channel; bq then holds this stage's rescaled fragments (q * s per
+// channel) and qsum[t][0] the head's zero term sum_c q_c z_c (see rescale_qfrag).
+template <int BITS, int NT, bool FULL, bool CH = false>
 __device__ __forceinline__ void compute_stage(uint32_t sb, int nvalid, const uint32_t (&bq)[NT][8][2],
                                               const float (&qsum)[NT][2], State<NT>& st,
                                               float* logit_out, int logit_stride, int rep,
                                               int lane, const FragOffs& fo) {
-  using F = Fmt<BITS>;
+  using F = Fmt<BITS, CH>;
   constexpr int kSub = F::kST / 16;
   constexpr float kLn2 = 0.6931471805599453f;
   const int gid = lane >> 2, tig = lane & 3;
@@ -357,18 +369,26 @@ __device__ __forceinline__ void compute_stage(uint32_t sb, int nvalid, const uin
             mma16816(acc[t][gr], pa[2 * s], pb[2 * s], pa[2 * s + 1], pb[2 * s + 1],
                      bq[t][gr * 4 + s][0], bq[t][gr * 4 + s][1]);
       }
-      const uint2 ma = lds64(sb + F::kOffKM + (sub * 16 + gid) * 8);
-      const uint2 mb = lds64(sb + F::kOffKM + (sub * 16 + gid + 8) * 8);
-      const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(&ma.x));
-      const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&ma.y));
-      const float2 b0 = __half22float2(*reinterpret_cast<const __half2*>(&mb.x));
-      const float2 b1 = __half22float2(*reinterpret_cast<const __half2*>(&mb.y));
+      if constexpr (CH) {
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const float da0 = acc[t][0][0] + acc[t][0][1], da1 = acc[t][1][0] + acc[t][1][1];
-        const float db0 = acc[t][0][2] + acc[t][0][3], db1 = acc[t][1][2] + acc[t][1][3];
-        x[sub][t][0] = a0.x * da0 + a1.x * da1 + a0.y * qsum[t][0] + a1.y * qsum[t][1];
-        x[sub][t][1] = b0.x * db0 + b1.x * db1 + b0.y * qsum[t][0] + b1.y * qsum[t][1];
+        for (int t = 0; t < NT; ++t) {
+          x[sub][t][0] = ((acc[t][0][0] + acc[t][0][1]) + (acc[t][1][0] + acc[t][1][1])) + qsum[t][0];
+          x[sub][t][1] = ((acc[t][0][2] + acc[t][0][3]) + (acc[t][1][2] + acc[t][1][3])) + qsum[t][0];
+        }
+      } else {
+        const uint2 ma = lds64(sb + F::kOffKM + (sub * 16 + gid) * 8);
+        const uint2 mb = lds64(sb + F::kOffKM + (sub * 16 + gid + 8) * 8);
+        const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(&ma.x));
+        const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&ma.y));
+        const float2 b0 = __half22float2(*reinterpret_cast<const __half2*>(&mb.x));
+        const float2 b1 = __half22float2(*reinterpret_cast<const __half2*>(&mb.y));
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const float da0 = acc[t][0][0] + acc[t][0][1], da1 = acc[t][1][0] + acc[t][1][1];
+          const float db0 = acc[t][0][2] + acc[t][0][3], db1 = acc[t][1][2] + acc[t][1][3];
+          x[sub][t][0] = a0.x * da0 + a1.x * da1 + a0.y * qsum[t][0] + a1.y * qsum[t][1];
+          x[sub][t][1] = b0.x * db0 + b1.x * db1 + b0.y * qsum[t][0] + b1.y * qsum[t][1];
+        }
       }
     }
     // natural logits out (important tier) and masking of rows past the end
@@ -518,10 +538,11 @@ __device__ __forceinline__ void load_qfrag(const uint32_t* qf, int unit, int tie
 // group sums of the same scaled values.  Warp 0 (format 0) and warp 4 (format 1) then gather
 // their lane-order fragments (word 16t + 2s + i = bq[t][s][i], words 32..35 = qsum[NT][2]).
 // Every thread of the CTA must call this (it holds a barrier).
-template <int HI, int LO, int NT>
+template <int HI, int LO, int NT, bool CK = false>
 __device__ __forceinline__ void prep_unit(const Params& P, int unit) {
   __shared__ uint32_t sq[2][8][kD];   // (hi, lo) pairs
   __shared__ float sgs[2][8][4];      // per-warp partial sums: [format][head][warp of the format]
+  __shared__ float sqf[CK ? 8 : 1][kD];  // per-channel keys: the scaled query in fp32
   const int t = threadIdx.x, lane = t & 31;
   const int b = unit / P.Hkv, g = unit % P.Hkv;
   if (t < 256) {
@@ -537,6 +558,7 @@ __device__ __forceinline__ void prep_unit(const Params& P, int unit) {
         x *= kLogitScale;
       }
       sq[f][h][c] = split_pack(x);
+      if (CK && f == 1) sqf[h][c] = x;
       float sum = x;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
@@ -585,32 +607,96 @@ __device__ __forceinline__ void prep_unit(const Params& P, int unit) {
     uint4* dst = reinterpret_cast<uint4*>(P.qf_out + ((static_cast<long>(unit) * 2 + f) * 32 + lane) * kQW);
 #pragma unroll
     for (int i = 0; i < kQW / 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    if (CK && f == 1) {  // the same lane order, fp32, for the per-stage rescaling
+      float* qd = P.qc + (static_cast<long>(unit) * 32 + lane) * kQC;
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt) {
+        const int head = tt * 4 + (gid >> 1);
+#pragma unroll
+        for (int s2 = 0; s2 < 8; ++s2) {
+          const int sp = s2 & 3, base = (s2 >> 2) * 64 + tig * 16;
+          const int c0 = base + k_ca<LO>(2 * sp), c1 = base + k_cb<LO>(2 * sp);
+          const int c2 = base + k_ca<LO>(2 * sp + 1), c3 = base + k_cb<LO>(2 * sp + 1);
+          const bool on = tt < NT;
+          reinterpret_cast<float4*>(qd + tt * 32 + s2 * 4)[0] =
+              on ? make_float4(sqf[head][c0], sqf[head][c1], sqf[head][c2], sqf[head][c3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+    }
   }
 }
 
 // The query fragments of every (batch, key head): one CTA of 256 threads per unit.
-template <int HI, int LO, int NT>
+template <int HI, int LO, int NT, bool CK>
 __global__ void __launch_bounds__(256) decode_qprep_kernel(Params P) {
   pdl_wait();
   pdl_trigger();
-  prep_unit<HI, LO, NT>(P, blockIdx.x);
+  prep_unit<HI, LO, NT, CK>(P, blockIdx.x);
 }
 
 // First kernel of a decode step, one CTA of 288 threads per (batch, key head): the last warp
 // appends the new token to the important tier (and clears the unit's demotion ticket), the
 // rest prepare the query fragments.
-template <int HI, int LO, int NT>
+template <int HI, int LO, int NT, bool CK>
 __global__ void __launch_bounds__(288) decode_step_prep_kernel(AppendArgs a, Params P) {
   pdl_wait();
   pdl_trigger();
   if (threadIdx.x >= 256) append_item(a, blockIdx.x, threadIdx.x & 31);
-  prep_unit<HI, LO, NT>(P, blockIdx.x);
+  prep_unit<HI, LO, NT, CK>(P, blockIdx.x);
+}
+
+// Per-channel keys: the query fragments of one stage.  The stage's keys carry a scale s_c and
+// zero z_c per channel (the group's meta row in shared memory at `km`), so
+//   q . k~ = sum_c (q_c s_c) code_c + sum_c q_c z_c.
+// Each lane forms its fragment words from the fp32 query (already scaled by log2(e)/sqrt(D),
+// in its own lane order, `q32`): q_c s_c split into fp16 (hi, lo) parts as the prep does, the
+// part of its column (hi for even gid, lo for odd); and the zero term of its head, summed over
+// the 4 lanes that hold the head's 128 channels, then handed to the lanes whose accumulator
+// rows belong to that head (zt[t] for head t * 4 + tig).
+__device__ __forceinline__ uint32_t part_pack(float a, float b, bool lo_part) {
+  const float ha = __uint_as_float(__float_as_uint(a) & 0xffffe000u);
+  const float hb = __uint_as_float(__float_as_uint(b) & 0xffffe000u);
+  const __half2 h = __floats2half2_rn(lo_part ? a - ha : ha, lo_part ? b - hb : hb);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 template <int BITS, int NT>
+__device__ __forceinline__ void rescale_qfrag(uint32_t km, const float* q32, int lane, uint32_t (&bqs)[NT][8][2],
+                                              float (&zt)[NT][2]) {
+  const int gid = lane >> 2, tig = lane & 3;
+  const bool lo_part = (gid & 1) != 0;
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    float zp = 0.f;
+#pragma unroll
+    for (int s2 = 0; s2 < 8; ++s2) {
+      const float4 qv = __ldg(reinterpret_cast<const float4*>(q32 + t * 32 + s2 * 4));
+      const int sp = s2 & 3, base = (s2 >> 2) * 64 + tig * 16;
+      const int c0 = base + k_ca<BITS>(2 * sp), c1 = base + k_cb<BITS>(2 * sp);
+      const int c2 = base + k_ca<BITS>(2 * sp + 1), c3 = base + k_cb<BITS>(2 * sp + 1);
+      uint32_t w0 = lds32(km + c0 * 4), w1 = lds32(km + c1 * 4), w2 = lds32(km + c2 * 4), w3 = lds32(km + c3 * 4);
+      const float2 m0 = __half22float2(*reinterpret_cast<const __half2*>(&w0));
+      const float2 m1 = __half22float2(*reinterpret_cast<const __half2*>(&w1));
+      const float2 m2 = __half22float2(*reinterpret_cast<const __half2*>(&w2));
+      const float2 m3 = __half22float2(*reinterpret_cast<const __half2*>(&w3));
+      zp = fmaf(qv.x, m0.y, fmaf(qv.y, m1.y, fmaf(qv.z, m2.y, fmaf(qv.w, m3.y, zp))));
+      bqs[t][s2][0] = part_pack(qv.x * m0.x, qv.y * m1.x, lo_part);
+      bqs[t][s2][1] = part_pack(qv.z * m2.x, qv.w * m3.x, lo_part);
+    }
+    zp += __shfl_xor_sync(0xffffffffu, zp, 1);
+    zp += __shfl_xor_sync(0xffffffffu, zp, 2);
+    zt[t][0] = __shfl_sync(0xffffffffu, zp, 8 * tig);
+    zt[t][1] = 0.f;
+  }
+}
+
+// One CTA's chunk of one tier.  fmt: which query fragments (0: the important tier's format,
+// 1: the low tier's); logits: write the natural logits of its tokens (important tier);
+// split_index: the CTA's row in the split workspace.  CH: per-channel keys (the low tier).
+template <int BITS, int NT, bool CH = false>
 __device__ void run_tier(const Params& P, const TierPtrs& tier, int unit, int split, int chunk,
-                         bool is_hi, uint8_t* smem) {
-  using F = Fmt<BITS>;
+                         int fmt, bool logits, int split_index, uint8_t* smem) {
+  using F = Fmt<BITS, CH>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = unit / P.Hkv, g = unit % P.Hkv;
   const int rep = P.rep;
@@ -627,7 +713,7 @@ __device__ void run_tier(const Params& P, const TierPtrs& tier, int unit, int sp
   const CopyLane<BITS> cl(lane);
   const uint8_t* gk = tier.k + row0 * F::kRB + lane * 16;
   const uint8_t* gv = tier.v + row0 * F::kRB + lane * 16;
-  const uint8_t* gkm = F::kQuant ? tier.km + row0 * 8 : nullptr;
+  const uint8_t* gkm = F::kQuant ? tier.km + (CH ? 0 : row0 * 8) : nullptr;
   const uint8_t* gvm = F::kQuant ? tier.vm + row0 * 8 : nullptr;
   int tok_issue = t_begin + warp * F::kST;  // first token of the next stage to issue
   int issued = 0;
@@ -635,12 +721,14 @@ __device__ void run_tier(const Params& P, const TierPtrs& tier, int unit, int sp
     if (issued < my_st) {
       const uint32_t sb = ring_s + (issued % kStages) * F::kStageBytes;
       const int nv = t_end - tok_issue;
-      if (nv >= F::kST) load_stage<BITS, true>(sb, gk, gv, gkm, gvm, nv, lane, cl);
-      else load_stage<BITS, false>(sb, gk, gv, gkm, gvm, nv, lane, cl);
+      // per-channel keys: the meta row of the stage's group of 64 slots
+      const uint8_t* km = CH ? gkm + (static_cast<long>(unit) * (tier.cap / kGS) + tok_issue / kGS) * (kD * 4) : gkm;
+      if (nv >= F::kST) load_stage<BITS, true, CH>(sb, gk, gv, km, gvm, nv, lane, cl);
+      else load_stage<BITS, false, CH>(sb, gk, gv, km, gvm, nv, lane, cl);
       gk += kRowStride * F::kRB;
       gv += kRowStride * F::kRB;
       if constexpr (F::kQuant) {
-        gkm += kRowStride * 8;
+        if constexpr (!CH) gkm += kRowStride * 8;
         gvm += kRowStride * 8;
       }
       tok_issue += kRowStride;
@@ -653,7 +741,8 @@ __device__ void run_tier(const Params& P, const TierPtrs& tier, int unit, int sp
   // this tier's query fragments, prepared once per (batch, key head) by the prep kernel
   uint32_t bq[NT][8][2];
   float qsum[NT][2];
-  load_qfrag<NT>(P.qf, unit, is_hi ? 0 : 1, lane, bq, qsum);
+  if constexpr (!CH) load_qfrag<NT>(P.qf, unit, fmt, lane, bq, qsum);
+  const float* q32 = CH ? P.qc + (static_cast<long>(unit) * 32 + lane) * kQC : nullptr;
 
   State<NT> st;
 #pragma unroll
@@ -668,7 +757,7 @@ __device__ void run_tier(const Params& P, const TierPtrs& tier, int unit, int sp
   }
 
   float* lrow = nullptr;
-  if (is_hi && P.hi_logits)
+  if (logits && P.hi_logits)
     lrow = P.hi_logits + (static_cast<long>(b) * P.Hq + g * rep) * tier.cap;
 
   const FragOffs fo = frag_offsets<BITS>(lane);
@@ -681,8 +770,9 @@ __device__ void run_tier(const Params& P, const TierPtrs& tier, int unit, int sp
     const int nv = min(F::kST, t_end - tok0);
     const uint32_t sb = ring_s + (k % kStages) * F::kStageBytes;
     float* lo = lrow ? lrow + tok0 : nullptr;
-    if (nv == F::kST) compute_stage<BITS, NT, true>(sb, nv, bq, qsum, st, lo, tier.cap, rep, lane, fo);
-    else compute_stage<BITS, NT, false>(sb, nv, bq, qsum, st, lo, tier.cap, rep, lane, fo);
+    if constexpr (CH) rescale_qfrag<BITS, NT>(sb + F::kOffKM, q32, lane, bq, qsum);
+    if (nv == F::kST) compute_stage<BITS, NT, true, CH>(sb, nv, bq, qsum, st, lo, tier.cap, rep, lane, fo);
+    else compute_stage<BITS, NT, false, CH>(sb, nv, bq, qsum, st, lo, tier.cap, rep, lane, fo);
     __syncwarp();
     tok0 += kRowStride;
   }
@@ -728,7 +818,6 @@ __device__ void run_tier(const Params& P, const TierPtrs& tier, int unit, int sp
   }
   __syncthreads();
   const int c = threadIdx.x;  // one channel per thread
-  const int split_index = is_hi ? split : P.nsplit_hi + split;
   for (int h = 0; h < rep; ++h) {
     float M = -INFINITY;
 #pragma unroll
@@ -750,15 +839,20 @@ __device__ void run_tier(const Params& P, const TierPtrs& tier, int unit, int sp
   }
 }
 
-template <int HI, int LO, int NT>
+// Splits [0, nsplit_hi): the important tier; then the low tier; with per-channel keys (CK)
+// the low tier's closed groups, then one CTA over the waiting pairs (FP16, attended with the
+// important tier's query fragments, no logits).
+template <int HI, int LO, int NT, bool CK>
 __global__ void __launch_bounds__(kThreads, 3) decode_partial_kernel(Params P) {
   extern __shared__ __align__(128) uint8_t smem[];
   pdl_wait();
   pdl_trigger();
   const int unit = blockIdx.y;
   const int sx = blockIdx.x;
-  if (sx < P.nsplit_hi) run_tier<HI, NT>(P, P.hi, unit, sx, P.chunk_hi, true, smem);
-  else run_tier<LO, NT>(P, P.lo, unit, sx - P.nsplit_hi, P.chunk_lo, false, smem);
+  if (sx < P.nsplit_hi) run_tier<HI, NT>(P, P.hi, unit, sx, P.chunk_hi, 0, true, sx, smem);
+  else if (!CK || sx < P.nsplit_hi + P.nsplit_lo)
+    run_tier<LO, NT, CK>(P, P.lo, unit, sx - P.nsplit_hi, P.chunk_lo, 1, false, sx, smem);
+  else if constexpr (CK) run_tier<16, NT>(P, P.pend, unit, 0, kGS, 0, false, sx, smem);
 }
 
 // K8: merge the split partials (base-2 max m, sum l, unnormalised o) of one query head
@@ -1016,25 +1110,25 @@ int record_hook(cudaEvent_t ev, cudaStream_t s) {
 
 // The query-fragment prep, then the split-K partial kernel (PDL after the prep); `after`:
 // the kernel launched just before on `s` is one of ours, so the prep may overlap its tail.
-template <int HI, int LO, int NT>
+template <int HI, int LO, int NT, bool CK>
 int launch(const Params& P, dim3 grid, cudaStream_t s, bool after, const AppendArgs* step) {
   const dim3 pgrid(grid.y);
   if (step != nullptr) {  // the step's token append and the query prep in one launch
-    if (int e = check_launch_after(launch_after(decode_step_prep_kernel<HI, LO, NT>, pgrid, dim3(288),
+    if (int e = check_launch_after(launch_after(decode_step_prep_kernel<HI, LO, NT, CK>, pgrid, dim3(288),
                                                 0, s, *step, P),
                                    "decode_step_prep_kernel"))
       return e;
   } else if (after) {
-    auto prep = decode_qprep_kernel<HI, LO, NT>;
+    auto prep = decode_qprep_kernel<HI, LO, NT, CK>;
     const dim3 pblock(256);
     if (int e = check_launch_after(launch_after(prep, pgrid, pblock, 0, s, P), "decode_qprep_kernel"))
       return e;
   } else {
-    decode_qprep_kernel<HI, LO, NT><<<pgrid, 256, 0, s>>>(P);
+    decode_qprep_kernel<HI, LO, NT, CK><<<pgrid, 256, 0, s>>>(P);
     if (int e = check_launch("decode_qprep_kernel")) return e;
   }
-  const int smem = kWarps * kStages * std::max(Fmt<HI>::kStageBytes, Fmt<LO>::kStageBytes);
-  auto kern = decode_partial_kernel<HI, LO, NT>;
+  const int smem = kWarps * kStages * std::max(Fmt<HI>::kStageBytes, Fmt<LO, CK>::kStageBytes);
+  auto kern = decode_partial_kernel<HI, LO, NT, CK>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return check_launch("decode_partial_kernel attribute");
   if (int e = record_hook(t_ev_begin, s)) return e;
@@ -1044,10 +1138,10 @@ int launch(const Params& P, dim3 grid, cudaStream_t s, bool after, const AppendA
   return record_hook(t_ev_end, s);
 }
 
-template <int HI, int LO>
+template <int HI, int LO, bool CK = false>
 int launch_nt(const Params& P, dim3 grid, cudaStream_t s, bool after, const AppendArgs* step) {
-  return P.rep <= 4 ? launch<HI, LO, 1>(P, grid, s, after, step)
-                    : launch<HI, LO, 2>(P, grid, s, after, step);
+  return P.rep <= 4 ? launch<HI, LO, 1, CK>(P, grid, s, after, step)
+                    : launch<HI, LO, 2, CK>(P, grid, s, after, step);
 }
 
 }  // namespace
@@ -1055,13 +1149,34 @@ int launch_nt(const Params& P, dim3 grid, cudaStream_t s, bool after, const Appe
 
 using namespace mikv;
 
+namespace mikv {
+namespace {
+// Decode workspace: split partials (o, then (m, l)), query fragments, and with per-channel
+// keys the fp32 query in the low tier's lane order; one more split row for the waiting pairs.
+struct DecWs {
+  size_t o, ml, qf, qc, total;
+  int smax;
+};
+DecWs dec_ws_layout(const mikv_cache* c) {
+  const Plan p = make_plan(c);
+  const bool ck = c->key_mode == MIKV_KEYS_PER_CHANNEL;
+  DecWs w;
+  w.smax = p.smax_hi + p.smax_lo + (ck ? 1 : 0);
+  const size_t rows = static_cast<size_t>(c->B) * c->Hq * w.smax;
+  const size_t units = static_cast<size_t>(c->B) * c->Hkv;
+  w.o = 0;
+  w.ml = align_up(rows * kD * sizeof(float), 256);
+  w.qf = w.ml + align_up(rows * 2 * sizeof(float), 256);
+  w.qc = w.qf + align_up(units * 2 * 32 * kQW * sizeof(uint32_t), 256);
+  w.total = w.qc + (ck ? align_up(units * 32 * kQC * sizeof(float), 256) : 0);
+  return w;
+}
+}  // namespace
+}  // namespace mikv
+
 extern "C" size_t mikv_decode_workspace_bytes(const mikv_cache* c) {
   if (validate_cache_public(c, "decode_workspace_bytes") != MIKV_OK) return 0;
-  const Plan p = make_plan(c);
-  const size_t rows = static_cast<size_t>(c->B) * c->Hq * (p.smax_hi + p.smax_lo);
-  const size_t units = static_cast<size_t>(c->B) * c->Hkv;
-  return align_up(rows * kD * sizeof(float), 256) + align_up(rows * 2 * sizeof(float), 256) +
-         align_up(units * 2 * 32 * kQW * sizeof(uint32_t), 256);
+  return dec_ws_layout(c).total;
 }
 
 namespace mikv {
@@ -1069,6 +1184,7 @@ int append_args(bool hi, const uint16_t* k, const uint16_t* v, int src_len, cons
                 int n_tokens, int pos_base, const float* src_scores, const mikv_cache* c,
                 unsigned* ticket, AppendArgs& a);
 int demote_args(const mikv_cache* c, const int32_t* victim, DemoteArgs& a);
+int channel_close_waiting(const mikv_cache* c, cudaStream_t s);
 
 namespace {
 // Validate the cache for attention and fill the partial-kernel parameters.
@@ -1086,9 +1202,10 @@ int prepare_decode(const uint16_t* q, const mikv_cache* c, float* hi_logits, voi
   const size_t need = mikv_decode_workspace_bytes(c);
   if (ws_bytes < need) return fail(MIKV_ESHAPE, "%s: workspace %zu < %zu", who, ws_bytes, need);
   const Plan pl = make_plan(c);
+  const bool ck = c->key_mode == MIKV_KEYS_PER_CHANNEL;
   P = Params{};
   P.q = reinterpret_cast<const __half*>(q);
-  P.bal = c->balancer;
+  P.bal = ck ? nullptr : c->balancer;  // per-channel keys are not balanced (FP16 important tier)
   P.hi = TierPtrs{static_cast<const uint8_t*>(c->k_hi), static_cast<const uint8_t*>(c->v_hi),
                   static_cast<const uint8_t*>(c->k_hi_meta), static_cast<const uint8_t*>(c->v_hi_meta),
                   c->cap_hi, c->n_hi};
@@ -1101,16 +1218,25 @@ int prepare_decode(const uint16_t* q, const mikv_cache* c, float* hi_logits, voi
   P.chunk_hi = pl.chunk_hi;
   P.chunk_lo = pl.chunk_lo;
   P.nsplit_hi = (c->n_hi + pl.chunk_hi - 1) / pl.chunk_hi;
-  const int nsplit_lo = (c->n_lo + pl.chunk_lo - 1) / pl.chunk_lo;
-  P.smax = pl.smax_hi + pl.smax_lo;
+  int n_pend = 0;
+  if (ck) {  // closed groups in the low tier's splits, the waiting pairs in one more CTA
+    n_pend = c->n_lo % kGS;
+    P.lo.n = c->n_lo - n_pend;
+    P.pend = TierPtrs{static_cast<const uint8_t*>(c->k_pend), static_cast<const uint8_t*>(c->v_pend), nullptr,
+                      nullptr, kGS, n_pend};
+  }
+  P.nsplit_lo = (P.lo.n + pl.chunk_lo - 1) / pl.chunk_lo;
+  const DecWs wl = dec_ws_layout(c);
+  P.smax = wl.smax;
   P.hi_logits = hi_logits;
-  const size_t rows = static_cast<size_t>(c->B) * c->Hq * P.smax;
-  P.ws_o = static_cast<float*>(ws);
-  P.ws_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + align_up(rows * kD * sizeof(float), 256));
-  P.qf_out = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + align_up(rows * kD * sizeof(float), 256) +
-                                         align_up(rows * 2 * sizeof(float), 256));
+  char* wsb = static_cast<char*>(ws);
+  P.ws_o = reinterpret_cast<float*>(wsb + wl.o);
+  P.ws_ml = reinterpret_cast<float*>(wsb + wl.ml);
+  P.qf_out = reinterpret_cast<uint32_t*>(wsb + wl.qf);
   P.qf = P.qf_out;
-  nsplit = P.nsplit_hi + nsplit_lo;
+  P.qc = ck ? reinterpret_cast<float*>(wsb + wl.qc) : nullptr;
+  nsplit = P.nsplit_hi + P.nsplit_lo + (n_pend > 0 ? 1 : 0);
+  if (nsplit < 1) return fail(MIKV_ESHAPE, "%s: nothing to attend", who);
   const int fmt = c->hi_bits * 100 + c->lo_bits;
   if (fmt != 1602 && fmt != 1604 && fmt != 1608 && fmt != 802 && fmt != 804 && fmt != 808 &&
       fmt != 402 && fmt != 404)
@@ -1123,6 +1249,9 @@ int prepare_decode(const uint16_t* q, const mikv_cache* c, float* hi_logits, voi
 int launch_partials(const Params& P, const mikv_cache* c, int nsplit, cudaStream_t s, bool after,
                     const AppendArgs* step) {
   const dim3 grid(nsplit, c->B * c->Hkv);
+  if (c->key_mode == MIKV_KEYS_PER_CHANNEL)
+    return c->lo_bits == 2 ? launch_nt<16, 2, true>(P, grid, s, after, step)
+                           : launch_nt<16, 4, true>(P, grid, s, after, step);
   int e;
   switch (c->hi_bits * 100 + c->lo_bits) {
     case 1602: e = launch_nt<16, 2>(P, grid, s, after, step); break;
@@ -1278,6 +1407,8 @@ extern "C" int mikv_decode_step(const uint16_t* q, const uint16_t* k_new, const 
   if (demote) {
     c->n_hi -= 1;
     c->n_lo += 1;
+    // per-channel keys: the demoted pair was the 64th waiting one, so its group closes
+    if (c->key_mode == MIKV_KEYS_PER_CHANNEL && c->n_lo % kGS == 0) return channel_close_waiting(c, s);
   }
   return MIKV_OK;
 }

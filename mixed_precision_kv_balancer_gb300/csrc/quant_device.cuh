@@ -65,6 +65,8 @@ struct DemoteArgs {
   const int32_t* victim;  // [B*Hkv]
   const float* bal;
   int units, hi_bits, lo_bits, cap_hi, cap_lo, n_hi, n_lo;
+  int key_mode;           // MIKV_KEYS_PER_CHANNEL: the pair joins the waiting buffer
+  __half *k_pend, *v_pend;  // [B*Hkv][64][D]
   uint8_t *k_hi, *v_hi;
   __half2 *k_hi_meta, *v_hi_meta;
   uint8_t *k_lo, *v_lo;
@@ -131,34 +133,43 @@ __device__ __forceinline__ void demote_one(const DemoteArgs& a, long unit, int v
       lsc = __ldcg(a.scores + last);  // may have been updated by another CTA
     }
   }
-  Row4 xk, xv;
-  if (a.hi_bits == 16) {
-    xk = load_fp16x4(reinterpret_cast<const __half*>(a.k_hi) + hs * kD + lane * 4);
-    xv = load_fp16x4(reinterpret_cast<const __half*>(a.v_hi) + hs * kD + lane * 4);
-    if (a.bal) {
-      const float4 bb = *reinterpret_cast<const float4*>(a.bal + unit * kD + lane * 4);
-      xk.x[0] = __fmul_rn(xk.x[0], bb.x);
-      xk.x[1] = __fmul_rn(xk.x[1], bb.y);
-      xk.x[2] = __fmul_rn(xk.x[2], bb.z);
-      xk.x[3] = __fmul_rn(xk.x[3], bb.w);
-    }
-  } else if (a.hi_bits == 8) {  // quantised tiers hold balanced keys already
-    xk = dequant_int8x4(a.k_hi + hs * hrb, a.k_hi_meta + hs * 2, lane);
-    xv = dequant_int8x4(a.v_hi + hs * hrb, a.v_hi_meta + hs * 2, lane);
+  if (a.key_mode == MIKV_KEYS_PER_CHANNEL) {
+    // per-channel keys (FP16 important tier): the pair waits unquantised in row n_lo % 64 of
+    // the buffer; the group is closed by a separate launch once 64 pairs wait
+    const long pr = unit * kGS + (a.n_lo & (kGS - 1));
+    reinterpret_cast<uint2*>(a.k_pend + pr * kD)[lane] = reinterpret_cast<const uint2*>(a.k_hi + hs * kD * 2)[lane];
+    reinterpret_cast<uint2*>(a.v_pend + pr * kD)[lane] = reinterpret_cast<const uint2*>(a.v_hi + hs * kD * 2)[lane];
+    if (lane == 0) a.pos_lo[ls] = a.pos_hi[hs];
   } else {
-    xk = dequant_int4x4(a.k_hi + hs * hrb, a.k_hi_meta + hs * 2, lane);
-    xv = dequant_int4x4(a.v_hi + hs * hrb, a.v_hi_meta + hs * 2, lane);
+    Row4 xk, xv;
+    if (a.hi_bits == 16) {
+      xk = load_fp16x4(reinterpret_cast<const __half*>(a.k_hi) + hs * kD + lane * 4);
+      xv = load_fp16x4(reinterpret_cast<const __half*>(a.v_hi) + hs * kD + lane * 4);
+      if (a.bal) {
+        const float4 bb = *reinterpret_cast<const float4*>(a.bal + unit * kD + lane * 4);
+        xk.x[0] = __fmul_rn(xk.x[0], bb.x);
+        xk.x[1] = __fmul_rn(xk.x[1], bb.y);
+        xk.x[2] = __fmul_rn(xk.x[2], bb.z);
+        xk.x[3] = __fmul_rn(xk.x[3], bb.w);
+      }
+    } else if (a.hi_bits == 8) {  // quantised tiers hold balanced keys already
+      xk = dequant_int8x4(a.k_hi + hs * hrb, a.k_hi_meta + hs * 2, lane);
+      xv = dequant_int8x4(a.v_hi + hs * hrb, a.v_hi_meta + hs * 2, lane);
+    } else {
+      xk = dequant_int4x4(a.k_hi + hs * hrb, a.k_hi_meta + hs * 2, lane);
+      xv = dequant_int4x4(a.v_hi + hs * hrb, a.v_hi_meta + hs * 2, lane);
+    }
+    const int vpos = lane == 0 ? a.pos_hi[hs] : 0;
+    const int rb = kD * a.lo_bits / 8;
+    uint32_t mk, mv;
+    const uint32_t pk = quantize4(xk, a.lo_bits, mk);
+    const uint32_t pv = quantize4(xv, a.lo_bits, mv);
+    store_codes(a.k_lo + ls * rb, lane, a.lo_bits, pk);
+    store_codes(a.v_lo + ls * rb, lane, a.lo_bits, pv);
+    store_meta(a.k_lo_meta + ls * 2, lane, mk);
+    store_meta(a.v_lo_meta + ls * 2, lane, mv);
+    if (lane == 0) a.pos_lo[ls] = vpos;
   }
-  const int vpos = lane == 0 ? a.pos_hi[hs] : 0;
-  const int rb = kD * a.lo_bits / 8;
-  uint32_t mk, mv;
-  const uint32_t pk = quantize4(xk, a.lo_bits, mk);
-  const uint32_t pv = quantize4(xv, a.lo_bits, mv);
-  store_codes(a.k_lo + ls * rb, lane, a.lo_bits, pk);
-  store_codes(a.v_lo + ls * rb, lane, a.lo_bits, pv);
-  store_meta(a.k_lo_meta + ls * 2, lane, mk);
-  store_meta(a.v_lo_meta + ls * 2, lane, mv);
-  if (lane == 0) a.pos_lo[ls] = vpos;
   __syncwarp();
   // swap-remove: the last important slot moves into the freed one
   if (move) {

@@ -299,6 +299,138 @@ __global__ void __launch_bounds__(kTileThreads) append_tile_kernel(AppendArgs a,
   reinterpret_cast<uint32_t*>(tensor ? a.dvm : a.dkm)[slot * 2 + g] = meta;
 }
 
+// ---------------------------------------------------------------------------------
+// Per-channel keys ([notes] Appendix C remarks; [paperlayer] C: group 64, keys per channel):
+// closing groups of 64 retained pairs.  Keys: per channel c, the per-token quantizer's rule
+// over the group's 64 values of c (s = fp16(fl(fl(mx - mn) / qmax)), z = fp16(mn),
+// code = clamp(rint_even(fl(fl(x - z) / s)), 0, qmax)), codes into the per-token rows (channel
+// c at bit c * bits), (s, z) into the group's meta row [D]; values: per token, as the
+// per-token tier.  No balancer.
+struct ChanArgs {
+  const __half* k;         // prefill: source [units][src_len][D]; closing: the waiting buffer
+  const __half* v;
+  const int32_t* src_pos;  // prefill: [units][n_tokens]; closing: null (rows 0 .. 63 in order)
+  long src_stride;         // rows per unit in k / v (src_len, or 64 for the buffer)
+  int src_len, n_tokens, pos_base;
+  int base_slot;           // first low-tier slot written (a multiple of 64)
+  int cap_lo, ngroups;     // full groups to close; a prefill's tail goes to the waiting buffer
+  uint8_t* k_lo;
+  uint8_t* v_lo;
+  __half2* k_meta;         // [units][cap_lo / 64][D]
+  __half2* v_meta;         // [units][cap_lo][2]
+  int32_t* pos_lo;         // written by a prefill (closing: positions are already in place)
+  __half* k_pend;          // [units][64][D]
+  __half* v_pend;
+};
+
+// CTA (group gi, unit), 128 threads.  gi < ngroups: gather the group's 64 key and value rows
+// (cp.async, 16 bytes), thread c quantises key channel c over the 64 rows (column extremes,
+// codes into a shared byte matrix), thread (row, half) quantises one value group of a row;
+// rows of key codes are packed at the end.  gi == ngroups (prefill only): the tail rows are
+// copied to the waiting buffer.
+template <int BITS>
+__global__ void __launch_bounds__(kTileThreads) channel_close_kernel(ChanArgs a) {
+  __shared__ __align__(16) __half ks[kGS][kD];        // keys, row-major
+  __shared__ __align__(16) uint8_t vs[kGS][kD * 2];   // values, 16-byte chunks swizzled by row
+  __shared__ __align__(16) uint8_t cs[kGS][kD];       // key codes
+  __shared__ __align__(16) float ones[kD];
+  __shared__ int ssrc[kGS];
+  const long unit = blockIdx.y;
+  const int gi = blockIdx.x, t = threadIdx.x;
+  const int j0 = gi * kGS;                               // first token of this CTA
+  const int nrow = min(kGS, a.n_tokens - j0);
+  if (t < kGS) {
+    int src = -1;
+    if (t < nrow) {
+      src = a.src_pos ? a.src_pos[unit * a.n_tokens + j0 + t] : j0 + t;
+      if (src < 0 || src >= a.src_len) src = -1;
+    }
+    ssrc[t] = src;
+    if (a.src_pos && src >= 0) a.pos_lo[unit * a.cap_lo + a.base_slot + j0 + t] = src + a.pos_base;
+  }
+  ones[t] = 1.f;
+  __syncthreads();
+  if (gi >= a.ngroups) {  // prefill tail: rows wait unquantised in buffer rows 0 .. nrow - 1
+    for (int i = t; i < nrow * 16 * 2; i += kTileThreads) {
+      const int tensor = i / (nrow * 16), r = (i >> 4) % nrow, c = i & 15;
+      const int src = ssrc[r];
+      if (src < 0) continue;
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>((tensor ? a.v : a.k) + (unit * a.src_stride + src) * kD) + c);
+      reinterpret_cast<uint4*>((tensor ? a.v_pend : a.k_pend) + (unit * kGS + r) * kD)[c] = w;
+    }
+    return;
+  }
+  // gather: 2 tensors x 64 rows x 16 chunks, 16 per thread, all in flight together
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const int r = (t >> 4) + 8 * m, c = t & 15;
+    const int src = ssrc[r];
+    const long off = (unit * a.src_stride + (src >= 0 ? src : 0)) * kD + c * 8;
+    cp_async16(smem_u32(&ks[r][c * 8]), a.k + off, src >= 0);
+    cp_async16(smem_u32(&vs[r][(c ^ (r & 7)) * 16]), a.v + off, src >= 0);
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+  constexpr int qmax = (1 << BITS) - 1;
+  {  // key channel t over the 64 rows
+    float mn = INFINITY, mx = -INFINITY;
+#pragma unroll 8
+    for (int r = 0; r < kGS; ++r) {
+      const float x = __half2float(ks[r][t]);
+      mn = fminf(mn, x);
+      mx = fmaxf(mx, x);
+    }
+    const float s32 = __fdiv_rn(__fsub_rn(mx, mn), static_cast<float>(qmax));
+    const __half sh = __float2half_rn(s32), zh = __float2half_rn(mn);
+    const float sf = __half2float(sh), zf = __half2float(zh);
+    const float rf = sf != 0.f ? __frcp_rn(sf) : 0.f;
+    a.k_meta[(unit * (a.cap_lo / kGS) + (a.base_slot + j0) / kGS) * kD + t] = __halves2half2(sh, zh);
+#pragma unroll 8
+    for (int r = 0; r < kGS; ++r) {
+      uint32_t code = 0;
+      if (sf != 0.f) {
+        const float d = __fsub_rn(__half2float(ks[r][t]), zf);
+        const float q = __fmul_rn(d, rf);
+        float qi = rintf(q);
+        if (fabsf(q - qi) > 0.5f - kTieGuard) qi = rint_div(d, sf);  // near a tie: exact quotient
+        code = static_cast<uint32_t>(fminf(fmaxf(qi, 0.f), static_cast<float>(qmax)));
+      }
+      cs[r][t] = static_cast<uint8_t>(code);
+    }
+  }
+  {  // value group (t >> 6) of row t % 64, per token
+    const int r = t & 63, g = t >> 6;
+    uint32_t out[64 * BITS / 32];
+    const uint32_t meta = quantize_group64<BITS>(vs[r], g, r, ones, false, out);
+    const long slot = unit * a.cap_lo + a.base_slot + j0 + r;
+    constexpr int kRB = kD * BITS / 8;
+    uint8_t* dst = a.v_lo + slot * kRB + g * (kRB / 2);
+#pragma unroll
+    for (int k = 0; k < 64 * BITS / 128; ++k)
+      reinterpret_cast<uint4*>(dst)[k] = make_uint4(out[4 * k], out[4 * k + 1], out[4 * k + 2], out[4 * k + 3]);
+    reinterpret_cast<uint32_t*>(a.v_meta)[slot * 2 + g] = meta;
+  }
+  __syncthreads();
+  {  // pack the key code rows: thread (row t % 64, half t / 64) packs 64 channels
+    const int r = t & 63, half = t >> 6;
+    constexpr int kPer = 32 / BITS;             // codes per 32-bit word
+    constexpr int kW = 64 / kPer;               // words per half row
+    uint32_t w[kW];
+#pragma unroll
+    for (int i = 0; i < kW; ++i) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) x |= static_cast<uint32_t>(cs[r][half * 64 + i * kPer + e]) << (BITS * e);
+      w[i] = x;
+    }
+    constexpr int kRB = kD * BITS / 8;
+    uint8_t* dst = a.k_lo + (unit * a.cap_lo + a.base_slot + j0 + r) * kRB + half * (kRB / 2);
+#pragma unroll
+    for (int k = 0; k < kW / 4; ++k) reinterpret_cast<uint4*>(dst)[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+  }
+}
+
 __global__ void __launch_bounds__(256) demote_kernel(DemoteArgs a) {
   const int lane = threadIdx.x & 31;
   const long unit = static_cast<long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
@@ -319,6 +451,17 @@ int validate_cache(const mikv_cache* c, const char* who) {
       c->n_lo > c->cap_lo)
     return fail(MIKV_ESHAPE, "%s: counts n_hi=%d/%d n_lo=%d/%d", who, c->n_hi, c->cap_hi, c->n_lo,
                 c->cap_lo);
+  if (c->key_mode != MIKV_KEYS_PER_TOKEN && c->key_mode != MIKV_KEYS_PER_CHANNEL)
+    return fail(MIKV_EINVAL, "%s: key_mode %d", who, c->key_mode);
+  if (c->key_mode == MIKV_KEYS_PER_CHANNEL) {
+    if (c->hi_bits != 16 || (c->lo_bits != 2 && c->lo_bits != 4))
+      return fail(MIKV_EUNSUPPORTED, "%s: per-channel keys need hi_bits 16 and lo_bits 2 or 4 (%d/%d)", who,
+                  c->hi_bits, c->lo_bits);
+    if (c->cap_lo % kGS) return fail(MIKV_ESHAPE, "%s: per-channel keys need cap_lo %% 64 == 0 (%d)", who, c->cap_lo);
+    if (!c->k_pend || !c->v_pend) return fail(MIKV_EINVAL, "%s: null waiting-pair buffer", who);
+    if (!aligned16(c->k_pend) || !aligned16(c->v_pend))
+      return fail(MIKV_EALIGN, "%s: waiting-pair buffers must be 16-byte aligned", who);
+  }
   return MIKV_OK;
 }
 
@@ -425,6 +568,9 @@ int demote_args(const mikv_cache* c, const int32_t* victim, DemoteArgs& a) {
   a.pos_hi = c->pos_hi;
   a.pos_lo = c->pos_lo;
   a.scores = c->scores;
+  a.key_mode = c->key_mode;
+  a.k_pend = static_cast<__half*>(c->k_pend);
+  a.v_pend = static_cast<__half*>(c->v_pend);
   if (!a.k_hi || !a.v_hi || !a.k_lo || !a.v_lo || !a.k_lo_meta || !a.v_lo_meta || !a.pos_hi ||
       !a.pos_lo || !a.scores || (c->hi_bits != 16 && (!a.k_hi_meta || !a.v_hi_meta)))
     return fail(MIKV_EINVAL, "demotion: null cache buffer");
@@ -432,6 +578,72 @@ int demote_args(const mikv_cache* c, const int32_t* victim, DemoteArgs& a) {
       !aligned16(a.k_lo_meta) || !aligned16(a.v_lo_meta))
     return fail(MIKV_EALIGN, "demotion: buffers must be 16-byte aligned");
   return MIKV_OK;
+}
+
+ChanArgs chan_args(const mikv_cache* c) {
+  ChanArgs a{};
+  a.cap_lo = c->cap_lo;
+  a.k_lo = static_cast<uint8_t*>(c->k_lo);
+  a.v_lo = static_cast<uint8_t*>(c->v_lo);
+  a.k_meta = static_cast<__half2*>(c->k_lo_meta);
+  a.v_meta = static_cast<__half2*>(c->v_lo_meta);
+  a.pos_lo = c->pos_lo;
+  a.k_pend = static_cast<__half*>(c->k_pend);
+  a.v_pend = static_cast<__half*>(c->v_pend);
+  return a;
+}
+
+int launch_close(const ChanArgs& a, dim3 grid, int bits, cudaStream_t s) {
+  if (bits == 2) channel_close_kernel<2><<<grid, kTileThreads, 0, s>>>(a);
+  else channel_close_kernel<4><<<grid, kTileThreads, 0, s>>>(a);
+  return check_launch("channel_close_kernel");
+}
+
+// Per-channel keys: the prefill's retained tokens (n_lo must be a multiple of 64): full groups
+// are closed at once, the tail waits in the buffer.
+int channel_append_lo(const uint16_t* k, const uint16_t* v, int src_len, const int32_t* src_pos, int n_tokens,
+                      int pos_base, const mikv_cache* c, cudaStream_t s) {
+  if (c->n_lo % kGS)
+    return fail(MIKV_ESHAPE, "quantize_append(LO): per-channel keys append to a closed group boundary (n_lo=%d)",
+                c->n_lo);
+  if ((!k || !v) && n_tokens > 0) return fail(MIKV_EINVAL, "quantize_append: null k/v");
+  if (n_tokens < 0 || src_len < 1) return fail(MIKV_ESHAPE, "quantize_append: n_tokens/src_len");
+  if (c->n_lo + n_tokens > c->cap_lo)
+    return fail(MIKV_ESHAPE, "quantize_append: tier capacity %d exceeded (%d + %d)", c->cap_lo, c->n_lo, n_tokens);
+  if (!c->k_lo || !c->v_lo || !c->k_lo_meta || !c->v_lo_meta || !c->pos_lo)
+    return fail(MIKV_EINVAL, "quantize_append: null tier buffer");
+  if (!aligned16(c->k_lo) || !aligned16(c->v_lo) || !aligned16(c->k_lo_meta) || !aligned16(c->v_lo_meta) ||
+      (k && !aligned16(k)) || (v && !aligned16(v)))
+    return fail(MIKV_EALIGN, "quantize_append: buffers must be 16-byte aligned");
+  if (n_tokens == 0) return MIKV_OK;
+  const long units = static_cast<long>(c->B) * c->Hkv;
+  if (units > 65535) return fail(MIKV_ESHAPE, "quantize_append: B*Hkv=%ld above 65535", units);
+  ChanArgs a = chan_args(c);
+  a.k = reinterpret_cast<const __half*>(k);
+  a.v = reinterpret_cast<const __half*>(v);
+  a.src_pos = src_pos;
+  a.src_stride = src_len;
+  a.src_len = src_len;
+  a.n_tokens = n_tokens;
+  a.pos_base = pos_base;
+  a.base_slot = c->n_lo;
+  a.ngroups = n_tokens / kGS;
+  const int ctas = a.ngroups + (n_tokens % kGS ? 1 : 0);
+  return launch_close(a, dim3(ctas, static_cast<unsigned>(units)), c->lo_bits, s);
+}
+
+// Per-channel keys: close the group whose 64 pairs wait in the buffer (c->n_lo is the count
+// with the 64th pair included, a multiple of 64).
+int channel_close_waiting(const mikv_cache* c, cudaStream_t s) {
+  ChanArgs a = chan_args(c);
+  a.k = static_cast<const __half*>(c->k_pend);
+  a.v = static_cast<const __half*>(c->v_pend);
+  a.src_stride = kGS;
+  a.src_len = kGS;
+  a.n_tokens = kGS;
+  a.base_slot = c->n_lo - kGS;
+  a.ngroups = 1;
+  return launch_close(a, dim3(1, static_cast<unsigned>(c->B * c->Hkv)), c->lo_bits, s);
 }
 
 }  // namespace mikv
@@ -445,8 +657,11 @@ extern "C" int mikv_quantize_append(int tier, const uint16_t* k, const uint16_t*
   cudaStream_t s = as_stream(stream);
   if (tier == MIKV_TIER_HI || tier == MIKV_TIER_LO) {
     const bool hi = tier == MIKV_TIER_HI;
-    if (int e = append_tokens(hi, k, v, src_len, src_pos, n_tokens, pos_base, src_scores, c, s))
+    if (!hi && c->key_mode == MIKV_KEYS_PER_CHANNEL) {
+      if (int e = channel_append_lo(k, v, src_len, src_pos, n_tokens, pos_base, c, s)) return e;
+    } else if (int e = append_tokens(hi, k, v, src_len, src_pos, n_tokens, pos_base, src_scores, c, s)) {
       return e;
+    }
     if (hi) c->n_hi += n_tokens;
     else c->n_lo += n_tokens;
     return MIKV_OK;
@@ -460,6 +675,8 @@ extern "C" int mikv_quantize_append(int tier, const uint16_t* k, const uint16_t*
     if (int e = check_launch("demote_kernel")) return e;
     c->n_hi -= 1;
     c->n_lo += 1;
+    // per-channel keys: the 64th waiting pair closes its group
+    if (c->key_mode == MIKV_KEYS_PER_CHANNEL && c->n_lo % kGS == 0) return channel_close_waiting(c, s);
     return MIKV_OK;
   }
   return fail(MIKV_EINVAL, "quantize_append: bad tier %d", tier);
