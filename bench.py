@@ -58,6 +58,8 @@ def parse():
                    help="skip the timing of the post-attention top-k over a full FP16 cache")
     p.add_argument("--no-sweep", action="store_true",
                    help="skip the low-tier width x budget sweep of the full-depth workload")
+    p.add_argument("--no-channel-keys", action="store_true",
+                   help="skip the per-channel key cache leg of the full-depth workload")
     p.add_argument("--sweep-layers", type=int, default=8)
     p.add_argument("--sweep-steps", type=int, default=8)
     p.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -98,7 +100,13 @@ def same_cache_shape(wl):
     return dataclasses.replace(wl, B=base.B, layers=base.layers) == base
 
 
-def cache_bytes(wl, n_hi, n_lo):
+def cache_bytes(wl, n_hi, n_lo, key_mode=0):
+    """Packed bytes one attention launch reads.  Per-channel keys (key_mode 1): closed groups
+    cost the same per token as per-token codes (the group's key meta, 512 B per 64 slots, is
+    8 B a token), the n_lo % 64 waiting pairs are FP16."""
+    if key_mode == 1:
+        wait = n_lo % 64
+        return wl.B * wl.Hkv * (n_hi * ROW_BYTES[16] + (n_lo - wait) * ROW_BYTES[wl.lo_bits] + wait * ROW_BYTES[16])
     return wl.B * wl.Hkv * (n_hi * ROW_BYTES[wl.hi_bits] + n_lo * ROW_BYTES[wl.lo_bits])
 
 
@@ -217,7 +225,7 @@ def oracle_sample(wl, seconds: float):
 
 
 # ------------------------------------------------------------------------------ GPU leg
-def decode_run(wl, rank, world, dev, warmup, steps, attn_steps, extra_steps=0):
+def decode_run(wl, rank, world, dev, warmup, steps, attn_steps, extra_steps=0, key_mode=0):
     """Prefill every layer of `wl` (untimed), then `warmup` untimed decode steps, `steps` timed
     steps (CUDA events around the whole region, none inside it) and `attn_steps` further steps
     with the split-K attention launch of every layer timed alone by library-recorded events.
@@ -236,7 +244,7 @@ def decode_run(wl, rank, world, dev, warmup, steps, attn_steps, extra_steps=0):
     layers = []
     prefill_ms = []
     for l in range(wl.layers):
-        c = MikvCache(wl.B, wl.Hq, wl.Hkv, wl.D, wl.hi_bits, wl.lo_bits, cap_hi, cap_lo, dev)
+        c = MikvCache(wl.B, wl.Hq, wl.Hkv, wl.D, wl.hi_bits, wl.lo_bits, cap_hi, cap_lo, dev, key_mode=key_mode)
         x = inputs.make_prefill(rank_seed(wl, rank), l, dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
@@ -273,7 +281,7 @@ def decode_run(wl, rank, world, dev, warmup, steps, attn_steps, extra_steps=0):
             if mode == "attn":
                 a0, a1 = attn_ev[len(attn_pairs)]
                 # tiers as attended (after the append)
-                attn_pairs.append((a0, a1, cache_bytes(wl, c.n_hi + 1, c.n_lo)))
+                attn_pairs.append((a0, a1, cache_bytes(wl, c.n_hi + 1, c.n_lo, key_mode)))
                 _lib.mikv_set_attention_events(a0, a1)
             c.decode_step(t["q"], t["k"], t["v"], L_before, wl.budget_pct, wl.window, policy=wl.policy)
         return 4 * len(layers)   # append, split-K attention, merge, score update/demotion
@@ -296,7 +304,7 @@ def decode_run(wl, rank, world, dev, warmup, steps, attn_steps, extra_steps=0):
     for s in range(warmup, total_steps):
         L = wl.T + s + 1
         kv_tokens += wl.B * L * wl.layers
-        read_bytes += [cache_bytes(wl, c.n_hi + 1, c.n_lo) for c in layers]
+        read_bytes += [cache_bytes(wl, c.n_hi + 1, c.n_lo, key_mode) for c in layers]
         launches += step(s)
     end.record()
     torch.cuda.synchronize()
@@ -338,6 +346,27 @@ def sweep_points(wl, rank, world, dev, layers, steps, warmup, peak):
         torch.cuda.empty_cache()
         gbs = r["attn_bytes_mean"] / (r["attn_ms_mean"] / 1e3) / 1e9
         out.append({"lo_bits": lo, "budget_pct": p, "layers": layers, "steps": steps,
+                    "kv_tokens_per_s": r["kv_tokens"] / (r["ms"] / 1e3),
+                    "decode_step_us_per_layer": r["step_ms_mean"] * 1e3,
+                    "attn_us_per_launch": r["attn_ms_mean"] * 1e3,
+                    "attn_bytes_per_launch": r["attn_bytes_mean"],
+                    "attn_gbs": gbs, "frac": gbs / peak, "clocks": r["clocks"]})
+    return out
+
+
+def channel_key_points(wl, rank, world, dev, layers, steps, warmup, peak):
+    """The per-channel key cache (the Appendix C alternative) on `layers` layers of the
+    workload's shape, INT2 and INT4: KV-tokens/s of the whole step, and the split-K attention
+    launch timed alone against the HBM peak."""
+    import torch
+    out = []
+    for lo in (2, 4):
+        pw = wl.scaled(lo_bits=lo, layers=layers)
+        r, ls, tk, _ = decode_run(pw, rank, world, dev, warmup, steps, steps, key_mode=1)
+        del ls, tk
+        torch.cuda.empty_cache()
+        gbs = r["attn_bytes_mean"] / (r["attn_ms_mean"] / 1e3) / 1e9
+        out.append({"lo_bits": lo, "budget_pct": wl.budget_pct, "layers": layers, "steps": steps,
                     "kv_tokens_per_s": r["kv_tokens"] / (r["ms"] / 1e3),
                     "decode_step_us_per_layer": r["step_ms_mean"] * 1e3,
                     "attn_us_per_launch": r["attn_ms_mean"] * 1e3,
@@ -480,6 +509,9 @@ def run_gpu(args, wl, rank, world):
         torch.cuda.empty_cache()
         res["sweep"] = sweep_points(wl, rank, world, dev, args.sweep_layers, args.sweep_steps,
                                     args.warmup, peaks()[0])
+    if not args.no_channel_keys and wl.name == "llama31_8b_full":
+        res["channel_keys"] = channel_key_points(wl, rank, world, dev, args.sweep_layers, args.sweep_steps,
+                                                 args.warmup, peaks()[0])
     return res
 
 
@@ -604,6 +636,13 @@ def main():
                     "step, and the split-K attention launch timed alone against the HBM peak"
                     % args.sweep_layers,
             "points": res["sweep"]}
+    if "channel_keys" in res:
+        line["channel_keys"] = {
+            "what": "per-channel keys in the low tier (groups of 64 slots, scale and zero per (group, "
+                    "channel); retained pairs wait in FP16 until 64 close a group), FP16 important tier, "
+                    "the workload's budget, each width on %d layers: KV-tokens/s of the whole step, and "
+                    "the split-K attention launch timed alone against the HBM peak" % args.sweep_layers,
+            "points": res["channel_keys"]}
     if "e2e_ms" in res:
         line["e2e"] = {"value": res["e2e_tokens"] / (res["e2e_ms"] / 1e3), "unit": "KV-tokens/s",
                        "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]}

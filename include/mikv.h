@@ -246,8 +246,14 @@ size_t mikv_select_workspace_bytes(int policy, int B, int Hkv, int Hq, int L, in
  *   and v; INT8: fl(fl(s*code)+z), already balanced); then the last hi slot
  *   (k, v, meta, pos, score) moves into the freed slot.  n_hi -= 1, n_lo += 1.
  *   k, v, src_len, pos_base, src_scores unused.
+ * Per-channel keys (c->key_mode == MIKV_KEYS_PER_CHANNEL): MIKV_TIER_LO requires n_lo % 64 == 0;
+ *   the first floor(n_tokens / 64) * 64 tokens close groups at once (keys per channel, values
+ *   per token), the rest wait in k_pend / v_pend.  MIKV_TIER_DEMOTE moves the victim's FP16
+ *   pair into the waiting buffer (no quantisation); when it is the 64th waiting pair, a second
+ *   launch closes the group.  MIKV_TIER_HI is unchanged (FP16 copy).
  * Counts in *c are updated on the host after a successful launch.
- * Errors: EINVAL, ESHAPE (capacity overflow, src_len), EALIGN, EUNSUPPORTED, ECUDA.
+ * Errors: EINVAL, ESHAPE (capacity overflow, src_len, a per-channel LO append off a group
+ * boundary), EALIGN, EUNSUPPORTED, ECUDA.
  */
 int mikv_quantize_append(int tier, const uint16_t* k, const uint16_t* v, int src_len,
                          const int32_t* src_pos, int n_tokens, int pos_base,
@@ -266,6 +272,9 @@ int mikv_quantize_append(int tier, const uint16_t* k, const uint16_t* v, int src
  *   hi_logits fp32 [B][Hq][cap_hi] (slots < n_hi written) or NULL
  *   ws >= mikv_decode_workspace_bytes(c) bytes (split-K partial results and the
  *   per-(batch, key head) query fragments).
+ * Per-channel keys: closed groups give logit = (q_h . (s (.) code + z)) / sqrt(D) with the
+ *   group's per-channel scale s and zero z (no balancer); waiting pairs are attended as FP16
+ *   with the original q, like the FP16 tier.  The workspace also holds the fp32 query.
  * Requires n_hi + n_lo >= 1.  Errors: EINVAL, ESHAPE, EALIGN, EUNSUPPORTED, ECUDA.
  */
 int mikv_decode_attention(const uint16_t* q, const mikv_cache* c, float* out, float* lse,
@@ -285,7 +294,8 @@ size_t mikv_decode_workspace_bytes(const mikv_cache* c);
  *      n_keep(pos + 1) tokens, the victim (see mikv_select(MIKV_DEMOTE)) is
  *      demoted.  MIKV_CRITICALKV never demotes.
  * The order follows H2O: evict after the step's attention ([notes] "Key
- * contributions 1)"; [paperlayer] 5).  ws >= mikv_decode_step_workspace_bytes(c)
+ * contributions 1)"; [paperlayer] 5).  Per-channel keys: the demoted pair joins the waiting
+ * buffer, and a fifth launch closes its group when it is the 64th.  ws >= mikv_decode_step_workspace_bytes(c)
  * (partials, the important-tier logits, per-chunk victim candidates).  Counts in
  * *c are updated.  Two calls must not share a workspace concurrently.
  * Errors: EINVAL, ESHAPE (capacity, budget, workspace), EALIGN, EUNSUPPORTED
@@ -342,8 +352,8 @@ size_t mikv_topk_attention_workspace_bytes(const mikv_cache* c, int budget_pct);
 
 /*
  * Per-channel group quantisation of retained-tier keys ([notes] Appendix C remarks;
- * [paperlayer] C: group size 64, keys quantised per channel): the first stage of the
- * per-channel key alternative, whose cache integration is not built.
+ * [paperlayer] C: group size 64, keys quantised per channel), standalone: the arithmetic the
+ * per-channel cache (mikv_cache.key_mode) applies when it closes a group.
  * k fp16 [units][n][D] (D = 128): each unit's keys in slot order.  The floor(n / 64) full
  * groups are quantised; the n mod 64 keys after them are left alone (they wait in FP16 until
  * a group is full).  Per (group, channel c), over the group's 64 values of channel c:

@@ -133,3 +133,30 @@ def test_host_side_rejections(lib):
     assert lib.mikv_set_attention_events(None, None) == 0
     # the wait-status query needs somewhere to write
     assert lib.mikv_wait_status(None, 0) == EINVAL
+
+
+def test_per_channel_key_mode_rejections(lib):
+    """Per-channel keys: only FP16 important tiers over INT2 / INT4, whole groups of capacity,
+    waiting-pair buffers present, LO appends on a group boundary; all rejected on the host."""
+    EINVAL, ESHAPE, EUNSUP = -1, -2, -4
+    fake = ctypes.c_void_p(4096)
+
+    def cache(**kw):
+        c = _cache(**{"key_mode": 1, "cap_lo": 128, **kw})
+        c.k_lo = c.v_lo = c.k_lo_meta = c.v_lo_meta = c.pos_lo = 4096
+        if "k_pend" not in kw:
+            c.k_pend = c.v_pend = 4096
+        return c
+
+    app = lambda c, n=1: lib.mikv_quantize_append(1, fake, fake, 8, fake, n, 0, None, ctypes.byref(c), None)
+    assert app(_cache(key_mode=7)) == EINVAL
+    assert app(cache(hi_bits=8)) == EUNSUP
+    assert app(cache(lo_bits=8)) == EUNSUP
+    assert app(cache(cap_lo=100)) == ESHAPE
+    c = cache(k_pend=None)
+    c.k_pend = c.v_pend = None
+    assert app(c) == EINVAL
+    assert app(cache(n_lo=10)) == ESHAPE                         # off a group boundary
+    assert b"group boundary" in lib.mikv_last_error()
+    assert lib.mikv_decode_workspace_bytes(ctypes.byref(cache(cap_hi=64))) > \
+        lib.mikv_decode_workspace_bytes(ctypes.byref(_cache(cap_hi=64, cap_lo=128)))

@@ -150,3 +150,81 @@ def test_channel_fused_step_equals_separate_calls():
             assert torch.equal(getattr(fused, nm)[:, :, :n], getattr(calls, nm)[:, :, :n]), nm
         assert torch.equal(fused.scores[:, :, :fused.n_hi], calls.scores[:, :, :calls.n_hi])
     assert closed
+
+
+class ChannelUnitMirror:
+    """Oracle per-channel cache of one (batch, key head) unit following the library's steps
+    (the library's victims; the oracle's float64 scores must rank each one first unless the two
+    lowest candidates are within the score bar of each other)."""
+
+    def __init__(self, wl, gc, x, info, b, g, steps):
+        self.wl, self.b, self.g = wl, b, g
+        kp = to_np(info["keep_pos"][b, g]).astype(np.int32)
+        ep = to_np(info["evict_pos"][b, g]).astype(np.int32)
+        cap_lo = -(-(len(ep) + steps + 1) // 64) * 64
+        self.oc = cq.ChannelKeyCache(1, 1, wl.Hq // wl.Hkv, 128, wl.lo_bits, len(kp) + steps + 1, cap_lo)
+        src_k, src_v = to_np(x["k"][b, g])[None, None], to_np(x["v"][b, g])[None, None]
+        ks = to_np(info["keep_scores"][b, g]).astype(np.float64)[None, None]
+        self.oc.append("hi", src_k, src_v, kp[None, None], 0, ks)
+        self.oc.append("lo", src_k, src_v, ep[None, None], 0)
+        self.near_ties = 0
+
+    def step(self, gc, tok, out, L_before, n_lo_before):
+        wl, oc, b, g = self.wl, self.oc, self.b, self.g
+        rep, L, W = wl.Hq // wl.Hkv, L_before + 1, wl.window
+        oc.append("hi", to_np(tok["k"][b, g])[None, None, None], to_np(tok["v"][b, g])[None, None, None],
+                  np.zeros((1, 1, 1), np.int32), L - 1)
+        q = to_np(tok["q"][b, g * rep:(g + 1) * rep])[None]
+        want, lse, logits = oc.attend(q)
+        from oracle import scores as osc
+        oc.scores[0, 0, :oc.n_hi] = osc.decode_score_update(oc.scores[0, 0, :oc.n_hi], logits[0], lse[0])
+        err = np.abs(to_np(out[b, g * rep:(g + 1) * rep]) - want[0]).max()
+        if gc.n_lo > n_lo_before:   # the library demoted: follow its victim
+            vpos = int(to_np(gc.pos_lo[b, g, n_lo_before]))
+            pos = oc.pos_hi[0, 0, :oc.n_hi]
+            j_lib = int(np.nonzero(pos == vpos)[0][0])
+            s = oc.scores[0, 0, :oc.n_hi]
+            j_or = osel.demote_victim(s.astype(np.float32), pos, L, W)
+            if j_lib != j_or:
+                assert abs(s[j_lib] - s[j_or]) <= 2 * SCORE_RTOL * np.abs(s).max()
+                self.near_ties += 1
+            oc.demote(np.array([[j_lib]], np.int32))
+        compare_unit(gc, oc, b, g, 0, 0)
+        got = to_np(gc.scores[b, g, :gc.n_hi]).astype(np.float64)
+        assert np.abs(got - oc.scores[0, 0, :oc.n_hi]).max() <= SCORE_RTOL * np.abs(oc.scores[0, 0, :oc.n_hi]).max()
+        return err
+
+
+@pytest.mark.parametrize("lo", [2, 4])
+def test_channel_fullsize_lockstep(lo):
+    """The full-depth workload's layer shape (B 4 here, T 8192, 20 % FP16, window 32) with
+    per-channel keys: 26 waiting pairs after prefill, a group closes at the 38th demotion;
+    sampled units follow an oracle cache step by step for 48 steps."""
+    wl = inputs.WORKLOADS["llama31_8b_full"].scaled(B=4, layers=1, lo_bits=lo)
+    d = dev()
+    steps = 48
+    x = inputs.make_prefill(wl, 0, d)
+    T, W = wl.T, wl.window
+    keep = osel.n_keep(T, wl.budget_pct, W)
+    gc = MikvCache(wl.B, wl.Hq, wl.Hkv, 128, 16, lo, keep + steps + 1, T - keep + steps + 1, d, key_mode=CH)
+    info = gc.prefill(x["q"], x["k"], x["v"], wl.budget_pct, W, keep_intermediates=True)
+    torch.cuda.synchronize()
+    assert gc.n_lo % 64 == 26
+    mirrors = [ChannelUnitMirror(wl, gc, x, info, b, g, steps) for b, g in ((0, 3), (3, 6))]
+    for m in mirrors:
+        compare_unit(gc, m.oc, m.b, m.g, 0, 0)
+    del x, info
+    worst, closed = 0.0, False
+    for s in range(steps):
+        tok = inputs.make_decode_token(wl, 0, s, d)
+        n_lo = gc.n_lo
+        out, _ = gc.decode_step(tok["q"], tok["k"], tok["v"], T + s, wl.budget_pct, W)
+        torch.cuda.synchronize()
+        closed |= gc.n_lo // 64 > n_lo // 64
+        for m in mirrors:
+            err = m.step(gc, tok, out, T + s, n_lo)
+            worst = max(worst, err)
+            assert err <= ATTN_TOL, (s, err)
+    assert closed
+    assert worst <= 1e-4, worst
+    assert sum(m.near_ties for m in mirrors) <= 1
