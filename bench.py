@@ -372,6 +372,29 @@ def channel_key_points(wl, rank, world, dev, layers, steps, warmup, peak):
                     "attn_us_per_launch": r["attn_ms_mean"] * 1e3,
                     "attn_bytes_per_launch": r["attn_bytes_mean"],
                     "attn_gbs": gbs, "frac": gbs / peak, "clocks": r["clocks"]})
+    # the standalone group quantiser over one layer's keys: (B * Hkv) units of T keys
+    from mixed_precision_kv_balancer_gb300 import _lib, inputs
+    k = inputs.make_prefill(wl.scaled(layers=1), 0, dev)["k"]
+    units, T = wl.B * wl.Hkv, wl.T
+    k = k.reshape(units, T, wl.D)
+    codes = torch.empty(units, T, wl.D * 2 // 8, dtype=torch.uint8, device=dev)
+    meta = torch.empty(units, T // 64, wl.D, 2, dtype=torch.float16, device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+    for i in range(3 + len(ev)):
+        if i >= 3:
+            ev[i - 3][0].record()
+        _lib.mikv_channel_quantize(k, 2, codes, meta)
+        if i >= 3:
+            ev[i - 3][1].record()
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    nbytes = units * T * wl.D * 2 + codes.numel() + meta.numel() * 2
+    gbs = nbytes / (ms / 1e3) / 1e9
+    out.append({"what": "mikv_channel_quantize, INT2, one layer's keys", "units": units, "keys": T,
+                "us_per_call": ms * 1e3, "bytes_per_call": nbytes, "gbs": gbs, "frac": gbs / peak,
+                "timing": "CUDA events around each of 20 calls (the keys are larger than L2)"})
+    del k, codes, meta
+    torch.cuda.empty_cache()
     return out
 
 

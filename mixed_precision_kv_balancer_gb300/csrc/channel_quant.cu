@@ -9,51 +9,11 @@
 #include "common.cuh"
 
 namespace mikv {
-namespace {
-
-constexpr int kCqGroup = 64;
-
-// One CTA per (group, unit), one thread per channel.
-__global__ void __launch_bounds__(kD) channel_group_quant_kernel(const __half* __restrict__ k, int n, int bits,
-                                                                 uint8_t* __restrict__ codes,
-                                                                 __half2* __restrict__ meta) {
-  __shared__ uint8_t cs[kCqGroup][kD];
-  const int grp = blockIdx.x, ngrp = gridDim.x;
-  const long unit = blockIdx.y;
-  const int c = threadIdx.x;
-  const __half* src = k + (unit * n + static_cast<long>(grp) * kCqGroup) * kD + c;
-  float x[kCqGroup];
-  float mn = INFINITY, mx = -INFINITY;
-#pragma unroll
-  for (int t = 0; t < kCqGroup; ++t) {
-    x[t] = __half2float(src[static_cast<long>(t) * kD]);
-    mn = fminf(mn, x[t]);
-    mx = fmaxf(mx, x[t]);
-  }
-  const int qmax = (1 << bits) - 1;
-  const float s32 = __fdiv_rn(__fsub_rn(mx, mn), static_cast<float>(qmax));
-  const __half sh = __float2half_rn(s32), zh = __float2half_rn(mn);
-  const float sf = __half2float(sh), zf = __half2float(zh);
-  meta[(unit * ngrp + grp) * kD + c] = __halves2half2(sh, zh);
-#pragma unroll
-  for (int t = 0; t < kCqGroup; ++t) {
-    int q = 0;
-    if (sf != 0.f) q = min(max(__float2int_rn(__fdiv_rn(__fsub_rn(x[t], zf), sf)), 0), qmax);
-    cs[t][c] = static_cast<uint8_t>(q);
-  }
-  __syncthreads();
-  // pack: row t holds kD * bits / 8 bytes; byte j carries channels j*per .. j*per + per - 1
-  const int per = 8 / bits, row_bytes = kD * bits / 8;
-  uint8_t* dst = codes + (unit * n + static_cast<long>(grp) * kCqGroup) * row_bytes;
-  for (int i = threadIdx.x; i < kCqGroup * row_bytes; i += kD) {
-    const int t = i / row_bytes, j = i % row_bytes;
-    uint32_t byte = 0;
-    for (int e = 0; e < per; ++e) byte |= static_cast<uint32_t>(cs[t][j * per + e]) << (e * bits);
-    dst[static_cast<long>(t) * row_bytes + j] = static_cast<uint8_t>(byte);
-  }
-}
-
-}  // namespace
+// In quantize.cu: the same group-closing kernel the per-channel cache uses, keys only (one CTA
+// per (group, unit): the group's 64 rows staged in shared memory with 16-byte copies, one
+// thread per channel, codes packed per row with 16-byte stores).
+int channel_quantize_keys(const __half* k, int units, int n, int bits, uint8_t* codes, __half2* meta,
+                          cudaStream_t s);
 }  // namespace mikv
 
 using namespace mikv;
@@ -65,9 +25,8 @@ extern "C" int mikv_channel_quantize(const uint16_t* k, int units, int n, int D,
   if (D != kD) return fail(MIKV_EUNSUPPORTED, "channel_quantize: D=%d (only %d)", D, kD);
   if (bits != 2 && bits != 4 && bits != 8) return fail(MIKV_EUNSUPPORTED, "channel_quantize: bits=%d", bits);
   if (units < 1 || n < 0 || units > 65535) return fail(MIKV_ESHAPE, "channel_quantize: units=%d n=%d", units, n);
-  const int ngrp = n / kCqGroup;
-  if (ngrp == 0) return MIKV_OK;  // every key is still pending
-  channel_group_quant_kernel<<<dim3(ngrp, units), kD, 0, as_stream(stream)>>>(
-      reinterpret_cast<const __half*>(k), n, bits, codes, reinterpret_cast<__half2*>(meta));
-  return check_launch("channel_group_quant_kernel");
+  if (!aligned16(k) || !aligned16(codes) || !aligned16(meta))
+    return fail(MIKV_EALIGN, "channel_quantize: k, codes and meta must be 16-byte aligned");
+  return channel_quantize_keys(reinterpret_cast<const __half*>(k), units, n, bits, codes,
+                               reinterpret_cast<__half2*>(meta), as_stream(stream));
 }

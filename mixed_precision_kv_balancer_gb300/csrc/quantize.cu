@@ -327,8 +327,8 @@ struct ChanArgs {
 // (cp.async, 16 bytes), thread c quantises key channel c over the 64 rows (column extremes,
 // codes into a shared byte matrix), thread (row, half) quantises one value group of a row;
 // rows of key codes are packed at the end.  gi == ngroups (prefill only): the tail rows are
-// copied to the waiting buffer.
-template <int BITS>
+// copied to the waiting buffer.  VALUES false: keys only (the standalone group quantiser).
+template <int BITS, bool VALUES = true>
 __global__ void __launch_bounds__(kTileThreads) channel_close_kernel(ChanArgs a) {
   __shared__ __align__(16) __half ks[kGS][kD];        // keys, row-major
   __shared__ __align__(16) uint8_t vs[kGS][kD * 2];   // values, 16-byte chunks swizzled by row
@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(kTileThreads) channel_close_kernel(ChanArgs a)
     const int src = ssrc[r];
     const long off = (unit * a.src_stride + (src >= 0 ? src : 0)) * kD + c * 8;
     cp_async16(smem_u32(&ks[r][c * 8]), a.k + off, src >= 0);
-    cp_async16(smem_u32(&vs[r][(c ^ (r & 7)) * 16]), a.v + off, src >= 0);
+    if (VALUES) cp_async16(smem_u32(&vs[r][(c ^ (r & 7)) * 16]), a.v + off, src >= 0);
   }
   cp_async_commit();
   cp_async_wait<0>();
@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(kTileThreads) channel_close_kernel(ChanArgs a)
       cs[r][t] = static_cast<uint8_t>(code);
     }
   }
-  {  // value group (t >> 6) of row t % 64, per token
+  if (VALUES) {  // value group (t >> 6) of row t % 64, per token
     const int r = t & 63, g = t >> 6;
     uint32_t out[64 * BITS / 32];
     const uint32_t meta = quantize_group64<BITS>(vs[r], g, r, ones, false, out);
@@ -597,6 +597,28 @@ int launch_close(const ChanArgs& a, dim3 grid, int bits, cudaStream_t s) {
   if (bits == 2) channel_close_kernel<2><<<grid, kTileThreads, 0, s>>>(a);
   else channel_close_kernel<4><<<grid, kTileThreads, 0, s>>>(a);
   return check_launch("channel_close_kernel");
+}
+
+// The standalone per-channel group quantiser (mikv_channel_quantize): keys [units][n][D], the
+// floor(n / 64) full groups of each unit quantised in place of rows, meta [units][n / 64][D].
+int channel_quantize_keys(const __half* k, int units, int n, int bits, uint8_t* codes, __half2* meta,
+                          cudaStream_t s) {
+  const int ngrp = n / kGS;
+  if (ngrp == 0) return MIKV_OK;  // every key is still waiting
+  ChanArgs a{};
+  a.k = k;
+  a.src_stride = n;
+  a.src_len = n;
+  a.n_tokens = ngrp * kGS;
+  a.cap_lo = n;  // code rows per unit; meta rows per unit = n / 64
+  a.ngroups = ngrp;
+  a.k_lo = codes;
+  a.k_meta = meta;
+  const dim3 grid(ngrp, units);
+  if (bits == 2) channel_close_kernel<2, false><<<grid, kTileThreads, 0, s>>>(a);
+  else if (bits == 4) channel_close_kernel<4, false><<<grid, kTileThreads, 0, s>>>(a);
+  else channel_close_kernel<8, false><<<grid, kTileThreads, 0, s>>>(a);
+  return check_launch("channel_close_kernel (keys)");
 }
 
 // Per-channel keys: the prefill's retained tokens (n_lo must be a multiple of 64): full groups
