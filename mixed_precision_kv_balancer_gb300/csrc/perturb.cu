@@ -12,15 +12,17 @@
 //
 // Layout: the projection comes as nn.Linear stores it, w_o_t = W_O^T [hidden][Hq*D], which is
 // already K-major (channels contiguous) for the tensor core.  A prep kernel writes, per head
-// and block of 32 batch rows, one 128-row fp16 operand tile: rows 0..63 hold o, rows 64..127
-// hold d = o - o^, each row scaled by a power of two (max magnitude in [2^13, 2^14)) and
-// written as two fp16 rows (hi = fp16(x), lo = fp16(x - hi): ~22 bits, so the products stay
-// near fp32 accuracy for differences of any size).  The main kernel (one CTA per 64 hidden columns
-// and batch block) streams, head by head, that tile and the head's 64 x 128 block of W_O^T
-// through a four-stage TMA ring (48 KB a stage: three stages in flight hide the L2 / DRAM
-// latency), multiplies them with tcgen05.mma (M 128, N 64, K 128, fp32
-// in TMEM), and the consumers add hi + lo, accumulate y over the heads in registers and sum
-// |z| of the d rows per head.  A last kernel adds the per-head partial sums in a fixed order.
+// and block of 64 batch rows, one 256-row fp16 operand tile: four rows per batch row, o and
+// d = o - o^ each scaled by a power of two (max magnitude in [2^13, 2^14)) and split into two
+// fp16 rows (hi = fp16(x), lo = fp16(x - hi): ~22 bits, so the products stay near fp32
+// accuracy for differences of any size).  The product kernel (one CTA per 128 hidden columns,
+// chunk of heads and batch block) streams, head by head, the head's 128 x 128 block of W_O^T
+// (the MMA's M operand) and the operand tile (N = 256) as 64-channel k-blocks through a
+// four-stage TMA ring, multiplies them with tcgen05.mma into one of two TMEM accumulators, and
+// the consumers add hi + lo, accumulate y over the chunk's heads in registers and sum |z| of
+// the d rows per (batch row, head).  Two small kernels add the chunks' y and the column
+// blocks' sums in a fixed order.  The four launches are chained with programmatic dependent
+// launch: each is placed while its predecessor runs and waits for it before its first read.
 #include <algorithm>
 
 #include "common.cuh"
@@ -65,6 +67,7 @@ __host__ __device__ inline int pt_chunk_begin(int Hq, int nch, int c) { return s
 // invs[(h * 64 * nbb + b) * 2 + {0: o, 1: d}] receives the inverse.  Rows b >= B are zero.
 __global__ void perturb_prep_kernel(const float* __restrict__ o, const float* __restrict__ o_hat, int B, int Hq,
                                     __half* __restrict__ a, float* __restrict__ invs) {
+  pdl_trigger();
   const int nbb = pt_blocks(B), Bp = nbb * kPtBatch;
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (w >= Hq * Bp) return;
@@ -162,6 +165,8 @@ __global__ void __launch_bounds__(kPtBlock, 1) perturb_tc_kernel(const __grid_co
   __shared__ uint32_t tslot;
   __shared__ float red[2][8][32];
   __shared__ int bad;
+  pdl_wait();  // the operand tiles and row scales come from the prep kernel
+  pdl_trigger();
   const int cb = blockIdx.x, hc = blockIdx.y, bb = blockIdx.z, nbb = gridDim.z, Bp = nbb * kPtBatch;
   const int ncb = hidden / kPtM;
   const int nch = gridDim.y;
@@ -271,6 +276,8 @@ __global__ void __launch_bounds__(kPtBlock, 1) perturb_tc_kernel(const __grid_co
 
 // y[b][c] = sum over the head chunks of their partials, in chunk order.
 __global__ void perturb_yreduce_kernel(const float* __restrict__ ypart, int nchunk, long n, float* __restrict__ y) {
+  pdl_wait();
+  pdl_trigger();
   for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<long>(gridDim.x) * blockDim.x) {
     float t = 0.f;
@@ -281,6 +288,7 @@ __global__ void perturb_yreduce_kernel(const float* __restrict__ ypart, int nchu
 
 // pert[b][h] = sum of the ncb column-block partial sums, in column order.  One warp per (b, h).
 __global__ void perturb_reduce_kernel(const float* __restrict__ part, int n, int nparts, float* __restrict__ pert) {
+  pdl_wait();
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (w >= n) return;
   float s = 0.f;
@@ -368,17 +376,21 @@ extern "C" int mikv_output_perturbation(const float* o, const float* o_hat, cons
   const int smem = kPtSmem + hmax * 2 * kPtBatch * static_cast<int>(sizeof(float));
   if (cudaFuncSetAttribute(perturb_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return check_launch("perturb_tc_kernel attribute");
-  perturb_tc_kernel<<<dim3(ncb, nch, nbb), kPtBlock, smem, s>>>(tw, to, B, Hq, hidden, invs, ypart, part);
-  if (int e = check_launch("perturb_tc_kernel")) return e;
+  if (int e = check_launch_after(launch_after(perturb_tc_kernel, dim3(ncb, nch, nbb), dim3(kPtBlock), smem, s, tw, to,
+                                              B, Hq, hidden, invs, ypart, part),
+                                 "perturb_tc_kernel"))
+    return e;
   if (y) {
     const long n = static_cast<long>(B) * hidden;
-    perturb_yreduce_kernel<<<static_cast<int>(std::min<long>((n + 255) / 256, 152L * 8)), 256, 0, s>>>(ypart, nch, n, y);
-    if (int e = check_launch("perturb_yreduce_kernel")) return e;
+    const int blocks = static_cast<int>(std::min<long>((n + 255) / 256, 152L * 8));
+    if (int e = check_launch_after(launch_after(perturb_yreduce_kernel, dim3(blocks), dim3(256), 0, s, ypart, nch, n, y),
+                                   "perturb_yreduce_kernel"))
+      return e;
   }
   if (!pert) return MIKV_OK;
   const int n = B * Hq;
-  perturb_reduce_kernel<<<(n + 7) / 8, 256, 0, s>>>(part, n, ncb, pert);
-  return check_launch("perturb_reduce_kernel");
+  return check_launch_after(launch_after(perturb_reduce_kernel, dim3((n + 7) / 8), dim3(256), 0, s, part, n, ncb, pert),
+                            "perturb_reduce_kernel");
 }
 
 namespace mikv {
