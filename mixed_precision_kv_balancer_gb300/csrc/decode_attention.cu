@@ -1050,7 +1050,10 @@ double byte_weight(int bits) { return bits == 16 ? 1.0 : bits == 8 ? 1.25 : bits
 // resident slots share the total, and the tail adds kTailFactor times the largest CTA.
 constexpr double kCtaOverhead = 183.0 * 1024;
 constexpr double kTailFactor = 2.13;
-constexpr double kMinWaves = 2.5;  // keep at least this many waves when the cache allows
+#ifndef MIKV_MIN_WAVES
+#define MIKV_MIN_WAVES 2.5
+#endif
+constexpr double kMinWaves = MIKV_MIN_WAVES;  // keep at least this many waves when the cache allows
 constexpr int kCtasPerSm = 3;
 
 struct Plan {
