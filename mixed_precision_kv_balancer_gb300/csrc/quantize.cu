@@ -333,6 +333,7 @@ __global__ void __launch_bounds__(kTileThreads) channel_close_kernel(ChanArgs a)
   __shared__ __align__(16) __half ks[kGS][kD];        // keys, row-major
   __shared__ __align__(16) uint8_t vs[kGS][kD * 2];   // values, 16-byte chunks swizzled by row
   __shared__ __align__(16) uint8_t cs[kGS][kD];       // key codes
+  __shared__ __half2 ext[2][kD / 2][2];                // per row half: (min, max) of channel pairs
   __shared__ __align__(16) float ones[kD];
   __shared__ int ssrc[kGS];
   const long unit = blockIdx.y;
@@ -373,30 +374,75 @@ __global__ void __launch_bounds__(kTileThreads) channel_close_kernel(ChanArgs a)
   cp_async_wait<0>();
   __syncthreads();
   constexpr int qmax = (1 << BITS) - 1;
-  {  // key channel t over the 64 rows
-    float mn = INFINITY, mx = -INFINITY;
+  {  // key channels (2 cp, 2 cp + 1), cp = t % 64, over rows 32 h .. 32 h + 31, h = t / 64: the
+     // pair's extremes in half2 arithmetic (exact), combined with the other half through shared
+     // memory, then the codes on packed fp32 pairs (the same quotient rule as the per-token tiers)
+    const int cp = t & 63, h = t >> 6, c = 2 * cp;
+    __half2 lo2 = __float2half2_rn(INFINITY), hi2 = __float2half2_rn(-INFINITY);
 #pragma unroll 8
-    for (int r = 0; r < kGS; ++r) {
-      const float x = __half2float(ks[r][t]);
-      mn = fminf(mn, x);
-      mx = fmaxf(mx, x);
+    for (int r = 32 * h; r < 32 * h + 32; ++r) {
+      const __half2 x = *reinterpret_cast<const __half2*>(&ks[r][c]);
+      lo2 = __hmin2(lo2, x);
+      hi2 = __hmax2(hi2, x);
     }
-    const float s32 = __fdiv_rn(__fsub_rn(mx, mn), static_cast<float>(qmax));
-    const __half sh = __float2half_rn(s32), zh = __float2half_rn(mn);
-    const float sf = __half2float(sh), zf = __half2float(zh);
-    const float rf = sf != 0.f ? __frcp_rn(sf) : 0.f;
-    a.k_meta[(unit * (a.cap_lo / kGS) + (a.base_slot + j0) / kGS) * kD + t] = __halves2half2(sh, zh);
-#pragma unroll 8
-    for (int r = 0; r < kGS; ++r) {
-      uint32_t code = 0;
-      if (sf != 0.f) {
-        const float d = __fsub_rn(__half2float(ks[r][t]), zf);
-        const float q = __fmul_rn(d, rf);
-        float qi = rintf(q);
-        if (fabsf(q - qi) > 0.5f - kTieGuard) qi = rint_div(d, sf);  // near a tie: exact quotient
-        code = static_cast<uint32_t>(fminf(fmaxf(qi, 0.f), static_cast<float>(qmax)));
+    ext[h][cp][0] = lo2;
+    ext[h][cp][1] = hi2;
+    __syncthreads();
+    lo2 = __hmin2(ext[0][cp][0], ext[1][cp][0]);
+    hi2 = __hmax2(ext[0][cp][1], ext[1][cp][1]);
+    const float2 mn = __half22float2(lo2), mx = __half22float2(hi2);
+    const float s0 = __fdiv_rn(__fsub_rn(mx.x, mn.x), static_cast<float>(qmax));
+    const float s1 = __fdiv_rn(__fsub_rn(mx.y, mn.y), static_cast<float>(qmax));
+    const __half sh0 = __float2half_rn(s0), zh0 = __float2half_rn(mn.x);
+    const __half sh1 = __float2half_rn(s1), zh1 = __float2half_rn(mn.y);
+    const float sf0 = __half2float(sh0), zf0 = __half2float(zh0), sf1 = __half2float(sh1), zf1 = __half2float(zh1);
+    const float rf0 = sf0 != 0.f ? __frcp_rn(sf0) : 0.f, rf1 = sf1 != 0.f ? __frcp_rn(sf1) : 0.f;
+    if (h == 0) {
+      __half2* km = a.k_meta + (unit * (a.cap_lo / kGS) + (a.base_slot + j0) / kGS) * kD + c;
+      km[0] = __halves2half2(sh0, zh0);
+      km[1] = __halves2half2(sh1, zh1);
+    }
+    // extremes' quotients: inside (-1/2, qmax + 1/2) no value of the channel needs the clamp
+    const bool fast = sf0 != 0.f && sf1 != 0.f &&
+                      __fmul_rn(__fsub_rn(mn.x, zf0), rf0) > -0.5f + kRangeGuard &&
+                      __fmul_rn(__fsub_rn(mx.x, zf0), rf0) < qmax + 0.5f - kRangeGuard &&
+                      __fmul_rn(__fsub_rn(mn.y, zf1), rf1) > -0.5f + kRangeGuard &&
+                      __fmul_rn(__fsub_rn(mx.y, zf1), rf1) < qmax + 0.5f - kRangeGuard;
+    if (fast) {
+      const float2 nz = make_float2(-zf0, -zf1), r2 = make_float2(rf0, rf1);
+      const float2 mg = make_float2(kRoundMagic, kRoundMagic), nmg = make_float2(-kRoundMagic, -kRoundMagic);
+#pragma unroll 4
+      for (int r = 32 * h; r < 32 * h + 32; ++r) {
+        const float2 d = add2_rn(__half22float2(*reinterpret_cast<const __half2*>(&ks[r][c])), nz);
+        const float2 q = mul2_rn(d, r2);
+        float2 qi = add2_rn(add2_rn(q, mg), nmg);
+        const float2 e = __ffma2_rn(qi, make_float2(-1.f, -1.f), q);  // q - qi, exact
+        if (fmaxf(fabsf(e.x), fabsf(e.y)) > 0.5f - kTieGuard) {       // rare: near a tie
+          if (fabsf(e.x) > 0.5f - kTieGuard) qi.x = rint_div(d.x, sf0);
+          if (fabsf(e.y) > 0.5f - kTieGuard) qi.y = rint_div(d.y, sf1);
+        }
+        *reinterpret_cast<uint16_t*>(&cs[r][c]) =
+            static_cast<uint16_t>((__float_as_uint(qi.x + 8388608.f) & 0xffu) |
+                                  ((__float_as_uint(qi.y + 8388608.f) & 0xffu) << 8));
       }
-      cs[r][t] = static_cast<uint8_t>(code);
+    } else {  // a constant channel (scale 0: codes 0), or one whose extremes need the clamp
+#pragma unroll 4
+      for (int r = 32 * h; r < 32 * h + 32; ++r) {
+        const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&ks[r][c]));
+        uint32_t code[2] = {0u, 0u};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float sf = e ? sf1 : sf0, zf = e ? zf1 : zf0, rf = e ? rf1 : rf0;
+          if (sf != 0.f) {
+            const float d = __fsub_rn(e ? x.y : x.x, zf);
+            const float q = __fmul_rn(d, rf);
+            float qi = rintf(q);
+            if (fabsf(q - qi) > 0.5f - kTieGuard) qi = rint_div(d, sf);  // near a tie: exact quotient
+            code[e] = static_cast<uint32_t>(fminf(fmaxf(qi, 0.f), static_cast<float>(qmax)));
+          }
+        }
+        *reinterpret_cast<uint16_t*>(&cs[r][c]) = static_cast<uint16_t>(code[0] | (code[1] << 8));
+      }
     }
   }
   if (VALUES) {  // value group (t >> 6) of row t % 64, per token

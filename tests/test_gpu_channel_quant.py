@@ -33,3 +33,25 @@ def test_channel_quantize_bit_exact(bits, units, n):
             np.testing.assert_array_equal(gm[u, gi], m_o)
         # rows of the pending keys are not written
         assert np.all(gc[u, 64 * (n // 64):] == 0xAB)
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_channel_quantize_near_ties_bit_exact(bits):
+    """Every channel's 64 values on, or one fp16 step beside, the half-integer points of the
+    channel's own grid (both ends present), so the quotient (x - z) / s meets rounding ties:
+    the packed fast path and its exact-division fallback must match the oracle."""
+    from test_gpu_parity import _tie_rows
+    rng = np.random.default_rng(90 + bits)
+    qmax = 2 ** bits - 1
+    units = 3
+    k = np.stack([_tie_rows(rng, 128, qmax)[:, :64].T for _ in range(units)]).astype(np.float16)  # [u][64][128]
+    rb = 128 * bits // 8
+    codes = torch.zeros((units, 64, rb), dtype=torch.uint8, device=dev())
+    meta = torch.zeros((units, 1, 128, 2), dtype=torch.float16, device=dev())
+    _lib.mikv_channel_quantize(torch.from_numpy(np.ascontiguousarray(k)).to(dev()), bits, codes, meta)
+    torch.cuda.synchronize()
+    gc, gm = to_np(codes), to_np(meta.view(torch.int16)).view(np.uint16)
+    for u in range(units):
+        c_o, m_o = cq.quantize_channel_group(k[u], bits)
+        np.testing.assert_array_equal(gm[u, 0], m_o)
+        np.testing.assert_array_equal(gc[u], oq.pack_codes(c_o, bits))
