@@ -384,19 +384,30 @@ int mikv_set_attention_events(void* begin, void* end);
  * K6's V.W_O norms in mikv_select(MIKV_CRITICALKV) with w_o, K9 in
  * mikv_output_perturbation) hand tiles between a TMA/MMA thread and their consumer warps
  * through mbarriers, and every wait there gives up after ~4 million polls instead of
- * spinning for ever.  No wait is expected to run out; if one does, the kernel keeps the
- * hand-off order (so that every copy and MMA it issued still completes before it exits),
- * writes NaN into the outputs of the affected CTA (prefill scores and -lse rows, V.W_O
- * norms, perturbation and y partial sums), and sets a bit in a device-side status word.
+ * spinning for ever.  No wait is expected to run out; if one does, the thread that gave up
+ * issues no further copy or MMA, its later waits poll only ~1000 times each (so a stuck
+ * pipeline still ends in a bounded time, and what was issued before has that long to land),
+ * the kernel writes NaN into the outputs of the affected CTA (prefill scores and -lse rows,
+ * V.W_O norms, perturbation and y partial sums) and sets a bit in a device-side status word.
  * The call that launched it has already returned MIKV_OK (launches are asynchronous).
  * mikv_wait_status stores the OR of the bits set since the last clear in *bits:
  *   1 = K3 pass 1 (row log-sum-exp), 2 = K3 pass 2 (column sums), 4 = K6 (V.W_O norms),
- *   8 = K9 (output perturbation)
+ *   8 = K9 (output perturbation), 16 = mikv_wait_probe
  * and clears them if `clear` is non-zero.  It copies synchronously: call it after the work
  * in question has completed (e.g. after synchronising its stream).
  * Errors: EINVAL (null bits), ECUDA (the copy failed).
  */
 int mikv_wait_status(unsigned* bits, int clear);
+
+/*
+ * Self-check of the give-up path above (no counterpart in the papers): one thread waits, with
+ * the same bounded wait as the tensor-core kernels, on an mbarrier of one arrival that it
+ * makes itself only if `arrive` is non-zero.  Without the arrival the first wait gives up
+ * after `polls` polls (1 .. 2^24), a second one after the short limit, and status bit 16 is
+ * set; with it nothing is set.  No memory is read or written but that bit; the launch does
+ * not disturb the context.  Stream-ordered.  Errors: EINVAL (polls), ECUDA (launch).
+ */
+int mikv_wait_probe(int64_t polls, int arrive, void* stream);
 
 /* Message of the last failed call on this thread ("" if none). */
 const char* mikv_last_error(void);

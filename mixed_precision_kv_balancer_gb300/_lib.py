@@ -28,7 +28,7 @@ EXPORTS = (
     "mikv_output_perturbation", "mikv_output_perturbation_workspace_bytes",
     "mikv_topk_attention", "mikv_topk_attention_workspace_bytes",
     "mikv_channel_quantize",
-    "mikv_set_attention_events", "mikv_wait_status", "mikv_last_error",
+    "mikv_set_attention_events", "mikv_wait_status", "mikv_wait_probe", "mikv_last_error",
 )
 
 
@@ -88,6 +88,7 @@ def load() -> ctypes.CDLL:
         "mikv_channel_quantize": (I, [P, I, I, I, I, P, P, P]),
         "mikv_set_attention_events": (I, [P, P]),
         "mikv_wait_status": (I, [ctypes.POINTER(ctypes.c_uint), I]),
+        "mikv_wait_probe": (I, [ctypes.c_int64, I, P]),
         "mikv_last_error": (ctypes.c_char_p, []),
     }
     for name, (res, args) in sig.items():
@@ -236,7 +237,7 @@ def mikv_set_attention_events(begin=None, end=None):
 
 
 WAIT_BITS = {1: "K3 pass 1 (row log-sum-exp)", 2: "K3 pass 2 (column sums)", 4: "K6 (V.W_O norms)",
-             8: "K9 (output perturbation)"}
+             8: "K9 (output perturbation)", 16: "mikv_wait_probe"}
 
 
 def mikv_wait_status(clear=True) -> int:
@@ -245,3 +246,8 @@ def mikv_wait_status(clear=True) -> int:
     v = ctypes.c_uint(0)
     _check("mikv_wait_status", load().mikv_wait_status(ctypes.byref(v), int(bool(clear))))
     return v.value
+
+
+def mikv_wait_probe(polls, arrive, stream=None):
+    """One bounded mbarrier wait that gives up (sets wait-status bit 16) unless `arrive`."""
+    _check("mikv_wait_probe", load().mikv_wait_probe(int(polls), int(bool(arrive)), _stream(stream)))

@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(kPtBlock, 1) perturb_tc_kernel(const __grid_co
     sinv[j] = invs[(static_cast<long>(h0 + j / (2 * kPtBatch)) * Bp + bb * kPtBatch) * 2 + j % (2 * kPtBatch)];
   if (tid == 0) bad = 0;
   const uint32_t tbase = tc::ring_setup(ring, &tslot, kPtThreads, 2 * kPtN);  // (its barrier publishes sinv)
-  bool ok = true;
+  tc::Waits w;
   if (tid == kPtThreads) {
     // producer.  Step s = k-block s % 2 of head h0 + s / 2: the W^T k-block at rows cb*128,
     // channels h*128 + 64*(s % 2), and the operand tile's k-block, into stage s % kPtRing.
@@ -203,27 +203,29 @@ __global__ void __launch_bounds__(kPtBlock, 1) perturb_tc_kernel(const __grid_co
     for (int st = 0; st < nsteps && st < kPtRing; ++st) load(st, st);
     for (int st = 0; st < nsteps; ++st) {
       const int b = st % kPtRing, hl = st / 2, a = hl & 1;
-      ok = tc::mbar_wait(smem_u32(&ring.full[b]), (st / kPtRing) & 1) && ok;
-      if (st % 2 == 0 && hl >= 2) ok = tc::mbar_wait(smem_u32(&ring.freed[a]), ((hl - 2) / 2) & 1) && ok;
+      w(smem_u32(&ring.full[b]), (st / kPtRing) & 1);
+      if (st % 2 == 0 && hl >= 2) w(smem_u32(&ring.freed[a]), ((hl - 2) / 2) & 1);
       tc::fence_after_sync();
       const uint32_t sw = s0 + b * kPtStage;
-      mma_w_o_kblock(tbase + a * kPtN, sw, sw + kPtWBytes, st % 2 == 1);
-      tc::commit(smem_u32(&ring.empty[b]));
-      if (st % 2 == 1) tc::commit(smem_u32(&ring.mma[a]));
+      if (w.ok) {  // after a give-up nothing more is issued
+        mma_w_o_kblock(tbase + a * kPtN, sw, sw + kPtWBytes, st % 2 == 1);
+        tc::commit(smem_u32(&ring.empty[b]));
+        if (st % 2 == 1) tc::commit(smem_u32(&ring.mma[a]));
+      }
       const int p = st - 1;
       if (p >= 0 && p + kPtRing < nsteps) {
-        ok = tc::mbar_wait(smem_u32(&ring.empty[p % kPtRing]), (p / kPtRing) & 1) && ok;
-        load(p + kPtRing, p % kPtRing);
+        w(smem_u32(&ring.empty[p % kPtRing]), (p / kPtRing) & 1);
+        if (w.ok) load(p + kPtRing, p % kPtRing);
       }
     }
     for (int st = nsteps > kPtRing ? nsteps - kPtRing : 0; st < nsteps; ++st)  // stages never refilled
-      ok = tc::mbar_wait(smem_u32(&ring.empty[st % kPtRing]), (st / kPtRing) & 1) && ok;
+      w(smem_u32(&ring.empty[st % kPtRing]), (st / kPtRing) & 1);
   } else if (tid < kPtThreads) {
     float y[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) y[i] = 0.f;
     for (int s = 0; s < nh; ++s) {
-      ok = tc::ring_acquire(ring, s) && ok;
+      tc::ring_acquire(ring, s, w);
       const float* si = sinv + s * 2 * kPtBatch + half * 64;  // (b_local, o | d) of this half
       float za[32];
 #pragma unroll
@@ -257,7 +259,7 @@ __global__ void __launch_bounds__(kPtBlock, 1) perturb_tc_kernel(const __grid_co
       }
     }
   }
-  if (!ok) {
+  if (!w.ok) {
     atomicExch(&bad, 1);
     tc::report_giveup(tc::kGiveupPerturb);
   }

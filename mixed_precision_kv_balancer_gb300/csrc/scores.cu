@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(kTcBlock, 2) row_lse_tc_kernel(const __grid_co
   const int t0 = rb * kTcTile;
   if (tid == 0) bad = 0;
   const uint32_t tbase = tc::cta_setup(bar, &tslot, kTcThreads, kTcCols);
-  bool ok = true;
+  tc::Waits w;
   float m = -INFINITY, l = 0.f, lc = 0.f;
   const int t = t0 + row;  // a consumer's query row
   if (tid == kTcThreads) {
@@ -96,24 +96,28 @@ __global__ void __launch_bounds__(kTcBlock, 2) row_lse_tc_kernel(const __grid_co
       tc::mbar_expect_tx(smem_u32(&bar.load[j]), tc::kTileBytes);
       tc::tma_tile(sk0 + j * tc::kTileBytes, &tk, krow0 + j * kTcTile, smem_u32(&bar.load[j]));
     }
-    ok = tc::mbar_wait(smem_u32(&bar.fixed), 0) && ok;
+    w(smem_u32(&bar.fixed), 0);
     for (int kt = 0; kt <= rb; ++kt) {
       const int buf = kt & 1;
-      ok = tc::mbar_wait(smem_u32(&bar.load[buf]), (kt >> 1) & 1) && ok;
-      if (kt >= 2) ok = tc::mbar_wait(smem_u32(&bar.freed[buf]), ((kt - 2) >> 1) & 1) && ok;
+      w(smem_u32(&bar.load[buf]), (kt >> 1) & 1);
+      if (kt >= 2) w(smem_u32(&bar.freed[buf]), ((kt - 2) >> 1) & 1);
       tc::fence_after_sync();
-      tc::mma_tile(tbase + buf * kTcTile, sq, sk0 + buf * tc::kTileBytes, kTcIdesc);
-      tc::commit(smem_u32(&bar.mma[buf]));
+      if (w.ok) {  // after a give-up nothing more is issued
+        tc::mma_tile(tbase + buf * kTcTile, sq, sk0 + buf * tc::kTileBytes, kTcIdesc);
+        tc::commit(smem_u32(&bar.mma[buf]));
+      }
       if (kt + 2 <= rb) {
-        ok = tc::mbar_wait(smem_u32(&bar.mma[buf]), (kt >> 1) & 1) && ok;
-        tc::mbar_expect_tx(smem_u32(&bar.load[buf]), tc::kTileBytes);
-        tc::tma_tile(sk0 + buf * tc::kTileBytes, &tk, krow0 + (kt + 2) * kTcTile, smem_u32(&bar.load[buf]));
+        w(smem_u32(&bar.mma[buf]), (kt >> 1) & 1);
+        if (w.ok) {
+          tc::mbar_expect_tx(smem_u32(&bar.load[buf]), tc::kTileBytes);
+          tc::tma_tile(sk0 + buf * tc::kTileBytes, &tk, krow0 + (kt + 2) * kTcTile, smem_u32(&bar.load[buf]));
+        }
       }
     }
   } else if (tid < kTcThreads) {
     for (int kt = 0; kt <= rb; ++kt) {
       const int buf = kt & 1;
-      ok = tc::mbar_wait(smem_u32(&bar.mma[buf]), (kt >> 1) & 1) && ok;
+      w(smem_u32(&bar.mma[buf]), (kt >> 1) & 1);
       tc::fence_after_sync();
       // this thread's 64 raw dot products: row t, keys kt*128 + half*64 ..
       float s[kTcHalf];
@@ -184,7 +188,7 @@ __global__ void __launch_bounds__(kTcBlock, 2) row_lse_tc_kernel(const __grid_co
       xl[row] = l - lc;
     }
   }
-  if (!ok) {
+  if (!w.ok) {
     atomicExch(&bad, 1);
     tc::report_giveup(tc::kGiveupRowLse);
   }
@@ -222,7 +226,7 @@ __global__ void __launch_bounds__(kTcBlock, 2) col_sum_tc_kernel(const __grid_co
   const int ntile = rep * per;  // tiles of this CTA, head-major
   if (tid == 0) bad = 0;
   const uint32_t tbase = tc::cta_setup(bar, &tslot, kTcThreads, kTcCols);
-  bool ok = true;
+  tc::Waits w;
   const int i = i0 + row;  // a consumer's key
   float tot = 0.f;
   if (tid == kTcThreads) {
@@ -242,25 +246,27 @@ __global__ void __launch_bounds__(kTcBlock, 2) col_sum_tc_kernel(const __grid_co
     tc::tma_tile(sk, &tk, unit * T + i0, smem_u32(&bar.fixed));
     load_q(0);
     if (ntile > 1) load_q(1);
-    ok = tc::mbar_wait(smem_u32(&bar.fixed), 0) && ok;
+    w(smem_u32(&bar.fixed), 0);
     for (int n = 0; n < ntile; ++n) {
       const int buf = n & 1;
-      ok = tc::mbar_wait(smem_u32(&bar.load[buf]), (n >> 1) & 1) && ok;
+      w(smem_u32(&bar.load[buf]), (n >> 1) & 1);
       // accumulator buf is free once every consumer has read tile n - 2 from TMEM
-      if (n >= 2) ok = tc::mbar_wait(smem_u32(&bar.freed[buf]), ((n - 2) >> 1) & 1) && ok;
+      if (n >= 2) w(smem_u32(&bar.freed[buf]), ((n - 2) >> 1) & 1);
       tc::fence_after_sync();
-      tc::mma_tile(tbase + buf * kTcTile, sk, sq0 + buf * tc::kTileBytes, kTcIdesc);
-      tc::commit(smem_u32(&bar.mma[buf]));
+      if (w.ok) {  // after a give-up nothing more is issued
+        tc::mma_tile(tbase + buf * kTcTile, sk, sq0 + buf * tc::kTileBytes, kTcIdesc);
+        tc::commit(smem_u32(&bar.mma[buf]));
+      }
       if (n + 2 < ntile) {  // Q buffer buf is free once MMA n is done
-        ok = tc::mbar_wait(smem_u32(&bar.mma[buf]), (n >> 1) & 1) && ok;
-        load_q(n + 2);
+        w(smem_u32(&bar.mma[buf]), (n >> 1) & 1);
+        if (w.ok) load_q(n + 2);
       }
     }
   } else if (tid < kTcThreads) {
     float col = 0.f, colc = 0.f;
     for (int n = 0; n < ntile; ++n) {
       const int buf = n & 1;
-      ok = tc::mbar_wait(smem_u32(&bar.mma[buf]), (n >> 1) & 1) && ok;
+      w(smem_u32(&bar.mma[buf]), (n >> 1) & 1);
       tc::fence_after_sync();
       const int qt = kbi + n % per;
       const int cq = qt * kTcTile + half * kTcHalf;  // query of this thread's column 0
@@ -323,7 +329,7 @@ __global__ void __launch_bounds__(kTcBlock, 2) col_sum_tc_kernel(const __grid_co
       }
     }
   }
-  if (!ok) {
+  if (!w.ok) {
     atomicExch(&bad, 1);
     tc::report_giveup(tc::kGiveupColSum);
   }

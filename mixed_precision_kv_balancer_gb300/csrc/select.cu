@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(kVwoBlock, 2) vwo_norm_tc_kernel(const __grid_
   const int ntile = rep * per;     // tiles of this CTA, head-major
   if (tid == 0) bad = 0;
   const uint32_t tbase = tc::cta_setup(bar, &tslot, kVwoThreads, kVwoCols);
-  bool ok = true;
+  tc::Waits w;
   const int i = i0 + row;  // a consumer's token
   if (tid == kVwoThreads) {
     // producer.  Tile n: head g*rep + n / per, columns (n % per) * 128 ..: rows of W^T, the
@@ -309,24 +309,26 @@ __global__ void __launch_bounds__(kVwoBlock, 2) vwo_norm_tc_kernel(const __grid_
     tc::tma_tile(sv, &tv, unit * L + i0, smem_u32(&bar.fixed));
     load_w(0);
     if (ntile > 1) load_w(1);
-    ok = tc::mbar_wait(smem_u32(&bar.fixed), 0) && ok;
+    w(smem_u32(&bar.fixed), 0);
     for (int n = 0; n < ntile; ++n) {
       const int buf = n & 1;
-      ok = tc::mbar_wait(smem_u32(&bar.load[buf]), (n >> 1) & 1) && ok;
-      if (n >= 2) ok = tc::mbar_wait(smem_u32(&bar.freed[buf]), ((n - 2) >> 1) & 1) && ok;
+      w(smem_u32(&bar.load[buf]), (n >> 1) & 1);
+      if (n >= 2) w(smem_u32(&bar.freed[buf]), ((n - 2) >> 1) & 1);
       tc::fence_after_sync();
-      tc::mma_tile(tbase + buf * kVwoN, sv, sw0 + buf * tc::kTileBytes, kVwoIdesc);
-      tc::commit(smem_u32(&bar.mma[buf]));
+      if (w.ok) {  // after a give-up nothing more is issued
+        tc::mma_tile(tbase + buf * kVwoN, sv, sw0 + buf * tc::kTileBytes, kVwoIdesc);
+        tc::commit(smem_u32(&bar.mma[buf]));
+      }
       if (n + 2 < ntile) {  // W buffer buf is free once MMA n is done
-        ok = tc::mbar_wait(smem_u32(&bar.mma[buf]), (n >> 1) & 1) && ok;
-        load_w(n + 2);
+        w(smem_u32(&bar.mma[buf]), (n >> 1) & 1);
+        if (w.ok) load_w(n + 2);
       }
     }
   } else if (tid < kVwoThreads) {
     float run = 0.f, comp = 0.f;
     for (int n = 0; n < ntile; ++n) {
       const int buf = n & 1;
-      ok = tc::mbar_wait(smem_u32(&bar.mma[buf]), (n >> 1) & 1) && ok;
+      w(smem_u32(&bar.mma[buf]), (n >> 1) & 1);
       tc::fence_after_sync();
       float c0[32], c1[32];
       const uint32_t lane_addr =
@@ -357,7 +359,7 @@ __global__ void __launch_bounds__(kVwoBlock, 2) vwo_norm_tc_kernel(const __grid_
       }
     }
   }
-  if (!ok) {
+  if (!w.ok) {
     atomicExch(&bad, 1);
     tc::report_giveup(tc::kGiveupVwo);
   }

@@ -85,6 +85,7 @@ constexpr unsigned kGiveupRowLse = 1u;   // K3 pass 1, row_lse_tc_kernel
 constexpr unsigned kGiveupColSum = 2u;   // K3 pass 2, col_sum_tc_kernel
 constexpr unsigned kGiveupVwo = 4u;      // K6, vwo_norm_tc_kernel
 constexpr unsigned kGiveupPerturb = 8u;  // K9, perturb_tc_kernel
+constexpr unsigned kGiveupProbe = 16u;   // wait_probe_kernel (mikv_wait_probe)
 
 // The wait-status word of the translation unit that includes this header (internal
 // linkage: one word per source file, each read by that file's wait_giveups()).
@@ -107,7 +108,7 @@ static inline int wait_giveups(unsigned* out, bool clear) {
 }
 
 // Wait for phase `parity` of the mbarrier, giving up after `limit` polls; true if it completed.
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, long limit = 1L << 22) {
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, long limit) {
   uint32_t done = 0;
   for (long it = 0; it < limit && !done; ++it) {
     asm volatile(
@@ -119,6 +120,23 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, long l
   }
   return done != 0;
 }
+
+constexpr long kWaitPolls = 1L << 22;              // polls before a wait gives up
+constexpr long kWaitPollsAfterGiveup = 1L << 10;   // polls of each later wait of that thread
+
+// One thread's waits.  After its first give-up (`ok` false) the thread issues no further
+// copies or MMAs (the producers test `ok` before each) and its remaining waits poll briefly,
+// so that a stuck pipeline still ends in a bounded time; the kernel then marks its outputs
+// and sets its status bit.
+struct Waits {
+  bool ok = true;
+  long polls = kWaitPolls;
+  __device__ __forceinline__ bool operator()(uint32_t mbar, uint32_t parity) {
+    const bool done = mbar_wait(mbar, parity, ok ? polls : kWaitPollsAfterGiveup);
+    ok = ok && done;
+    return done;
+  }
+};
 
 __device__ __forceinline__ void fence_before_sync() {
   asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
@@ -255,44 +273,11 @@ __device__ __forceinline__ uint32_t ring_setup(Ring<R, NACC>& r, uint32_t* tslot
   return *tslot;
 }
 
-// The producer lane, steps 0 .. nsteps-1.  load(s, b, mbar) issues step s's copies into
-// buffer b with their expect_tx on mbar; mma(s, b, a) issues its MMAs from buffer b into
-// accumulator a.  Step s's MMAs go out once its buffer landed and its accumulator's
-// previous step (s - NACC) was released; then the buffer of step s - 1 is refilled with step
-// s - 1 + R as soon as step s - 1's MMAs are done (step s's already queue behind them), so a
-// copy has R - 1 MMA durations to land.  The resident tiles are awaited on `fixed` before
-// the first MMA, and the last MMAs before returning, so no arrival is left in flight when
-// the CTA retires.  False if a wait gave up.
-template <int R, int NACC, class Load, class Mma>
-__device__ __forceinline__ bool ring_produce(Ring<R, NACC>& r, int nsteps, Load load, Mma mma) {
-  bool ok = true;
-  for (int s = 0; s < nsteps && s < R; ++s) load(s, s, smem_u32(&r.full[s]));
-  ok = mbar_wait(smem_u32(&r.fixed), 0) && ok;
-  for (int s = 0; s < nsteps; ++s) {
-    const int b = s % R, a = s % NACC;
-    ok = mbar_wait(smem_u32(&r.full[b]), (s / R) & 1) && ok;
-    if (s >= NACC) ok = mbar_wait(smem_u32(&r.freed[a]), (s / NACC - 1) & 1) && ok;
-    fence_after_sync();
-    mma(s, b, a);
-    commit(smem_u32(&r.mma[a]));
-    commit(smem_u32(&r.empty[b]));
-    const int p = s - 1;
-    if (p >= 0 && p + R < nsteps) {
-      ok = mbar_wait(smem_u32(&r.empty[p % R]), (p / R) & 1) && ok;
-      load(p + R, p % R, smem_u32(&r.full[p % R]));
-    }
-  }
-  for (int s = nsteps > R ? nsteps - R : 0; s < nsteps; ++s)  // buffers never refilled
-    ok = mbar_wait(smem_u32(&r.empty[s % R]), (s / R) & 1) && ok;
-  return ok;
-}
-
 // Consumer side of step s: wait for its accumulator; release it after the last tcgen05.ld.
 template <int R, int NACC>
-__device__ __forceinline__ bool ring_acquire(Ring<R, NACC>& r, int s) {
-  const bool ok = mbar_wait(smem_u32(&r.mma[s % NACC]), (s / NACC) & 1);
+__device__ __forceinline__ void ring_acquire(Ring<R, NACC>& r, int s, Waits& w) {
+  w(smem_u32(&r.mma[s % NACC]), (s / NACC) & 1);
   fence_after_sync();
-  return ok;
 }
 template <int R, int NACC>
 __device__ __forceinline__ void ring_release(Ring<R, NACC>& r, int s) {

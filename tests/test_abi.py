@@ -133,6 +133,9 @@ def test_host_side_rejections(lib):
     assert lib.mikv_set_attention_events(None, None) == 0
     # the wait-status query needs somewhere to write
     assert lib.mikv_wait_status(None, 0) == EINVAL
+    # the wait probe's poll count is bounded on the host
+    assert lib.mikv_wait_probe(0, 0, None) == EINVAL
+    assert lib.mikv_wait_probe((1 << 24) + 1, 0, None) == EINVAL
 
 
 def test_per_channel_key_mode_rejections(lib):

@@ -504,3 +504,25 @@ def test_tensor_core_kernels_report_no_wait_giveup():
     torch.cuda.synchronize()
     assert _lib.mikv_wait_status(clear=True) == 0
     assert torch.isfinite(y).all() and torch.isfinite(pert).all()
+
+
+def test_wait_give_up_is_reported():
+    """A bounded wait that runs out (an mbarrier that nobody arrives on) sets its status bit,
+    the query reads and clears it, and the context stays usable; with the arrival made, the
+    same wait completes and sets nothing."""
+    _lib.mikv_wait_status(clear=True)
+    _lib.mikv_wait_probe(1000, arrive=True)
+    torch.cuda.synchronize()
+    assert _lib.mikv_wait_status(clear=True) == 0
+    _lib.mikv_wait_probe(1000, arrive=False)
+    torch.cuda.synchronize()
+    assert _lib.mikv_wait_status(clear=False) == 16
+    assert _lib.mikv_wait_status(clear=True) == 16
+    assert _lib.mikv_wait_status(clear=True) == 0
+    # the context still runs work: a balancer call matches the oracle
+    wl = _wl(B=1, Hq=4, Hkv=2, T=40, n_outlier=2)
+    x = inputs.make_prefill(wl, 5, "cpu")
+    got = torch.empty(1, 2, 128, dtype=torch.float32, device=dev())
+    _lib.mikv_balance_prefill(x["q"].to(dev()), x["k"].to(dev()), got)
+    want = obal.channel_balancer(x["q"].numpy(), x["k"].numpy())
+    np.testing.assert_array_equal(to_np(got).view(np.uint32), want.view(np.uint32))
