@@ -642,7 +642,7 @@ def main():
             "what": "y = o . W_O and per-head ||(o - o_hat) . W_O^(h)||_1 (prep, tcgen05 product, two ordered "
                     "reductions, chained with programmatic dependent launch)",
             "shape": {"batch": wl.B, "q_heads": wl.Hq, "head_dim": wl.D, "hidden": res["pert_hidden"]},
-            "us_per_call": res["pert_ms"] * 1e3, "launches_per_call": 4,
+            "us_per_call": res["pert_ms"] * 1e3, "launches_per_call": 3,
             "bytes_per_call": res["pert_bytes"], "gbs": gbs, "frac_of_hbm_peak": gbs / peak,
             "timing": "CUDA events around each of 20 calls, L2 flushed (256 MB write) before each"}
     if "topk_ms" in res:

@@ -20,9 +20,10 @@
 // (the MMA's M operand) and the operand tile (N = 256) as 64-channel k-blocks through a
 // four-stage TMA ring, multiplies them with tcgen05.mma into one of two TMEM accumulators, and
 // the consumers add hi + lo, accumulate y over the chunk's heads in registers and sum |z| of
-// the d rows per (batch row, head).  Two small kernels add the chunks' y and the column
-// blocks' sums in a fixed order.  The four launches are chained with programmatic dependent
-// launch: each is placed while its predecessor runs and waits for it before its first read.
+// the d rows per (batch row, head).  One small kernel adds the chunks' y and the column
+// blocks' sums in a fixed order.  The three launches are chained with programmatic dependent
+// launch: each is placed while its predecessor runs and waits for it before reading what the
+// predecessor writes (the product kernel requests its first W_O^T k-blocks before that wait).
 #include <algorithm>
 
 #include "common.cuh"
@@ -165,7 +166,6 @@ __global__ void __launch_bounds__(kPtBlock, 1) perturb_tc_kernel(const __grid_co
   __shared__ uint32_t tslot;
   __shared__ float red[2][8][32];
   __shared__ int bad;
-  pdl_wait();  // the operand tiles and row scales come from the prep kernel
   pdl_trigger();
   const int cb = blockIdx.x, hc = blockIdx.y, bb = blockIdx.z, nbb = gridDim.z, Bp = nbb * kPtBatch;
   const int ncb = hidden / kPtM;
@@ -175,32 +175,44 @@ __global__ void __launch_bounds__(kPtBlock, 1) perturb_tc_kernel(const __grid_co
   const int col = cb * kPtM + (warp & 3) * 32 + lane;  // a consumer's hidden column
   const uint32_t s0 = tc::smem_base(sm);
   float* sinv = reinterpret_cast<float*>(sm + (s0 - smem_u32(sm)) + kPtRing * kPtStage);  // [nh][64][2]
+  if (tid == 0) bad = 0;
+  const uint32_t tbase = tc::ring_setup(ring, &tslot, kPtThreads, 2 * kPtN);
+  tc::Waits w;
+  // Step s = k-block s % 2 of head h0 + s / 2: the W^T k-block at rows cb*128, channels
+  // h*128 + 64*(s % 2), and the operand tile's k-block, into stage s % kPtRing (one
+  // transaction count on full[stage] for both copies).
+  const int nsteps = 2 * nh;
+  auto load_w = [&](int s, int st) {
+    const int h = h0 + s / 2, kb = s % 2;
+    const uint32_t sw = s0 + st * kPtStage, mb = smem_u32(&ring.full[st]);
+    tc::mbar_expect_tx(mb, kPtStage);
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(sw), "l"(&tw), "r"(h * kD + kb * 64), "r"(cb * kPtM), "r"(mb)
+        : "memory");
+  };
+  auto load_o = [&](int s, int st) {
+    const int h = h0 + s / 2, kb = s % 2;
+    const uint32_t so = s0 + st * kPtStage + kPtWBytes, mb = smem_u32(&ring.full[st]);
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(so), "l"(&to), "r"(kb * 64), "r"((h * nbb + bb) * kPtN), "r"(mb)
+        : "memory");
+  };
+  // W_O^T is an input of the call, complete before the prep kernel (a normal launch) started,
+  // and this kernel starts only after that: its first k-blocks are requested before waiting
+  // for the prep kernel's operand tiles and row scales.
+  if (tid == kPtThreads)
+    for (int st = 0; st < nsteps && st < kPtRing; ++st) load_w(st, st);
+  pdl_wait();
   for (int j = tid; j < nh * 2 * kPtBatch; j += kPtBlock)
     sinv[j] = invs[(static_cast<long>(h0 + j / (2 * kPtBatch)) * Bp + bb * kPtBatch) * 2 + j % (2 * kPtBatch)];
-  if (tid == 0) bad = 0;
-  const uint32_t tbase = tc::ring_setup(ring, &tslot, kPtThreads, 2 * kPtN);  // (its barrier publishes sinv)
-  tc::Waits w;
+  __syncthreads();  // publishes sinv
   if (tid == kPtThreads) {
-    // producer.  Step s = k-block s % 2 of head h0 + s / 2: the W^T k-block at rows cb*128,
-    // channels h*128 + 64*(s % 2), and the operand tile's k-block, into stage s % kPtRing.
-    // The head's accumulator (h & 1) is committed after its second k-block; the first waits
-    // until head h - 2 was read from it.  A stage is refilled (step s - 1 + kPtRing) once the
-    // MMAs of step s - 1 are done, while step s's queue behind them.
-    const int nsteps = 2 * nh;
-    auto load = [&](int s, int st) {
-      const int h = h0 + s / 2, kb = s % 2;
-      const uint32_t sw = s0 + st * kPtStage, so = sw + kPtWBytes, mb = smem_u32(&ring.full[st]);
-      tc::mbar_expect_tx(mb, kPtStage);
-      asm volatile(
-          "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-          " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(sw), "l"(&tw), "r"(h * kD + kb * 64), "r"(cb * kPtM), "r"(mb)
-          : "memory");
-      asm volatile(
-          "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-          " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(so), "l"(&to), "r"(kb * 64), "r"((h * nbb + bb) * kPtN), "r"(mb)
-          : "memory");
-    };
-    for (int st = 0; st < nsteps && st < kPtRing; ++st) load(st, st);
+    // producer.  The head's accumulator (h & 1) is committed after its second k-block; the
+    // first waits until head h - 2 was read from it.  A stage is refilled (step s - 1 +
+    // kPtRing) once the MMAs of step s - 1 are done, while step s's queue behind them.
+    for (int st = 0; st < nsteps && st < kPtRing; ++st) load_o(st, st);
     for (int st = 0; st < nsteps; ++st) {
       const int b = st % kPtRing, hl = st / 2, a = hl & 1;
       w(smem_u32(&ring.full[b]), (st / kPtRing) & 1);
@@ -215,7 +227,10 @@ __global__ void __launch_bounds__(kPtBlock, 1) perturb_tc_kernel(const __grid_co
       const int p = st - 1;
       if (p >= 0 && p + kPtRing < nsteps) {
         w(smem_u32(&ring.empty[p % kPtRing]), (p / kPtRing) & 1);
-        if (w.ok) load(p + kPtRing, p % kPtRing);
+        if (w.ok) {
+          load_w(p + kPtRing, p % kPtRing);
+          load_o(p + kPtRing, p % kPtRing);
+        }
       }
     }
     for (int st = nsteps > kPtRing ? nsteps - kPtRing : 0; st < nsteps; ++st)  // stages never refilled
@@ -276,22 +291,24 @@ __global__ void __launch_bounds__(kPtBlock, 1) perturb_tc_kernel(const __grid_co
     }
 }
 
-// y[b][c] = sum over the head chunks of their partials, in chunk order.
-__global__ void perturb_yreduce_kernel(const float* __restrict__ ypart, int nchunk, long n, float* __restrict__ y) {
+// Both ordered reductions in one launch.  Blocks [0, yblocks): y[b][c] = the sum of the head
+// chunks' partials, in chunk order (grid-stride over the ny elements).  The other blocks:
+// pert[b][h] = the sum of the ncb column-block partial sums, in column order, one warp per
+// (b, h) (lane j adds parts j, j + 32, ..., then a butterfly over the lanes).
+__global__ void perturb_reduce_kernel(const float* __restrict__ ypart, int nchunk, long ny, float* __restrict__ y,
+                                      int yblocks, const float* __restrict__ part, int n, int nparts,
+                                      float* __restrict__ pert) {
   pdl_wait();
-  pdl_trigger();
-  for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<long>(gridDim.x) * blockDim.x) {
-    float t = 0.f;
-    for (int c = 0; c < nchunk; ++c) t += ypart[c * n + i];
-    y[i] = t;
+  if (static_cast<int>(blockIdx.x) < yblocks) {
+    for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < ny;
+         i += static_cast<long>(yblocks) * blockDim.x) {
+      float t = 0.f;
+      for (int c = 0; c < nchunk; ++c) t += ypart[c * ny + i];
+      y[i] = t;
+    }
+    return;
   }
-}
-
-// pert[b][h] = sum of the ncb column-block partial sums, in column order.  One warp per (b, h).
-__global__ void perturb_reduce_kernel(const float* __restrict__ part, int n, int nparts, float* __restrict__ pert) {
-  pdl_wait();
-  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const int w = ((blockIdx.x - yblocks) * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (w >= n) return;
   float s = 0.f;
   for (int j = lane; j < nparts; j += 32) s += part[static_cast<long>(w) * nparts + j];
@@ -382,16 +399,11 @@ extern "C" int mikv_output_perturbation(const float* o, const float* o_hat, cons
                                               B, Hq, hidden, invs, ypart, part),
                                  "perturb_tc_kernel"))
     return e;
-  if (y) {
-    const long n = static_cast<long>(B) * hidden;
-    const int blocks = static_cast<int>(std::min<long>((n + 255) / 256, 152L * 8));
-    if (int e = check_launch_after(launch_after(perturb_yreduce_kernel, dim3(blocks), dim3(256), 0, s, ypart, nch, n, y),
-                                   "perturb_yreduce_kernel"))
-      return e;
-  }
-  if (!pert) return MIKV_OK;
-  const int n = B * Hq;
-  return check_launch_after(launch_after(perturb_reduce_kernel, dim3((n + 7) / 8), dim3(256), 0, s, part, n, ncb, pert),
+  const long ny = y ? static_cast<long>(B) * hidden : 0;
+  const int yblocks = static_cast<int>(std::min<long>((ny + 255) / 256, 152L * 8));
+  const int n = pert ? B * Hq : 0;
+  return check_launch_after(launch_after(perturb_reduce_kernel, dim3(yblocks + (n + 7) / 8), dim3(256), 0, s, ypart,
+                                         nch, ny, y, yblocks, part, n, ncb, pert),
                             "perturb_reduce_kernel");
 }
 
