@@ -856,26 +856,35 @@ __global__ void __launch_bounds__(kThreads, 3) decode_partial_kernel(Params P) {
 }
 
 // K8: merge the split partials (base-2 max m, sum l, unnormalised o) of one query head
-// (row = b*Hq + h) into its output row and natural log-sum-exp.  The CTA holds G groups of
-// kD threads (thread = channel); group g folds splits g, g+G, g+2G, ... in ascending order
-// and the group sums are then added in group order.  G depends on nsplit only, so every
-// caller of this kernel gets the same bits.
-int merge_groups(int nsplit) { return nsplit >= 96 ? 8 : (nsplit >= 48 ? 4 : (nsplit >= 12 ? 2 : 1)); }
+// (row = b*Hq + h) into its output row and natural log-sum-exp.  G groups of threads fold the
+// splits: group g takes splits g, g+G, g+2G, ... in ascending order, and the group sums are
+// then added in group order.  G is the smallest power of two that leaves at most 8 splits to a
+// group (at most 32); a CTA holds G groups of kD / chunks channels (thread = channel), so a
+// row spreads over `chunks` CTAs once G passes 8.  G depends on nsplit only, so every caller
+// of this kernel gets the same bits.
+__host__ __device__ inline int merge_groups(int nsplit) {
+  int g = 1;
+  while (g < 32 && g * 8 < nsplit) g *= 2;
+  return g;
+}
+__host__ __device__ inline int merge_chunks(int nsplit) { return merge_groups(nsplit) > 8 ? merge_groups(nsplit) / 8 : 1; }
 
-__global__ void __launch_bounds__(8 * kD) decode_merge_kernel(const float* __restrict__ ws_o,
-                                                              const float* __restrict__ ws_ml,
-                                                              int smax, int nsplit,
-                                                              float* __restrict__ out,
-                                                              float* __restrict__ lse) {
-  __shared__ float so[7][kD];
-  __shared__ float sl[7];
+__global__ void __launch_bounds__(1024) decode_merge_kernel(const float* __restrict__ ws_o,
+                                                            const float* __restrict__ ws_ml,
+                                                            int smax, int nsplit,
+                                                            float* __restrict__ out,
+                                                            float* __restrict__ lse) {
+  __shared__ float so[1024];  // (group - 1, channel) sums of groups 1 .. G-1
+  __shared__ float sl[32];
   __shared__ float smx[32];
   pdl_wait();
   pdl_trigger();
-  const int G = blockDim.x / kD;
-  const int c = threadIdx.x % kD, gi = threadIdx.x / kD;
+  const int chunks = merge_chunks(nsplit);
+  const int G = blockDim.x * chunks / kD, CC = blockDim.x / G;
+  const int cl = threadIdx.x % CC, gi = threadIdx.x / CC;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const long row = blockIdx.x;
+  const long row = blockIdx.x / chunks;
+  const int c = static_cast<int>(blockIdx.x % chunks) * CC + cl;
   const float* ml = ws_ml + row * smax * 2;
   // the running maxima: max is exact in any order
   float M = -INFINITY;
@@ -895,13 +904,13 @@ __global__ void __launch_bounds__(8 * kD) decode_merge_kernel(const float* __res
     O += sc * ws_o[(row * smax + s) * kD + c];
   }
   if (gi > 0) {
-    so[gi - 1][c] = O;
-    if (c == 0) sl[gi - 1] = L;
+    so[(gi - 1) * CC + cl] = O;
+    if (cl == 0) sl[gi - 1] = L;
   }
   __syncthreads();
   if (gi > 0) return;
   for (int g = 1; g < G; ++g) {
-    O += so[g - 1][c];
+    O += so[(g - 1) * CC + cl];
     L += sl[g - 1];
   }
   out[row * kD + c] = O / L;
@@ -1054,6 +1063,11 @@ constexpr double kTailFactor = 2.13;
 #define MIKV_MIN_WAVES 2.5
 #endif
 constexpr double kMinWaves = MIKV_MIN_WAVES;  // keep at least this many waves when the cache allows
+// With few (batch, key head) units every unit is cut into very many splits to fill that many
+// waves, and the per-CTA fixed cost and the merge of the splits dominate: below this many
+// units one wave suffices (measured at batch 1 / 8 key heads: 37.9 vs 39.5 us per layer-step;
+// at 256 units fewer waves were slower).
+constexpr int kFewUnits = 64;
 constexpr int kCtasPerSm = 3;
 
 struct Plan {
@@ -1062,7 +1076,8 @@ struct Plan {
 
 // Split plan from the capacities (so the workspace fits every count up to them).  Each tier
 // is cut into equal chunks of whole warp-stages; over a geometric range of per-CTA targets
-// the plan with the lowest modelled makespan (among those with >= kMinWaves waves) wins.
+// the plan with the lowest modelled makespan (among those with >= kMinWaves waves, one wave
+// below kFewUnits units) wins.
 Plan make_plan(const mikv_cache* c) {
   const double units = static_cast<double>(c->B) * c->Hkv;
   const double slots = static_cast<double>(kNumSMs) * kCtasPerSm;
@@ -1089,7 +1104,7 @@ Plan make_plan(const mikv_cache* c) {
       have_first = true;
     }
     const double ctas = units * (p.smax_hi + p.smax_lo);
-    if (ctas < kMinWaves * slots) continue;
+    if (ctas < (units < kFewUnits ? 1.0 : kMinWaves) * slots) continue;
     const double largest = std::max(std::min(p.chunk_hi, c->cap_hi) * wb_hi,
                                     std::min(p.chunk_lo, c->cap_lo) * wb_lo);
     const double t = (total + ctas * kCtaOverhead) / slots + kTailFactor * largest;
@@ -1297,7 +1312,8 @@ extern "C" int mikv_decode_attention(const uint16_t* q, const mikv_cache* c, flo
   cudaStream_t s = as_stream(stream);
   if (int e = launch_partials(P, c, nsplit, s, false, nullptr)) return e;
   return check_launch_after(
-      launch_after(decode_merge_kernel, dim3(c->B * c->Hq), dim3(kD * merge_groups(nsplit)), 0, s,
+      launch_after(decode_merge_kernel, dim3(c->B * c->Hq * merge_chunks(nsplit)),
+                   dim3(kD * merge_groups(nsplit) / merge_chunks(nsplit)), 0, s,
                    P.ws_o, P.ws_ml, P.smax, nsplit, out, lse),
       "decode_merge_kernel");
 }
@@ -1375,7 +1391,8 @@ extern "C" int mikv_decode_step(const uint16_t* q, const uint16_t* k_new, const 
   c->n_hi += 1;
   // 3. merge
   if (int e = check_launch_after(
-          launch_after(decode_merge_kernel, dim3(c->B * c->Hq), dim3(kD * merge_groups(nsplit)), 0,
+          launch_after(decode_merge_kernel, dim3(c->B * c->Hq * merge_chunks(nsplit)),
+                       dim3(kD * merge_groups(nsplit) / merge_chunks(nsplit)), 0,
                        s, P.ws_o, P.ws_ml, P.smax, nsplit, out, lse),
           "decode_merge_kernel"))
     return e;
