@@ -209,6 +209,8 @@ ATTN_CASES = [
     (4, 2, 2, 32, 8, 800, 20, 32),      # INT4 important tier over INT2
     (4, 4, 1, 40, 8, 500, 30, 16),      # INT4 / INT4, GQA 5
     (16, 2, 2, 8, 2, 1, 100, 1),        # a one-token context
+    (16, 2, 1, 4, 1, 16384, 20, 32),    # one unit: ~80 splits, the merge in 16 groups over 2 CTAs a head
+    (16, 2, 1, 4, 1, 32768, 40, 32),    # one unit: ~280 splits, 32 groups over 4 CTAs a head
 ]
 
 
