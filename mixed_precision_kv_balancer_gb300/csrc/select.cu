@@ -67,9 +67,20 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int& total) {
   return before + x - v;
 }
 
+// Order keys of a row, read from global memory (converted on each read) or from a staged
+// shared-memory copy.
+struct GlobalKeys {
+  const float* k;
+  __device__ __forceinline__ uint32_t operator()(int i) const { return order_key(k[i]); }
+};
+struct SharedKeys {
+  const uint32_t* k;
+  __device__ __forceinline__ uint32_t operator()(int i) const { return k[i]; }
+};
+
 // Mark (flag = 1) the `take` best candidates (flag == 0) by key, ties to lower positions.
-__device__ void topk_mark(const float* __restrict__ key, int L, int take, uint8_t* flag,
-                          unsigned* hist, int* scratch) {
+template <class Keys>
+__device__ void topk_mark(Keys key, int L, int take, uint8_t* flag, unsigned* hist, int* scratch) {
   if (take <= 0) return;
   const int tid = threadIdx.x;
   uint32_t prefix = 0, mask = 0;
@@ -79,7 +90,7 @@ __device__ void topk_mark(const float* __restrict__ key, int L, int take, uint8_
     __syncthreads();
     for (int i = tid; i < L; i += blockDim.x) {
       if (flag[i] != 0) continue;
-      const uint32_t u = order_key(key[i]);
+      const uint32_t u = key(i);
       if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
     }
     __syncthreads();
@@ -126,12 +137,12 @@ __device__ void topk_mark(const float* __restrict__ key, int L, int take, uint8_
   const int lo = min(L, tid * per), hi = min(L, lo + per);
   int ties = 0;
   for (int i = lo; i < hi; ++i)
-    if (flag[i] == 0 && order_key(key[i]) == prefix) ++ties;
+    if (flag[i] == 0 && key(i) == prefix) ++ties;
   int total;
   int rank = block_exclusive_scan(ties, scratch + 2, total);
   for (int i = lo; i < hi; ++i) {
     if (flag[i] != 0) continue;
-    const uint32_t u = order_key(key[i]);
+    const uint32_t u = key(i);
     if (u > prefix) flag[i] = 3;  // temporary: taken in this stage
     else if (u == prefix) {
       if (rank < remaining) flag[i] = 3;
@@ -146,20 +157,37 @@ __device__ void topk_mark(const float* __restrict__ key, int L, int take, uint8_
 
 // One CTA per (batch, key head).  flag: 0 evicted, 1 taken by a stage, 2 recent window.
 // key1 rows are `stride1` floats apart (L for the score arrays, the slot capacity for logits).
+// STAGE: the row's order keys are read once into shared memory (L x 4 bytes before the L
+// flag bytes) and the five passes of each stage read them there.
+template <bool STAGE>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(
     const float* __restrict__ key1, long stride1, const float* __restrict__ key2, int L, int window,
     int take1, int take2, int n_keep, int32_t* __restrict__ keep_pos, int32_t* __restrict__ evict_pos,
     float* __restrict__ keep_scores) {
-  extern __shared__ uint8_t flag[];
+  extern __shared__ __align__(16) uint8_t sel_smem[];
+  uint32_t* skey = reinterpret_cast<uint32_t*>(sel_smem);
+  uint8_t* flag = STAGE ? sel_smem + static_cast<size_t>(L) * 4 : sel_smem;
   __shared__ unsigned hist[256];
   __shared__ int scratch[2 + 32];
   const long unit = blockIdx.x;
   const float* k1 = key1 + unit * stride1;
   const int w = min(window, L);
-  for (int i = threadIdx.x; i < L; i += blockDim.x) flag[i] = (i >= L - w) ? 2 : 0;
+  for (int i = threadIdx.x; i < L; i += blockDim.x) {
+    flag[i] = (i >= L - w) ? 2 : 0;
+    if (STAGE) skey[i] = order_key(k1[i]);
+  }
   __syncthreads();
-  topk_mark(k1, L, take1, flag, hist, scratch);
-  if (key2) topk_mark(key2 + unit * L, L, take2, flag, hist, scratch);
+  if (STAGE) topk_mark(SharedKeys{skey}, L, take1, flag, hist, scratch);
+  else topk_mark(GlobalKeys{k1}, L, take1, flag, hist, scratch);
+  if (key2) {
+    if (STAGE) {
+      for (int i = threadIdx.x; i < L; i += blockDim.x) skey[i] = order_key(key2[unit * L + i]);
+      __syncthreads();
+      topk_mark(SharedKeys{skey}, L, take2, flag, hist, scratch);
+    } else {
+      topk_mark(GlobalKeys{key2 + unit * L}, L, take2, flag, hist, scratch);
+    }
+  }
   // compaction in position order
   const int per = (L + blockDim.x - 1) / blockDim.x;
   const int lo = min(L, static_cast<int>(threadIdx.x) * per), hi = min(L, lo + per);
@@ -183,6 +211,23 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
       ++ep;
     }
   }
+}
+
+// Rows of up to kSelStageMax / 5 keys are staged in shared memory (4 bytes of key and one of
+// flag per position); longer rows are read from global memory in every pass.
+constexpr int kSelStageMax = 200 * 1024;
+inline int sel_threads(int units) { return kSelThreads; }
+int launch_select(int units, const float* key1, long stride1, const float* key2, int L, int window, int take1,
+                  int take2, int n_keep, int32_t* keep_pos, int32_t* evict_pos, float* keep_scores,
+                  cudaStream_t s) {
+  const bool stage = static_cast<long>(L) * 5 <= kSelStageMax;
+  const int smem = stage ? L * 5 : L;
+  auto kern = stage ? select_kernel<true> : select_kernel<false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return check_launch("select_kernel attribute");
+  kern<<<units, sel_threads(units), smem, s>>>(key1, stride1, key2, L, window, take1, take2, n_keep, keep_pos,
+                                               evict_pos, keep_scores);
+  return check_launch("select_kernel");
 }
 
 // Demotion victim: among slots j < n_hi with pos < L - window, the minimum of
@@ -539,11 +584,8 @@ extern "C" int mikv_select(int policy, const mikv_cache* c, int L, int budget_pc
     if (int e = check_launch("ckey_kernel")) return e;
     key2 = ckey;
   }
-  if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L) != cudaSuccess)
-    return check_launch("select_kernel attribute");
-  select_kernel<<<units, kSelThreads, L, s>>>(scores, L, key2, L, window, take1, take2, n_keep,
-                                               keep_pos, evict_pos, keep_scores);
-  return check_launch("select_kernel");
+  return launch_select(units, scores, L, key2, L, window, take1, take2, n_keep, keep_pos, evict_pos,
+                       keep_scores, s);
 }
 
 extern "C" size_t mikv_topk_attention_workspace_bytes(const mikv_cache* c, int budget_pct) {
@@ -576,10 +618,7 @@ extern "C" int mikv_topk_attention(const uint16_t* q, const mikv_cache* c, int b
   cudaStream_t s = as_stream(stream);
   const int units = c->B * c->Hq;
   // 2. per query head, the k largest logits (ties to the lower slot), slots ascending
-  if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L) != cudaSuccess)
-    return check_launch("select_kernel attribute");
-  select_kernel<<<units, kSelThreads, L, s>>>(logits, c->cap_hi, nullptr, L, 0, k, 0, k, keep, evict, nullptr);
-  if (int e = check_launch("select_kernel")) return e;
+  if (int e = launch_select(units, logits, c->cap_hi, nullptr, L, 0, k, 0, k, keep, evict, nullptr, s)) return e;
   // 3. attention over the kept tokens alone
   topk_attend_kernel<<<units, kTkThreads, 0, s>>>(logits, c->cap_hi, keep, k, reinterpret_cast<const __half*>(c->v_hi),
                                           c->Hq, c->Hkv, out, lse);
