@@ -216,7 +216,6 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
 // Rows of up to kSelStageMax / 5 keys are staged in shared memory (4 bytes of key and one of
 // flag per position); longer rows are read from global memory in every pass.
 constexpr int kSelStageMax = 200 * 1024;
-inline int sel_threads(int units) { return kSelThreads; }
 int launch_select(int units, const float* key1, long stride1, const float* key2, int L, int window, int take1,
                   int take2, int n_keep, int32_t* keep_pos, int32_t* evict_pos, float* keep_scores,
                   cudaStream_t s) {
@@ -225,7 +224,7 @@ int launch_select(int units, const float* key1, long stride1, const float* key2,
   auto kern = stage ? select_kernel<true> : select_kernel<false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return check_launch("select_kernel attribute");
-  kern<<<units, sel_threads(units), smem, s>>>(key1, stride1, key2, L, window, take1, take2, n_keep, keep_pos,
+  kern<<<units, kSelThreads, smem, s>>>(key1, stride1, key2, L, window, take1, take2, n_keep, keep_pos,
                                                evict_pos, keep_scores);
   return check_launch("select_kernel");
 }
