@@ -418,14 +418,15 @@ __global__ void __launch_bounds__(kVwoBlock, 2) vwo_norm_tc_kernel(const __grid_
 // first and applies top-k sparsity after it, an upper-bound proxy).  Reading: per query head
 // the k = max(1, floor(p * L / 100)) largest logits (ties to the lower slot) are kept and the
 // output is attention over them alone, the softmax renormalised over the kept set.
-// topk_attend_kernel: one CTA per (batch, query head), four row groups of one thread per
-// channel: the max of the kept logits, then the kept tokens in chunks (weights exp(l - m) and
-// slot indices in shared memory); group r adds w * v[slot][d] over the chunk's tokens
-// j = r (mod 4), one coalesced 256-byte row per token, four rows in flight per channel; the
-// groups' sums are added at the end.
+// topk_attend_kernel: one CTA per (batch, query head): the max of the kept logits, then the
+// kept tokens in chunks (weights exp(l - m) and slot indices in shared memory).  Sixteen
+// threads share a V row, eight channels (16 bytes) each, so the CTA's 512 threads take 32 rows
+// at a time, rows j = slot (mod 32), several 16-byte loads in flight per thread; the 32 slots'
+// sums are then added in slot order.
 constexpr int kTkChunk = 1024;
-constexpr int kTkGroups = 4;
-constexpr int kTkThreads = kTkGroups * kD;
+constexpr int kTkThreads = 512;
+constexpr int kTkRowThreads = kD / 8;                      // threads per V row
+constexpr int kTkSlots = kTkThreads / kTkRowThreads;       // rows taken at a time
 
 __global__ void __launch_bounds__(kTkThreads) topk_attend_kernel(const float* __restrict__ logits, int cap,
                                                                 const int32_t* __restrict__ keep, int k,
@@ -434,13 +435,13 @@ __global__ void __launch_bounds__(kTkThreads) topk_attend_kernel(const float* __
   __shared__ float w[kTkChunk];
   __shared__ int idx[kTkChunk];
   __shared__ float red[kTkThreads / 32];
-  __shared__ float part[kTkGroups - 1][kD];
+  __shared__ float part[kTkSlots][kD];
   const int bh = blockIdx.x, b = bh / Hq, h = bh % Hq, g = h / (Hq / Hkv);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int d = tid % kD, grp = tid / kD;
+  const int slot = tid / kTkRowThreads, c8 = (tid % kTkRowThreads) * 8;
   const float* lg = logits + static_cast<long>(bh) * cap;
   const int32_t* kp = keep + static_cast<long>(bh) * k;
-  const __half* vb = v + static_cast<long>(b * Hkv + g) * cap * kD;
+  const __half* vb = v + static_cast<long>(b * Hkv + g) * cap * kD + c8;
   float m = -INFINITY;
   for (int j = tid; j < k; j += kTkThreads) m = fmaxf(m, lg[kp[j]]);
 #pragma unroll
@@ -451,7 +452,8 @@ __global__ void __launch_bounds__(kTkThreads) topk_attend_kernel(const float* __
 #pragma unroll
   for (int i = 1; i < kTkThreads / 32; ++i) m = fmaxf(m, red[i]);
   __syncthreads();
-  float acc = 0.f, tsum = 0.f;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float tsum = 0.f;
   for (int c0 = 0; c0 < k; c0 += kTkChunk) {
     const int n = min(kTkChunk, k - c0);
     for (int j = tid; j < n; j += kTkThreads) {
@@ -463,22 +465,33 @@ __global__ void __launch_bounds__(kTkThreads) topk_attend_kernel(const float* __
     }
     __syncthreads();
 #pragma unroll 4
-    for (int j = grp; j < n; j += kTkGroups) acc = fmaf(w[j], __half2float(vb[static_cast<long>(idx[j]) * kD + d]), acc);
+    for (int j = slot; j < n; j += kTkSlots) {
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(vb + static_cast<long>(idx[j]) * kD));
+      const float wj = w[j];
+      const __half2* hv = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __half22float2(hv[q]);
+        acc[2 * q] = fmaf(wj, f.x, acc[2 * q]);
+        acc[2 * q + 1] = fmaf(wj, f.y, acc[2 * q + 1]);
+      }
+    }
     __syncthreads();
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) tsum += __shfl_xor_sync(0xffffffffu, tsum, off);
   if (lane == 0) red[warp] = tsum;
-  if (grp > 0) part[grp - 1][d] = acc;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) part[slot][c8 + q] = acc[q];
   __syncthreads();
-  if (grp == 0) {
+  if (tid < kD) {
     float tot = 0.f;
 #pragma unroll
     for (int i = 0; i < kTkThreads / 32; ++i) tot += red[i];
-#pragma unroll
-    for (int r = 0; r < kTkGroups - 1; ++r) acc += part[r][d];
-    out[static_cast<long>(bh) * kD + d] = acc / tot;
-    if (d == 0 && lse) lse[bh] = m + logf(tot);
+    float o = 0.f;
+    for (int r = 0; r < kTkSlots; ++r) o += part[r][tid];
+    out[static_cast<long>(bh) * kD + tid] = o / tot;
+    if (tid == 0 && lse) lse[bh] = m + logf(tot);
   }
 }
 
