@@ -22,6 +22,7 @@
 // |.| per row (per-step partials added with Kahan compensation).
 #include <algorithm>
 #include <cmath>
+#include <type_traits>
 
 #include "common.cuh"
 #include "tcgen05.cuh"
@@ -88,7 +89,25 @@ __device__ void topk_mark(Keys key, int L, int take, uint8_t* flag, unsigned* hi
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
     __syncthreads();
-    for (int i = tid; i < L; i += blockDim.x) {
+    int i0 = 0;
+    if constexpr (std::is_same<Keys, SharedKeys>::value) {
+      // staged rows: four keys and their four flags per load (the flags start L * 4 bytes
+      // after the keys, so both are 16- and 4-byte aligned)
+      const uint4* k4 = reinterpret_cast<const uint4*>(key.k);
+      const uint32_t* f4 = reinterpret_cast<const uint32_t*>(flag);
+      for (int q = tid; q < (L >> 2); q += blockDim.x) {
+        const uint32_t fl = f4[q];
+        if (fl == 0x01010101u * (fl & 0xffu) && (fl & 0xffu) != 0) continue;  // all four taken
+        const uint4 u4 = k4[q];
+        const uint32_t uu[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (((fl >> (8 * e)) & 0xffu) == 0 && (uu[e] & mask) == prefix)
+            atomicAdd(&hist[(uu[e] >> shift) & 255u], 1u);
+      }
+      i0 = L & ~3;
+    }
+    for (int i = i0 + tid; i < L; i += blockDim.x) {
       if (flag[i] != 0) continue;
       const uint32_t u = key(i);
       if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
