@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   int kp = block_exclusive_scan(kept, scratch + 2, total);
   int ep = lo - kp;
   int32_t* kout = keep_pos + unit * n_keep;
-  int32_t* eout = evict_pos + unit * (L - n_keep);
+  int32_t* eout = evict_pos ? evict_pos + unit * (L - n_keep) : nullptr;  // null: not wanted
   float* sout = keep_scores ? keep_scores + unit * n_keep : nullptr;
   for (int i = lo; i < hi; ++i) {
     if (flag[i] != 0) {
@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
       }
       ++kp;
     } else {
-      if (ep < L - n_keep) eout[ep] = i;
+      if (eout && ep < L - n_keep) eout[ep] = i;
       ++ep;
     }
   }
@@ -517,7 +517,7 @@ __global__ void __launch_bounds__(kTkThreads) topk_attend_kernel(const float* __
 int topk_count(int L, int budget_pct) { return std::max(1, static_cast<int>(static_cast<long>(budget_pct) * L / 100)); }
 
 struct TopkWs {
-  size_t dec, out, lse, logits, keep, evict, total;
+  size_t dec, out, lse, logits, keep, total;
 };
 TopkWs topk_ws_layout(const mikv_cache* c, int k) {
   const size_t bh = static_cast<size_t>(c->B) * c->Hq;
@@ -527,8 +527,7 @@ TopkWs topk_ws_layout(const mikv_cache* c, int k) {
   t.lse = t.out + align_up(bh * kD * sizeof(float), 256);
   t.logits = t.lse + align_up(bh * sizeof(float), 256);
   t.keep = t.logits + align_up(bh * c->cap_hi * sizeof(float), 256);
-  t.evict = t.keep + align_up(bh * k * sizeof(int32_t), 256);
-  t.total = t.evict + align_up(bh * (c->n_hi - k) * sizeof(int32_t), 256);
+  t.total = t.keep + align_up(bh * k * sizeof(int32_t), 256);
   return t;
 }
 
@@ -643,13 +642,12 @@ extern "C" int mikv_topk_attention(const uint16_t* q, const mikv_cache* c, int b
   float* full_lse = reinterpret_cast<float*>(w + t.lse);
   float* logits = reinterpret_cast<float*>(w + t.logits);
   int32_t* keep = keep_idx ? keep_idx : reinterpret_cast<int32_t*>(w + t.keep);
-  int32_t* evict = reinterpret_cast<int32_t*>(w + t.evict);
   // 1. the full attention map: every logit of the cache (and the full-cache output)
   if (int e = mikv_decode_attention(q, c, full_out, full_lse, logits, w + t.dec, t.out, stream)) return e;
   cudaStream_t s = as_stream(stream);
   const int units = c->B * c->Hq;
   // 2. per query head, the k largest logits (ties to the lower slot), slots ascending
-  if (int e = launch_select(units, logits, c->cap_hi, nullptr, L, 0, k, 0, k, keep, evict, nullptr, s)) return e;
+  if (int e = launch_select(units, logits, c->cap_hi, nullptr, L, 0, k, 0, k, keep, nullptr, nullptr, s)) return e;
   // 3. attention over the kept tokens alone
   topk_attend_kernel<<<units, kTkThreads, 0, s>>>(logits, c->cap_hi, keep, k, reinterpret_cast<const __half*>(c->v_hi),
                                           c->Hq, c->Hkv, out, lse);
