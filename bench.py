@@ -651,8 +651,8 @@ def main():
     if "pert_ms" in res:
         gbs = res["pert_bytes"] / (res["pert_ms"] / 1e3) / 1e9
         line["output_perturbation"] = {
-            "what": "y = o . W_O and per-head ||(o - o_hat) . W_O^(h)||_1 (prep, tcgen05 product, two ordered "
-                    "reductions, chained with programmatic dependent launch)",
+            "what": "y = o . W_O and per-head ||(o - o_hat) . W_O^(h)||_1 (prep, tcgen05 product, both ordered "
+                    "reductions in one launch; chained with programmatic dependent launch)",
             "shape": {"batch": wl.B, "q_heads": wl.Hq, "head_dim": wl.D, "hidden": res["pert_hidden"]},
             "us_per_call": res["pert_ms"] * 1e3, "launches_per_call": 3,
             "bytes_per_call": res["pert_bytes"], "gbs": gbs, "frac_of_hbm_peak": gbs / peak,
