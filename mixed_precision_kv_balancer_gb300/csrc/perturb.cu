@@ -18,7 +18,8 @@
 // accuracy for differences of any size).  The product kernel (one CTA per 128 hidden columns,
 // chunk of heads and batch block) streams, head by head, the head's 128 x 128 block of W_O^T
 // (the MMA's M operand) and the operand tile (N = 256) as 64-channel k-blocks through a
-// four-stage TMA ring, multiplies them with tcgen05.mma into one of two TMEM accumulators, and
+// four-stage TMA ring (one thread issues the copies, another the MMAs, so neither waits on
+// the other's barriers), multiplies them with tcgen05.mma into one of two TMEM accumulators, and
 // the consumers add hi + lo, accumulate y over the chunk's heads in registers and sum |z| of
 // the d rows per (batch row, head).  One small kernel adds the chunks' y and the column
 // blocks' sums in a fixed order.  The three launches are chained with programmatic dependent
@@ -36,7 +37,8 @@ constexpr int kPtM = tc::kTileRows;              // hidden columns per CTA (the 
 constexpr int kPtBatch = 64;                     // batch rows per block
 constexpr int kPtN = 4 * kPtBatch;               // operand rows: (o, d) x (hi, lo) per batch row
 constexpr int kPtThreads = 256;                  // consumers
-constexpr int kPtBlock = kPtThreads + 32;        // + the producer warp
+constexpr int kPtBlock = kPtThreads + 64;        // + the copy warp and the MMA warp
+constexpr int kPtCopyThread = kPtThreads, kPtMmaThread = kPtThreads + 32;
 constexpr int kPtWBytes = kPtM * 64 * 2;         // one 64-channel k-block of the W^T block: 16 KB
 constexpr int kPtOBytes = kPtN * 64 * 2;         // one k-block of the operand tile: 32 KB
 constexpr int kPtStage = kPtWBytes + kPtOBytes;  // 48 KB
@@ -202,17 +204,28 @@ __global__ void __launch_bounds__(kPtBlock, 1) perturb_tc_kernel(const __grid_co
   // W_O^T is an input of the call, complete before the prep kernel (a normal launch) started,
   // and this kernel starts only after that: its first k-blocks are requested before waiting
   // for the prep kernel's operand tiles and row scales.
-  if (tid == kPtThreads)
+  if (tid == kPtCopyThread)
     for (int st = 0; st < nsteps && st < kPtRing; ++st) load_w(st, st);
   pdl_wait();
   for (int j = tid; j < nh * 2 * kPtBatch; j += kPtBlock)
     sinv[j] = invs[(static_cast<long>(h0 + j / (2 * kPtBatch)) * Bp + bb * kPtBatch) * 2 + j % (2 * kPtBatch)];
   __syncthreads();  // publishes sinv
-  if (tid == kPtThreads) {
-    // producer.  The head's accumulator (h & 1) is committed after its second k-block; the
-    // first waits until head h - 2 was read from it.  A stage is refilled (step s - 1 +
-    // kPtRing) once the MMAs of step s - 1 are done, while step s's queue behind them.
+  if (tid == kPtCopyThread) {
+    // copies: step st into stage st % kPtRing once the MMAs of step st - kPtRing are done
     for (int st = 0; st < nsteps && st < kPtRing; ++st) load_o(st, st);
+    for (int st = kPtRing; st < nsteps; ++st) {
+      const int b = st % kPtRing;
+      w(smem_u32(&ring.empty[b]), (st / kPtRing - 1) & 1);
+      if (w.ok) {  // after a give-up nothing more is issued
+        load_w(st, b);
+        load_o(st, b);
+      }
+    }
+    for (int st = nsteps > kPtRing ? nsteps - kPtRing : 0; st < nsteps; ++st)  // the last commits landed
+      w(smem_u32(&ring.empty[st % kPtRing]), (st / kPtRing) & 1);
+  } else if (tid == kPtMmaThread) {
+    // MMAs: step st as soon as its stage landed; the head's accumulator (h & 1) is committed
+    // after its second k-block, and the first waits until head h - 2 was read from it
     for (int st = 0; st < nsteps; ++st) {
       const int b = st % kPtRing, hl = st / 2, a = hl & 1;
       w(smem_u32(&ring.full[b]), (st / kPtRing) & 1);
@@ -224,17 +237,7 @@ __global__ void __launch_bounds__(kPtBlock, 1) perturb_tc_kernel(const __grid_co
         tc::commit(smem_u32(&ring.empty[b]));
         if (st % 2 == 1) tc::commit(smem_u32(&ring.mma[a]));
       }
-      const int p = st - 1;
-      if (p >= 0 && p + kPtRing < nsteps) {
-        w(smem_u32(&ring.empty[p % kPtRing]), (p / kPtRing) & 1);
-        if (w.ok) {
-          load_w(p + kPtRing, p % kPtRing);
-          load_o(p + kPtRing, p % kPtRing);
-        }
-      }
     }
-    for (int st = nsteps > kPtRing ? nsteps - kPtRing : 0; st < nsteps; ++st)  // stages never refilled
-      w(smem_u32(&ring.empty[st % kPtRing]), (st / kPtRing) & 1);
   } else if (tid < kPtThreads) {
     float y[32];
 #pragma unroll
