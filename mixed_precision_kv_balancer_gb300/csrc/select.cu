@@ -314,7 +314,8 @@ __global__ void ckey_kernel(const float* __restrict__ s_head, const float* __res
 // (128 x 128, fp32 in TMEM) by tcgen05.mma, and the consumers (two threads per token, 64
 // columns each) add |C|.  The same producer / consumer pipeline as the prefill scores.
 constexpr int kVwoThreads = 256;                        // consumers
-constexpr int kVwoBlock = kVwoThreads + 32;             // + the producer warp
+constexpr int kVwoBlock = kVwoThreads + 64;             // + the copy and MMA warps
+constexpr int kVwoCopyThread = kVwoThreads, kVwoMmaThread = kVwoThreads + 32;
 constexpr int kVwoN = tc::kTileRows;                    // hidden columns per tile
 constexpr int kVwoCols = 2 * kVwoN;                     // two TMEM accumulators
 constexpr int kVwoSmem = 3 * tc::kTileBytes + 1024;
@@ -353,8 +354,8 @@ __global__ void __launch_bounds__(kVwoBlock, 2) vwo_norm_tc_kernel(const __grid_
   const uint32_t tbase = tc::cta_setup(bar, &tslot, kVwoThreads, kVwoCols);
   tc::Waits w;
   const int i = i0 + row;  // a consumer's token
-  if (tid == kVwoThreads) {
-    // producer.  Tile n: head g*rep + n / per, columns (n % per) * 128 ..: rows of W^T, the
+  if (tid == kVwoCopyThread) {
+    // copies.  Tile n: head g*rep + n / per, columns (n % per) * 128 ..: rows of W^T, the
     // head's 128 channels at x = h * 128
     auto load_w = [&](int n) {
       const int h = g * rep + n / per, cb = n % per;
@@ -372,19 +373,21 @@ __global__ void __launch_bounds__(kVwoBlock, 2) vwo_norm_tc_kernel(const __grid_
     tc::tma_tile(sv, &tv, unit * L + i0, smem_u32(&bar.fixed));
     load_w(0);
     if (ntile > 1) load_w(1);
+    for (int n = 0; n + 2 < ntile; ++n) {  // W buffer n & 1 is free once MMA n is done
+      w(smem_u32(&bar.mma[n & 1]), (n >> 1) & 1);
+      if (w.ok) load_w(n + 2);  // after a give-up nothing more is issued
+    }
+  } else if (tid == kVwoMmaThread) {
+    // MMAs: tile n as soon as its W tile is in and accumulator n & 1 was read (tile n - 2)
     w(smem_u32(&bar.fixed), 0);
     for (int n = 0; n < ntile; ++n) {
       const int buf = n & 1;
       w(smem_u32(&bar.load[buf]), (n >> 1) & 1);
       if (n >= 2) w(smem_u32(&bar.freed[buf]), ((n - 2) >> 1) & 1);
       tc::fence_after_sync();
-      if (w.ok) {  // after a give-up nothing more is issued
+      if (w.ok) {
         tc::mma_tile(tbase + buf * kVwoN, sv, sw0 + buf * tc::kTileBytes, kVwoIdesc);
         tc::commit(smem_u32(&bar.mma[buf]));
-      }
-      if (n + 2 < ntile) {  // W buffer buf is free once MMA n is done
-        w(smem_u32(&bar.mma[buf]), (n >> 1) & 1);
-        if (w.ok) load_w(n + 2);
       }
     }
   } else if (tid < kVwoThreads) {
