@@ -1056,10 +1056,11 @@ __global__ void __launch_bounds__(kEpiThreads) decode_score_demote_kernel(EpiArg
 // host-side split plan
 int row_cost(int bits) { return bits == 16 ? 512 : 2 * (kD * bits / 8) + 16; }
 // Relative time per byte of a tier: low-bit codes cost more unpacking per byte.  INT2 at 3.0
-// (an INT2-only launch runs at about half the FP16 rate, but in a mixed launch smaller INT2
-// chunks balance the grid better; measured over 2.0 .. 4.0: FP16 / INT2 at 20 % 124.1 ->
-// 120.2 us, Llama-2-7B 43.4 -> 41.6 us, INT2 only 106.0 -> 107.1 us).
-double byte_weight(int bits) { return bits == 16 ? 1.0 : bits == 8 ? 1.25 : bits == 4 ? 1.5 : 3.0; }
+// and INT4 at 2.0, above their plain rate ratios, because in a mixed launch smaller low-bit
+// chunks balance the grid better (measured over INT2 2.0 .. 4.0 and INT4 1.5 .. 2.5: FP16 /
+// INT2 at 20 % 124.1 -> 120.2 us, Llama-2-7B 43.4 -> 41.6 us, FP16 / INT4 at 10 % 132.9 ->
+// 129.8 us, INT4 / INT2 111.3 -> 108.6 us; INT2 only 106.0 -> 107.1 us).
+double byte_weight(int bits) { return bits == 16 ? 1.0 : bits == 8 ? 1.25 : bits == 4 ? 2.0 : 3.0; }
 // Makespan model of the split-K grid, fitted to measured attention times over several
 // plans and cache shapes: a CTA costs its weighted bytes plus a fixed kCtaOverhead, the
 // resident slots share the total, and the tail adds kTailFactor times the largest CTA.
