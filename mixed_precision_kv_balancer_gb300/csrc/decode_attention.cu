@@ -1070,13 +1070,13 @@ constexpr double kTailFactor = 2.13;
 #define MIKV_MIN_WAVES 2.5
 #endif
 constexpr double kMinWaves = MIKV_MIN_WAVES;  // keep at least this many waves when the cache allows
-// CTA slots per SM that the plan counts: three (the two-column-tile form runs two per SM, and
-// its plans were measured with this count)
 // With few (batch, key head) units every unit is cut into very many splits to fill that many
 // waves, and the per-CTA fixed cost and the merge of the splits dominate: below this many
 // units one wave suffices (measured at batch 1 / 8 key heads: 37.9 vs 39.5 us per layer-step;
 // at 256 units fewer waves were slower).
 constexpr int kFewUnits = 64;
+// CTA slots per SM that the plan counts: three (the two-column-tile form runs two per SM; its
+// plans were measured with this count).
 constexpr int kCtasPerSm = 3;
 
 struct Plan {
