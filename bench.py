@@ -419,45 +419,53 @@ def run_gpu(args, wl, rank, world):
         host_out = [torch.empty(wl.B, wl.Hq, wl.D, dtype=torch.float32).pin_memory() for _ in range(wl.layers)]
         h2d = sum(t.numel() * t.element_size() for t in host_in[0][0].values()) * wl.layers
         d2h = sum(t.numel() * t.element_size() for t in host_out)
-        # device staging per (layer, parity of the step): the copies run on their own stream and
-        # overlap the other layers' attention; events order each copy against its consumer
+        # device staging per (parity of the step, layer): the copies run on their own stream and
+        # overlap the other steps' attention.  Step i + 1's inputs are copied in while step i
+        # runs, and step i's outputs are copied out while step i + 1 runs; events order each
+        # copy against its consumer once per step, so the 32 layers of a step stay one chain of
+        # programmatically dependent launches (an event between two launches would break it)
         dev_in = [[{n: torch.empty_like(t, device=dev) for n, t in host_in[0][l].items()} for l in range(wl.layers)]
                   for _ in range(2)]
         dev_out = [[torch.empty(wl.B, wl.Hq, wl.D, dtype=torch.float32, device=dev) for _ in range(wl.layers)]
                    for _ in range(2)]
         copy_s = torch.cuda.Stream(device=dev)
         comp_s = torch.cuda.current_stream(dev)
-        in_ready = [[torch.cuda.Event() for _ in range(wl.layers)] for _ in range(2)]
-        out_ready = [[torch.cuda.Event() for _ in range(wl.layers)] for _ in range(2)]
-        out_taken = [[torch.cuda.Event() for _ in range(wl.layers)] for _ in range(2)]
-        in_used = [[torch.cuda.Event() for _ in range(wl.layers)] for _ in range(2)]
+        in_ready = [torch.cuda.Event() for _ in range(2)]
+        step_done = [torch.cuda.Event() for _ in range(2)]
+        out_taken = [torch.cuda.Event() for _ in range(2)]
+
+        def copy_in(i):  # step i's inputs, all layers, into buffer i & 1 (free once step i - 2 ran)
+            with torch.cuda.stream(copy_s):
+                if i >= 2:
+                    copy_s.wait_event(step_done[i & 1])
+                for l in range(wl.layers):
+                    for n in ("q", "k", "v"):
+                        dev_in[i & 1][l][n].copy_(host_in[i][l][n], non_blocking=True)
+                in_ready[i & 1].record(copy_s)
+
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0 = time.perf_counter()
         e0.record()
         e2e_tokens = 0
+        copy_in(0)
         for i, s in enumerate(range(e2e_first, e2e_first + args.steps)):
             L_before = wl.T + s
             par = i & 1
-            with torch.cuda.stream(copy_s):  # this step's inputs, all layers
-                for l in range(wl.layers):
-                    if i >= 2:
-                        copy_s.wait_event(in_used[par][l])      # step i - 2 has read this buffer
-                    for n in ("q", "k", "v"):
-                        dev_in[par][l][n].copy_(host_in[i][l][n], non_blocking=True)
-                    in_ready[par][l].record(copy_s)
+            comp_s.wait_event(in_ready[par])
+            if i >= 2:
+                comp_s.wait_event(out_taken[par])  # step i - 2's outputs were copied out
             for l, c in enumerate(layers):
-                comp_s.wait_event(in_ready[par][l])
-                if i >= 2:
-                    comp_s.wait_event(out_taken[par][l])        # step i - 2's output was copied out
                 c.decode_step(dev_in[par][l]["q"], dev_in[par][l]["k"], dev_in[par][l]["v"], L_before,
                               wl.budget_pct, wl.window, policy=wl.policy, out=dev_out[par][l])
-                in_used[par][l].record(comp_s)
-                out_ready[par][l].record(comp_s)
-                with torch.cuda.stream(copy_s):
-                    copy_s.wait_event(out_ready[par][l])
+            step_done[par].record(comp_s)
+            if i + 1 < args.steps:
+                copy_in(i + 1)
+            with torch.cuda.stream(copy_s):  # this step's outputs, all layers
+                copy_s.wait_event(step_done[par])
+                for l in range(wl.layers):
                     host_out[l].copy_(dev_out[par][l], non_blocking=True)
-                    out_taken[par][l].record(copy_s)
+                out_taken[par].record(copy_s)
             e2e_tokens += wl.B * (L_before + 1) * wl.layers
         comp_s.wait_stream(copy_s)
         e1.record()
