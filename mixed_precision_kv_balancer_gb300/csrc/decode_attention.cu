@@ -1091,7 +1091,11 @@ Plan make_plan(const mikv_cache* c) {
   const double units = static_cast<double>(c->B) * c->Hkv;
   const double slots = static_cast<double>(kNumSMs) * kCtasPerSm;
   const double wb_hi = row_cost(c->hi_bits) * byte_weight(c->hi_bits);  // per token
-  const double wb_lo = row_cost(c->lo_bits) * byte_weight(c->lo_bits);
+  // five to eight query heads per key head double the low tier's MMA and softmax work per
+  // byte (the two-column-tile form): its bytes weigh 1.5 times more (measured at the
+  // Qwen2.5-32B shape: 25.4 -> 25.0 us per attention launch, 37.7 -> 36.3 us per step; 2.0 was
+  // slower than 1.0)
+  const double wb_lo = row_cost(c->lo_bits) * byte_weight(c->lo_bits) * (c->Hq / c->Hkv > 4 ? 1.5 : 1.0);
   const double total = units * (c->cap_hi * wb_hi + c->cap_lo * wb_lo);
   auto chunk_for = [](int cap, double wb, int bits, double target) {
     const int quantum = kWarps * stage_tokens(bits);
