@@ -9,17 +9,20 @@
 // and "Theoretical framework" (projected value state V W_O).
 //
 // Selection is exact integer work on the float bit patterns: one CTA per
-// (batch, key head) runs an MSB-first radix select (4 x 8-bit digits) over
-// order-preserving 32-bit keys to find the b-th best value, takes every
-// candidate above it and, among candidates equal to it, the lowest positions
-// (block-wide prefix count in position order), then writes the kept and evicted
-// positions in ascending order with a block scan.  The result is unique, so it
-// is bit-exact against any correct implementation given the same scores.
+// (batch, key head) runs an MSB-first radix select (digits of 12, 10 and 10
+// bits) over order-preserving 32-bit keys to find the b-th best value, takes
+// every candidate above it and, among candidates equal to it, the lowest
+// positions (block-wide prefix count in position order), then writes the kept
+// and evicted positions in ascending order with a block scan.  The candidates
+// left in the first digit's bin (a few percent of a row of logits or scores)
+// are compacted into a shared-memory list, so the later digits visit only
+// them.  The result is unique, so it is bit-exact against any correct
+// implementation given the same scores.
 //
 // K6, N[b][h][i] = || v_i . W_O[h*D:(h+1)*D, :] ||_1, is a dense GEMM
-// (L x 128) x (128 x hidden) per query head on tensor cores (mma.sync
-// m16n8k16, fp32 accumulate) whose output is never stored: the epilogue sums
-// |.| per row (per-step partials added with Kahan compensation).
+// (L x 128) x (128 x hidden) per query head on the tcgen05 tensor cores (fp16
+// operands, fp32 accumulate in tensor memory) whose output is never stored:
+// the epilogue sums |.| per row.
 #include <algorithm>
 #include <cmath>
 #include <type_traits>
@@ -79,75 +82,177 @@ struct SharedKeys {
   __device__ __forceinline__ uint32_t operator()(int i) const { return k[i]; }
 };
 
-// Mark (flag = 1) the `take` best candidates (flag == 0) by key, ties to lower positions.
+// Radix digits of the 32-bit order key, high to low: 12 bits (sign, exponent and three
+// mantissa bits, which already splits a row of logits or scores finely), then 10 and 10.
+constexpr int kSelBins1 = 4096;
+constexpr int kSelBins = 1024;
+
+// The digit d where the count of candidates in bins above d first reaches `remaining`
+// (scanning nb - 1 -> 0), into scratch[0], and what is left to take inside bin d, into
+// scratch[1]; if every bin together holds fewer than `remaining`, d = 0 with the count above
+// it.  Thread t of the NT owns the NB / NT bins from NB - 1 - t * (NB / NT) down.  The caller
+// synchronises before reading scratch; scratch[0..1] are written only after every thread has
+// passed the barriers of the block scan, so a result read before the next search is safe.
+template <int NB, int NT>
+__device__ __forceinline__ void digit_search(const unsigned* hist, int remaining, int* scratch) {
+  constexpr int per = NB / NT;
+  const int top = NB - 1 - static_cast<int>(threadIdx.x) * per;
+  int sum = 0;
+#pragma unroll
+  for (int j = 0; j < per; ++j) sum += static_cast<int>(hist[top - j]);
+  int total;
+  int above = block_exclusive_scan(sum, scratch + 2, total);
+  if (above < remaining && remaining <= above + sum) {
+    int d = top;
+    for (int j = 0; j < per; ++j) {
+      d = top - j;
+      const int c = static_cast<int>(hist[d]);
+      if (above + c >= remaining) break;
+      above += c;
+    }
+    scratch[0] = d;
+    scratch[1] = remaining - above;
+  } else if (threadIdx.x == NT - 1 && above + sum < remaining) {
+    scratch[0] = 0;
+    scratch[1] = remaining - (above + sum - static_cast<int>(hist[0]));
+  }
+}
+
+// Histogram of the digit (u >> shift) & dmask over the candidates (flag == 0) of the whole row
+// whose key u matches `prefix` under `mask`.
 template <class Keys>
-__device__ void topk_mark(Keys key, int L, int take, uint8_t* flag, unsigned* hist, int* scratch) {
+__device__ __forceinline__ void hist_row(Keys key, int L, const uint8_t* flag, unsigned* hist, int shift,
+                                         uint32_t dmask, uint32_t mask, uint32_t prefix) {
+  const int tid = threadIdx.x;
+  int i0 = 0;
+  if constexpr (std::is_same<Keys, SharedKeys>::value) {
+    // staged rows: four keys and their four flags per load (the flags start L * 4 bytes
+    // after the keys, so both are 16- and 4-byte aligned)
+    const uint4* k4 = reinterpret_cast<const uint4*>(key.k);
+    const uint32_t* f4 = reinterpret_cast<const uint32_t*>(flag);
+    for (int q = tid; q < (L >> 2); q += blockDim.x) {
+      const uint32_t fl = f4[q];
+      if (fl == 0x01010101u * (fl & 0xffu) && (fl & 0xffu) != 0) continue;  // all four taken
+      const uint4 u4 = k4[q];
+      const uint32_t uu[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (((fl >> (8 * e)) & 0xffu) == 0 && (uu[e] & mask) == prefix)
+          atomicAdd(&hist[(uu[e] >> shift) & dmask], 1u);
+    }
+    i0 = L & ~3;
+  }
+  for (int i = i0 + tid; i < L; i += blockDim.x) {
+    if (flag[i] != 0) continue;
+    const uint32_t u = key(i);
+    if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & dmask], 1u);
+  }
+}
+
+// Mark (flag = 1) the `take` best candidates (flag == 0) by key, ties to lower positions.
+// hA holds kSelBins1 counters, hB kSelBins.  After the first digit the candidates left in its
+// bin are copied, in position order, to the list ckey / cpos when they fit in `cap` entries,
+// and the last two digits and the final marking visit only that list; otherwise they visit
+// the whole row.
+template <class Keys>
+__device__ void topk_mark(Keys key, int L, int take, uint8_t* flag, unsigned* hA, unsigned* hB, int* scratch,
+                          uint32_t* ckey, uint16_t* cpos, int cap) {
   if (take <= 0) return;
   const int tid = threadIdx.x;
-  uint32_t prefix = 0, mask = 0;
-  int remaining = take;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
-    int i0 = 0;
+  for (int i = tid; i < kSelBins1; i += blockDim.x) hA[i] = 0;
+  for (int i = tid; i < kSelBins; i += blockDim.x) hB[i] = 0;
+  __syncthreads();
+  hist_row(key, L, flag, hA, 20, kSelBins1 - 1, 0u, 0u);
+  __syncthreads();
+  digit_search<kSelBins1, kSelThreads>(hA, take, scratch);
+  __syncthreads();
+  const uint32_t d1 = static_cast<uint32_t>(scratch[0]);
+  uint32_t prefix = d1 << 20, mask = 0xfff00000u;
+  int remaining = scratch[1];
+  const int n1 = static_cast<int>(hA[d1]);
+  __syncthreads();
+  for (int i = tid; i < kSelBins; i += blockDim.x) hA[i] = 0;  // the third digit's counters
+
+  if (cap > 0 && n1 <= cap) {
+    // candidates above bin d1 are taken now; those in it go to the list, in position order
+    // (each thread a contiguous run of at most 64 positions, placed by a block scan)
+    const int per = ((L + static_cast<int>(blockDim.x) - 1) / static_cast<int>(blockDim.x) + 3) & ~3;
+    const int lo = min(L, tid * per), hi = min(L, lo + per);
+    uint64_t cm = 0;
+    int cnt = 0;
+    auto visit = [&](int i, uint32_t u) {
+      const uint32_t t = u >> 20;
+      if (t > d1) {
+        flag[i] = 1;
+      } else if (t == d1) {
+        cm |= 1ull << (i - lo);
+        ++cnt;
+      }
+    };
+    int i = lo;
     if constexpr (std::is_same<Keys, SharedKeys>::value) {
-      // staged rows: four keys and their four flags per load (the flags start L * 4 bytes
-      // after the keys, so both are 16- and 4-byte aligned)
-      const uint4* k4 = reinterpret_cast<const uint4*>(key.k);
-      const uint32_t* f4 = reinterpret_cast<const uint32_t*>(flag);
-      for (int q = tid; q < (L >> 2); q += blockDim.x) {
-        const uint32_t fl = f4[q];
-        if (fl == 0x01010101u * (fl & 0xffu) && (fl & 0xffu) != 0) continue;  // all four taken
-        const uint4 u4 = k4[q];
+      for (; i + 4 <= hi; i += 4) {  // lo is a multiple of 4: aligned uint4 keys, uint32 flags
+        const uint32_t fl = *reinterpret_cast<const uint32_t*>(flag + i);
+        if (fl == 0x01010101u * (fl & 0xffu) && (fl & 0xffu) != 0) continue;
+        const uint4 u4 = *reinterpret_cast<const uint4*>(key.k + i);
         const uint32_t uu[4] = {u4.x, u4.y, u4.z, u4.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          if (((fl >> (8 * e)) & 0xffu) == 0 && (uu[e] & mask) == prefix)
-            atomicAdd(&hist[(uu[e] >> shift) & 255u], 1u);
+          if (((fl >> (8 * e)) & 0xffu) == 0) visit(i + e, uu[e]);
       }
-      i0 = L & ~3;
     }
-    for (int i = i0 + tid; i < L; i += blockDim.x) {
-      if (flag[i] != 0) continue;
-      const uint32_t u = key(i);
-      if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+    for (; i < hi; ++i)
+      if (flag[i] == 0) visit(i, key(i));
+    int total;
+    int at = block_exclusive_scan(cnt, scratch + 2, total);
+    while (cm) {
+      const int i = lo + __ffsll(static_cast<long long>(cm)) - 1;
+      cm &= cm - 1;
+      ckey[at] = key(i);
+      cpos[at] = static_cast<uint16_t>(i);
+      ++at;
     }
     __syncthreads();
-    // the digit d where the count of candidates in bins above d first reaches `remaining`
-    // (scanning 255 -> 0): one warp, lane l holding bins 255 - 8l .. 248 - 8l; if every bin
-    // together holds fewer than `remaining`, d = 0 with the count above it
-    if (tid < 32) {
-      int c[8], sum = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = static_cast<int>(hist[255 - 8 * tid - j]);
-        sum += c[j];
+    for (int shift = 10; shift >= 0; shift -= 10) {
+      unsigned* h = shift ? hB : hA;
+      for (int j = tid; j < n1; j += blockDim.x) {
+        const uint32_t u = ckey[j];
+        if ((u & mask) == prefix) atomicAdd(&h[(u >> shift) & (kSelBins - 1)], 1u);
       }
-      int incl = sum;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (tid >= off) incl += y;
-      }
-      int above = incl - sum;  // candidates in the bins above this lane's first one
-      if (above < remaining && remaining <= incl) {
-        int d = 255 - 8 * tid;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          d = 255 - 8 * tid - j;
-          if (above + c[j] >= remaining) break;
-          above += c[j];
-        }
-        scratch[0] = d;
-        scratch[1] = remaining - above;
-      } else if (tid == 31 && incl < remaining) {
-        scratch[0] = 0;
-        scratch[1] = remaining - (incl - c[7]);
+      __syncthreads();
+      digit_search<kSelBins, kSelThreads>(h, remaining, scratch);
+      __syncthreads();
+      prefix |= static_cast<uint32_t>(scratch[0]) << shift;
+      mask |= static_cast<uint32_t>(kSelBins - 1) << shift;
+      remaining = scratch[1];
+      __syncthreads();
+    }
+    // list entries above prefix are taken; `remaining` of those equal to it, first in the list
+    const int pc = (n1 + static_cast<int>(blockDim.x) - 1) / static_cast<int>(blockDim.x);
+    const int clo = min(n1, tid * pc), chi = min(n1, clo + pc);
+    int ties = 0;
+    for (int j = clo; j < chi; ++j) ties += ckey[j] == prefix;
+    int rank = block_exclusive_scan(ties, scratch + 2, total);
+    for (int j = clo; j < chi; ++j) {
+      const uint32_t u = ckey[j];
+      if (u > prefix) flag[cpos[j]] = 1;
+      else if (u == prefix) {
+        if (rank < remaining) flag[cpos[j]] = 1;
+        ++rank;
       }
     }
+    __syncthreads();
+    return;
+  }
+
+  for (int shift = 10; shift >= 0; shift -= 10) {
+    unsigned* h = shift ? hB : hA;
+    hist_row(key, L, flag, h, shift, kSelBins - 1, mask, prefix);
+    __syncthreads();
+    digit_search<kSelBins, kSelThreads>(h, remaining, scratch);
     __syncthreads();
     prefix |= static_cast<uint32_t>(scratch[0]) << shift;
-    mask |= 255u << shift;
+    mask |= static_cast<uint32_t>(kSelBins - 1) << shift;
     remaining = scratch[1];
     __syncthreads();
   }
@@ -162,49 +267,71 @@ __device__ void topk_mark(Keys key, int L, int take, uint8_t* flag, unsigned* hi
   for (int i = lo; i < hi; ++i) {
     if (flag[i] != 0) continue;
     const uint32_t u = key(i);
-    if (u > prefix) flag[i] = 3;  // temporary: taken in this stage
+    if (u > prefix) flag[i] = 1;
     else if (u == prefix) {
-      if (rank < remaining) flag[i] = 3;
+      if (rank < remaining) flag[i] = 1;
       ++rank;
     }
   }
   __syncthreads();
-  for (int i = tid; i < L; i += blockDim.x)
-    if (flag[i] == 3) flag[i] = 1;
-  __syncthreads();
+}
+
+// skey[i] = order_key(row[i]), i < L, by the NT threads of the block: kBatch coalesced loads
+// in flight per thread (at fixed offsets from one address) before the stores.
+template <int kBatch, int NT>
+__device__ __forceinline__ void stage_row(const float* __restrict__ row, int L, uint32_t* skey) {
+  for (int base = threadIdx.x; base < L; base += kBatch * NT) {
+    const float* r = row + base;
+    float v[kBatch];
+    if (base + (kBatch - 1) * NT < L) {
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) v[j] = __ldg(r + j * NT);
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) skey[base + j * NT] = order_key(v[j]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) v[j] = base + j * NT < L ? __ldg(r + j * NT) : 0.f;
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j)
+        if (base + j * NT < L) skey[base + j * NT] = order_key(v[j]);
+    }
+  }
 }
 
 // One CTA per (batch, key head).  flag: 0 evicted, 1 taken by a stage, 2 recent window.
 // key1 rows are `stride1` floats apart (L for the score arrays, the slot capacity for logits).
 // STAGE: the row's order keys are read once into shared memory (L x 4 bytes before the L
-// flag bytes) and the five passes of each stage read them there.
+// flag bytes) and every pass of each stage reads them there.  After the flags, from byte
+// `list_off`, the candidate list: `cap` keys, then `cap` 16-bit positions.
 template <bool STAGE>
-__global__ void __launch_bounds__(kSelThreads) select_kernel(
+__global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     const float* __restrict__ key1, long stride1, const float* __restrict__ key2, int L, int window,
     int take1, int take2, int n_keep, int32_t* __restrict__ keep_pos, int32_t* __restrict__ evict_pos,
-    float* __restrict__ keep_scores) {
+    float* __restrict__ keep_scores, int list_off, int cap) {
   extern __shared__ __align__(16) uint8_t sel_smem[];
   uint32_t* skey = reinterpret_cast<uint32_t*>(sel_smem);
   uint8_t* flag = STAGE ? sel_smem + static_cast<size_t>(L) * 4 : sel_smem;
-  __shared__ unsigned hist[256];
+  uint32_t* ckey = reinterpret_cast<uint32_t*>(sel_smem + list_off);
+  uint16_t* cpos = reinterpret_cast<uint16_t*>(ckey + cap);
+  __shared__ unsigned hA[kSelBins1], hB[kSelBins];
   __shared__ int scratch[2 + 32];
   const long unit = blockIdx.x;
   const float* k1 = key1 + unit * stride1;
   const int w = min(window, L);
-  for (int i = threadIdx.x; i < L; i += blockDim.x) {
-    flag[i] = (i >= L - w) ? 2 : 0;
-    if (STAGE) skey[i] = order_key(k1[i]);
+  if (STAGE) {
+    stage_row<4, kSelThreads>(k1, L, skey);
   }
+  for (int i = threadIdx.x; i < L; i += blockDim.x) flag[i] = (i >= L - w) ? 2 : 0;
   __syncthreads();
-  if (STAGE) topk_mark(SharedKeys{skey}, L, take1, flag, hist, scratch);
-  else topk_mark(GlobalKeys{k1}, L, take1, flag, hist, scratch);
+  if (STAGE) topk_mark(SharedKeys{skey}, L, take1, flag, hA, hB, scratch, ckey, cpos, cap);
+  else topk_mark(GlobalKeys{k1}, L, take1, flag, hA, hB, scratch, ckey, cpos, cap);
   if (key2) {
     if (STAGE) {
-      for (int i = threadIdx.x; i < L; i += blockDim.x) skey[i] = order_key(key2[unit * L + i]);
+      stage_row<4, kSelThreads>(key2 + unit * L, L, skey);
       __syncthreads();
-      topk_mark(SharedKeys{skey}, L, take2, flag, hist, scratch);
+      topk_mark(SharedKeys{skey}, L, take2, flag, hA, hB, scratch, ckey, cpos, cap);
     } else {
-      topk_mark(GlobalKeys{key2 + unit * L}, L, take2, flag, hist, scratch);
+      topk_mark(GlobalKeys{key2 + unit * L}, L, take2, flag, hA, hB, scratch, ckey, cpos, cap);
     }
   }
   // compaction in position order
@@ -232,19 +359,205 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   }
 }
 
+// Rows of up to kMaskRow positions: thread t of kMaskThreads owns the kMaskKeys consecutive
+// positions from t * kMaskKeys, and keeps their taken / window / candidate states as bit masks
+// in registers; the staged keys are read back from shared memory (16 bytes at a time) only by
+// the loops that need them, and after the first digit only by the threads that still hold a
+// candidate.  With many keys per thread the fixed cost of a row (histogram clears, block scans,
+// barriers) is shared by fewer threads.  Same result as select_kernel.
+constexpr int kMaskKeys = 16;
+constexpr int kMaskRow = 8192;
+constexpr int kMaskThreads = kMaskRow / kMaskKeys;
+constexpr int kMaskMinBlocks = kMaskThreads >= 1024 ? 2 : 4;
+
+// Bits j < kMaskKeys of the positions p0 + j in [lo, hi).
+__device__ __forceinline__ uint32_t span_bits(int p0, int lo, int hi) {
+  const int a = max(lo - p0, 0), b = min(hi - p0, kMaskKeys);
+  return a < b ? static_cast<uint32_t>(((1ull << b) - 1ull) & ~((1ull << a) - 1ull)) : 0u;
+}
+
+__device__ __forceinline__ void clear_hists(unsigned* hA, unsigned* hB) {
+  for (int i = threadIdx.x; i < kSelBins1; i += kMaskThreads) hA[i] = 0;
+  for (int i = threadIdx.x; i < kSelBins; i += kMaskThreads) hB[i] = 0;
+}
+
+// The eight staged keys of positions p .. p + 7, p a multiple of 8 (past L: 0, never a candidate).
+__device__ __forceinline__ void keys8(const uint32_t* skey, int L, int p, uint32_t (&u)[8]) {
+  if (p + 8 <= L) {
+    const uint4 a = *reinterpret_cast<const uint4*>(skey + p);
+    const uint4 b = *reinterpret_cast<const uint4*>(skey + p + 4);
+    u[0] = a.x; u[1] = a.y; u[2] = a.z; u[3] = a.w;
+    u[4] = b.x; u[5] = b.y; u[6] = b.z; u[7] = b.w;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) u[j] = p + j < L ? skey[p + j] : 0u;
+  }
+}
+
+// Set in `taken` the bits of the `take` best candidates of the block (bits of `cand`), by key,
+// ties to lower positions: digits of 12, 10 and 10 bits; after each digit the candidates in the
+// chosen bin stay in `eq`, those above it are taken.  hA and hB are zero on entry (cleared
+// before the barrier that ends the row's staging).
+__device__ __forceinline__ void mask_mark(const uint32_t* skey, int L, uint32_t cand, int take, uint32_t& taken,
+                                          unsigned* hA, unsigned* hB, int* scratch) {
+  if (take <= 0) return;
+  const int tid = threadIdx.x, p0 = tid * kMaskKeys;
+#pragma unroll
+  for (int c = 0; c < kMaskKeys / 8; ++c) {
+    const uint32_t m = (cand >> (8 * c)) & 0xffu;
+    if (!m) continue;
+    uint32_t u[8];
+    keys8(skey, L, p0 + 8 * c, u);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if ((m >> j) & 1u) atomicAdd(&hA[u[j] >> 20], 1u);
+  }
+  __syncthreads();
+  digit_search<kSelBins1, kMaskThreads>(hA, take, scratch);
+  __syncthreads();
+  uint32_t d = static_cast<uint32_t>(scratch[0]);
+  int remaining = scratch[1];
+  // hA is read no more in this digit: clear the part the third digit counts in
+  for (int i = tid; i < kSelBins; i += kMaskThreads) hA[i] = 0;
+  uint32_t eq = 0;
+#pragma unroll
+  for (int c = 0; c < kMaskKeys / 8; ++c) {
+    const uint32_t m = (cand >> (8 * c)) & 0xffu;
+    if (!m) continue;
+    uint32_t u[8];
+    keys8(skey, L, p0 + 8 * c, u);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t t = u[j] >> 20;
+      if ((m >> j) & 1u) {
+        if (t > d) taken |= 1u << (8 * c + j);
+        else if (t == d) eq |= 1u << (8 * c + j);
+      }
+    }
+  }
+  for (int shift = 10; shift >= 0; shift -= 10) {
+    unsigned* h = shift ? hB : hA;
+#pragma unroll
+    for (int c = 0; c < kMaskKeys / 8; ++c) {
+      const uint32_t m = (eq >> (8 * c)) & 0xffu;
+      if (!m) continue;
+      uint32_t u[8];
+      keys8(skey, L, p0 + 8 * c, u);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if ((m >> j) & 1u) atomicAdd(&h[(u[j] >> shift) & (kSelBins - 1)], 1u);
+    }
+    __syncthreads();
+    digit_search<kSelBins, kMaskThreads>(h, remaining, scratch);
+    __syncthreads();
+    d = static_cast<uint32_t>(scratch[0]);
+    remaining = scratch[1];
+#pragma unroll
+    for (int c = 0; c < kMaskKeys / 8; ++c) {
+      const uint32_t m = (eq >> (8 * c)) & 0xffu;
+      if (!m) continue;
+      uint32_t u[8];
+      keys8(skey, L, p0 + 8 * c, u);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t t = (u[j] >> shift) & (kSelBins - 1);
+        if ((m >> j) & 1u) {
+          if (t > d) taken |= 1u << (8 * c + j);
+          if (t != d) eq &= ~(1u << (8 * c + j));
+        }
+      }
+    }
+  }
+  // eq: the candidates equal to the threshold key; the first `remaining` in position order
+  int total;
+  int rank = block_exclusive_scan(__popc(eq), scratch + 2, total);
+  for (uint32_t m = eq; m; m &= m - 1) {
+    if (rank < remaining) taken |= m & (0u - m);
+    ++rank;
+  }
+}
+
+__global__ void __launch_bounds__(kMaskThreads, kMaskMinBlocks) select_mask_kernel(
+    const float* __restrict__ key1, long stride1, const float* __restrict__ key2, int L, int window,
+    int take1, int take2, int n_keep, int32_t* __restrict__ keep_pos, int32_t* __restrict__ evict_pos,
+    float* __restrict__ keep_scores) {
+  extern __shared__ __align__(16) uint8_t sel_smem[];
+  uint32_t* skey = reinterpret_cast<uint32_t*>(sel_smem);  // L keys
+  __shared__ unsigned hA[kSelBins1], hB[kSelBins];
+  __shared__ int scratch[2 + 32];
+  const long unit = blockIdx.x;
+  const float* k1 = key1 + unit * stride1;
+  const int w = min(window, L);
+  const int p0 = threadIdx.x * kMaskKeys;
+  uint32_t taken = 0;
+  clear_hists(hA, hB);
+  stage_row<16, kMaskThreads>(k1, L, skey);
+  __syncthreads();
+  mask_mark(skey, L, span_bits(p0, 0, L - w), take1, taken, hA, hB, scratch);
+  if (key2) {
+    __syncthreads();  // every read of the first row's keys and of the histograms is done
+    clear_hists(hA, hB);
+    stage_row<16, kMaskThreads>(key2 + unit * L, L, skey);
+    __syncthreads();
+    mask_mark(skey, L, span_bits(p0, 0, L - w) & ~taken, take2, taken, hA, hB, scratch);
+  }
+  // compaction in position order.  Kept positions alone: each thread stores its own.  With
+  // scores or evicted positions: the kept positions, then the evicted, into shared memory (over
+  // the keys, read no more), then copied out with coalesced stores.
+  const uint32_t valid = span_bits(p0, 0, L);
+  const uint32_t kept = taken | span_bits(p0, L - w, L);
+  int total;
+  int kp = block_exclusive_scan(__popc(kept), scratch + 2, total);
+  if (!keep_scores && !evict_pos) {
+    int32_t* kout = keep_pos + unit * n_keep;
+    for (uint32_t m = kept; m; m &= m - 1, ++kp)
+      if (kp < n_keep) kout[kp] = p0 + __ffs(m) - 1;
+    return;
+  }
+  int ep = total + min(p0, L) - kp;
+  int32_t* pos = reinterpret_cast<int32_t*>(skey);
+  for (uint32_t m = kept; m; m &= m - 1) pos[kp++] = p0 + __ffs(m) - 1;
+  for (uint32_t m = valid & ~kept; m; m &= m - 1) pos[ep++] = p0 + __ffs(m) - 1;
+  __syncthreads();
+  const int nk = min(n_keep, total);
+  int32_t* kout = keep_pos + unit * n_keep;
+  for (int j = threadIdx.x; j < nk; j += kMaskThreads) kout[j] = pos[j];
+  if (keep_scores) {
+    float* sout = keep_scores + unit * n_keep;
+#pragma unroll 1
+    for (int j = threadIdx.x; j < nk; j += kMaskThreads) sout[j] = k1[pos[j]];
+  }
+  if (evict_pos) {  // null: not wanted
+    const int ne = min(L - n_keep, L - total);
+    int32_t* eout = evict_pos + unit * (L - n_keep);
+    for (int j = threadIdx.x; j < ne; j += kMaskThreads) eout[j] = pos[total + j];
+  }
+}
+
 // Rows of up to kSelStageMax / 5 keys are staged in shared memory (4 bytes of key and one of
-// flag per position); longer rows are read from global memory in every pass.
+// flag per position); longer rows are read from global memory in every pass.  The candidate
+// list takes up to L / 8 entries of 6 bytes in what is left (none beyond 65536 positions).
 constexpr int kSelStageMax = 200 * 1024;
 int launch_select(int units, const float* key1, long stride1, const float* key2, int L, int window, int take1,
                   int take2, int n_keep, int32_t* keep_pos, int32_t* evict_pos, float* keep_scores,
                   cudaStream_t s) {
+  if (L <= kMaskRow) {
+    const int smem = (L * 4 + 15) & ~15;
+    if (cudaFuncSetAttribute(select_mask_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return check_launch("select_mask_kernel attribute");
+    select_mask_kernel<<<units, kMaskThreads, smem, s>>>(key1, stride1, key2, L, window, take1, take2, n_keep,
+                                                         keep_pos, evict_pos, keep_scores);
+    return check_launch("select_mask_kernel");
+  }
   const bool stage = static_cast<long>(L) * 5 <= kSelStageMax;
-  const int smem = stage ? L * 5 : L;
+  const int list_off = ((stage ? L * 5 : L) + 15) & ~15;
+  const int cap = L <= 65536 ? std::max(0, std::min(L / 8 + 32, (kSelStageMax - list_off) / 6)) : 0;
+  const int smem = list_off + cap * 6;
   auto kern = stage ? select_kernel<true> : select_kernel<false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return check_launch("select_kernel attribute");
   kern<<<units, kSelThreads, smem, s>>>(key1, stride1, key2, L, window, take1, take2, n_keep, keep_pos,
-                                               evict_pos, keep_scores);
+                                               evict_pos, keep_scores, list_off, cap);
   return check_launch("select_kernel");
 }
 

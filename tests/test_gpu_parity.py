@@ -320,10 +320,14 @@ def _score_tensor(rng, B, Hkv, L, ties):
     return rng.random((B, Hkv, L)).astype(np.float32) * 10
 
 
+# Paths: rows up to 40960 keys are staged in shared memory; up to 65536 keys the candidates of
+# the first digit's bin go to a list when they fit in L/8 + 32 entries (the tie and constant
+# rows overflow it); 100000 keys take the whole-row passes with keys read from global memory.
 @pytest.mark.parametrize("L,p,W,ties", [(512, 20, 32, False), (512, 20, 32, True), (4097, 25, 32, True),
                                         (33, 50, 40, False), (1000, 0, 0, True), (1000, 100, 5, False),
                                         (32768, 40, 32, False), (131072, 20, 64, True), (1, 20, 0, False),
-                                        (2048, 30, 16, "const")])
+                                        (2048, 30, 16, "const"), (40961, 25, 16, False), (65536, 20, 32, False),
+                                        (100000, 20, 32, False)])
 def test_select_h2o_bit_exact(L, p, W, ties):
     rng = np.random.default_rng(L + p)
     B, Hkv = 2, 3
