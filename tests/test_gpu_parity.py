@@ -320,14 +320,17 @@ def _score_tensor(rng, B, Hkv, L, ties):
     return rng.random((B, Hkv, L)).astype(np.float32) * 10
 
 
-# Paths: rows up to 40960 keys are staged in shared memory; up to 65536 keys the candidates of
-# the first digit's bin go to a list when they fit in L/8 + 32 entries (the tie and constant
-# rows overflow it); 100000 keys take the whole-row passes with keys read from global memory.
+# Paths: rows up to 8192 keys take the 512-thread bit-mask kernel (8192 itself, and a window
+# of half the row); longer rows up to 40960 keys are staged in shared memory; up to 65536 keys
+# the candidates of the first digit's bin go to a list when they fit in L/8 + 32 entries (the
+# tie and constant rows overflow it); 100000 keys take the whole-row passes with keys read from
+# global memory.
 @pytest.mark.parametrize("L,p,W,ties", [(512, 20, 32, False), (512, 20, 32, True), (4097, 25, 32, True),
                                         (33, 50, 40, False), (1000, 0, 0, True), (1000, 100, 5, False),
                                         (32768, 40, 32, False), (131072, 20, 64, True), (1, 20, 0, False),
                                         (2048, 30, 16, "const"), (40961, 25, 16, False), (65536, 20, 32, False),
-                                        (100000, 20, 32, False)])
+                                        (100000, 20, 32, False), (8192, 20, 32, False), (8192, 20, 32, True),
+                                        (8193, 20, 32, False), (8193, 20, 32, True), (7999, 10, 4000, False)])
 def test_select_h2o_bit_exact(L, p, W, ties):
     rng = np.random.default_rng(L + p)
     B, Hkv = 2, 3
@@ -349,7 +352,8 @@ def test_select_h2o_bit_exact(L, p, W, ties):
 
 
 @pytest.mark.parametrize("L,p,W,rep,ties", [(600, 40, 32, 5, False), (600, 40, 32, 5, True),
-                                            (32768, 40, 32, 5, False), (257, 30, 8, 1, True)])
+                                            (32768, 40, 32, 5, False), (257, 30, 8, 1, True),
+                                            (8192, 30, 32, 4, False), (8193, 30, 32, 4, True)])
 def test_select_criticalkv_bit_exact(L, p, W, rep, ties):
     rng = np.random.default_rng(L * 3 + rep)
     B, Hkv = 1, 2
