@@ -331,7 +331,7 @@ struct ChanArgs {
 template <int BITS, bool VALUES = true>
 __global__ void __launch_bounds__(kTileThreads) channel_close_kernel(ChanArgs a) {
   __shared__ __align__(16) __half ks[kGS][kD];        // keys, row-major
-  __shared__ __align__(16) uint8_t vs[kGS][kD * 2];   // values, 16-byte chunks swizzled by row
+  __shared__ __align__(16) uint8_t vs[VALUES ? kGS : 1][kD * 2];  // values, 16-byte chunks swizzled by row
   __shared__ __align__(16) uint8_t cs[kGS][kD];       // key codes
   __shared__ __half2 ext[2][kD / 2][2];                // per row half: (min, max) of channel pairs
   __shared__ __align__(16) float ones[kD];
