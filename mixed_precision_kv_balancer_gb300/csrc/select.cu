@@ -13,11 +13,14 @@
 // bits) over order-preserving 32-bit keys to find the b-th best value, takes
 // every candidate above it and, among candidates equal to it, the lowest
 // positions (block-wide prefix count in position order), then writes the kept
-// and evicted positions in ascending order with a block scan.  The candidates
-// left in the first digit's bin (a few percent of a row of logits or scores)
-// are compacted into a shared-memory list, so the later digits visit only
-// them.  The result is unique, so it is bit-exact against any correct
-// implementation given the same scores.
+// and evicted positions in ascending order with a block scan.  Rows of up to
+// 8192 positions take 512 threads, each holding the states of 16 consecutive
+// positions as bit masks, so after the first digit (whose bin keeps a few
+// percent of a row of logits or scores) only the threads still holding a
+// candidate read keys again.  Longer rows take 1024 threads with a flag byte
+// per position, the first digit's candidates compacted into a shared-memory
+// list when they fit.  The result is unique, so it is bit-exact against any
+// correct implementation given the same scores.
 //
 // K6, N[b][h][i] = || v_i . W_O[h*D:(h+1)*D, :] ||_1, is a dense GEMM
 // (L x 128) x (128 x hidden) per query head on the tcgen05 tensor cores (fp16
