@@ -38,6 +38,18 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool v
   int n = valid ? 16 : 0;
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n));
 }
+// The same for data read once per pass over a buffer far larger than L2: the line is marked
+// to be evicted first, so what smaller kernels write and read back soon after stays in L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void cp_async16_once(uint32_t dst, const void* src, bool valid, uint64_t policy) {
+  int n = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n" ::"r"(dst), "l"(src), "r"(n),
+               "l"(policy));
+}
 // 8-byte async copy (L1-allocating form, the only one with 8-byte granularity).
 __device__ __forceinline__ void cp_async8(uint32_t dst, const void* src, bool valid) {
   int n = valid ? 8 : 0;

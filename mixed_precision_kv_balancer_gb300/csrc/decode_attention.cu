@@ -144,13 +144,14 @@ __device__ __forceinline__ void load_stage(uint32_t sb, const uint8_t* gk, const
                                            const uint8_t* gkm, const uint8_t* gvm, int nvalid,
                                            int lane, const CopyLane<BITS>& cl) {
   using F = Fmt<BITS, CH>;
+  const uint64_t once = l2_evict_first_policy();  // each cache row is read once per step
 #pragma unroll
   for (int it = 0; it < F::kST / F::kRowsPerIt; ++it) {
     const bool ok = FULL || cl.rl + it * F::kRowsPerIt < nvalid;
     const uint32_t dst = ((it & 1) ? cl.d1 : cl.d0) + it * F::kRowsPerIt * F::kRS;
     // a zero-filled chunk reads nothing; it still gets the stage's first chunk (valid)
-    cp_async16(sb + dst, ok ? gk + it * 512 : gk - lane * 16, ok);
-    cp_async16(sb + F::kOffV + dst, ok ? gv + it * 512 : gv - lane * 16, ok);
+    cp_async16_once(sb + dst, ok ? gk + it * 512 : gk - lane * 16, ok, once);
+    cp_async16_once(sb + F::kOffV + dst, ok ? gv + it * 512 : gv - lane * 16, ok, once);
   }
   if constexpr (F::kQuant) {
     if constexpr (CH) cp_async16(sb + F::kOffKM + lane * 16, gkm + lane * 16, true);  // the group's key meta
