@@ -88,7 +88,7 @@ def workload(args):
 # DRAM bytes (read + write) of one decode_partial_kernel launch per (batch, key head) unit,
 # from ncu (dram__bytes_read.sum + dram__bytes_write.sum) on the full-depth workload at
 # batch 32, one layer; the launch's traffic grows with the units it processes.
-TRAFFIC_PER_UNIT = {"llama31_8b_full": (351.579392e6 + 10.090496e6) / (32 * 8)}
+TRAFFIC_PER_UNIT = {"llama31_8b_full": (351.550976e6 + 4.793856e6) / (32 * 8)}
 
 
 def same_cache_shape(wl):
