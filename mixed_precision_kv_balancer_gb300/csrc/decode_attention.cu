@@ -11,7 +11,9 @@
 // Design (split-K flash decoding, one pass over the packed cache):
 // * Grid (splits, B*Hkv).  A CTA owns a contiguous chunk of ONE tier of one
 //   (batch, key head); its 4 warps stream stages of that chunk through private
-//   shared-memory rings filled by 16-byte cp.async (zero-filled past the end).
+//   shared-memory rings filled by 16-byte cp.async (zero-filled past the end),
+//   the cache rows marked evict-first in L2 (each is read once per step), so
+//   the partials and logits the step's later launches read back stay in L2.
 // * Every query head of the key head's group is served by the same pass: the
 //   group is the mma's N dimension, so the cache is read once per key head.
 // * QK^T: m16n8k16 with 16 tokens as M and the columns (head, hi|lo) as N.  The
